@@ -1,0 +1,119 @@
+"""Planted mistakes in the oracle must each fail at least one pin.
+
+Each case swaps one oracle function for a plausibly wrong variant (on the CPU, for
+the duration of the test only) and checks that the named pins reject it.
+"""
+import math
+
+import numpy as np
+import pytest
+
+import oracle as O
+import oracle.dllm_oracle as OD
+from tests import test_oracle_pins as P
+
+
+def _rope_adjacent_pairs(v, positions, theta):
+    v = np.asarray(v, np.float64)
+    hd = v.shape[-1]
+    ang = np.asarray(positions, np.float64)[:, None] * O.rope_inv_freq(hd, theta)[None, :]
+    c, s = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    ev, od = v[..., 0::2], v[..., 1::2]
+    out = np.empty_like(v)
+    out[..., 0::2] = ev * c - od * s
+    out[..., 1::2] = od * c + ev * s
+    return out
+
+
+def _rope_wrong_sign(v, positions, theta):
+    v = np.asarray(v, np.float64)
+    half = v.shape[-1] // 2
+    ang = np.asarray(positions, np.float64)[:, None] * O.rope_inv_freq(v.shape[-1], theta)[None, :]
+    c, s = np.cos(ang)[:, None, :], np.sin(ang)[:, None, :]
+    lo, hi = v[..., :half], v[..., half:]
+    return np.concatenate([lo * c + hi * s, hi * c - lo * s], axis=-1)
+
+
+def _inv_freq_wrong_exponent(head_dim, theta):
+    i = np.arange(head_dim // 2, dtype=np.float64)
+    return np.power(float(theta), -i / head_dim)
+
+
+def _project_kv_swapped(x, w, n_heads):
+    q, k, v = _orig_project(x, w, n_heads)
+    return q, v, k
+
+
+def _attention_scale_1_over_d(q, K, V, vis=None):
+    q = np.asarray(q, float)
+    return _att(q, np.asarray(K, float), np.asarray(V, float), vis, 1.0 / q.shape[-1])
+
+
+def _att(q, K, V, vis, scale, subtract_max=True):
+    s = np.einsum("qhd,khd->hqk", q, K) * scale
+    if vis is not None:
+        s = np.where(np.asarray(vis, bool)[None], s, -np.inf)
+    m = s.max(-1, keepdims=True) if subtract_max else 0.0
+    with np.errstate(over="ignore", invalid="ignore"):
+        e = np.exp(s - m)
+        p = e / e.sum(-1, keepdims=True)
+    return np.einsum("hqk,khd->qhd", p, V)
+
+
+def _attention_no_max(q, K, V, vis=None):
+    return _att(np.asarray(q, float), np.asarray(K, float), np.asarray(V, float), vis,
+                1.0 / math.sqrt(np.shape(q)[-1]), subtract_max=False)
+
+
+def _visible_base_blind_to_mask(qview, kview):
+    q = np.asarray(qview)[:, None]
+    k = np.asarray(kview)[None, :]
+    return (k == O.KVIEW_SHARED) | ((q == O.VIEW_MASK) & (k == O.KVIEW_MASK)) | ((q == O.VIEW_DRAFT) & (k == O.KVIEW_DRAFT))
+
+
+def _topk_ties_high(mass, block_lo, block_len, k):
+    B, S = mass.shape
+    out = np.empty((B, k), np.int32)
+    for b in range(B):
+        cand = [p for p in range(S) if not (block_lo[b] <= p < block_lo[b] + block_len)]
+        cand.sort(key=lambda p: (-float(mass[b, p]), -p))
+        out[b] = cand[:k]
+    return out
+
+
+def _e4m3_round_away(y):
+    y = np.asarray(y, np.float64)
+    a = np.abs(y)
+    _, ex = np.frexp(a)
+    e = np.clip(ex - 1, -6, 8)
+    quantum = np.ldexp(1.0, e - 3)
+    q = np.floor(a / quantum + 0.5) * quantum
+    return np.sign(y) * np.minimum(q, 448.0)
+
+
+_orig_project = OD.project_qkv
+
+CASES = [
+    ("rope", _rope_adjacent_pairs, [P.test_rope_golden_pairing_and_frequency]),
+    ("rope", _rope_wrong_sign, [P.test_rope_golden_hd2]),
+    ("rope_inv_freq", _inv_freq_wrong_exponent, [P.test_rope_golden_pairing_and_frequency]),
+    ("project_qkv", _project_kv_swapped, [P.test_projection_identity_weights]),
+    ("attention", _attention_scale_1_over_d, [P.test_attention_golden_weights]),
+    ("attention", _attention_no_max, [P.test_attention_permutation_invariant_and_shift_stable]),
+    ("visible", _visible_base_blind_to_mask, [P.test_visibility_truth_table]),
+    ("kv_topk", _topk_ties_high, [P.test_topk_ties_take_lower_position_and_permutation_equivariance]),
+    ("e4m3_quantize", _e4m3_round_away, [P.test_e4m3_quantize_matches_library_rounding_in_range]),
+]
+
+
+@pytest.mark.parametrize("name,bad,pins", CASES, ids=[f"{c[0]}-{c[1].__name__}" for c in CASES])
+def test_planted_mistake_is_caught(monkeypatch, name, bad, pins):
+    monkeypatch.setattr(OD, name, bad)
+    monkeypatch.setattr(O, name, bad)
+    caught = 0
+    for pin in pins:
+        try:
+            pin()
+        except (AssertionError, ValueError, FloatingPointError):
+            caught += 1
+    assert caught == len(pins), f"planted mistake in {name} slipped past {pins}"

@@ -1,0 +1,363 @@
+"""Pins for the fp64 oracle: closed forms, invariants, brute force, one library routine.
+
+None of these re-type the oracle's own formula: each checks a property or value that
+the mathematics of the step fixes independently of how the oracle computes it.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+import oracle as O
+import workloads as W
+
+GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "closed_forms.json")))
+
+
+def _rng(s=0):
+    return np.random.default_rng(1234 + s)
+
+
+# ----------------------------------------------------------------------------- RoPE
+def test_rope_golden_hd2():
+    for c in GOLD["rope_hd2"]["cases"]:
+        y = O.rope(np.array(c["x"])[None, None, :], np.array([c["p"]]), theta=10000.0)
+        np.testing.assert_allclose(y[0, 0], c["y"], rtol=0, atol=1e-15)
+
+
+def test_rope_golden_pairing_and_frequency():
+    g = GOLD["rope_hd4_theta100"]
+    for c in g["cases"]:
+        y = O.rope(np.array(c["x"])[None, None, :], np.array([g["p"]]), theta=100.0)
+        np.testing.assert_allclose(y[0, 0], c["y"], rtol=0, atol=1e-15)
+
+
+def test_rope_preserves_norm():
+    r = _rng()
+    v = r.standard_normal((50, 3, 128))
+    p = r.integers(0, 5000, 50)
+    y = O.rope(v, p, 500000.0)
+    np.testing.assert_allclose(np.linalg.norm(y, axis=-1), np.linalg.norm(v, axis=-1), rtol=1e-13)
+
+
+def test_rope_dot_depends_only_on_offset():
+    r = _rng(1)
+    q = r.standard_normal((1, 2, 64))
+    k = r.standard_normal((1, 2, 64))
+    for p, pk, c in [(5, 3, 100), (0, 70, 1000), (127, 0, 2500)]:
+        d1 = np.sum(O.rope(q, np.array([p]), 1e4) * O.rope(k, np.array([pk]), 1e4), axis=-1)
+        d2 = np.sum(O.rope(q, np.array([p + c]), 1e4) * O.rope(k, np.array([pk + c]), 1e4), axis=-1)
+        np.testing.assert_allclose(d1, d2, rtol=1e-10, atol=1e-10)
+
+
+def test_rope_position_zero_is_identity():
+    v = _rng(2).standard_normal((4, 2, 16))
+    np.testing.assert_array_equal(O.rope(v, np.zeros(4, int), 1e4), v)
+
+
+# ----------------------------------------------------------------------- projection
+def test_projection_identity_weights():
+    D, H = 8, 2
+    eye = np.eye(D)
+    w = np.concatenate([eye, 2 * eye, 3 * eye])  # [3D][D]
+    x = _rng(3).standard_normal((5, D))
+    q, k, v = O.project_qkv(x, w, H)
+    np.testing.assert_array_equal(q.reshape(5, D), x)
+    np.testing.assert_array_equal(k.reshape(5, D), 2 * x)
+    np.testing.assert_array_equal(v.reshape(5, D), 3 * x)
+
+
+def test_projection_row_permutation_permutes_features():
+    D, H = 8, 2
+    r = _rng(4)
+    w = r.standard_normal((3 * D, D))
+    perm = r.permutation(3 * D)
+    x = r.standard_normal((3, D))
+    q, k, v = O.project_qkv(x, w, H)
+    y = np.concatenate([q.reshape(3, D), k.reshape(3, D), v.reshape(3, D)], axis=1)
+    q2, k2, v2 = O.project_qkv(x, w[perm], H)
+    y2 = np.concatenate([q2.reshape(3, D), k2.reshape(3, D), v2.reshape(3, D)], axis=1)
+    np.testing.assert_allclose(y2, y[:, perm], rtol=1e-14)
+
+
+def test_projection_head_split_brute_force():
+    D, H, hd = 6, 3, 2
+    r = _rng(5)
+    w = r.standard_normal((3 * D, D))
+    x = r.standard_normal((2, D))
+    q, k, v = O.project_qkv(x, w, H)
+    for t in range(2):
+        for part, arr in enumerate((q, k, v)):
+            for h in range(H):
+                for i in range(hd):
+                    n = part * D + h * hd + i
+                    ref = sum(x[t, c] * w[n, c] for c in range(D))
+                    assert abs(arr[t, h, i] - ref) < 1e-12
+
+
+# ------------------------------------------------------------------------ attention
+def test_attention_golden_weights():
+    g = GOLD["attention_weights_1234"]
+    q = np.array(g["q"])[None, None, :]
+    K = np.array([[math.log(a), 0, 0, 0] for a in g["a"]])[:, None, :]
+    V = np.array(g["v"], float)[:, None, :]
+    o = O.attention(q, K, V)
+    np.testing.assert_allclose(o[0, 0], g["o"], rtol=1e-13)
+
+
+def test_attention_identical_keys_gives_mean_of_v():
+    r = _rng(6)
+    k = r.standard_normal(16)
+    K = np.tile(k, (9, 2, 1))  # 9 keys, 2 heads
+    V = r.standard_normal((9, 2, 16))
+    q = r.standard_normal((3, 2, 16))
+    np.testing.assert_allclose(O.attention(q, K, V), np.broadcast_to(V.mean(0), (3, 2, 16)), rtol=1e-12)
+
+
+def test_attention_single_visible_key():
+    r = _rng(7)
+    K, V = r.standard_normal((6, 1, 8)), r.standard_normal((6, 1, 8))
+    q = r.standard_normal((2, 1, 8))
+    vis = np.zeros((2, 6), bool)
+    vis[0, 4] = vis[1, 1] = True
+    o = O.attention(q, K, V, vis)
+    np.testing.assert_allclose(o[0, 0], V[4, 0], rtol=1e-14)
+    np.testing.assert_allclose(o[1, 0], V[1, 0], rtol=1e-14)
+
+
+def test_attention_permutation_invariant_and_shift_stable():
+    r = _rng(8)
+    q, K, V = r.standard_normal((4, 2, 8)), r.standard_normal((10, 2, 8)), r.standard_normal((10, 2, 8))
+    perm = r.permutation(10)
+    np.testing.assert_allclose(O.attention(q, K[perm], V[perm]), O.attention(q, K, V), rtol=1e-12)
+    # huge logits must not overflow (max subtraction): scale q by 1e3
+    o = O.attention(1e3 * q, K, V)
+    assert np.all(np.isfinite(o))
+
+
+def test_attention_brute_force_tiny_python_loops():
+    # B=1, H=1, hd=8, S=4, 2-token block: pure-Python step against the oracle step.
+    r = _rng(9)
+    D, H, hd, S = 8, 1, 8, 4
+    theta = 10000.0
+    w = r.standard_normal((3 * D, D)) * 0.3
+    x_pre = r.standard_normal((1, 2, D))
+    x = r.standard_normal((1, 2, D))
+    pre_pos = np.array([[0, 3]])
+    pos = np.array([[1, 2]])
+
+    def proj(row):
+        return [sum(row[c] * w[n, c] for c in range(D)) for n in range(3 * D)]
+
+    def rot(vec, p):
+        half = hd // 2
+        out = list(vec)
+        for i in range(half):
+            a = p * theta ** (-2.0 * i / hd)
+            out[i] = vec[i] * math.cos(a) - vec[i + half] * math.sin(a)
+            out[i + half] = vec[i + half] * math.cos(a) + vec[i] * math.sin(a)
+        return out
+
+    Kc = [None] * S
+    Vc = [None] * S
+    for t in range(2):
+        y = proj(x_pre[0, t])
+        Kc[pre_pos[0, t]] = rot(y[D:2 * D], pre_pos[0, t])
+        Vc[pre_pos[0, t]] = y[2 * D:]
+    qs = []
+    for t in range(2):
+        y = proj(x[0, t])
+        Kc[pos[0, t]] = rot(y[D:2 * D], pos[0, t])
+        Vc[pos[0, t]] = y[2 * D:]
+        qs.append(rot(y[:D], pos[0, t]))
+    expect = []
+    for t in range(2):
+        s = [sum(qs[t][i] * Kc[j][i] for i in range(hd)) / math.sqrt(hd) for j in range(S)]
+        m = max(s)
+        e = [math.exp(v - m) for v in s]
+        z = sum(e)
+        expect.append([sum(e[j] / z * Vc[j][i] for j in range(S)) for i in range(hd)])
+
+    cache = O.OracleCache(1, S, 0, H, hd)
+    O.write_rows(cache, w, x_pre, pre_pos, theta)
+    out, _ = O.step(cache, w, theta, x, pos)
+    np.testing.assert_allclose(out[0], np.array(expect), rtol=1e-12, atol=1e-13)
+
+
+# --------------------------------------------------------------------- Flash-Verify
+def test_visibility_truth_table():
+    # rows: query view BASE, DRAFT, MASK; columns: key view SHARED, MASK, DRAFT, NONE
+    qv = np.array([O.VIEW_BASE, O.VIEW_DRAFT, O.VIEW_MASK])
+    kv = np.array([O.KVIEW_SHARED, O.KVIEW_MASK, O.KVIEW_DRAFT, O.KVIEW_NONE])
+    expect = np.array([[1, 1, 0, 0],
+                       [1, 0, 1, 0],
+                       [1, 1, 0, 0]], bool)
+    np.testing.assert_array_equal(O.visible(qv, kv), expect)
+
+
+def _verify_case(seed=0, **kw):
+    args = dict(batch=2, d_model=256, head_dim=128, max_pos=96, block=16, gen_lo=48, search=6, tail_slots=8)
+    args.update(kw)
+    return W.make(4, seed=seed, **args)
+
+
+def _run(wl, x=None, positions=None, view=None):
+    s = wl.shape
+    cache = O.OracleCache(s.batch, s.max_pos, s.tail_slots, s.n_heads, s.head_dim)
+    O.write_rows(cache, wl.w, wl.pre_x, wl.pre_pos, s.rope_theta)
+    return O.step(cache, wl.w, s.rope_theta, wl.x if x is None else x,
+                  wl.positions if positions is None else positions, view)[0], cache
+
+
+def test_verify_draft_equal_mask_gives_identical_views():
+    wl = _verify_case()
+    x = wl.x.copy()
+    n_blk = wl.block_len
+    for b in range(wl.shape.batch):
+        # draft rows take exactly the x of their mask-view twin
+        for t in range(n_blk, x.shape[1]):
+            twin = np.where((wl.positions[b, :n_blk] == wl.positions[b, t]) & (wl.view[b, :n_blk] == O.VIEW_MASK))[0]
+            assert len(twin) == 1
+            x[b, t] = x[b, twin[0]]
+    out, _ = _run(wl, x=x, view=wl.view)
+    for b in range(wl.shape.batch):
+        for t in range(n_blk, x.shape[1]):
+            twin = np.where((wl.positions[b, :n_blk] == wl.positions[b, t]) & (wl.view[b, :n_blk] == O.VIEW_MASK))[0][0]
+            np.testing.assert_allclose(out[b, t], out[b, twin], rtol=1e-12, atol=1e-14)
+
+
+def test_verify_empty_search_set_is_the_ordinary_step():
+    wl = _verify_case()
+    n_blk = wl.block_len
+    x, pos = wl.x[:, :n_blk], wl.positions[:, :n_blk]
+    base_view = np.zeros_like(wl.view[:, :n_blk])
+    out_a, _ = _run(wl, x=x, positions=pos, view=base_view)
+    out_b, _ = _run(wl, x=x, positions=pos, view=None)
+    np.testing.assert_array_equal(out_a, out_b)
+
+
+def test_verify_base_rows_never_see_draft_views():
+    wl = _verify_case()
+    n_blk = wl.block_len
+    full, _ = _run(wl, view=wl.view)
+    plain, _ = _run(wl, x=wl.x[:, :n_blk], positions=wl.positions[:, :n_blk], view=wl.view[:, :n_blk])
+    base = wl.view[:, :n_blk] != O.VIEW_DRAFT
+    np.testing.assert_allclose(full[:, :n_blk][base], plain[base], rtol=1e-12, atol=1e-14)
+
+
+def test_verify_draft_rows_use_tail_slots():
+    wl = _verify_case()
+    _, cache = _run(wl, view=wl.view)
+    S = wl.shape.max_pos
+    n_draft = int((wl.view[0] == O.VIEW_DRAFT).sum())
+    assert cache.written[0, S:S + n_draft].all() and not cache.written[0, S + n_draft:].any()
+
+
+# ---------------------------------------------------------------------------- drift
+def test_cosine_special_cases():
+    v = _rng(10).standard_normal(300)
+    assert abs(O.cosine(v, v) - 1) < 1e-15
+    assert abs(O.cosine(v, -v) + 1) < 1e-15
+    assert abs(O.cosine(v, 3.5 * v) - 1) < 1e-15
+    e1, e2 = np.eye(2)
+    assert O.cosine(e1, e2) == 0.0
+
+
+def test_topk_brute_force_and_block_exclusion():
+    r = _rng(11)
+    B, S, k = 3, 64, 7
+    mass = r.random((B, S)).astype(np.float32)
+    lo = np.array([0, 20, 57])
+    blen = 7
+    mass[1, 20:27] = 10.0  # block masses are the largest, but excluded
+    idx = O.kv_topk(mass, lo, blen, k)
+    for b in range(B):
+        cand = np.array([p for p in range(S) if not (lo[b] <= p < lo[b] + blen)])
+        order = np.lexsort((cand, -mass[b, cand].astype(np.float64)))
+        np.testing.assert_array_equal(idx[b], cand[order[:k]])
+
+
+def test_topk_ties_take_lower_position_and_permutation_equivariance():
+    mass = np.zeros((1, 10), np.float32)
+    mass[0, [2, 5, 7]] = 0.5
+    idx = O.kv_topk(mass, np.array([9]), 1, 4)
+    np.testing.assert_array_equal(idx[0], [2, 5, 7, 0])
+    r = _rng(12)
+    m = r.random((1, 40)).astype(np.float32)
+    perm = r.permutation(40)
+    a = O.kv_topk(m, np.array([40]), 0, 5)[0]
+    b = O.kv_topk(m[:, perm], np.array([40]), 0, 5)[0]
+    inv = np.argsort(perm)
+    np.testing.assert_array_equal(np.sort(perm[b]), np.sort(a))
+    assert set(inv[a]) == set(b)
+
+
+def test_drift_is_one_when_probe_equals_cached_token():
+    wl = W.make(3, batch=2, d_model=256, head_dim=128, max_pos=96, gen_lo=48, block=16, drift_k=5)
+    s = wl.shape
+    cache = O.OracleCache(s.batch, s.max_pos, 0, s.n_heads, s.head_dim)
+    O.write_rows(cache, wl.w, wl.pre_x, wl.pre_pos, s.rope_theta)
+    idx = O.kv_topk(wl.mass, wl.block_lo, wl.block_len, 5)
+    xp = np.stack([np.stack([wl.prefill_row(b, int(p)) for p in idx[b]]) for b in range(s.batch)])
+    _, probe = O.step(cache, wl.w, s.rope_theta, wl.x[:, :0], wl.positions[:, :0], kv_x=xp, kv_pos=idx, probe=True)
+    cos = O.kv_drift(cache, idx, probe)
+    np.testing.assert_allclose(cos, 1.0, rtol=0, atol=1e-12)
+    # noisy probes drift below one
+    _, probe2 = O.step(cache, wl.w, s.rope_theta, wl.x[:, :0], wl.positions[:, :0],
+                       kv_x=wl.probe_rows(idx), kv_pos=idx, probe=True)
+    c2 = O.kv_drift(cache, idx, probe2)
+    assert np.all(c2 < 1.0) and np.all(c2 > 0.9)
+
+
+# ------------------------------------------------------------------------------ FP8
+def test_e4m3_named_values():
+    for code, val in GOLD["e4m3_named_values"]["codes"].items():
+        assert O.e4m3_decode(int(code, 16)) == val
+
+
+def test_e4m3_table_matches_library_cast():
+    torch = pytest.importorskip("torch")
+    codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+    lib = codes.view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    tab = O.e4m3_table()
+    nan = np.isnan(tab)
+    np.testing.assert_array_equal(nan, np.isnan(lib))
+    np.testing.assert_array_equal(tab[~nan], lib[~nan])
+
+
+def test_e4m3_quantize_matches_library_rounding_in_range():
+    torch = pytest.importorskip("torch")
+    r = _rng(13)
+    y = np.concatenate([r.standard_normal(20000) * s for s in (1e-3, 0.05, 1, 30, 200)])
+    y = y[np.abs(y) <= 448]
+    # exact midpoints between neighbouring codes decide the tie rule (to even)
+    tab = np.unique(O.e4m3_table()[np.isfinite(O.e4m3_table())])
+    y = np.concatenate([y, 0.5 * (tab[1:] + tab[:-1])])
+    lib = torch.from_numpy(y).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    np.testing.assert_array_equal(O.e4m3_quantize(y), lib)
+
+
+def test_e4m3_saturation_roundtrip_and_error_bound():
+    np.testing.assert_array_equal(O.e4m3_quantize(np.array([500.0, 1e6, -1000.0, 464.0])), [448, 448, -448, 448])
+    tab = O.e4m3_table()
+    fin = tab[np.isfinite(tab)]
+    np.testing.assert_array_equal(O.e4m3_quantize(fin), fin)
+    y = _rng(14).uniform(-448, 448, 100000)
+    err = np.abs(O.e4m3_quantize(y) - y)
+    normal = np.abs(y) >= 2 ** -6
+    assert np.all(err[normal] <= 2 ** -4 * np.abs(y[normal]) + 1e-300)
+    assert np.all(err[~normal] <= 2 ** -10)
+
+
+def test_fp8_group_quantize_scale_and_zero_group():
+    v = _rng(15).standard_normal(128)
+    deq, scale = O.fp8_group_quantize(v)
+    amax = np.max(np.abs(v))
+    assert scale == amax / 448.0
+    i = np.argmax(np.abs(v))
+    assert abs(deq[i] - v[i]) <= 1e-12 * amax
+    assert np.max(np.abs(deq - v)) <= 2 ** -4 * amax
+    z, s0 = O.fp8_group_quantize(np.zeros(128))
+    assert s0 == 1.0 and not np.any(z)
