@@ -1,0 +1,378 @@
+#!/usr/bin/env python
+"""Throughput of one cached-attention denoising step of a LLaDA-8B attention layer.
+
+One step (the timed unit) on the batch-32 workload: top-32 selection of the previous
+step's most-attended positions, the fused QKV projection + rotary embedding + cache
+write of the 32-token active block of every sequence plus the K/V of the 32 tracked
+tokens (probes), bidirectional attention of the block over the 1024-slot cache, and
+the K/V cosine-drift reduction with its refresh flag.  Inputs are seeded synthetic
+arrays from ``workloads``; the cache (512 MiB) and the weights are resident in HBM.
+
+Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 oracle instead,
+on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "layer-steps/s & fraction of roofline (TC % / HBM GB/s), LLaDA-8B layer, bs 1-32"
+UNIT = "layer-steps/s"
+L2_BYTES = 126 * 2 ** 20
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=30)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=3, choices=[2, 3])
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
+    return ap.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        d = json.load(open(path))
+        return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
+                "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
+    return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}
+
+
+# ----------------------------------------------------------------------------- clocks
+class Clocks:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+        try:
+            self.p = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
+                                       "--format=csv,noheader,nounits", "-lms", "200"],
+                                      stdout=self.f, stderr=subprocess.DEVNULL)
+        except OSError:
+            self.p = None
+
+    def stop(self):
+        if self.p is None:
+            return None
+        self.p.terminate()
+        try:
+            self.p.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.p.kill()
+        rows = []
+        for line in open(self.f.name):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 9:
+                rows.append(parts)
+        os.unlink(self.f.name)
+        if not rows:
+            return None
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
+        reasons = set()
+        for r in rows:
+            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), r[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------- workload
+def algorithmic(wl):
+    """FLOPs of the projection and bytes of the attention, counting each tensor once."""
+    s = wl.shape
+    B, D, H, hd, S = s.batch, s.D, s.n_heads, s.head_dim, s.max_pos
+    n_tok = wl.x.shape[1]
+    k = wl.drift_k
+    proj_flops = 2.0 * B * n_tok * 3 * D * D + 2.0 * B * k * 2 * D * D
+    proj_bytes = 3 * D * D * 2 + B * (n_tok + k) * D * 2 + B * n_tok * 3 * D * 2 + B * k * 2 * D * 2
+    attn_bytes = B * H * S * hd * 2 * 2 + 2 * B * n_tok * D * 2
+    attn_flops = 4.0 * B * H * n_tok * S * hd
+    drift_bytes = B * k * 2 * D * 2 * 2
+    return dict(proj_flops=proj_flops, proj_bytes=proj_bytes, attn_bytes=attn_bytes, attn_flops=attn_flops,
+                drift_bytes=drift_bytes)
+
+
+def run_ours(args, rank, world, local):
+    import torch
+    import workloads as W
+    from denoising_step_attention_qkv_b300 import capi
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    wl = _with_drift_inputs(W.make(args.config))
+    s = wl.shape
+    B, D, S = s.batch, s.D, s.max_pos
+    k = wl.drift_k
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).to(dev)
+
+    cache = capi.Cache(1, B, S, s.n_heads, s.head_dim, capi.DLLM_BF16, s.rope_theta, 0, device=dev)
+    w = bf(wl.w)
+    capi.dllm_cache_step(cache.handle, 0, None, w, None, None, None, kv_x=bf(wl.pre_x),
+                         kv_positions=torch.from_numpy(wl.pre_pos).to(dev))
+    x = bf(wl.x)
+    pos = torch.from_numpy(wl.positions).to(dev)
+    out = torch.empty_like(x)
+    mass = torch.from_numpy(wl.mass).to(dev)
+    block_lo = torch.from_numpy(wl.block_lo).to(dev)
+    idx = torch.empty((B, k), dtype=torch.int32, device=dev)
+    probe = torch.empty((B, k, 2, D), dtype=torch.bfloat16, device=dev)
+    cos = torch.empty((B, k, 2), dtype=torch.float32, device=dev)
+    refresh = torch.empty(B, dtype=torch.int32, device=dev)
+    capi.dllm_kv_topk(mass, block_lo, wl.block_len, k, idx)
+    x_probe = bf(wl.probe_rows(idx.cpu().numpy()))  # hidden states of the tracked tokens
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        capi.dllm_kv_topk(mass, block_lo, wl.block_len, k, idx, stream)
+        ev[1].record(stream)
+        capi.dllm_cache_project(cache.handle, 0, x, w, pos, None, out, kv_x=x_probe, kv_positions=idx,
+                                probe_kv=probe, stream=stream)
+        ev[2].record(stream)
+        capi.dllm_cache_attend(cache.handle, 0, pos, None, out, stream=stream)
+        ev[3].record(stream)
+        capi.dllm_kv_drift(cache.handle, 0, idx, probe, wl.gamma, cos, refresh, stream=stream)
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    for _ in range(max(args.warmup, 3)):
+        ev[0].record(stream)
+        step()
+        ev[4].record(stream)
+    torch.cuda.synchronize(dev)
+    rc, bits = cache.status()
+    if rc != capi.DLLM_OK:
+        raise RuntimeError(f"device status {bits:#x} after warm-up")
+
+    # ---- timed region: K steps, L2 flushed between steps (outside the events)
+    per = {"step": [], "topk": [], "project": [], "attend": [], "drift": []}
+    clocks = Clocks(local) if rank == 0 else None
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(dev)
+    evs = []
+    t_wall = time.perf_counter()
+    for _ in range(args.steps):
+        flush.zero_()
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        ev[0].record(stream)
+        step()
+        ev[4].record(stream)
+        evs.append(ev)
+    torch.cuda.synchronize(dev)
+    t_wall = time.perf_counter() - t_wall
+    if world > 1:
+        torch.distributed.barrier()
+    clk = clocks.stop() if clocks else None
+    for ev in evs:
+        per["step"].append(ev[0].elapsed_time(ev[4]))
+        per["topk"].append(ev[0].elapsed_time(ev[1]))
+        per["project"].append(ev[1].elapsed_time(ev[2]))
+        per["attend"].append(ev[2].elapsed_time(ev[3]))
+        per["drift"].append(ev[3].elapsed_time(ev[4]))
+    total_ms = sum(per["step"])
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * args.steps / (total_ms / 1e3)
+
+    # ---- end to end through the C ABI with host buffers (copies inside the timed region)
+    e2e = None
+    if not args.no_e2e:
+        h_x = x.cpu().pin_memory()
+        h_probe = x_probe.cpu().pin_memory()
+        h_pos = pos.cpu().pin_memory()
+        h_mass = mass.cpu().pin_memory()
+        h_lo = block_lo.cpu().pin_memory()
+        h_out = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+        h_cos = torch.empty(cos.shape, dtype=cos.dtype, pin_memory=True)
+        h_ref = torch.empty(refresh.shape, dtype=refresh.dtype, pin_memory=True)
+        ins = [(x, h_x), (x_probe, h_probe), (pos, h_pos), (mass, h_mass), (block_lo, h_lo)]
+        outs = [(h_out, out), (h_cos, cos), (h_ref, refresh)]
+        h2d = sum(h.numel() * h.element_size() for _, h in ins)
+        d2h = sum(h.numel() * h.element_size() for h, _ in outs)
+
+        def e2e_step():
+            for d_, h_ in ins:
+                d_.copy_(h_, non_blocking=True)
+            step()
+            for h_, d_ in outs:
+                h_.copy_(d_, non_blocking=True)
+
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize(dev)
+        ts = []
+        for _ in range(args.steps):
+            flush.zero_()
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+            e0 = torch.cuda.Event(enable_timing=True)
+            e1 = torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            e2e_step()
+            e1.record(stream)
+            e1.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        e2e_ms = sum(ts)
+        if world > 1:
+            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+            e2e_ms = float(t.item())
+        e2e = {"value": world * args.steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h}
+
+    rc, bits = cache.status()
+    if rc != capi.DLLM_OK:
+        raise RuntimeError(f"device status {bits:#x}")
+
+    alg = algorithmic(wl)
+    pk = peaks()
+    mean = {kname: statistics.mean(v) for kname, v in per.items()}
+    proj_tflops = alg["proj_flops"] / (mean["project"] * 1e-3) / 1e12
+    attn_gbs = alg["attn_bytes"] / (mean["attend"] * 1e-3) / 1e9
+    kernels = {
+        "project": {"ms": mean["project"], "bound": "tensor", "achieved": proj_tflops, "unit": "TFLOP/s",
+                    "peak": pk["bf16_tflops"], "frac": proj_tflops / pk["bf16_tflops"],
+                    "algorithmic_flops": alg["proj_flops"]},
+        "attend": {"ms": mean["attend"], "bound": "hbm", "achieved": attn_gbs, "unit": "GB/s",
+                   "peak": pk["hbm_gbs"], "frac": attn_gbs / pk["hbm_gbs"], "algorithmic_bytes": alg["attn_bytes"]},
+        "topk": {"ms": mean["topk"]},
+        "drift": {"ms": mean["drift"], "achieved_gbs": alg["drift_bytes"] / (mean["drift"] * 1e-3) / 1e9},
+    }
+    dom = "project" if mean["project"] >= mean["attend"] else "attend"
+    kd = kernels[dom]
+    roofline = {"kernel": dom, "bound": kd["bound"], "achieved": kd["achieved"], "peak": kd["peak"],
+                "unit": kd["unit"], "frac": kd["frac"], "traffic": None,
+                "peak_source": pk["source"] + (" burst" if kd["bound"] == "tensor" else "")}
+    n_launch_per_step = 5 + (1 if B * s.n_heads < torch.cuda.get_device_properties(dev).multi_processor_count else 0)
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "batch": B, "d_model": D, "n_heads": s.n_heads, "head_dim": s.head_dim,
+                   "cache_positions": S, "block": wl.block_len, "tracked_topk": k, "rope_theta": s.rope_theta,
+                   "l2": "flushed between steps (256 MiB write)", "parallelism": f"replicas x{world}"},
+        "tokens_per_s": value * B * wl.block_len,
+        "roofline": roofline, "kernels": kernels, "e2e": e2e, "clocks": clk,
+        "gpu_launches": n_launch_per_step * args.steps, "wall_s_timed": t_wall,
+    }
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return line, wl
+
+
+# --------------------------------------------------------------------- CPU (oracle)
+class OracleSample:
+    """The fp64 oracle on sequence 0 of the workload: the cache of that sequence is
+    filled once (untimed state before the step); ``rep()`` runs and times the whole
+    step for it (top-k, probe projection, block projection + attention, drift)."""
+
+    def __init__(self, wl):
+        import oracle as O
+        self.O, self.wl = O, wl
+        s = wl.shape
+        self.one = lambda a: None if a is None else a[0:1]  # noqa: E731
+        self.cache = O.OracleCache(1, s.max_pos, 0, s.n_heads, s.head_dim)
+        O.write_rows(self.cache, wl.w, self.one(wl.pre_x), self.one(wl.pre_pos), s.rope_theta)
+        try:
+            from threadpoolctl import threadpool_info
+            self.cores = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
+        except Exception:
+            self.cores = os.cpu_count()
+
+    def rep(self) -> float:
+        O, wl, one, s = self.O, self.wl, self.one, self.wl.shape
+        t0 = time.perf_counter()
+        idx = O.kv_topk(one(wl.mass), one(wl.block_lo), wl.block_len, wl.drift_k)
+        xp = wl.probe_rows(idx)
+        _, probe = O.step(self.cache, wl.w, s.rope_theta, one(wl.x)[:, :0], one(wl.positions)[:, :0], kv_x=xp,
+                          kv_pos=idx, probe=True)
+        O.step(self.cache, wl.w, s.rope_theta, one(wl.x), one(wl.positions))
+        cos = O.kv_drift(self.cache, idx, probe)
+        _ = cos.min() < wl.gamma
+        return time.perf_counter() - t0
+
+
+def _with_drift_inputs(wl):
+    if wl.mass is None:  # batch-1 shape: track 32 positions under a uniform mass
+        wl.mass = np.full((wl.shape.batch, wl.shape.max_pos), 1.0 / wl.shape.max_pos, np.float32)
+        wl.drift_k = 32
+    return wl
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        import workloads as W
+        wl = _with_drift_inputs(W.make(args.config))
+        sample = OracleSample(wl)
+        for _ in range(args.warmup):
+            sample.rep()
+        per_seq = [sample.rep() for _ in range(args.steps)]
+        total = sum(per_seq) * wl.shape.batch  # a layer-step covers the whole batch
+        value = args.steps / total
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+                "data": "synthetic", "config": {"workload": wl.name, "batch": wl.shape.batch},
+                "cpu_baseline": {"value": value, "unit": UNIT, "cores": sample.cores, "kind": "oracle",
+                                 "sample": "each step: the whole step for sequence 0 of the batch (top-k, probe "
+                                           "and block projection, attention, drift); time x batch size"},
+                "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
+
+    line, wl = run_ours(args, rank, world, local)
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        sample = OracleSample(wl)
+        reps = []
+        while sum(reps) < args.cpu_seconds or len(reps) < 2:
+            reps.append(sample.rep())
+        sec = statistics.mean(reps) * wl.shape.batch
+        line["cpu_baseline"] = {"value": 1.0 / sec, "unit": UNIT, "cores": sample.cores, "kind": "oracle",
+                                "sample": f"{len(reps)} repetitions of the whole step for sequence 0 of "
+                                          f"{wl.shape.batch} (top-k, probe and block projection, attention, "
+                                          f"drift); time x batch size"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

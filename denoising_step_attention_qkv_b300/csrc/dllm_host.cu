@@ -1,0 +1,456 @@
+// Host side of the C ABI: argument checks, the flat cache allocator, the rotary
+// table, TMA descriptors, tile/split selection and kernel launches.
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "internal.h"
+
+using namespace dllm;
+
+namespace {
+
+int from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return DLLM_OK;
+  if (e == cudaErrorMemoryAllocation) return DLLM_EOOM;
+  return DLLM_ECUDA;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int elem_bytes_of(int kv_dtype) { return kv_dtype == DLLM_F32 ? 4 : (kv_dtype == DLLM_BF16 ? 2 : 1); }
+
+// Shape checks shared by dllm_cache_bytes and dllm_cache_alloc.
+int check_desc(const dllm_cache_desc* d) {
+  if (!d) return DLLM_EINVAL;
+  if (d->n_layers < 1 || d->batch < 1 || d->max_pos < 1 || d->tail_slots < 0 || d->n_heads < 1 || d->head_dim < 2)
+    return DLLM_EINVAL;
+  if (d->kv_dtype != DLLM_F32 && d->kv_dtype != DLLM_BF16 && d->kv_dtype != DLLM_E4M3) return DLLM_EINVAL;
+  if (!(d->rope_theta > 0.0) || !std::isfinite(d->rope_theta)) return DLLM_EINVAL;
+  if ((long long)d->max_pos + d->tail_slots > (1 << 24)) return DLLM_EINVAL;
+  if ((long long)d->n_heads * d->head_dim > 65536) return DLLM_EINVAL;
+  if (d->kv_dtype == DLLM_F32) {
+    if (d->head_dim % 4 != 0 || d->head_dim > 256) return DLLM_EUNSUPPORTED;
+  } else {
+    if (d->head_dim != kHd) return DLLM_EUNSUPPORTED;
+  }
+  return DLLM_OK;
+}
+
+size_t kv_bytes_of(const dllm_cache_desc* d) {
+  return (size_t)d->n_layers * d->batch * (size_t)(d->max_pos + d->tail_slots) * 2 * d->n_heads * d->head_dim *
+         elem_bytes_of(d->kv_dtype);
+}
+size_t scale_bytes_of(const dllm_cache_desc* d) {
+  if (d->kv_dtype != DLLM_E4M3) return 0;
+  return (size_t)d->n_layers * d->batch * (size_t)(d->max_pos + d->tail_slots) * 2 * d->n_heads * sizeof(float);
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// 2-D tile map over a row-major [rows][cols] bf16 matrix with 128-byte swizzle.
+bool map_2d_bf16(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, uint32_t box_cols, uint32_t box_rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {cols, rows};
+  cuuint64_t strides[1] = {cols * 2};
+  cuuint32_t box[2] = {box_cols, box_rows};
+  cuuint32_t es[2] = {1, 1};
+  return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, es,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// 3-D tile map over one layer of the cache viewed as [B*slots][2H][hd].
+bool map_cache(CUtensorMap* m, const void* layer, int kv_dtype, int hd, int H, uint64_t rows) {
+  auto enc = encode_fn();
+  if (!enc) return false;
+  const uint32_t eb = kv_dtype == DLLM_E4M3 ? 1 : 2;
+  cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)(2 * H), rows};
+  cuuint64_t strides[2] = {(cuuint64_t)hd * eb, (cuuint64_t)2 * H * hd * eb};
+  cuuint32_t box[3] = {128u / eb, 1, (cuuint32_t)kKeyTile};
+  cuuint32_t es[3] = {1, 1, 1};
+  const CUtensorMapDataType dt = kv_dtype == DLLM_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+  return enc(m, dt, 3, const_cast<void*>(layer), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
+             CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+}  // namespace
+
+extern "C" {
+
+size_t dllm_cache_bytes(const dllm_cache_desc* desc) {
+  if (check_desc(desc) != DLLM_OK) return 0;
+  return kv_bytes_of(desc) + scale_bytes_of(desc);
+}
+
+int dllm_cache_alloc(const dllm_cache_desc* desc, dllm_cache** out) {
+  if (!out) return DLLM_EINVAL;
+  *out = nullptr;
+  int rc = check_desc(desc);
+  if (rc != DLLM_OK) return rc;
+  const size_t kvb = kv_bytes_of(desc), scb = scale_bytes_of(desc);
+  if (desc->external_buf) {
+    if (desc->external_bytes < kvb + scb) return DLLM_EINVAL;
+    if (reinterpret_cast<uintptr_t>(desc->external_buf) & 255u) return DLLM_EINVAL;
+  }
+  dllm_cache* c = new (std::nothrow) dllm_cache();
+  if (!c) return DLLM_EOOM;
+  c->desc = *desc;
+  c->slots = desc->max_pos + desc->tail_slots;
+  c->elem_bytes = elem_bytes_of(desc->kv_dtype);
+  c->kv_bytes = kvb;
+  c->scale_bytes = scb;
+  c->layer_elems = (size_t)desc->batch * c->slots * 2 * desc->n_heads * desc->head_dim;
+  c->layer_scales = desc->kv_dtype == DLLM_E4M3 ? (size_t)desc->batch * c->slots * 2 * desc->n_heads : 0;
+
+  auto fail = [&](int code) {
+    dllm_cache_free(c);
+    return code;
+  };
+  cudaError_t e = cudaGetDevice(&c->device);
+  if (e != cudaSuccess) return fail(from_cuda(e));
+  e = cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device);
+  if (e != cudaSuccess) return fail(from_cuda(e));
+
+  if (desc->external_buf) {
+    c->kv = desc->external_buf;
+    c->owns_kv = false;
+  } else {
+    e = cudaMalloc(&c->kv, kvb + scb);
+    if (e != cudaSuccess) return fail(from_cuda(e));
+    c->owns_kv = true;
+  }
+  c->scale = scb ? reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(c->kv) + kvb) : nullptr;
+
+  // rotary table: angle p * theta^(-2i/hd) in fp64, cos/sin rounded to fp32
+  const int half = desc->head_dim / 2;
+  std::vector<float2> tab((size_t)desc->max_pos * half);
+  for (int p = 0; p < desc->max_pos; ++p)
+    for (int i = 0; i < half; ++i) {
+      const double a = (double)p * std::pow(desc->rope_theta, -2.0 * i / desc->head_dim);
+      tab[(size_t)p * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+    }
+  e = cudaMalloc(&c->rope, tab.size() * sizeof(float2));
+  if (e != cudaSuccess) return fail(from_cuda(e));
+  e = cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return fail(from_cuda(e));
+
+  e = cudaMalloc(&c->status, sizeof(int));
+  if (e != cudaSuccess) return fail(from_cuda(e));
+  e = cudaMemset(c->status, 0, sizeof(int));
+  if (e != cudaSuccess) return fail(from_cuda(e));
+
+  // split-KV partials: at most 2 * (2 * SMs) units of kQChunk rows
+  if (desc->kv_dtype != DLLM_F32) {
+    c->ws_floats = (size_t)4 * c->sm_count * kQChunk * (kHd + 2);
+    e = cudaMalloc(&c->ws, c->ws_floats * sizeof(float));
+    if (e != cudaSuccess) return fail(from_cuda(e));
+  }
+  *out = c;
+  return DLLM_OK;
+}
+
+int dllm_cache_free(dllm_cache* c) {
+  if (!c) return DLLM_OK;
+  cudaDeviceSynchronize();
+  if (c->owns_kv && c->kv) cudaFree(c->kv);
+  if (c->rope) cudaFree(c->rope);
+  if (c->status) cudaFree(c->status);
+  if (c->ws) cudaFree(c->ws);
+  delete c;
+  return DLLM_OK;
+}
+
+int dllm_cache_get_layout(const dllm_cache* c, dllm_cache_layout* out) {
+  if (!c || !out) return DLLM_EINVAL;
+  out->kv = c->kv;
+  out->scale = c->scale;
+  out->kv_bytes = c->kv_bytes;
+  out->scale_bytes = c->scale_bytes;
+  out->layer_elems = c->layer_elems;
+  out->slots = c->slots;
+  out->elem_bytes = c->elem_bytes;
+  return DLLM_OK;
+}
+
+}  // extern "C"
+
+namespace {
+
+struct StepArgs {
+  int layer;
+  const void* x;
+  const void* w_qkv;
+  const int32_t* positions;
+  const uint8_t* view;
+  int n_tok;
+  void* out;
+  const void* kv_x;
+  const int32_t* kv_positions;
+  int n_kv;
+  void* probe_kv;
+  cudaStream_t s;
+};
+
+void* layer_kv(dllm_cache* c, int layer) {
+  return reinterpret_cast<uint8_t*>(c->kv) + (size_t)layer * c->layer_elems * c->elem_bytes;
+}
+float* layer_scale(dllm_cache* c, int layer) {
+  return c->scale ? c->scale + (size_t)layer * c->layer_scales : nullptr;
+}
+
+int check_common(dllm_cache* c, int layer, int n_tok, const int32_t* positions, void* out) {
+  if (!c || layer < 0 || layer >= c->desc.n_layers || n_tok < 0) return DLLM_EINVAL;
+  if (n_tok > 0 && (!positions || !out)) return DLLM_EINVAL;
+  if (!aligned16(out)) return DLLM_EINVAL;
+  if ((long long)c->desc.batch * n_tok > (1ll << 30)) return DLLM_EINVAL;
+  return DLLM_OK;
+}
+
+int check_project(dllm_cache* c, const StepArgs& a) {
+  int rc = check_common(c, a.layer, a.n_tok, a.positions, a.out);
+  if (rc) return rc;
+  if (a.n_kv < 0 || !a.w_qkv) return DLLM_EINVAL;
+  if (a.n_tok > 0 && !a.x) return DLLM_EINVAL;
+  if (a.n_kv > 0 && (!a.kv_x || !a.kv_positions)) return DLLM_EINVAL;
+  if (!aligned16(a.x) || !aligned16(a.w_qkv) || !aligned16(a.kv_x) || !aligned16(a.probe_kv)) return DLLM_EINVAL;
+  if (a.n_tok > 0 && a.x == a.out) return DLLM_EINVAL;
+  if ((long long)c->desc.batch * a.n_kv > (1ll << 30)) return DLLM_EINVAL;
+  if (c->desc.kv_dtype != DLLM_F32 && (c->desc.n_heads * c->desc.head_dim) % kHd != 0) return DLLM_EUNSUPPORTED;
+  return DLLM_OK;
+}
+
+int check_attend(dllm_cache* c, int layer, int n_tok, const int32_t* positions, const uint8_t* view, void* out) {
+  int rc = check_common(c, layer, n_tok, positions, out);
+  if (rc) return rc;
+  const dllm_cache_desc& d = c->desc;
+  if (view && d.max_pos > 32 * 512) return DLLM_EUNSUPPORTED;
+  if (d.kv_dtype == DLLM_F32 && (size_t)(d.max_pos + d.tail_slots + d.head_dim + 32) * 4 > 200 * 1024)
+    return DLLM_EUNSUPPORTED;
+  if (d.kv_dtype == DLLM_E4M3) return DLLM_EUNSUPPORTED;  // FP8 attention: not yet built
+  return DLLM_OK;
+}
+
+ProjParams make_proj(dllm_cache* c, const StepArgs& a) {
+  const dllm_cache_desc& d = c->desc;
+  ProjParams p{};
+  p.D = d.n_heads * d.head_dim;
+  p.H = d.n_heads;
+  p.n_tok = a.n_tok;
+  p.n_kv = a.n_kv;
+  p.m_q = d.batch * a.n_tok;
+  p.m_kv = d.batch * a.n_kv;
+  p.positions = a.positions;
+  p.view = a.view;
+  p.kv_positions = a.kv_positions;
+  p.q_out = a.out;
+  p.cache_kv = layer_kv(c, a.layer);
+  p.cache_scale = layer_scale(c, a.layer);
+  p.probe = a.probe_kv;
+  p.kv_dtype = d.kv_dtype;
+  p.max_pos = d.max_pos;
+  p.tail = d.tail_slots;
+  p.slots = c->slots;
+  p.rope = c->rope;
+  p.status = c->status;
+  return p;
+}
+
+int do_project(dllm_cache* c, const StepArgs& a) {
+  if (a.n_tok == 0 && a.n_kv == 0) return DLLM_OK;
+  const dllm_cache_desc& d = c->desc;
+  ProjParams p = make_proj(c, a);
+  const int D = p.D;
+  int rc;
+  if (d.kv_dtype == DLLM_F32) {
+    rc = launch_proj_f32(p, (const float*)a.x, (const float*)a.kv_x, (const float*)a.w_qkv, d.head_dim, a.s);
+    return rc ? from_cuda((cudaError_t)rc) : DLLM_OK;
+  }
+  int bn = (D % 256 == 0) ? 256 : 128;
+  auto tiles_for = [&](int bnv) {
+    return (long long)ceil_div(p.m_q, 128) * (3 * D / bnv) + (long long)ceil_div(p.m_kv, 128) * (2 * D / bnv);
+  };
+  if (bn == 256 && tiles_for(256) < c->sm_count) bn = 128;
+  p.mt_q = ceil_div(p.m_q, 128);
+  p.mt_kv = ceil_div(p.m_kv, 128);
+  p.nt_q = 3 * D / bn;
+  p.nt_kv = 2 * D / bn;
+  p.tiles_q = p.mt_q * p.nt_q;
+  p.tiles_total = p.tiles_q + p.mt_kv * p.nt_kv;
+  p.k_blocks = D / 64;
+  p.m_fastest = ((size_t)(p.m_q + p.m_kv) * D * 2 <= ((size_t)48 << 20)) ? 1 : 0;
+
+  CUtensorMap tm_w, tm_x, tm_xkv;
+  if (!map_2d_bf16(&tm_w, a.w_qkv, D, 3 * (uint64_t)D, 64, bn)) return DLLM_ECUDA;
+  if (p.m_q > 0) {
+    if (!map_2d_bf16(&tm_x, a.x, D, p.m_q, 64, 128)) return DLLM_ECUDA;
+  } else {
+    tm_x = tm_w;
+  }
+  if (p.m_kv > 0) {
+    if (!map_2d_bf16(&tm_xkv, a.kv_x, D, p.m_kv, 64, 128)) return DLLM_ECUDA;
+  } else {
+    tm_xkv = tm_w;
+  }
+  const int grid = p.tiles_total < c->sm_count ? p.tiles_total : c->sm_count;
+  rc = launch_proj_tc(p, tm_x, tm_xkv, tm_w, bn, grid, a.s);
+  return rc ? from_cuda((cudaError_t)rc) : DLLM_OK;
+}
+
+int do_attend(dllm_cache* c, int layer, const int32_t* positions, const uint8_t* view, int n_tok, void* out,
+              cudaStream_t s) {
+  if (n_tok == 0) return DLLM_OK;
+  const dllm_cache_desc& d = c->desc;
+  const int B = d.batch, H = d.n_heads, hd = d.head_dim, D = H * hd;
+  AttnParams a{};
+  a.B = B;
+  a.H = H;
+  a.D = D;
+  a.n_tok = n_tok;
+  a.max_pos = d.max_pos;
+  a.tail = d.tail_slots;
+  a.slots = c->slots;
+  a.view = view;
+  a.positions = positions;
+  a.out = out;
+  a.ws = c->ws;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)hd));
+  a.kv_scale = layer_scale(c, layer);
+  a.kv_dtype = d.kv_dtype;
+  a.status = c->status;
+  int rc;
+  if (d.kv_dtype == DLLM_F32) {
+    rc = launch_attn_f32(a, (const float*)layer_kv(c, layer), hd, s);
+    return rc ? from_cuda((cudaError_t)rc) : DLLM_OK;
+  }
+  a.nq_pad = n_tok <= 32 ? 32 : 64;
+  a.n_qchunks = ceil_div(n_tok, kQChunk);
+  a.key_tiles = ceil_div(d.max_pos + (view ? d.tail_slots : 0), kKeyTile);
+  const int base = B * H * a.n_qchunks;
+  int splits = 1;
+  if (base < c->sm_count) {
+    splits = ceil_div(c->sm_count, base);
+    if (splits > a.key_tiles) splits = a.key_tiles;
+  }
+  a.tiles_per_split = ceil_div(a.key_tiles, splits);
+  a.n_splits = ceil_div(a.key_tiles, a.tiles_per_split);
+  a.units = base * a.n_splits;
+  if (a.n_splits > 1 && (size_t)a.units * kQChunk * (kHd + 2) > c->ws_floats) return DLLM_EUNSUPPORTED;
+
+  CUtensorMap tm_q, tm_kv;
+  if (!map_2d_bf16(&tm_q, out, D, (uint64_t)B * n_tok, 64, a.nq_pad)) return DLLM_ECUDA;
+  if (!map_cache(&tm_kv, layer_kv(c, layer), d.kv_dtype, hd, H, (uint64_t)B * c->slots)) return DLLM_ECUDA;
+  const int grid = a.units < c->sm_count ? a.units : c->sm_count;
+  rc = launch_attn_tc(a, tm_q, tm_kv, grid, s);
+  if (rc) return from_cuda((cudaError_t)rc);
+  if (a.n_splits > 1) {
+    rc = launch_attn_combine(a, s);
+    if (rc) return from_cuda((cudaError_t)rc);
+  }
+  return DLLM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int dllm_cache_project(dllm_cache* c, int layer, const void* x, const void* w_qkv, const int32_t* positions,
+                       const uint8_t* view, int n_tok, void* out, const void* kv_x, const int32_t* kv_positions,
+                       int n_kv, void* probe_kv, void* stream) {
+  StepArgs a{layer, x, w_qkv, positions, view, n_tok, out, kv_x, kv_positions, n_kv, probe_kv,
+             reinterpret_cast<cudaStream_t>(stream)};
+  int rc = check_project(c, a);
+  if (rc) return rc;
+  return do_project(c, a);
+}
+
+int dllm_cache_attend(dllm_cache* c, int layer, const int32_t* positions, const uint8_t* view, int n_tok, void* out,
+                      void* stream) {
+  int rc = check_attend(c, layer, n_tok, positions, view, out);
+  if (rc) return rc;
+  return do_attend(c, layer, positions, view, n_tok, out, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int dllm_cache_step(dllm_cache* c, int layer, const void* x, const void* w_qkv, const int32_t* positions,
+                    const uint8_t* view, int n_tok, void* out, const void* kv_x, const int32_t* kv_positions, int n_kv,
+                    void* probe_kv, void* stream) {
+  StepArgs a{layer, x, w_qkv, positions, view, n_tok, out, kv_x, kv_positions, n_kv, probe_kv,
+             reinterpret_cast<cudaStream_t>(stream)};
+  int rc = check_project(c, a);
+  if (rc) return rc;
+  if (n_tok > 0) {
+    rc = check_attend(c, layer, n_tok, positions, view, out);
+    if (rc) return rc;
+  }
+  rc = do_project(c, a);
+  if (rc) return rc;
+  return do_attend(c, layer, positions, view, n_tok, out, a.s);
+}
+
+int dllm_kv_topk(const float* mass, int batch, int n_pos, const int32_t* block_lo, int block_len, int k, int32_t* idx,
+                 void* stream) {
+  if (!mass || !block_lo || !idx || batch < 1 || n_pos < 1 || n_pos > 16384 || block_len < 0 || k < 1 ||
+      k > n_pos - block_len)
+    return DLLM_EINVAL;
+  return from_cuda((cudaError_t)launch_topk(mass, batch, n_pos, block_lo, block_len, k, idx,
+                                            reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dllm_kv_drift(const dllm_cache* c, int layer, const int32_t* idx, int k, const void* probe_kv, float gamma,
+                  float* cos, int32_t* refresh, void* stream) {
+  if (!c || layer < 0 || layer >= c->desc.n_layers || !idx || k < 1 || !probe_kv || !cos) return DLLM_EINVAL;
+  if (!aligned16(probe_kv)) return DLLM_EINVAL;
+  const dllm_cache_desc& d = c->desc;
+  const void* kvl = reinterpret_cast<const uint8_t*>(c->kv) + (size_t)layer * c->layer_elems * c->elem_bytes;
+  const float* scl = c->scale ? c->scale + (size_t)layer * c->layer_scales : nullptr;
+  return from_cuda((cudaError_t)launch_drift(kvl, scl, d.kv_dtype, d.batch, c->slots, d.max_pos, d.n_heads, d.head_dim,
+                                             idx, k, probe_kv, gamma, cos, refresh, c->status,
+                                             reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dllm_cache_status(dllm_cache* c, int* device_bits) {
+  if (!c) return DLLM_EINVAL;
+  cudaError_t e = cudaDeviceSynchronize();
+  if (e != cudaSuccess) return from_cuda(e);
+  int bits = 0;
+  e = cudaMemcpy(&bits, c->status, sizeof(int), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return from_cuda(e);
+  e = cudaMemset(c->status, 0, sizeof(int));
+  if (e != cudaSuccess) return from_cuda(e);
+  if (device_bits) *device_bits = bits;
+  return bits ? DLLM_EDEVICE : DLLM_OK;
+}
+
+const char* dllm_strerror(int s) {
+  switch (s) {
+    case DLLM_OK: return "ok";
+    case DLLM_EINVAL: return "invalid argument";
+    case DLLM_EOOM: return "out of device memory";
+    case DLLM_ECUDA: return "CUDA error";
+    case DLLM_EDEVICE: return "device-side range error or timeout (see status bits)";
+    case DLLM_EUNSUPPORTED: return "unsupported configuration";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

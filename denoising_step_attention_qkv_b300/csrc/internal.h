@@ -1,0 +1,98 @@
+// Host/device shared definitions of the library (not part of the public ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/dllm_cache.h"
+
+struct dllm_cache {
+  dllm_cache_desc desc;
+  int device;
+  int sm_count;
+  void* kv;
+  float* scale;
+  bool owns_kv;
+  size_t kv_bytes, scale_bytes;
+  size_t layer_elems;   // K/V elements per layer
+  size_t layer_scales;  // scales per layer (e4m3)
+  int slots;            // max_pos + tail_slots
+  int elem_bytes;
+  float2* rope;  // [max_pos][head_dim/2] (cos, sin), fp32 rounded from fp64
+  int* status;   // device status word
+  float* ws;     // split-KV partials
+  size_t ws_floats;
+};
+
+namespace dllm {
+
+constexpr int kHd = 128;         // head_dim of the tensor-core path
+constexpr int kQChunk = 64;      // query rows per attention work unit (tensor-core path)
+constexpr int kKeyTile = 128;    // keys per attention tile
+
+// ---------------------------------------------------------------- fused projection
+struct ProjParams {
+  int D, H;
+  int n_tok, n_kv;    // rows per sequence: query rows, K/V-only rows
+  int m_q, m_kv;      // total rows
+  int mt_q, mt_kv;    // 128-row tiles
+  int nt_q, nt_kv;    // column tiles per row tile (3D/BN, 2D/BN)
+  int tiles_q, tiles_total;
+  int k_blocks;       // D / 64
+  int m_fastest;      // tile raster: row tiles vary fastest
+  const int32_t* positions;
+  const uint8_t* view;
+  const int32_t* kv_positions;
+  void* q_out;        // act [m_q][D]
+  void* cache_kv;     // this layer: [B][slots][2][H][hd]
+  float* cache_scale; // this layer: [B][slots][2][H] (e4m3)
+  void* probe;        // act [m_kv][2][D] or null
+  int kv_dtype;
+  int max_pos, tail, slots;
+  const float2* rope;
+  int* status;
+};
+
+// ------------------------------------------------------------------------ attention
+struct AttnParams {
+  int B, H, D, n_tok;
+  int max_pos, tail, slots;
+  int nq_pad;        // query columns per unit (multiple of 16, <= kQChunk)
+  int n_qchunks;
+  int key_tiles;     // 128-key tiles covering the attended slot range
+  int n_splits, tiles_per_split;
+  int units;         // B * H * n_qchunks * n_splits
+  const uint8_t* view;
+  const int32_t* positions;
+  void* out;         // act [B][n_tok][D]: rotated Q in, attention output out
+  float* ws;         // split partials: [units][nq_pad][hd] O, then [units][nq_pad][2] (m, l)
+  float scale_log2;  // log2(e) / sqrt(hd)
+  const float* kv_scale;  // this layer, e4m3 only
+  int kv_dtype;
+  int* status;
+};
+
+// Launchers (return a cudaError_t cast to int, 0 on success).
+int launch_proj_tc(const ProjParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_xkv,
+                   const CUtensorMap& tm_w, int bn, int grid, cudaStream_t s);
+int launch_attn_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, int grid,
+                   cudaStream_t s);
+int launch_attn_combine(const AttnParams& p, cudaStream_t s);
+
+int launch_proj_f32(const ProjParams& p, const float* x, const float* xkv, const float* w, int hd,
+                    cudaStream_t s);
+int launch_attn_f32(const AttnParams& p, const float* kv_layer, int hd, cudaStream_t s);
+
+int launch_topk(const float* mass, int batch, int n_pos, const int32_t* block_lo, int block_len, int k,
+                int32_t* idx, cudaStream_t s);
+int launch_drift(const void* kv_layer, const float* scale_layer, int kv_dtype, int B, int slots, int max_pos,
+                 int H, int hd, const int32_t* idx, int k, const void* probe, float gamma, float* cos,
+                 int32_t* refresh, int* status, cudaStream_t s);
+
+size_t proj_tc_smem_bytes(int bn);
+size_t attn_tc_smem_bytes();
+
+}  // namespace dllm

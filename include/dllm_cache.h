@@ -1,0 +1,224 @@
+/*
+ * dllm_cache.h -- C ABI of the per-layer, per-denoising-step cached attention of a
+ * masked diffusion LLM, for NVIDIA B300 (sm_103a).
+ *
+ * One step of one layer (the pipeline of "Flash-dLLM: IO-aware KV caching and
+ * parallel decoding", paragraph 2: QKV projection -> rotary embedding -> cache write
+ * -> attention) runs as two kernels on the caller's stream:
+ *
+ *   1. a fused tcgen05/TMEM GEMM that projects the active rows, applies the rotary
+ *      embedding at their absolute positions and scatter-writes K/V straight into the
+ *      flat cache (the intermediates never round-trip through HBM);
+ *   2. bidirectional (non-causal) attention of the step's query rows over every
+ *      visible cache slot ("LaCache: Exact Caching and Precision-Adaptive Inference
+ *      for Diffusion Large Language Models", technical summary, Problem Statement).
+ *
+ * Conventions shared by every call:
+ *   - Every tensor argument is a DEVICE pointer owned by the caller, unless stated.
+ *     All tensors are dense row-major with the layout given beside them; base
+ *     addresses must be 16-byte aligned.
+ *   - D = n_heads * head_dim.  "act" is the activation type: fp32 for a DLLM_F32
+ *     cache, bf16 for DLLM_BF16 and DLLM_E4M3 caches.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream) and never synchronise, except dllm_cache_alloc/free/status.
+ *   - Every call returns a dllm_status.  Argument errors are detected on the host
+ *     before anything is launched and leave all buffers untouched.  Range errors in
+ *     device-resident index data (a position outside [0, max_pos), too many draft
+ *     rows for the tail, an unknown view tag) cannot be seen by the host: the kernel
+ *     skips the offending row and sets a bit in the cache's device status word, which
+ *     dllm_cache_status() returns.  A pipeline wait that exceeds its time limit
+ *     (about one second) also sets a bit there and ends the kernel cleanly instead of
+ *     hanging.
+ *   - Nothing here falls back to the CPU.  Without a usable sm_103a device every
+ *     call that launches work returns DLLM_ECUDA.
+ */
+#ifndef DLLM_CACHE_H
+#define DLLM_CACHE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DLLM_OK = 0,
+  DLLM_EINVAL = 1,       /* bad argument (shape, null pointer, alignment, dtype) */
+  DLLM_EOOM = 2,         /* device allocation failed */
+  DLLM_ECUDA = 3,        /* a CUDA runtime/driver call failed (no device, bad launch) */
+  DLLM_EDEVICE = 4,      /* dllm_cache_status only: the device status word is non-zero */
+  DLLM_EUNSUPPORTED = 5  /* valid but not supported by these kernels (e.g. head_dim) */
+} dllm_status;
+
+/* Bits of the device status word (see dllm_cache_status). */
+#define DLLM_DEV_BAD_POSITION 0x1 /* a row's position is outside [0, max_pos) */
+#define DLLM_DEV_BAD_VIEW 0x2     /* a view tag is not BASE/DRAFT/MASK */
+#define DLLM_DEV_TAIL_FULL 0x4    /* more DRAFT rows in a sequence than tail_slots */
+#define DLLM_DEV_TIMEOUT 0x8      /* a pipeline wait ran out of time; the kernel quit */
+#define DLLM_DEV_BAD_INDEX 0x10   /* a top-k / drift index is outside [0, max_pos) */
+
+/* Cache storage types. */
+#define DLLM_F32 0  /* fp32 K/V, fp32 activations (SIMT fp32 kernels) */
+#define DLLM_BF16 1 /* bf16 K/V, bf16 activations (tcgen05 kernels) */
+#define DLLM_E4M3 2 /* FP8-e4m3 K/V with one fp32 scale per (slot, K|V, head), bf16 activations */
+
+/* Row view tags for Flash-Verify ("Flash-dLLM ...", paragraph 3).  A BASE row is an
+ * ordinary block token.  A search-set token appears twice: as a MASK row (its own
+ * position/slot, filled with the mask embedding) and as a DRAFT row (same absolute
+ * position for the rotary embedding, but written to a tail slot).  Visibility: key j
+ * is visible to query q iff view(j) is SHARED (any slot not written by a MASK or DRAFT
+ * row of this step), or view(j) == view(q), or (view(q) == BASE and view(j) == MASK).
+ * The r-th DRAFT row of a sequence (in row order) writes tail slot max_pos + r. */
+#define DLLM_VIEW_BASE 0
+#define DLLM_VIEW_DRAFT 1
+#define DLLM_VIEW_MASK 2
+
+typedef struct dllm_cache dllm_cache; /* opaque; owns or wraps one flat K/V buffer */
+
+typedef struct {
+  int n_layers;      /* layers held by the cache (>= 1) */
+  int batch;         /* sequences B (>= 1) */
+  int max_pos;       /* regular slots per sequence = positions 0..max_pos-1 (>= 1) */
+  int tail_slots;    /* extra slots per sequence for Flash-Verify draft views (>= 0) */
+  int n_heads;       /* H (>= 1) */
+  int head_dim;      /* hd: 128 for DLLM_BF16/DLLM_E4M3; a multiple of 4, <= 256, for DLLM_F32 */
+  int kv_dtype;      /* DLLM_F32 | DLLM_BF16 | DLLM_E4M3 */
+  double rope_theta; /* rotary base (> 0), e.g. 10000 or 500000 */
+  void* external_buf;    /* optional caller device buffer of >= dllm_cache_bytes() bytes,
+                            256-byte aligned; NULL = the library allocates and owns it */
+  size_t external_bytes; /* size of external_buf */
+} dllm_cache_desc;
+
+/* Layout of the flat buffer, for callers that read or fill the cache directly.
+ *   kv:    [n_layers][batch][max_pos + tail_slots][2 (K,V)][n_heads][head_dim],
+ *          element type fp32 / bf16 / e4m3 per kv_dtype; K is stored after the
+ *          rotary embedding.
+ *   scale: (DLLM_E4M3 only, else NULL) fp32 [n_layers][batch][max_pos + tail_slots][2][n_heads];
+ *          the stored value of element i is e4m3(code_i) * scale.                    */
+typedef struct {
+  void* kv;
+  float* scale;
+  size_t kv_bytes;
+  size_t scale_bytes;
+  size_t layer_elems; /* elements of kv per layer */
+  int slots;          /* max_pos + tail_slots */
+  int elem_bytes;     /* 4, 2 or 1 */
+} dllm_cache_layout;
+
+/* Bytes of the flat K/V (+ scale) buffer that `desc` needs; 0 if `desc` is invalid.
+ * Host only, no CUDA call.  Flash-dLLM paragraph 5: one flat, preallocated cache. */
+size_t dllm_cache_bytes(const dllm_cache_desc* desc);
+
+/* Create a cache for `desc` on the current device.  Allocates (or wraps
+ * external_buf for) the K/V buffer, plus small library-owned buffers: the rotary
+ * cos/sin table (fp32 from fp64, [max_pos][head_dim/2]), the device status word and a
+ * split-KV workspace of a few MB.  The K/V contents are left uninitialised.
+ * Returns DLLM_EINVAL for a bad desc, DLLM_EUNSUPPORTED for an unsupported head_dim,
+ * DLLM_EOOM / DLLM_ECUDA on device failure; *out is NULL on error. */
+int dllm_cache_alloc(const dllm_cache_desc* desc, dllm_cache** out);
+
+/* Release the cache and every library-owned buffer (not external_buf).  Waits for the
+ * device to finish.  NULL is accepted. */
+int dllm_cache_free(dllm_cache* cache);
+
+/* Fill *out with the buffer layout of `cache`. */
+int dllm_cache_get_layout(const dllm_cache* cache, dllm_cache_layout* out);
+
+/* One denoising step of one layer (Flash-dLLM paragraph 2; LaCache Methodology 1:
+ * the cached state is the projected, rotary-embedded K/V of each token).
+ *
+ *   layer         0 <= layer < n_layers
+ *   x             act [batch][n_tok][D]: hidden states of the step's query rows
+ *   w_qkv         act [3D][D]: row n holds output feature n; the mathematical projection
+ *                 is [q|k|v] = x . W with W = transpose(w_qkv) of shape [D][3D]; features 0..D-1
+ *                 are Q, D..2D-1 K, 2D..3D-1 V, head-major (h*head_dim + i); no bias
+ *   positions     int32 [batch][n_tok]: absolute position of each row (rotary angle and,
+ *                 for BASE/MASK rows, the cache slot); must be distinct within a
+ *                 sequence among non-DRAFT rows
+ *   view          uint8 [batch][n_tok] DLLM_VIEW_* tags, or NULL (all BASE, and the tail
+ *                 slots are not attended)
+ *   n_tok         query rows per sequence (>= 0)
+ *   out           act [batch][n_tok][D]: attention output per head, heads concatenated
+ *                 (before any output projection).  Also used as scratch for the rotated
+ *                 Q during the call, so it must not alias x.
+ *   kv_x          act [batch][n_kv][D] or NULL: K/V-only rows (no query, no output)
+ *   kv_positions  int32 [batch][n_kv]: their absolute positions
+ *   n_kv          K/V-only rows per sequence (>= 0)
+ *   probe_kv      act [batch][n_kv][2][D] or NULL.  NULL: the K/V-only rows are written
+ *                 into the cache at their positions (a refresh of those slots).  Non-NULL:
+ *                 the cache is left alone and their rotated K (index 0) and V (index 1)
+ *                 go here instead (probes for dllm_kv_drift).
+ *   stream        cudaStream_t
+ *
+ * Order of effects: all cache writes of the step (K/V-only rows and query rows) happen
+ * before any attention read, so the block attends to its own fresh K/V.  Each query
+ * row then attends, per head, over slots 0..max_pos-1 and over the tail slots written
+ * by this step's DRAFT rows, with the visibility rule given above, scores scaled by
+ * 1/sqrt(head_dim) and an fp32 softmax. */
+int dllm_cache_step(dllm_cache* cache, int layer,
+                    const void* x, const void* w_qkv,
+                    const int32_t* positions, const uint8_t* view, int n_tok,
+                    void* out,
+                    const void* kv_x, const int32_t* kv_positions, int n_kv,
+                    void* probe_kv,
+                    void* stream);
+
+/* The two halves of dllm_cache_step, for callers that schedule or time them apart;
+ * dllm_cache_step(...) is exactly dllm_cache_project(...) followed by
+ * dllm_cache_attend(...) on the same stream with the same arguments.
+ *
+ * dllm_cache_project: the fused projection + rotary embedding + cache (or probe)
+ *   write of dllm_cache_step; the rotated Q of the query rows is left in `out`
+ *   (act [batch][n_tok][D]).  Arguments as for dllm_cache_step.
+ * dllm_cache_attend: the attention half.  `out` must hold the rotated Q that
+ *   dllm_cache_project left for the same positions / view / n_tok; it is overwritten
+ *   with the attention output.  Errors as for dllm_cache_step. */
+int dllm_cache_project(dllm_cache* cache, int layer,
+                       const void* x, const void* w_qkv,
+                       const int32_t* positions, const uint8_t* view, int n_tok,
+                       void* out,
+                       const void* kv_x, const int32_t* kv_positions, int n_kv,
+                       void* probe_kv,
+                       void* stream);
+int dllm_cache_attend(dllm_cache* cache, int layer,
+                      const int32_t* positions, const uint8_t* view, int n_tok,
+                      void* out, void* stream);
+
+/* Top-k most-attended positions ("Flash-dLLM ...", paragraph 4: a fixed budget of the
+ * top 32 most-attended tokens; "Elastic-Cache", Core idea: the previous step's
+ * most-attended tokens).
+ *
+ *   mass      fp32 [batch][n_pos]: previous-step attention mass per position (finite)
+ *   block_lo  int32 [batch]: first position of each sequence's active block; positions
+ *             block_lo .. block_lo+block_len-1 are not candidates
+ *   idx       int32 [batch][k] out: candidate positions ordered by mass descending, ties
+ *             to the lower position; k <= n_pos - block_len, n_pos <= 16384 */
+int dllm_kv_topk(const float* mass, int batch, int n_pos, const int32_t* block_lo, int block_len,
+                 int k, int32_t* idx, void* stream);
+
+/* Attention-aware drift test ("Elastic-Cache", Core idea and Algorithm knobs).
+ *
+ *   idx       int32 [batch][k]: tracked positions (slots) in `layer`
+ *   probe_kv  act [batch][k][2][D]: freshly computed K/V of the same tokens
+ *             (dllm_cache_step with probe_kv)
+ *   cos       fp32 [batch][k][2] out: cosine similarity between cached and probe
+ *             K (index 0) and V (index 1), each over the full D-vector of the token
+ *             (FP8 caches are dequantised first)
+ *   refresh   int32 [batch] out, or NULL: 1 where min over that sequence's cos < gamma
+ *             (the layer's cache has drifted and deeper layers should be recomputed),
+ *             else 0 */
+int dllm_kv_drift(const dllm_cache* cache, int layer, const int32_t* idx, int k,
+                  const void* probe_kv, float gamma, float* cos, int32_t* refresh, void* stream);
+
+/* Synchronise the device, read the cache's device status word into *device_bits (may
+ * be NULL) and clear it.  Returns DLLM_EDEVICE if any bit was set, else DLLM_OK. */
+int dllm_cache_status(dllm_cache* cache, int* device_bits);
+
+/* Static, human-readable name of a dllm_status. */
+const char* dllm_strerror(int status);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* DLLM_CACHE_H */

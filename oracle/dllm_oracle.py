@@ -55,7 +55,7 @@ import numpy as np
 
 __all__ = [
     "VIEW_BASE", "VIEW_DRAFT", "VIEW_MASK", "KVIEW_SHARED", "KVIEW_MASK", "KVIEW_DRAFT", "KVIEW_NONE",
-    "rope_inv_freq", "rope", "project_qkv", "row_slots", "key_views", "visible", "attention",
+    "rope_inv_freq", "rope", "project_qkv", "project_head", "row_slots", "key_views", "visible", "attention",
     "OracleCache", "write_rows", "step", "kv_topk", "cosine", "kv_drift",
     "e4m3_decode", "e4m3_table", "e4m3_quantize", "fp8_group_quantize",
 ]
@@ -107,6 +107,18 @@ def project_qkv(x: np.ndarray, w: np.ndarray, n_heads: int):
     k = y[:, D:2 * D].reshape(-1, n_heads, hd)
     v = y[:, 2 * D:3 * D].reshape(-1, n_heads, hd)
     return q, k, v
+
+
+def project_head(x: np.ndarray, w: np.ndarray, n_heads: int, h: int):
+    """q, k, v of head ``h`` only ([n][hd] each): output features part*D + h*hd + i."""
+    x = np.asarray(x, dtype=np.float64)
+    D = w.shape[1]
+    hd = D // n_heads
+    out = []
+    for part in range(3):
+        rows = np.asarray(w[part * D + h * hd: part * D + (h + 1) * hd], dtype=np.float64)
+        out.append(x @ rows.T)
+    return tuple(out)
 
 
 # ------------------------------------------------------------------------------------

@@ -1,0 +1,119 @@
+"""CUDA path vs fp64 oracle on identical seeded inputs, through the C ABI.
+
+Bounds (max|gpu - oracle| <= tol * max|oracle|): 1e-4 fp32, 2e-2 bf16, 6e-2 FP8 cache.
+Slot sets and top-k indices are compared bit-exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import workloads as W
+from tests import gpu_harness as G
+from denoising_step_attention_qkv_b300 import capi
+
+pytestmark = pytest.mark.gpu
+
+
+def _check_step(wl, probe_idx=None):
+    cache = G.make_cache(wl)
+    out, probe = G.run_gpu(wl, cache, probe_idx)
+    o_out, ocache, o_probe = G.run_oracle(wl, probe_idx)
+    tol = G.TOL[wl.shape.kv]
+    G.compare_cache(cache, ocache, tol)
+    G.assert_close(out.reshape(o_out.shape), o_out, tol if wl.shape.kv != "e4m3" else G.TOL["e4m3"], "attention out")
+    if probe_idx is not None:
+        G.assert_close(probe, o_probe, G.TOL[wl.shape.act], "probe K/V")
+    return cache, out, probe, ocache, o_probe
+
+
+# ------------------------------------------------------------------------------ fp32
+def test_config1_tiny_f32_full():
+    _check_step(W.make(1))
+
+
+def test_f32_ragged_small():
+    wl = W.make(1, batch=3, d_model=192, head_dim=64, max_pos=77, block=5, gen_lo=30, fixed_lo=None)
+    _check_step(wl)
+
+
+# ------------------------------------------------------------------------------ bf16
+SMALL_BF16 = [
+    # B, D, S, block: ragged GEMM row tiles, ragged key tile, split-KV + combine
+    dict(batch=3, d_model=512, max_pos=300, block=40, gen_lo=200),
+    # 128-key tiles exactly, one 32-row chunk, splits
+    dict(batch=2, d_model=256, max_pos=256, block=32, gen_lo=128),
+    # enough tiles for the 256-wide GEMM tile, 5 key tiles
+    dict(batch=4, d_model=1024, max_pos=640, block=32, gen_lo=512),
+    # many units: no key split
+    dict(batch=40, d_model=512, max_pos=200, block=16, gen_lo=128),
+    # more than one 64-query chunk
+    dict(batch=2, d_model=256, max_pos=400, block=100, gen_lo=200),
+]
+
+
+@pytest.mark.parametrize("kw", SMALL_BF16, ids=[f"B{k['batch']}-D{k['d_model']}-S{k['max_pos']}-n{k['block']}" for k in SMALL_BF16])
+def test_bf16_step_small(kw):
+    wl = W.make(2, head_dim=128, fixed_lo=None, **kw)
+    _check_step(wl)
+
+
+def test_bf16_config2_full():
+    _check_step(W.make(2))
+
+
+# ---------------------------------------------------------------------- Flash-Verify
+def test_verify_small():
+    wl = W.make(4, batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200, search=6, tail_slots=8)
+    _check_step(wl)
+
+
+def test_verify_draft_equals_mask_views_identical():
+    wl = W.make(4, batch=2, d_model=256, head_dim=128, max_pos=200, block=16, gen_lo=128, search=5, tail_slots=8)
+    nb = wl.block_len
+    for b in range(wl.shape.batch):
+        for t in range(nb, wl.x.shape[1]):
+            twin = np.where((wl.positions[b, :nb] == wl.positions[b, t]) & (wl.view[b, :nb] == W.VIEW_MASK))[0][0]
+            wl.x[b, t] = wl.x[b, twin]
+    cache = G.make_cache(wl)
+    out, _ = G.run_gpu(wl, cache)
+    for b in range(wl.shape.batch):
+        for t in range(nb, wl.x.shape[1]):
+            twin = np.where((wl.positions[b, :nb] == wl.positions[b, t]) & (wl.view[b, :nb] == W.VIEW_MASK))[0][0]
+            np.testing.assert_array_equal(out[b, t], out[b, twin])
+
+
+# ----------------------------------------------------------------------- drift, top-k
+def _topk_gpu(wl):
+    mass = torch.from_numpy(wl.mass).cuda()
+    lo = torch.from_numpy(wl.block_lo).cuda()
+    idx = torch.empty((wl.shape.batch, wl.drift_k), dtype=torch.int32, device="cuda")
+    capi.dllm_kv_topk(mass, lo, wl.block_len, wl.drift_k, idx)
+    return idx.cpu().numpy()
+
+
+def test_topk_bit_exact_with_ties():
+    wl = W.make(3, batch=5, d_model=256, head_dim=128, max_pos=1000, block=32, gen_lo=512, drift_k=32)
+    wl.mass[1, 100:140] = 0.25  # ties across the cut
+    wl.mass[2, :] = 0.0         # all equal
+    wl.mass[3, wl.block_lo[3]:wl.block_lo[3] + 32] = 10.0  # block dominates but is excluded
+    np.testing.assert_array_equal(_topk_gpu(wl), O.kv_topk(wl.mass, wl.block_lo, wl.block_len, wl.drift_k))
+
+
+def test_drift_small():
+    wl = W.make(3, batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200, drift_k=8)
+    idx = _topk_gpu(wl)
+    np.testing.assert_array_equal(idx, O.kv_topk(wl.mass, wl.block_lo, wl.block_len, wl.drift_k))
+    cache, out, probe, ocache, o_probe = _check_step(wl, probe_idx=idx)
+    cos = torch.empty((wl.shape.batch, wl.drift_k, 2), dtype=torch.float32, device="cuda")
+    refresh = torch.empty(wl.shape.batch, dtype=torch.int32, device="cuda")
+    capi.dllm_kv_drift(cache.handle, 0, G.idev(idx), torch.from_numpy(probe).to(torch.bfloat16).cuda(), 0.9, cos,
+                       refresh)
+    o_cos = O.kv_drift(ocache, idx, o_probe)
+    G.assert_close(cos.double().cpu().numpy(), o_cos, G.TOL["bf16"], "drift cos")
+    g_cos = cos.cpu().numpy().reshape(wl.shape.batch, -1)
+    # the flag is the kernel's own fp32 decision; away from the threshold it must match the oracle's
+    np.testing.assert_array_equal(refresh.cpu().numpy(), (g_cos.min(1) < np.float32(0.9)).astype(np.int32))
+    o_min = o_cos.reshape(wl.shape.batch, -1).min(1)
+    far = np.abs(o_min - 0.9) > 1e-2
+    np.testing.assert_array_equal(refresh.cpu().numpy()[far], (o_min[far] < 0.9).astype(np.int32))

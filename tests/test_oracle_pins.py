@@ -88,6 +88,7 @@ def test_projection_head_split_brute_force():
     w = r.standard_normal((3 * D, D))
     x = r.standard_normal((2, D))
     q, k, v = O.project_qkv(x, w, H)
+    heads = [O.project_head(x, w, H, h) for h in range(H)]
     for t in range(2):
         for part, arr in enumerate((q, k, v)):
             for h in range(H):
@@ -95,6 +96,7 @@ def test_projection_head_split_brute_force():
                     n = part * D + h * hd + i
                     ref = sum(x[t, c] * w[n, c] for c in range(D))
                     assert abs(arr[t, h, i] - ref) < 1e-12
+                    assert abs(heads[h][part][t, i] - ref) < 1e-12
 
 
 # ------------------------------------------------------------------------ attention
