@@ -23,7 +23,7 @@ DLLM_VIEW_BASE, DLLM_VIEW_DRAFT, DLLM_VIEW_MASK = 0, 1, 2
 DEV_BAD_POSITION, DEV_BAD_VIEW, DEV_TAIL_FULL, DEV_TIMEOUT, DEV_BAD_INDEX = 0x1, 0x2, 0x4, 0x8, 0x10
 
 EXPORTS = ("dllm_cache_bytes", "dllm_cache_alloc", "dllm_cache_free", "dllm_cache_get_layout", "dllm_cache_step",
-           "dllm_cache_project", "dllm_cache_attend", "dllm_kv_topk", "dllm_kv_drift", "dllm_cache_status", "dllm_strerror")
+           "dllm_cache_project", "dllm_cache_attend", "dllm_cache_attend_noalloc", "dllm_kv_topk", "dllm_kv_drift", "dllm_cache_status", "dllm_strerror")
 
 
 class dllm_cache_desc(ctypes.Structure):
@@ -62,6 +62,7 @@ def lib() -> ctypes.CDLL:
                                       c_void_p, c_void_p, c_int, c_void_p, c_void_p]
         L.dllm_cache_project.argtypes = L.dllm_cache_step.argtypes
         L.dllm_cache_attend.argtypes = [c_void_p, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p]
+        L.dllm_cache_attend_noalloc.argtypes = L.dllm_cache_attend.argtypes
         L.dllm_kv_topk.argtypes = [c_void_p, c_int, c_int, c_void_p, c_int, c_int, c_void_p, c_void_p]
         L.dllm_kv_drift.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_float, c_void_p, c_void_p, c_void_p]
         L.dllm_cache_status.argtypes = [c_void_p, POINTER(c_int)]
@@ -143,6 +144,13 @@ def dllm_cache_attend(handle, layer: int, positions: torch.Tensor, view: Optiona
                       stream=None) -> None:
     _check("dllm_cache_attend", lib().dllm_cache_attend(handle, int(layer), _ptr(positions), _ptr(view),
                                                         int(positions.shape[-1]), _ptr(out), _stream(stream)))
+
+
+def dllm_cache_attend_noalloc(handle, layer: int, positions: torch.Tensor, view: Optional[torch.Tensor],
+                              out: torch.Tensor, stream=None) -> None:
+    """dllm_cache_attend with its scratch in a fixed static device array (no allocation)."""
+    _check("dllm_cache_attend_noalloc", lib().dllm_cache_attend_noalloc(
+        handle, int(layer), _ptr(positions), _ptr(view), int(positions.shape[-1]), _ptr(out), _stream(stream)))
 
 
 def dllm_kv_topk(mass: torch.Tensor, block_lo: torch.Tensor, block_len: int, k: int, idx: torch.Tensor,

@@ -454,3 +454,100 @@ const char* dllm_strerror(int s) {
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------------
+// dllm_cache_attend_noalloc: the attention half with its split-KV scratch in a static
+// device array instead of the cache's workspace, so the call itself never allocates.
+// ------------------------------------------------------------------------------------
+namespace {
+
+// Partial (O, m, l) states of the key splits.  One copy per device that loads this
+// library, kept until the process exits.  Every call shares it: calls whose kernels
+// overlap on the GPU race on it.  Nothing here has to start at zero, because the merge
+// only reads partials that the same call wrote just before.
+static __device__ __align__(256) float g_noalloc_scratch[DLLM_NOALLOC_SCRATCH_BYTES / sizeof(float)];
+
+constexpr int kMaxDevices = 256;
+std::mutex g_noalloc_mu;
+float* g_noalloc_addr[kMaxDevices] = {};
+
+// Device address of g_noalloc_scratch on the current device.  Host code cannot use
+// the symbol itself (it names a host-side shadow), so the address is looked up once
+// per device, with that device current, and cached.
+int noalloc_scratch_address(float** out) {
+  int dev = -1;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (dev < 0 || dev >= kMaxDevices) return DLLM_ECUDA;
+  std::lock_guard<std::mutex> lock(g_noalloc_mu);
+  if (!g_noalloc_addr[dev]) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+    if (e != cudaSuccess) return from_cuda(e);
+    g_noalloc_addr[dev] = static_cast<float*>(p);
+  }
+  *out = g_noalloc_addr[dev];
+  return DLLM_OK;
+}
+
+}  // namespace
+
+extern "C" int dllm_cache_attend_noalloc(dllm_cache* c, int layer, const int32_t* positions, const uint8_t* view,
+                                         int n_tok, void* out, void* stream) {
+  int rc = check_attend(c, layer, n_tok, positions, view, out);
+  if (rc) return rc;
+  if (n_tok == 0) return DLLM_OK;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const dllm_cache_desc& d = c->desc;
+  const int B = d.batch, H = d.n_heads, hd = d.head_dim, D = H * hd;
+  AttnParams a{};
+  a.B = B;
+  a.H = H;
+  a.D = D;
+  a.n_tok = n_tok;
+  a.max_pos = d.max_pos;
+  a.tail = d.tail_slots;
+  a.slots = c->slots;
+  a.view = view;
+  a.positions = positions;
+  a.out = out;
+  a.ws = nullptr;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)hd));
+  a.kv_scale = layer_scale(c, layer);
+  a.kv_dtype = d.kv_dtype;
+  a.status = c->status;
+  if (d.kv_dtype == DLLM_F32) {  // the fp32 kernel keeps no partial state
+    rc = launch_attn_f32(a, (const float*)layer_kv(c, layer), hd, s);
+    return rc ? from_cuda((cudaError_t)rc) : DLLM_OK;
+  }
+  // same work split as dllm_cache_attend, so both produce the same result
+  a.nq_pad = n_tok <= 32 ? 32 : 64;
+  a.n_qchunks = ceil_div(n_tok, kQChunk);
+  a.key_tiles = ceil_div(d.max_pos + (view ? d.tail_slots : 0), kKeyTile);
+  const int base = B * H * a.n_qchunks;
+  int splits = 1;
+  if (base < c->sm_count) {
+    splits = ceil_div(c->sm_count, base);
+    if (splits > a.key_tiles) splits = a.key_tiles;
+  }
+  a.tiles_per_split = ceil_div(a.key_tiles, splits);
+  a.n_splits = ceil_div(a.key_tiles, a.tiles_per_split);
+  a.units = base * a.n_splits;
+  if (a.n_splits > 1) {
+    const size_t need = (size_t)a.units * kQChunk * (kHd + 2) * sizeof(float);
+    if (need > (size_t)DLLM_NOALLOC_SCRATCH_BYTES) return DLLM_EUNSUPPORTED;
+    rc = noalloc_scratch_address(&a.ws);
+    if (rc) return rc;
+  }
+  CUtensorMap tm_q, tm_kv;
+  if (!map_2d_bf16(&tm_q, out, D, (uint64_t)B * n_tok, 64, a.nq_pad)) return DLLM_ECUDA;
+  if (!map_cache(&tm_kv, layer_kv(c, layer), d.kv_dtype, hd, H, (uint64_t)B * c->slots)) return DLLM_ECUDA;
+  const int grid = a.units < c->sm_count ? a.units : c->sm_count;
+  rc = launch_attn_tc(a, tm_q, tm_kv, grid, s);
+  if (rc) return from_cuda((cudaError_t)rc);
+  if (a.n_splits > 1) {
+    rc = launch_attn_combine(a, s);
+    if (rc) return from_cuda((cudaError_t)rc);
+  }
+  return DLLM_OK;
+}

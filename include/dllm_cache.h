@@ -211,6 +211,35 @@ int dllm_kv_topk(const float* mass, int batch, int n_pos, const int32_t* block_l
 int dllm_kv_drift(const dllm_cache* cache, int layer, const int32_t* idx, int k,
                   const void* probe_kv, float gamma, float* cos, int32_t* refresh, void* stream);
 
+/* Scratch capacity of dllm_cache_attend_noalloc, in bytes (8 MiB). */
+#define DLLM_NOALLOC_SCRATCH_BYTES (8u << 20)
+
+/* dllm_cache_attend for callers that cannot allocate device memory.  The pages have
+ * no counterpart to this call; it exists for how the library is hosted, not for the
+ * method.  Some callers must not call cudaMalloc at all: a serving engine that has
+ * already handed its whole device memory budget to its own pool (a new allocation
+ * would fail or break that budget), or a latency-critical decode loop that cannot
+ * take the device-wide synchronisation cudaMalloc may cause.  This call allocates
+ * nothing: when the work is split over keys, the partial softmax states go to one
+ * fixed array of DLLM_NOALLOC_SCRATCH_BYTES in the library's own device memory, which
+ * every device that loads the library holds until the process exits.
+ *
+ * Arguments, results and errors are those of dllm_cache_attend, plus:
+ *   - DLLM_EUNSUPPORTED when the split partial states of this call would need more
+ *     than DLLM_NOALLOC_SCRATCH_BYTES (units * 64 query rows * 130 floats each; it
+ *     happens only when batch * n_heads is below the SM count and the key range is
+ *     long); nothing is launched then.
+ *   - The first call on each device looks up the device address of that array (with
+ *     the device current) and remembers it; make this first call before any stream
+ *     capture begins.
+ *   - Every call on a device shares the same array and leaves its contents behind.
+ *     Nothing in it needs to start at zero.  Calls whose kernels overlap on the GPU
+ *     (different streams without ordering between them) race on it and give wrong
+ *     results; order them on one stream or with events. */
+int dllm_cache_attend_noalloc(dllm_cache* cache, int layer,
+                              const int32_t* positions, const uint8_t* view, int n_tok,
+                              void* out, void* stream);
+
 /* Synchronise the device, read the cache's device status word into *device_bits (may
  * be NULL) and clear it.  Returns DLLM_EDEVICE if any bit was set, else DLLM_OK. */
 int dllm_cache_status(dllm_cache* cache, int* device_bits);
