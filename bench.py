@@ -35,8 +35,8 @@ L2_BYTES = 126 * 2 ** 20
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=30)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=3, choices=[2, 3])
     ap.add_argument("--no-e2e", action="store_true")
@@ -63,44 +63,83 @@ def peaks():
 
 # ----------------------------------------------------------------------------- clocks
 class Clocks:
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    """Samples the SM clock and the clock-event reasons of one GPU through NVML every
+    2 ms on a background thread while the timed region runs (falls back to
+    ``nvidia-smi -lms 100`` when NVML is not importable)."""
 
-    def __init__(self, gpu_index: int):
-        self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+
+    def __init__(self, torch_device):
+        import threading
+        self.samples, self.reason_bits, self.max_mhz = [], 0, None
+        self.stop_evt = threading.Event()
+        self.thread = None
+        self.proc = None
         try:
-            self.p = subprocess.Popen(["nvidia-smi", "-i", str(gpu_index), f"--query-gpu={self.FIELDS}",
-                                       "--format=csv,noheader,nounits", "-lms", "200"],
-                                      stdout=self.f, stderr=subprocess.DEVNULL)
-        except OSError:
-            self.p = None
+            import pynvml as N
+            N.nvmlInit()
+            props = __import__("torch").cuda.get_device_properties(torch_device)
+            h = None
+            try:
+                bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
+                h = N.nvmlDeviceGetHandleByPciBusId(bus)
+            except Exception:
+                h = N.nvmlDeviceGetHandleByIndex(0)
+            self.N, self.h = N, h
+            self.max_mhz = N.nvmlDeviceGetMaxClockInfo(h, N.NVML_CLOCK_SM)
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+            self.thread.start()
+        except Exception:
+            self.N = None
+            self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
+            try:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+            except OSError:
+                self.proc = None
+
+    def _poll(self):
+        N, h = self.N, self.h
+        while not self.stop_evt.is_set():
+            try:
+                self.samples.append(N.nvmlDeviceGetClockInfo(h, N.NVML_CLOCK_SM))
+                self.reason_bits |= int(N.nvmlDeviceGetCurrentClocksEventReasons(h))
+            except Exception:
+                try:
+                    self.reason_bits |= int(N.nvmlDeviceGetCurrentClocksThrottleReasons(h))
+                except Exception:
+                    pass
+            self.stop_evt.wait(0.002)
 
     def stop(self):
-        if self.p is None:
+        if self.thread is not None:
+            self.stop_evt.set()
+            self.thread.join()
+            reasons = sorted(v for k, v in self.REASONS.items() if self.reason_bits & k)
+            if not self.samples:
+                return None
+            return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz, "reasons": reasons,
+                    "samples": len(self.samples), "source": "nvml, 2 ms polling during the timed region"}
+        if self.proc is None:
             return None
-        self.p.terminate()
-        try:
-            self.p.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.p.kill()
-        rows = []
-        for line in open(self.f.name):
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) == 9:
-                rows.append(parts)
+        self.proc.terminate()
+        self.proc.wait()
+        rows = [ln.split(",") for ln in open(self.f.name) if ln.count(",") == 2]
         os.unlink(self.f.name)
-        if not rows:
+        sm = [float(r[0]) for r in rows if r[0].strip().replace(".", "").isdigit()]
+        if not sm:
             return None
-        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
-        mx = max(float(r[2]) for r in rows if r[2].replace(".", "").isdigit())
-        reasons = set()
+        bits = 0
         for r in rows:
-            for name, val in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"), r[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": mx, "reasons": sorted(reasons),
-                "samples": len(rows)}
+            try:
+                bits |= int(r[2].strip(), 16)
+            except ValueError:
+                pass
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][1]),
+                "reasons": sorted(v for k, v in self.REASONS.items() if bits & k), "samples": len(sm),
+                "source": "nvidia-smi -lms 100"}
 
 
 # --------------------------------------------------------------------------- workload
@@ -177,7 +216,7 @@ def run_ours(args, rank, world, local):
 
     # ---- timed region: K steps, L2 flushed between steps (outside the events)
     per = {"step": [], "topk": [], "project": [], "attend": [], "drift": []}
-    clocks = Clocks(local) if rank == 0 else None
+    clocks = Clocks(dev) if rank == 0 else None
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)

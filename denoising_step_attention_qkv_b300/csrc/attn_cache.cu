@@ -19,6 +19,13 @@
 // S, P and O are double-buffered so the loads, both MMAs and the softmax overlap.
 // With few units, keys are split across CTAs and a second kernel merges the partial
 // (O, m, l) states.
+//
+// FP8-e4m3 cache ("LaCache ...", Methodology 2: per-group FP8; one group here = one
+// head of one token, K or V, with an fp32 scale): TMA stages the e4m3 tiles (half the
+// bytes of bf16) in a 3-deep ring and four converter warps widen them to bf16 in the
+// MMA operand layout (exact: every e4m3 value is a bf16 value).  The K scale of a key
+// multiplies that key's scores in fp32, and the V scale multiplies its probabilities
+// before they are rounded for the PV MMA, so dequantisation adds no rounding step.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -28,20 +35,32 @@
 namespace dllm {
 namespace {
 
-constexpr int kThreads = 192;
-constexpr int KST = 3;
-constexpr int VST = 2;
 constexpr uint32_t kTileBytes = kKeyTile * kHd * 2;  // 32 KB (bf16 K or V tile)
+constexpr uint32_t kTile8Bytes = kKeyTile * kHd;     // 16 KB (e4m3 tile)
 constexpr uint32_t kQBytes = kQChunk * kHd * 2;      // 16 KB
 constexpr uint32_t kPBytes = kQChunk * kKeyTile * 2; // 16 KB
 constexpr int kMaxBitmapWords = 512;                 // MASK-slot bitmap: max_pos <= 16384
 
+// Per cache type: MMA-operand rings for K and V, e4m3 staging rings, thread count.
+template <bool FP8>
+struct Cfg {
+  static constexpr int KST = FP8 ? 1 : 3;
+  static constexpr int VST = FP8 ? 1 : 2;
+  static constexpr int SST = FP8 ? 3 : 1;
+  static constexpr uint32_t kStageBytes = FP8 ? kTile8Bytes : 1024;
+  static constexpr int kThreads = FP8 ? 320 : 192;  // + 4 converter warps for FP8
+};
+
+template <bool FP8>
 struct Smem {
+  using C = Cfg<FP8>;
   // all operand tiles 1024-byte aligned
   uint8_t q[kQBytes];
-  uint8_t k[KST][kTileBytes];
-  uint8_t v[VST][kTileBytes];
+  uint8_t k[C::KST][kTileBytes];
+  uint8_t v[C::VST][kTileBytes];
   uint8_t p[2][kPBytes];
+  uint8_t sk[C::SST][C::kStageBytes];  // e4m3 staging (FP8 only)
+  uint8_t sv[C::SST][C::kStageBytes];
   float red_max[4][kQChunk];
   float red_sum[2][4][kQChunk];
   float m_run[kQChunk];
@@ -52,8 +71,10 @@ struct Smem {
   uint32_t draft_qmask[2];
   int n_draft;
   uint64_t q_full, q_empty;
-  uint64_t k_full[KST], k_empty[KST];
-  uint64_t v_full[VST], v_empty[VST];
+  uint64_t k_full[C::KST], k_empty[C::KST];
+  uint64_t v_full[C::VST], v_empty[C::VST];
+  uint64_t sk_full[C::SST], sk_empty[C::SST];
+  uint64_t sv_full[C::SST], sv_empty[C::SST];
   uint64_t s_full[2], s_free[2];
   uint64_t p_full[2], p_empty[2];
   uint64_t o_full[2], o_free[2];
@@ -61,6 +82,23 @@ struct Smem {
   uint32_t tmem_base;
   int abort_flag;
 };
+static_assert(sizeof(Smem<false>) + 1024 <= 232448, "shared memory budget (bf16)");
+static_assert(sizeof(Smem<true>) + 1024 <= 232448, "shared memory budget (e4m3)");
+
+// Widen 16 e4m3 codes to 16 bf16 values (exact).
+DEVI void widen16(const uint4 in, uint4& lo, uint4& hi) {
+  const __nv_fp8x2_storage_t* pr = reinterpret_cast<const __nv_fp8x2_storage_t*>(&in);
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __half2 h(__nv_cvt_fp8x2_to_halfraw2(pr[i], __NV_E4M3));
+    const float2 f = __half22float2(h);
+    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
+    w[i] = *reinterpret_cast<const uint32_t*>(&b);
+  }
+  lo = make_uint4(w[0], w[1], w[2], w[3]);
+  hi = make_uint4(w[4], w[5], w[6], w[7]);
+}
 
 struct Unit {
   int b, h, qc, split, t0, t1;
@@ -99,12 +137,14 @@ DEVI float reduce_scatter32(float (&v)[32], int lane) {
   return v[0];
 }
 
-template <int NQ>
-__global__ void __launch_bounds__(kThreads, 1)
+template <int NQ, bool FP8>
+__global__ void __launch_bounds__(Cfg<FP8>::kThreads, 1)
     attn_cache_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                   const AttnParams p) {
+  using C = Cfg<FP8>;
+  constexpr int KST = C::KST, VST = C::VST, SST = C::SST;
   extern __shared__ uint8_t smem_raw[];
-  Smem& S = *reinterpret_cast<Smem*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
+  Smem<FP8>& S = *reinterpret_cast<Smem<FP8>*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
   volatile int* abort_flag = &S.abort_flag;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
@@ -114,8 +154,15 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (threadIdx.x == 0) {
     mbar_init(&S.q_full, 1);
     mbar_init(&S.q_empty, 1);
-    for (int i = 0; i < KST; ++i) { mbar_init(&S.k_full[i], 1); mbar_init(&S.k_empty[i], 1); }
-    for (int i = 0; i < VST; ++i) { mbar_init(&S.v_full[i], 1); mbar_init(&S.v_empty[i], 1); }
+    // bf16: operand tiles are filled by TMA (one arrival + bytes); e4m3: by 4 converter warps
+    for (int i = 0; i < KST; ++i) { mbar_init(&S.k_full[i], FP8 ? 4 : 1); mbar_init(&S.k_empty[i], 1); }
+    for (int i = 0; i < VST; ++i) { mbar_init(&S.v_full[i], FP8 ? 4 : 1); mbar_init(&S.v_empty[i], 1); }
+    for (int i = 0; i < SST; ++i) {
+      mbar_init(&S.sk_full[i], 1);
+      mbar_init(&S.sk_empty[i], 4);
+      mbar_init(&S.sv_full[i], 1);
+      mbar_init(&S.sv_empty[i], 4);
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S.s_full[i], 1);
       mbar_init(&S.s_free[i], 4);
@@ -145,7 +192,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint64_t pol_q = policy_evict_last();
     int ks = 0, vs = 0;
     uint32_t kph = 0, vph = 0, qph = 0;
-    const bool fp8 = p.kv_dtype == DLLM_E4M3;
     bool ok = true;
     for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
       const Unit x = decode_unit(p, u);
@@ -158,36 +204,45 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int slot0 = x.b * p.slots;
       for (int t = x.t0; t < x.t1; ++t) {
         const int key0 = slot0 + t * kKeyTile;
-        if (!mbar_wait(&S.k_empty[ks], kph ^ 1u, abort_flag)) { ok = false; break; }
-        if (fp8) {
-          mbar_arrive_expect_tx(&S.k_full[ks], kTileBytes / 2);
-          tma_load_3d(S.k[ks], &tm_kv, &S.k_full[ks], 0, x.h, key0, pol_stream);
+        if constexpr (FP8) {
+          // e4m3 tiles into the staging rings (one 128-byte-wide box each)
+          if (!mbar_wait(&S.sk_empty[ks], kph ^ 1u, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(&S.sk_full[ks], kTile8Bytes);
+          tma_load_3d(S.sk[ks], &tm_kv, &S.sk_full[ks], 0, x.h, key0, pol_stream);
+          if (!mbar_wait(&S.sv_empty[ks], kph ^ 1u, abort_flag)) { ok = false; break; }
+          mbar_arrive_expect_tx(&S.sv_full[ks], kTile8Bytes);
+          tma_load_3d(S.sv[ks], &tm_kv, &S.sv_full[ks], 0, p.H + x.h, key0, pol_stream);
+          if (++ks == SST) { ks = 0; kph ^= 1u; }
         } else {
+          if (!mbar_wait(&S.k_empty[ks], kph ^ 1u, abort_flag)) { ok = false; break; }
           mbar_arrive_expect_tx(&S.k_full[ks], kTileBytes);
           tma_load_3d(S.k[ks], &tm_kv, &S.k_full[ks], 0, x.h, key0, pol_stream);
           tma_load_3d(S.k[ks] + kTileBytes / 2, &tm_kv, &S.k_full[ks], 64, x.h, key0, pol_stream);
-        }
-        if (++ks == KST) { ks = 0; kph ^= 1u; }
-        if (!mbar_wait(&S.v_empty[vs], vph ^ 1u, abort_flag)) { ok = false; break; }
-        if (fp8) {
-          mbar_arrive_expect_tx(&S.v_full[vs], kTileBytes / 2);
-          tma_load_3d(S.v[vs], &tm_kv, &S.v_full[vs], 0, p.H + x.h, key0, pol_stream);
-        } else {
+          if (++ks == KST) { ks = 0; kph ^= 1u; }
+          if (!mbar_wait(&S.v_empty[vs], vph ^ 1u, abort_flag)) { ok = false; break; }
           mbar_arrive_expect_tx(&S.v_full[vs], kTileBytes);
           tma_load_3d(S.v[vs], &tm_kv, &S.v_full[vs], 0, p.H + x.h, key0, pol_stream);
           tma_load_3d(S.v[vs] + kTileBytes / 2, &tm_kv, &S.v_full[vs], 64, p.H + x.h, key0, pol_stream);
+          if (++vs == VST) { vs = 0; vph ^= 1u; }
         }
-        if (++vs == VST) { vs = 0; vph ^= 1u; }
       }
     }
     if (!ok) {
       *abort_flag = 1;
       atomicOr(p.status, DLLM_DEV_TIMEOUT);
     }
+    // let every copy issued here land before the CTA can exit
     volatile int never = 0;
     mbar_wait(&S.q_full, qph ^ 1u, &never);
-    for (int i = 0; i < KST; ++i) mbar_wait(&S.k_full[i], (i < ks) ? kph : (kph ^ 1u), &never);
-    for (int i = 0; i < VST; ++i) mbar_wait(&S.v_full[i], (i < vs) ? vph : (vph ^ 1u), &never);
+    if constexpr (FP8) {
+      for (int i = 0; i < SST; ++i) {
+        mbar_wait(&S.sk_full[i], (i < ks) ? kph : (kph ^ 1u), &never);
+        mbar_wait(&S.sv_full[i], (i < ks) ? kph : (kph ^ 1u), &never);
+      }
+    } else {
+      for (int i = 0; i < KST; ++i) mbar_wait(&S.k_full[i], (i < ks) ? kph : (kph ^ 1u), &never);
+      for (int i = 0; i < VST; ++i) mbar_wait(&S.v_full[i], (i < vs) ? vph : (vph ^ 1u), &never);
+    }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------------ MMA issuer
     constexpr uint32_t idesc_s = idesc_bf16(128, NQ, false, false);
@@ -256,13 +311,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_commit(&S.drain);
     volatile int never = 0;
     mbar_wait(&S.drain, 0, &never);
-  } else if (warp >= 2) {
+  } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------------ softmax warps
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;  // key within the tile (S^T) / hd index (O^T)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const bool has_view = p.view != nullptr;
-    const bool fp8 = p.kv_dtype == DLLM_E4M3;
+    constexpr bool fp8 = FP8;
     uint32_t s_cnt = 0, pv_cnt = 0;
     int vs = 0;  // V ring position, mirrors the producer
     uint32_t vph = 0;
@@ -376,7 +431,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           // Slots past the regular region that no query sees may hold anything (stale
           // draft views, the next sequence, never-written memory).  Their P is 0, but
           // 0 * NaN would still poison O, so their V rows are zeroed before the PV MMA.
-          if ((t + 1) * kKeyTile > p.max_pos && vis == 0ull && j >= p.max_pos) {
+          if (!FP8 && (t + 1) * kKeyTile > p.max_pos && vis == 0ull && j >= p.max_pos) {
             if (!mbar_wait(&S.v_full[vs], vph, abort_flag)) { ok = false; break; }
             uint4* row0 = reinterpret_cast<uint4*>(S.v[vs] + r * 128);
             uint4* row1 = reinterpret_cast<uint4*>(S.v[vs] + kTileBytes / 2 + r * 128);
@@ -481,6 +536,81 @@ __global__ void __launch_bounds__(kThreads, 1)
       *abort_flag = 1;
       atomicOr(p.status, DLLM_DEV_TIMEOUT);
     }
+  } else if (FP8 && warp >= 6) {
+    // ------------------------------------------------------------------ e4m3 -> bf16 converters
+    // Thread r widens key row r of each staged tile into both 64-column halves of the
+    // operand tile, keeping the 128-byte swizzle.  V rows of slots that no query can
+    // see are written as zeros (their probability is 0, and 0 * NaN must not reach O).
+    const int r = (warp & 3) * 32 + lane;
+    int ss = 0, ko = 0, vo = 0;
+    uint32_t sph = 0, kph = 0, vph = 0;
+    bool ok = true;
+    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+      const Unit x = decode_unit(p, u);
+      int n_draft = 0;
+      if (p.view) {
+        for (int t = 0; t < p.n_tok; ++t) n_draft += (p.view[x.b * p.n_tok + t] == DLLM_VIEW_DRAFT);
+        n_draft = min(n_draft, p.tail);
+      }
+      const int kend = p.max_pos + n_draft;
+      for (int t = x.t0; t < x.t1; ++t) {
+        const int j = t * kKeyTile + r;
+        const uint32_t sw = static_cast<uint32_t>(r & 7);
+        // K
+        if (!mbar_wait(&S.sk_full[ss], sph, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&S.k_empty[ko], kph ^ 1u, abort_flag)) { ok = false; break; }
+        {
+          const uint8_t* src = S.sk[ss] + r * 128;
+          uint8_t* dst = S.k[ko] + r * 128;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            const uint4 in = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
+            uint4 lo, hi;
+            widen16(in, lo, hi);
+            uint8_t* half = dst + (c >> 2) * (kTileBytes / 2);
+            const uint32_t c0 = (c & 3) * 2;
+            *reinterpret_cast<uint4*>(half + ((c0 ^ sw) << 4)) = lo;
+            *reinterpret_cast<uint4*>(half + (((c0 + 1) ^ sw) << 4)) = hi;
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&S.k_full[ko]);
+          mbar_arrive(&S.sk_empty[ss]);
+        }
+        if (++ko == KST) { ko = 0; kph ^= 1u; }
+        // V
+        if (!mbar_wait(&S.sv_full[ss], sph, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(&S.v_empty[vo], vph ^ 1u, abort_flag)) { ok = false; break; }
+        {
+          const uint8_t* src = S.sv[ss] + r * 128;
+          uint8_t* dst = S.v[vo] + r * 128;
+          const bool zero = j >= kend;
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
+            if (!zero) widen16(*reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4)), lo, hi);
+            uint8_t* half = dst + (c >> 2) * (kTileBytes / 2);
+            const uint32_t c0 = (c & 3) * 2;
+            *reinterpret_cast<uint4*>(half + ((c0 ^ sw) << 4)) = lo;
+            *reinterpret_cast<uint4*>(half + (((c0 + 1) ^ sw) << 4)) = hi;
+          }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          mbar_arrive(&S.v_full[vo]);
+          mbar_arrive(&S.sv_empty[ss]);
+        }
+        if (++vo == VST) { vo = 0; vph ^= 1u; }
+        if (++ss == SST) { ss = 0; sph ^= 1u; }
+      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      atomicOr(p.status, DLLM_DEV_TIMEOUT);
+    }
   }
 
   tc_fence_before();
@@ -520,22 +650,23 @@ __global__ void __launch_bounds__(kHd) attn_combine(const AttnParams p) {
 
 }  // namespace
 
-size_t attn_tc_smem_bytes() { return sizeof(Smem) + 1024; }
+size_t attn_tc_smem_bytes() { return sizeof(Smem<true>) + 1024; }
+
+template <int NQ, bool FP8>
+int launch_one(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, int grid, cudaStream_t s) {
+  const size_t smem = sizeof(Smem<FP8>) + 1024;
+  cudaError_t e =
+      cudaFuncSetAttribute(attn_cache_tc<NQ, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return (int)e;
+  attn_cache_tc<NQ, FP8><<<grid, Cfg<FP8>::kThreads, smem, s>>>(tm_q, tm_kv, p);
+  return (int)cudaGetLastError();
+}
 
 int launch_attn_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, int grid,
                    cudaStream_t s) {
-  const size_t smem = attn_tc_smem_bytes();
-  cudaError_t e;
-  if (p.nq_pad <= 32) {
-    e = cudaFuncSetAttribute(attn_cache_tc<32>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return (int)e;
-    attn_cache_tc<32><<<grid, kThreads, smem, s>>>(tm_q, tm_kv, p);
-  } else {
-    e = cudaFuncSetAttribute(attn_cache_tc<64>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return (int)e;
-    attn_cache_tc<64><<<grid, kThreads, smem, s>>>(tm_q, tm_kv, p);
-  }
-  return (int)cudaGetLastError();
+  const bool fp8 = p.kv_dtype == DLLM_E4M3;
+  if (p.nq_pad <= 32) return fp8 ? launch_one<32, true>(p, tm_q, tm_kv, grid, s) : launch_one<32, false>(p, tm_q, tm_kv, grid, s);
+  return fp8 ? launch_one<64, true>(p, tm_q, tm_kv, grid, s) : launch_one<64, false>(p, tm_q, tm_kv, grid, s);
 }
 
 int launch_attn_combine(const AttnParams& p, cudaStream_t s) {

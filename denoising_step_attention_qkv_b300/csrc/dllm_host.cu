@@ -247,7 +247,6 @@ int check_attend(dllm_cache* c, int layer, int n_tok, const int32_t* positions, 
   if (view && d.max_pos > 32 * 512) return DLLM_EUNSUPPORTED;
   if (d.kv_dtype == DLLM_F32 && (size_t)(d.max_pos + d.tail_slots + d.head_dim + 32) * 4 > 200 * 1024)
     return DLLM_EUNSUPPORTED;
-  if (d.kv_dtype == DLLM_E4M3) return DLLM_EUNSUPPORTED;  // FP8 attention: not yet built
   return DLLM_OK;
 }
 

@@ -202,14 +202,29 @@ def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, vis: Optional[np.ndar
 # ------------------------------------------------------------------------------------
 
 class OracleCache:
-    """K/V of one layer for B sequences, ``max_pos + tail_slots`` slots each, fp64."""
+    """K/V of one layer for B sequences, ``max_pos + tail_slots`` slots each, fp64.
 
-    def __init__(self, batch: int, max_pos: int, tail_slots: int, n_heads: int, head_dim: int):
+    ``kv="e4m3"``: the cache stores FP8 ([LaCache] Methodology 2, per-group FP8): every
+    (token, head) vector of K and of V written into it is one quantisation group and
+    is kept as its dequantised value ``e4m3(x / s) * s`` with ``s = amax / 448``.
+    ``kv="exact"`` keeps the fp64 values.
+    """
+
+    def __init__(self, batch: int, max_pos: int, tail_slots: int, n_heads: int, head_dim: int, kv: str = "exact"):
         self.B, self.S, self.T, self.H, self.hd = batch, max_pos, tail_slots, n_heads, head_dim
+        if kv not in ("exact", "e4m3"):
+            raise ValueError(kv)
+        self.kv = kv
         n = max_pos + tail_slots
         self.K = np.zeros((batch, n, n_heads, head_dim))
         self.V = np.zeros((batch, n, n_heads, head_dim))
         self.written = np.zeros((batch, n), bool)
+
+    def stored(self, vec: np.ndarray) -> np.ndarray:
+        """What the cache keeps for one (token, head) K or V vector."""
+        if self.kv == "e4m3":
+            return fp8_group_quantize(vec)[0]
+        return vec
 
 
 def write_rows(cache: OracleCache, w: np.ndarray, x: np.ndarray, positions: np.ndarray, theta: float,
@@ -228,8 +243,9 @@ def write_rows(cache: OracleCache, w: np.ndarray, x: np.ndarray, positions: np.n
         for t, s in enumerate(sl):
             if not (0 <= s < cache.S + cache.T):
                 raise IndexError("slot out of range")
-            cache.K[b, s] = k[t]
-            cache.V[b, s] = v[t]
+            for h in range(cache.H):
+                cache.K[b, s, h] = cache.stored(k[t, h])
+                cache.V[b, s, h] = cache.stored(v[t, h])
             cache.written[b, s] = True
         qs.append(q)
     return np.stack(qs)

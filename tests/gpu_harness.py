@@ -82,9 +82,12 @@ def run_gpu(wl: W.Workload, cache: capi.Cache, probe_idx: np.ndarray = None, lay
     return out.double().cpu().numpy(), (None if probe is None else probe.double().cpu().numpy())
 
 
-def run_oracle(wl: W.Workload, probe_idx: np.ndarray = None):
+def run_oracle(wl: W.Workload, probe_idx: np.ndarray = None, exact: bool = False):
+    """Oracle of the workload; an FP8 cache is modelled (its quantisation is a step of the
+    computation) unless ``exact`` asks for the unquantised diagnostic."""
     s = wl.shape
-    cache = O.OracleCache(s.batch, s.max_pos, s.tail_slots, s.n_heads, s.head_dim)
+    kv = "e4m3" if (s.kv == "e4m3" and not exact) else "exact"
+    cache = O.OracleCache(s.batch, s.max_pos, s.tail_slots, s.n_heads, s.head_dim, kv=kv)
     if wl.pre_x is not None:
         O.write_rows(cache, wl.w, wl.pre_x, wl.pre_pos, s.rope_theta)
     probe = None
@@ -119,3 +122,111 @@ def compare_cache(cache: capi.Cache, ocache: O.OracleCache, tol: float):
     ek = assert_close(kv[:, :, 0][written], ocache.K[written], tol, "cache K")
     ev = assert_close(kv[:, :, 1][written], ocache.V[written], tol, "cache V")
     return ek, ev
+
+
+# ------------------------------------------------------------------------------------
+# Full-size workloads: the GPU runs the whole step; the oracle recomputes sampled
+# (sequence, head) pairs one by one.
+# ------------------------------------------------------------------------------------
+
+def expected_written(wl: W.Workload, probe: bool = False) -> np.ndarray:
+    """bool [B][slots]: slots the step (and its prefill) must write - index logic only."""
+    s = wl.shape
+    n = s.max_pos + s.tail_slots
+    w = np.zeros((s.batch, n), bool)
+    for b in range(s.batch):
+        if wl.pre_pos is not None:
+            w[b, wl.pre_pos[b]] = True
+        if wl.kv_pos is not None and not probe:
+            w[b, wl.kv_pos[b]] = True
+        vb = None if wl.view is None else wl.view[b]
+        w[b, O.row_slots(wl.positions[b], vb, s.max_pos)] = True
+    return w
+
+
+def written_slots_fast(cache: capi.Cache, layer: int = 0) -> np.ndarray:
+    raw = cache.kv(layer)
+    if raw.dtype == torch.bfloat16:
+        bits = raw.view(torch.int16) != -1
+    elif raw.dtype == torch.float32:
+        bits = raw.view(torch.int32) != -1
+    else:
+        bits = raw != 0xFF
+    return bits.flatten(2).any(-1).cpu().numpy()
+
+
+def gpu_head(cache: capi.Cache, b: int, h: int, layer: int = 0) -> np.ndarray:
+    """Dequantised K/V of one (sequence, head): float64 [slots][2][hd]."""
+    kv = cache.kv(layer)[b, :, :, h, :]
+    if cache.desc.kv_dtype == capi.DLLM_E4M3:
+        vals = kv.view(torch.float8_e4m3fn).to(torch.float32) * cache.scale(layer)[b, :, :, h][..., None]
+        return vals.double().cpu().numpy()
+    return kv.double().cpu().numpy()
+
+
+def oracle_head(wl: W.Workload, b: int, h: int, probe_idx: np.ndarray = None, exact: bool = False):
+    """fp64 oracle restricted to head h of sequence b.
+
+    Returns (out [n_tok][hd], K [slots][hd], V [slots][hd], written [slots], probe or None)
+    with probe = (K [k][hd], V [k][hd]) of the tracked tokens."""
+    s = wl.shape
+    hd = s.head_dim
+    n = s.max_pos + s.tail_slots
+    K = np.zeros((n, hd))
+    V = np.zeros((n, hd))
+    written = np.zeros(n, bool)
+    store = O.OracleCache(1, 1, 0, 1, hd, kv="e4m3" if (s.kv == "e4m3" and not exact) else "exact").stored
+
+    def put(x_rows, pos, slots):
+        q, k, v = O.project_head(x_rows, wl.w, s.n_heads, h)
+        q = O.rope(q[:, None, :], pos, s.rope_theta)[:, 0]
+        k = O.rope(k[:, None, :], pos, s.rope_theta)[:, 0]
+        K[slots] = np.stack([store(r) for r in k])
+        V[slots] = np.stack([store(r) for r in v])
+        written[slots] = True
+        return q
+
+    if wl.pre_x is not None:
+        put(wl.pre_x[b], wl.pre_pos[b], wl.pre_pos[b])
+    if wl.kv_x is not None and probe_idx is None:
+        put(wl.kv_x[b], wl.kv_pos[b], wl.kv_pos[b])
+    vb = None if wl.view is None else wl.view[b]
+    slots = O.row_slots(wl.positions[b], vb, s.max_pos)
+    q = put(wl.x[b], wl.positions[b], slots)
+    kview = O.key_views(wl.positions[b], vb, s.max_pos, n)
+    qview = np.zeros(len(slots), np.int64) if vb is None else vb.astype(np.int64)
+    vis = O.visible(qview, kview)
+    assert written[vis.any(0)].all()
+    out = O.attention(q[:, None, :], K[:, None, :], V[:, None, :], vis)[:, 0]
+    probe = None
+    if probe_idx is not None:
+        xp = wl.probe_rows(probe_idx[b:b + 1], b0=b)[0]
+        _, kp, vp = O.project_head(xp, wl.w, s.n_heads, h)
+        kp = O.rope(kp[:, None, :], probe_idx[b], s.rope_theta)[:, 0]
+        probe = (kp, vp)
+    return out, K, V, written, probe
+
+
+def check_sampled(wl: W.Workload, cache: capi.Cache, out: np.ndarray, samples, probe_gpu: np.ndarray = None,
+                  probe_idx: np.ndarray = None, exact_diag_tol: float = None):
+    """Written-slot set in full (bit-exact), then cache, output and probes on sampled heads."""
+    s = wl.shape
+    np.testing.assert_array_equal(written_slots_fast(cache), expected_written(wl, probe_idx is not None),
+                                  err_msg="set of written cache slots")
+    tol = TOL[s.kv]
+    hd = s.head_dim
+    errs = []
+    for b, h in samples:
+        o, K, V, written, probe = oracle_head(wl, b, h, probe_idx)
+        g = gpu_head(cache, b, h)
+        errs.append(assert_close(g[written, 0], K[written], tol, f"cache K (b={b}, h={h})"))
+        errs.append(assert_close(g[written, 1], V[written], tol, f"cache V (b={b}, h={h})"))
+        errs.append(assert_close(out[b][:, h * hd:(h + 1) * hd], o, tol, f"out (b={b}, h={h})"))
+        if exact_diag_tol is not None:  # FP8 cache against the unquantised oracle: the encoding's own error
+            oe = oracle_head(wl, b, h, exact=True)[0]
+            assert_close(out[b][:, h * hd:(h + 1) * hd], oe, exact_diag_tol, f"out vs unquantised (b={b}, h={h})")
+        if probe is not None:
+            pg = probe_gpu[b][:, :, h * hd:(h + 1) * hd]
+            errs.append(assert_close(pg[:, 0], probe[0], TOL[s.act], f"probe K (b={b}, h={h})"))
+            errs.append(assert_close(pg[:, 1], probe[1], TOL[s.act], f"probe V (b={b}, h={h})"))
+    return max(errs)

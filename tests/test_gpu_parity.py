@@ -21,7 +21,9 @@ def _check_step(wl, probe_idx=None):
     o_out, ocache, o_probe = G.run_oracle(wl, probe_idx)
     tol = G.TOL[wl.shape.kv]
     G.compare_cache(cache, ocache, tol)
-    G.assert_close(out.reshape(o_out.shape), o_out, tol if wl.shape.kv != "e4m3" else G.TOL["e4m3"], "attention out")
+    G.assert_close(out.reshape(o_out.shape), o_out, tol, "attention out")
+    if wl.shape.kv == "e4m3":  # diagnostic: against the unquantised oracle the e4m3 encoding itself shows
+        G.assert_close(out.reshape(o_out.shape), G.run_oracle(wl, probe_idx, exact=True)[0], 0.15, "out vs exact")
     if probe_idx is not None:
         G.assert_close(probe, o_probe, G.TOL[wl.shape.act], "probe K/V")
     return cache, out, probe, ocache, o_probe
@@ -60,6 +62,24 @@ def test_bf16_step_small(kw):
 
 def test_bf16_config2_full():
     _check_step(W.make(2))
+
+
+# ------------------------------------------------------------------------------ FP8
+def test_fp8_refresh_small():
+    # full-sequence K/V refresh into an e4m3 cache, then the block attends over it
+    wl = W.make(5, batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200)
+    _check_step(wl)
+
+
+def test_fp8_prefill_then_step_small():
+    wl = W.make(2, kv="e4m3", batch=2, d_model=256, head_dim=128, max_pos=400, block=40, gen_lo=300, fixed_lo=None)
+    _check_step(wl)
+
+
+def test_fp8_verify_small():
+    wl = W.make(4, kv="e4m3", batch=3, d_model=256, head_dim=128, max_pos=300, block=16, gen_lo=200, search=6,
+                tail_slots=8)
+    _check_step(wl)
 
 
 # ---------------------------------------------------------------------- Flash-Verify

@@ -363,3 +363,22 @@ def test_fp8_group_quantize_scale_and_zero_group():
     assert np.max(np.abs(deq - v)) <= 2 ** -4 * amax
     z, s0 = O.fp8_group_quantize(np.zeros(128))
     assert s0 == 1.0 and not np.any(z)
+
+
+def test_fp8_cache_stores_group_quantised_values():
+    # an e4m3 cache keeps, per (token, head) group, exactly the group quantiser's output
+    r = _rng(16)
+    c = O.OracleCache(1, 4, 0, 2, 8, kv="e4m3")
+    w = r.standard_normal((3 * 16, 16))
+    x = r.standard_normal((1, 2, 16))
+    O.write_rows(c, w, x, np.array([[1, 3]]), 1e4)
+    _, k, v = O.project_qkv(x[0], w, 2)
+    k = O.rope(k, np.array([1, 3]), 1e4)
+    for t, s in enumerate([1, 3]):
+        for h in range(2):
+            np.testing.assert_array_equal(c.K[0, s, h], O.fp8_group_quantize(k[t, h])[0])
+            np.testing.assert_array_equal(c.V[0, s, h], O.fp8_group_quantize(v[t, h])[0])
+            # every stored value is an e4m3 value times the group scale
+            scale = np.max(np.abs(v[t, h])) / 448.0
+            codes = c.V[0, s, h] / scale
+            np.testing.assert_allclose(O.e4m3_quantize(codes), codes, rtol=1e-12)

@@ -125,19 +125,21 @@ class Workload:
     def prefill_row(self, b: int, p: int) -> np.ndarray:
         return hidden_row(self.seed, _S_PREFILL, b, p, self.shape)
 
-    def probe_rows(self, idx: np.ndarray) -> np.ndarray:
+    def probe_rows(self, idx: np.ndarray, b0: int = 0) -> np.ndarray:
         """Current hidden states of tracked tokens: prefill row + 0.1 * N(0,1).
 
-        ``idx`` is ``[B][k]`` positions; returns ``[B][k][D]`` storage-rounded.
+        ``idx`` is ``[n][k]`` positions of sequences ``b0 .. b0+n-1``; returns
+        ``[n][k][D]`` storage-rounded.
         """
         B, k = idx.shape
         out = np.empty((B, k, self.shape.D), np.float32)
-        for b in range(B):
+        for i in range(B):
+            b = b0 + i
             for j in range(k):
-                p = int(idx[b, j])
+                p = int(idx[i, j])
                 base = _rng(self.seed, _S_PREFILL, b, p).standard_normal(self.shape.D, dtype=np.float32)
                 noise = _rng(self.seed, _S_NOISE, b, p).standard_normal(self.shape.D, dtype=np.float32)
-                out[b, j] = base + np.float32(0.1) * noise
+                out[i, j] = base + np.float32(0.1) * noise
         return _store(out, self.shape.act)
 
 
