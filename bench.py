@@ -35,7 +35,7 @@ L2_BYTES = 126 * 2 ** 20
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--config", type=int, default=3, choices=[2, 3])
@@ -63,57 +63,68 @@ def peaks():
 
 # ----------------------------------------------------------------------------- clocks
 class Clocks:
-    """Samples the SM clock and the clock-event reasons of one GPU through NVML every
-    2 ms on a background thread while the timed region runs (falls back to
-    ``nvidia-smi -lms 100`` when NVML is not importable)."""
+    """Samples the SM clock and the clock-event reasons of the GPU that runs the bench,
+    every 5 ms on a background thread while the timed region runs.  It reads the
+    driver's NVML library through ctypes (the device is found by its PCI bus id); when
+    that library cannot be opened it falls back to ``nvidia-smi -lms 50``, keeping only
+    samples stamped inside the timed window."""
 
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    NVML_CLOCK_SM = 1
 
     def __init__(self, torch_device):
+        import ctypes
         import threading
         self.samples, self.reason_bits, self.max_mhz = [], 0, None
         self.stop_evt = threading.Event()
         self.thread = None
         self.proc = None
+        self.t0 = time.time()
         try:
-            import pynvml as N
-            N.nvmlInit()
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            if nv.nvmlInit_v2() != 0:
+                raise OSError("nvmlInit_v2 failed")
             props = __import__("torch").cuda.get_device_properties(torch_device)
-            h = None
-            try:
-                bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0"
-                h = N.nvmlDeviceGetHandleByPciBusId(bus)
-            except Exception:
-                h = N.nvmlDeviceGetHandleByIndex(0)
-            self.N, self.h = N, h
-            self.max_mhz = N.nvmlDeviceGetMaxClockInfo(h, N.NVML_CLOCK_SM)
+            bus = f"{props.pci_domain_id:08X}:{props.pci_bus_id:02X}:{props.pci_device_id:02X}.0".encode()
+            h = ctypes.c_void_p()
+            if nv.nvmlDeviceGetHandleByPciBusId_v2(ctypes.c_char_p(bus), ctypes.byref(h)) != 0:
+                raise OSError(f"no NVML device at {bus!r}")
+            mx = ctypes.c_uint()
+            if nv.nvmlDeviceGetMaxClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(mx)) != 0:
+                raise OSError("nvmlDeviceGetMaxClockInfo failed")
+            self.nv, self.h, self.max_mhz = nv, h, mx.value
             self.thread = threading.Thread(target=self._poll, daemon=True)
             self.thread.start()
-        except Exception:
-            self.N = None
+        except Exception as exc:  # no NVML library: sample with nvidia-smi instead
+            print(f"clock sampling: NVML unavailable ({exc!r}); using nvidia-smi", file=sys.stderr)
+            self.nv = None
             self.f = tempfile.NamedTemporaryFile("w+", suffix=".csv", delete=False)
             try:
                 self.proc = subprocess.Popen(
-                    ["nvidia-smi", "--query-gpu=clocks.sm,clocks.max.sm,clocks_event_reasons.active",
-                     "--format=csv,noheader,nounits", "-lms", "100"], stdout=self.f, stderr=subprocess.DEVNULL)
+                    ["nvidia-smi", f"--id={torch_device.index or 0}",
+                     "--query-gpu=timestamp,clocks.sm,clocks.max.sm,clocks_event_reasons.active",
+                     "--format=csv,noheader,nounits", "-lms", "50"], stdout=self.f, stderr=subprocess.DEVNULL)
+                time.sleep(0.5)
             except OSError:
                 self.proc = None
 
+    def start(self):
+        self.t0 = time.time()
+
     def _poll(self):
-        N, h = self.N, self.h
+        import ctypes
+        nv, h = self.nv, self.h
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
         while not self.stop_evt.is_set():
-            try:
-                self.samples.append(N.nvmlDeviceGetClockInfo(h, N.NVML_CLOCK_SM))
-                self.reason_bits |= int(N.nvmlDeviceGetCurrentClocksEventReasons(h))
-            except Exception:
-                try:
-                    self.reason_bits |= int(N.nvmlDeviceGetCurrentClocksThrottleReasons(h))
-                except Exception:
-                    pass
-            self.stop_evt.wait(0.002)
+            if nv.nvmlDeviceGetClockInfo(h, self.NVML_CLOCK_SM, ctypes.byref(clk)) == 0:
+                self.samples.append(clk.value)
+            if nv.nvmlDeviceGetCurrentClocksEventReasons(h, ctypes.byref(rs)) == 0:
+                self.reason_bits |= int(rs.value)
+            self.stop_evt.wait(0.005)
 
     def stop(self):
+        t1 = time.time()
         if self.thread is not None:
             self.stop_evt.set()
             self.thread.join()
@@ -121,25 +132,47 @@ class Clocks:
             if not self.samples:
                 return None
             return {"sm_mhz": statistics.median(self.samples), "sm_max_mhz": self.max_mhz, "reasons": reasons,
-                    "samples": len(self.samples), "source": "nvml, 2 ms polling during the timed region"}
+                    "samples": len(self.samples), "source": "NVML, 5 ms polling during the timed region"}
         if self.proc is None:
             return None
+        time.sleep(0.1)
         self.proc.terminate()
         self.proc.wait()
-        rows = [ln.split(",") for ln in open(self.f.name) if ln.count(",") == 2]
+        import datetime
+        sm, bits, mx = [], 0, None
+        for ln in open(self.f.name):
+            r = [x.strip() for x in ln.split(",")]
+            if len(r) != 4:
+                continue
+            try:
+                ts = datetime.datetime.strptime(r[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                if not (self.t0 <= ts <= t1):
+                    continue
+                sm.append(float(r[1]))
+                mx = float(r[2])
+                bits |= int(r[3], 16)
+            except ValueError:
+                continue
         os.unlink(self.f.name)
-        sm = [float(r[0]) for r in rows if r[0].strip().replace(".", "").isdigit()]
         if not sm:
             return None
-        bits = 0
-        for r in rows:
-            try:
-                bits |= int(r[2].strip(), 16)
-            except ValueError:
-                pass
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][1]),
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx,
                 "reasons": sorted(v for k, v in self.REASONS.items() if bits & k), "samples": len(sm),
-                "source": "nvidia-smi -lms 100"}
+                "source": "nvidia-smi -lms 50 inside the timed window"}
+
+
+# ------------------------------------------------------------------- job throughput
+def job_rate(local_ms: float, steps: int, world: int, device=None):
+    """Whole-job throughput from each rank's timed total: the slowest rank's time
+    (max over ranks) covers the steps of all ranks.  Returns (ms_per_step, steps/s)."""
+    total_ms = float(local_ms)
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    return total_ms / steps, world * steps / (total_ms / 1e3)
 
 
 # --------------------------------------------------------------------------- workload
@@ -220,6 +253,8 @@ def run_ours(args, rank, world, local):
     if world > 1:
         torch.distributed.barrier()
     torch.cuda.synchronize(dev)
+    if clocks:
+        clocks.start()
     evs = []
     t_wall = time.perf_counter()
     for _ in range(args.steps):
@@ -240,13 +275,7 @@ def run_ours(args, rank, world, local):
         per["project"].append(ev[1].elapsed_time(ev[2]))
         per["attend"].append(ev[2].elapsed_time(ev[3]))
         per["drift"].append(ev[3].elapsed_time(ev[4]))
-    total_ms = sum(per["step"])
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms = float(t.item())
-    ms_per_step = total_ms / args.steps
-    value = world * args.steps / (total_ms / 1e3)
+    ms_per_step, value = job_rate(sum(per["step"]), args.steps, world, dev)
 
     # ---- end to end through the C ABI with host buffers (copies inside the timed region)
     e2e = None
@@ -286,12 +315,8 @@ def run_ours(args, rank, world, local):
             e1.record(stream)
             e1.synchronize()
             ts.append(e0.elapsed_time(e1))
-        e2e_ms = sum(ts)
-        if world > 1:
-            t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-            torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-            e2e_ms = float(t.item())
-        e2e = {"value": world * args.steps / (e2e_ms / 1e3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        _, e2e_value = job_rate(sum(ts), args.steps, world, dev)
+        e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h}
 
     rc, bits = cache.status()

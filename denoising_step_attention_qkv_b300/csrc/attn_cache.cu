@@ -7,22 +7,27 @@
 // Flash-Verify draft and mask views must not see each other.
 //
 // Design (sm_103a).  A work unit is (sequence b, head h, chunk of <= NQ query rows,
-// key split).  Per 128-key tile the MMA warp computes S^T = K Q^T with tcgen05
-// (M = 128 keys, N = NQ queries, K = hd = 128) into TMEM, so each softmax thread owns
-// one key and holds that key's scores for every query.  Column (per-query) maxima and
-// sums are warp reduce-scatters plus a 4-warp exchange in shared memory; the online
-// softmax runs in fp32 with exp2.  Each thread writes its key's probabilities as bf16
-// into P^T (K-major, 128-byte swizzle) and the MMA warp computes O^T = V^T P^T
-// (M = hd, N = NQ, V read MN-major straight from the TMA-staged cache tile) into a
-// second TMEM buffer; the same threads fold it into fp32 register accumulators with
-// the running rescale.  K/V tiles stream through TMA rings (3 K + 2 V stages of 32 KB);
-// S, P and O are double-buffered so the loads, both MMAs and the softmax overlap.
-// With few units, keys are split across CTAs and a second kernel merges the partial
-// (O, m, l) states.
+// key split) and is processed by one persistent CTA.  Per 128-key tile the MMA warp
+// computes S^T = K Q^T with tcgen05 (M = 128 keys, N = NQ queries, K = hd = 128) into
+// TMEM, so a softmax thread owns one key and holds that key's scores for every query;
+// per-query maxima and sums are warp reduce-scatters plus a 4-warp exchange in shared
+// memory, and the online softmax runs in fp32 with exp2.  The thread writes its key's
+// probabilities as bf16 into P^T (K-major, 128-byte swizzle) and the MMA warp computes
+// O^T = V^T P^T (M = hd, N = NQ, V read MN-major straight from the TMA-staged cache
+// tile) into TMEM, which the same threads fold into fp32 register accumulators.
+//
+// The softmax of one tile is a chain of dependent steps, kept short: per-query maxima
+// come from redux.sync (one instruction per query and warp) and a 4-warp exchange;
+// the row sums are kept per thread (each thread rescales its own partial sums) and
+// reduced once per unit; exponentials use ex2.approx and two probabilities share one
+// packed bf16 conversion.  S, P and O are double-buffered so the loads, both MMAs and
+// the softmax overlap; K/V tiles stream through TMA rings and Q is double-buffered, so
+// the next unit's loads start while this one finishes.  With few units, keys are
+// split across CTAs and a second kernel merges the partial (O, m, l) states.
 //
 // FP8-e4m3 cache ("LaCache ...", Methodology 2: per-group FP8; one group here = one
 // head of one token, K or V, with an fp32 scale): TMA stages the e4m3 tiles (half the
-// bytes of bf16) in a 3-deep ring and four converter warps widen them to bf16 in the
+// bytes of bf16) in a 2- or 3-deep ring and four converter warps widen them to bf16 in the
 // MMA operand layout (exact: every e4m3 value is a bf16 value).  The K scale of a key
 // multiplies that key's scores in fp32, and the V scale multiplies its probabilities
 // before they are rounded for the PV MMA, so dequantisation adds no rounding step.
@@ -37,40 +42,40 @@ namespace {
 
 constexpr uint32_t kTileBytes = kKeyTile * kHd * 2;  // 32 KB (bf16 K or V tile)
 constexpr uint32_t kTile8Bytes = kKeyTile * kHd;     // 16 KB (e4m3 tile)
-constexpr uint32_t kQBytes = kQChunk * kHd * 2;      // 16 KB
-constexpr uint32_t kPBytes = kQChunk * kKeyTile * 2; // 16 KB
 constexpr int kMaxBitmapWords = 512;                 // MASK-slot bitmap: max_pos <= 16384
 
-// Per cache type: MMA-operand rings for K and V, e4m3 staging rings, thread count.
-template <bool FP8>
+// Per (query columns, cache type): MMA-operand rings for K and V, e4m3 staging rings,
+// thread count.
+template <int NQ, bool FP8>
 struct Cfg {
-  static constexpr int KST = FP8 ? 1 : 3;
+  static constexpr int KST = FP8 ? 1 : (NQ == 32 ? 3 : 2);
   static constexpr int VST = FP8 ? 1 : 2;
-  static constexpr int SST = FP8 ? 3 : 1;
+  static constexpr int SST = FP8 ? (NQ == 32 ? 3 : 2) : 1;
   static constexpr uint32_t kStageBytes = FP8 ? kTile8Bytes : 1024;
-  static constexpr int kThreads = FP8 ? 320 : 192;  // + 4 converter warps for FP8
+  static constexpr uint32_t kQBytes = NQ * kHd * 2;       // one Q chunk (two 64-column boxes)
+  static constexpr uint32_t kPBytes = NQ * kKeyTile * 2;  // one P^T tile (two 64-key halves)
+  static constexpr int kThreads = 64 + 128 + (FP8 ? 128 : 0);
 };
 
-template <bool FP8>
+template <int NQ, bool FP8>
 struct Smem {
-  using C = Cfg<FP8>;
+  using C = Cfg<NQ, FP8>;
   // all operand tiles 1024-byte aligned
-  uint8_t q[kQBytes];
+  uint8_t q[2][C::kQBytes];
   uint8_t k[C::KST][kTileBytes];
   uint8_t v[C::VST][kTileBytes];
-  uint8_t p[2][kPBytes];
+  uint8_t p[2][C::kPBytes];
   uint8_t sk[C::SST][C::kStageBytes];  // e4m3 staging (FP8 only)
   uint8_t sv[C::SST][C::kStageBytes];
-  float red_max[4][kQChunk];
-  float red_sum[2][4][kQChunk];
-  float m_run[kQChunk];
-  float l_run[kQChunk];
-  float m_use[kQChunk];
-  float alpha[2][kQChunk];
+  float red[4][NQ];  // per-warp column maxima (per tile) / partial sums (per unit)
+  float m_run[NQ];
+  float m_use[NQ];
+  float alpha[2][NQ];
+  float l_fin[NQ];
   uint32_t mask_bits[kMaxBitmapWords];
   uint32_t draft_qmask[2];
   int n_draft;
-  uint64_t q_full, q_empty;
+  uint64_t q_full[2], q_empty[2];
   uint64_t k_full[C::KST], k_empty[C::KST];
   uint64_t v_full[C::VST], v_empty[C::VST];
   uint64_t sk_full[C::SST], sk_empty[C::SST];
@@ -82,8 +87,10 @@ struct Smem {
   uint32_t tmem_base;
   int abort_flag;
 };
-static_assert(sizeof(Smem<false>) + 1024 <= 232448, "shared memory budget (bf16)");
-static_assert(sizeof(Smem<true>) + 1024 <= 232448, "shared memory budget (e4m3)");
+static_assert(sizeof(Smem<32, false>) + 1024 <= 232448, "shared memory budget (bf16, 32 queries)");
+static_assert(sizeof(Smem<64, false>) + 1024 <= 232448, "shared memory budget (bf16, 64 queries)");
+static_assert(sizeof(Smem<32, true>) + 1024 <= 232448, "shared memory budget (e4m3, 32 queries)");
+static_assert(sizeof(Smem<64, true>) + 1024 <= 232448, "shared memory budget (e4m3, 64 queries)");
 
 // Widen 16 e4m3 codes to 16 bf16 values (exact).
 DEVI void widen16(const uint4 in, uint4& lo, uint4& hi) {
@@ -117,12 +124,41 @@ DEVI Unit decode_unit(const AttnParams& p, int u) {
   return x;
 }
 
-DEVI void named_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+// Barrier among the four softmax warps.
+DEVI void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+// Maximum of v over the 32 lanes of the warp, in every lane.
+DEVI float warp_max(float v) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+  return r;
+}
+
+// 2^x (PTX ex2.approx.ftz.f32: relative error about 2^-22, far below the bf16 rounding
+// that every probability goes through; 2^-inf = +0).
+DEVI float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// Round (a, b) to bf16 and store a at byte address pa, b at pb (shared memory).
+DEVI void st_bf16_pair(uint32_t pa, uint32_t pb, float a, float b) {
+  uint32_t packed;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed) : "f"(b), "f"(a));  // hi = b, lo = a
+  asm volatile(
+      "{\n.reg .b16 lo, hi;\n"
+      "mov.b32 {lo, hi}, %2;\n"
+      "st.shared.b16 [%0], lo;\n"
+      "st.shared.b16 [%1], hi;\n}" ::"r"(pa), "r"(pb), "r"(packed)
+      : "memory");
+}
 
 // Reduce 32 per-lane values per column across the warp; afterwards lane i holds the
-// reduction of column i.  MAX selects max, otherwise sum.
+// reduction of column i.  MAX selects max, otherwise sum.  Each step halves the columns
+// a lane keeps and exchanges the other half with the lane whose id differs in that bit.
 template <bool MAX>
-DEVI float reduce_scatter32(float (&v)[32], int lane) {
+DEVI float reduce_scatter32(float* v, int lane) {
 #pragma unroll
   for (int w = 16; w >= 1; w >>= 1) {
     const bool upper = (lane & w) != 0;
@@ -138,22 +174,25 @@ DEVI float reduce_scatter32(float (&v)[32], int lane) {
 }
 
 template <int NQ, bool FP8>
-__global__ void __launch_bounds__(Cfg<FP8>::kThreads, 1)
+__global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     attn_cache_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
                   const AttnParams p) {
-  using C = Cfg<FP8>;
+  using C = Cfg<NQ, FP8>;
   constexpr int KST = C::KST, VST = C::VST, SST = C::SST;
   extern __shared__ uint8_t smem_raw[];
-  Smem<FP8>& S = *reinterpret_cast<Smem<FP8>*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
+  Smem<NQ, FP8>& S =
+      *reinterpret_cast<Smem<NQ, FP8>*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
   volatile int* abort_flag = &S.abort_flag;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   constexpr uint32_t kTmemCols = 4 * NQ;  // S[2] then O[2]
-  constexpr uint32_t kQBox = NQ * 128;    // bytes of one 64-column Q box / one P region
+  constexpr uint32_t kQBox = NQ * 128;    // bytes of one 64-column Q box / one 64-key P half
 
   if (threadIdx.x == 0) {
-    mbar_init(&S.q_full, 1);
-    mbar_init(&S.q_empty, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&S.q_full[i], 1);
+      mbar_init(&S.q_empty[i], 1);
+    }
     // bf16: operand tiles are filled by TMA (one arrival + bytes); e4m3: by 4 converter warps
     for (int i = 0; i < KST; ++i) { mbar_init(&S.k_full[i], FP8 ? 4 : 1); mbar_init(&S.k_empty[i], 1); }
     for (int i = 0; i < VST; ++i) { mbar_init(&S.v_full[i], FP8 ? 4 : 1); mbar_init(&S.v_empty[i], 1); }
@@ -190,17 +229,17 @@ __global__ void __launch_bounds__(Cfg<FP8>::kThreads, 1)
     // ------------------------------------------------------------------ TMA producer
     const uint64_t pol_stream = policy_evict_first();
     const uint64_t pol_q = policy_evict_last();
-    int ks = 0, vs = 0;
-    uint32_t kph = 0, vph = 0, qph = 0;
+    int ks = 0, vs = 0, uu = 0;
+    uint32_t kph = 0, vph = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uu) {
       const Unit x = decode_unit(p, u);
-      if (!mbar_wait(&S.q_empty, qph ^ 1u, abort_flag)) { ok = false; break; }
-      qph ^= 1u;
-      mbar_arrive_expect_tx(&S.q_full, 2 * kQBox);
+      const int qb = uu & 1;
+      if (!mbar_wait(&S.q_empty[qb], ((uu >> 1) & 1) ^ 1u, abort_flag)) { ok = false; break; }
+      mbar_arrive_expect_tx(&S.q_full[qb], 2 * kQBox);
       const int qrow = x.b * p.n_tok + x.qc * kQChunk;
-      tma_load_2d(S.q, &tm_q, &S.q_full, x.h * kHd, qrow, pol_q);
-      tma_load_2d(S.q + kQBox, &tm_q, &S.q_full, x.h * kHd + 64, qrow, pol_q);
+      tma_load_2d(S.q[qb], &tm_q, &S.q_full[qb], x.h * kHd, qrow, pol_q);
+      tma_load_2d(S.q[qb] + kQBox, &tm_q, &S.q_full[qb], x.h * kHd + 64, qrow, pol_q);
       const int slot0 = x.b * p.slots;
       for (int t = x.t0; t < x.t1; ++t) {
         const int key0 = slot0 + t * kKeyTile;
@@ -231,9 +270,12 @@ __global__ void __launch_bounds__(Cfg<FP8>::kThreads, 1)
       *abort_flag = 1;
       atomicOr(p.status, DLLM_DEV_TIMEOUT);
     }
-    // let every copy issued here land before the CTA can exit
+    // let every copy issued here land before the CTA can exit: on each ring slot, wait
+    // for the most recent phase armed on it (a slot never armed passes at once)
     volatile int never = 0;
-    mbar_wait(&S.q_full, qph ^ 1u, &never);
+    const int qn = uu & 1;
+    const uint32_t qph = (uu >> 1) & 1u;
+    for (int i = 0; i < 2; ++i) mbar_wait(&S.q_full[i], (i < qn) ? qph : (qph ^ 1u), &never);
     if constexpr (FP8) {
       for (int i = 0; i < SST; ++i) {
         mbar_wait(&S.sk_full[i], (i < ks) ? kph : (kph ^ 1u), &never);
@@ -245,13 +287,14 @@ __global__ void __launch_bounds__(Cfg<FP8>::kThreads, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------------ MMA issuer
+    // Per tile: S(t) = K(t) Q^T into S[t & 1], then P V of the previous tile into
+    // O[(t - 1) & 1], so the softmax of tile t - 1 overlaps the S MMA of tile t.
     constexpr uint32_t idesc_s = idesc_bf16(128, NQ, false, false);
     constexpr uint32_t idesc_o = idesc_bf16(128, NQ, true, false);
-    int ks = 0, vs = 0;
-    uint32_t kph = 0, vph = 0, qph = 0;
+    int ks = 0, vs = 0, uu = 0;
+    uint32_t kph = 0, vph = 0;
     uint32_t s_cnt = 0, pv_cnt = 0;
     bool ok = true;
-    const uint32_t q0 = smem_u32(S.q);
 
     auto issue_pv = [&]() -> bool {
       const uint32_t pb = pv_cnt & 1u, pph = (pv_cnt >> 1) & 1u;
@@ -276,11 +319,12 @@ __global__ void __launch_bounds__(Cfg<FP8>::kThreads, 1)
       return true;
     };
 
-    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uu) {
       const Unit x = decode_unit(p, u);
-      if (!mbar_wait(&S.q_full, qph, abort_flag)) { ok = false; break; }
-      qph ^= 1u;
+      const int qb = uu & 1;
+      if (!mbar_wait(&S.q_full[qb], (uu >> 1) & 1u, abort_flag)) { ok = false; break; }
       tc_fence_after();
+      const uint32_t q0 = smem_u32(S.q[qb]);
       for (int t = x.t0; t < x.t1 && ok; ++t) {
         const uint32_t sb = s_cnt & 1u, sph = (s_cnt >> 1) & 1u;
         if (!mbar_wait(&S.s_free[sb], sph ^ 1u, abort_flag)) { ok = false; break; }
@@ -301,7 +345,7 @@ __global__ void __launch_bounds__(Cfg<FP8>::kThreads, 1)
         if (t > x.t0 && !issue_pv()) { ok = false; break; }
       }
       if (!ok) break;
-      tc_commit(&S.q_empty);
+      tc_commit(&S.q_empty[qb]);
       if (x.t1 > x.t0 && !issue_pv()) { ok = false; break; }
     }
     if (!ok) {
@@ -313,30 +357,36 @@ __global__ void __launch_bounds__(Cfg<FP8>::kThreads, 1)
     mbar_wait(&S.drain, 0, &never);
   } else if (warp >= 2 && warp < 6) {
     // ------------------------------------------------------------------ softmax warps
+    // Warp w reads TMEM lanes 32 * (w % 4) .., so thread r owns key r of the S^T tile and
+    // hd index r of the O^T tile.  Every warp runs the same sequence of barriers; a
+    // failed wait is recorded and the sequence continues, so no warp is left waiting at
+    // a barrier.
     const int quarter = warp & 3;
-    const int r = quarter * 32 + lane;  // key within the tile (S^T) / hd index (O^T)
+    const int r = quarter * 32 + lane;
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const bool has_view = p.view != nullptr;
-    constexpr bool fp8 = FP8;
     uint32_t s_cnt = 0, pv_cnt = 0;
     int vs = 0;  // V ring position, mirrors the producer
     uint32_t vph = 0;
     bool ok = true;
+    auto wait = [&](uint64_t* bar, uint32_t par) {
+      if (!mbar_wait(bar, par, abort_flag)) {
+        ok = false;
+        *abort_flag = 1;
+      }
+    };
     const int mask_words = (p.max_pos + 31) >> 5;
 
-    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
       const Unit x = decode_unit(p, u);
       const int row0 = x.b * p.n_tok;  // first row of the sequence
       const int nrows = min(kQChunk, p.n_tok - x.qc * kQChunk);  // valid columns of this chunk
-      // ---- per-unit set-up: running state and Flash-Verify tags
-      if (r < NQ) {
-        S.m_run[r] = -INFINITY;
-        S.l_run[r] = 0.0f;
-      }
+      // ---- per-unit set-up: running max and Flash-Verify tags
+      if (r < NQ) S.m_run[r] = -INFINITY;
       if (has_view) {
         for (int w = r; w < mask_words; w += 128) S.mask_bits[w] = 0u;
         if (r == 0) S.n_draft = 0;
-        named_sync();
+        softmax_sync();
         int my_draft = 0;
         for (int t = r; t < p.n_tok; t += 128) {
           const int v = p.view[row0 + t];
@@ -348,34 +398,32 @@ __global__ void __launch_bounds__(Cfg<FP8>::kThreads, 1)
           }
         }
         if (my_draft) atomicAdd(&S.n_draft, my_draft);
-        if (quarter < 2) {
-          const int q = r;  // quarters 0,1 cover columns 0..63
-          const bool is_draft = q < nrows && p.view[row0 + x.qc * kQChunk + q] == DLLM_VIEW_DRAFT;
+        if (quarter < 2) {  // quarters 0 and 1 tag columns 0..63
+          const bool is_draft = r < nrows && p.view[row0 + x.qc * kQChunk + r] == DLLM_VIEW_DRAFT;
           const uint32_t bal = __ballot_sync(0xffffffffu, is_draft);
           if (lane == 0) S.draft_qmask[quarter] = bal;
         }
-        named_sync();
+        softmax_sync();
       }
       const int n_draft = has_view ? min(S.n_draft, p.tail) : 0;
       const uint64_t dmask = has_view ? (static_cast<uint64_t>(S.draft_qmask[1]) << 32) | S.draft_qmask[0] : 0ull;
-      float o_acc[NQ];
+      float o_acc[NQ];  // O^T row r (hd index r) for every query, relative to the running max
+      float l_part[NQ];  // this thread's key's share of each query's row sum
 #pragma unroll
-      for (int q = 0; q < NQ; ++q) o_acc[q] = 0.0f;
+      for (int q = 0; q < NQ; ++q) {
+        o_acc[q] = 0.0f;
+        l_part[q] = 0.0f;
+      }
 
       for (int t = x.t0; t < x.t1; ++t) {
         const uint32_t sb = s_cnt & 1u, sph = (s_cnt >> 1) & 1u;
-        const uint32_t tp = t & 1;  // parity slot for alpha / red_sum
+        const uint32_t tp = t & 1;  // parity slot for alpha
         // ---- A: scores of this thread's key for every query
-        if (!mbar_wait(&S.s_full[sb], sph, abort_flag)) { ok = false; break; }
+        wait(&S.s_full[sb], sph);
         tc_fence_after();
         float s[NQ];
 #pragma unroll
-        for (int c = 0; c < NQ; c += 32) {
-          float tmp[32];
-          tmem_ld32(tmem + lane_base + sb * NQ + c, tmp);
-#pragma unroll
-          for (int i = 0; i < 32; ++i) s[c + i] = tmp[i];
-        }
+        for (int c = 0; c < NQ; c += 32) tmem_ld32(tmem + lane_base + sb * NQ + c, *reinterpret_cast<float(*)[32]>(s + c));
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.s_free[sb]);
@@ -391,93 +439,103 @@ __global__ void __launch_bounds__(Cfg<FP8>::kThreads, 1)
           vis = (j < p.max_pos + n_draft) ? dmask : 0ull;
         }
         float k_scale = 1.0f, v_scale = 1.0f;
-        if (fp8 && vis) {
+        if (FP8 && vis) {
           const size_t srow = (static_cast<size_t>(x.b) * p.slots + j) * 2;
           k_scale = __ldg(p.kv_scale + srow * p.H + x.h);
           v_scale = __ldg(p.kv_scale + (srow + 1) * p.H + x.h);
         }
         const float sc = p.scale_log2 * k_scale;
+        if (vis == ~0ull) {
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) s[q] = ((vis >> q) & 1ull) ? s[q] * sc : -INFINITY;
-
-        // column maxima: warp reduce-scatter, then 4-warp exchange
+          for (int q = 0; q < NQ; ++q) s[q] *= sc;
+        } else {
 #pragma unroll
-        for (int c = 0; c < NQ; c += 32) {
-          float tmp[32];
-#pragma unroll
-          for (int i = 0; i < 32; ++i) tmp[i] = s[c + i];
-          S.red_max[quarter][c + lane] = reduce_scatter32<true>(tmp, lane);
+          for (int q = 0; q < NQ; ++q) s[q] = ((vis >> q) & 1ull) ? s[q] * sc : -INFINITY;
         }
-        named_sync();
-        // ---- B: column owners update running max / sum
+
+        // column maxima: one redux per query over the warp, then over the 4 warps
+        {
+          float mx[NQ];
+#pragma unroll
+          for (int q = 0; q < NQ; ++q) mx[q] = warp_max(s[q]);
+          if (lane == 0) {
+            float4* dst = reinterpret_cast<float4*>(S.red[quarter]);
+#pragma unroll
+            for (int q = 0; q < NQ; q += 4) dst[q / 4] = make_float4(mx[q], mx[q + 1], mx[q + 2], mx[q + 3]);
+          }
+        }
+        softmax_sync();
+        // ---- B: column owners update the running max and the rescale factor
         if (r < NQ) {
-          const float mt = fmaxf(fmaxf(S.red_max[0][r], S.red_max[1][r]), fmaxf(S.red_max[2][r], S.red_max[3][r]));
+          const float mt = fmaxf(fmaxf(S.red[0][r], S.red[1][r]), fmaxf(S.red[2][r], S.red[3][r]));
           const float m_old = S.m_run[r];
           const float m_new = fmaxf(m_old, mt);
           const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
-          const float a = exp2f(m_old - m_use);
-          if (t > x.t0) {
-            const uint32_t pp = tp ^ 1u;
-            const float ps = S.red_sum[pp][0][r] + S.red_sum[pp][1][r] + S.red_sum[pp][2][r] + S.red_sum[pp][3][r];
-            S.l_run[r] = S.l_run[r] * S.alpha[pp][r] + ps;
-          }
           S.m_run[r] = m_new;
           S.m_use[r] = m_use;
-          S.alpha[tp][r] = a;
+          S.alpha[tp][r] = fast_exp2(m_old - m_use);
         }
-        named_sync();
-        // ---- C: probabilities -> P^T (bf16, swizzled) and their column sums
+        softmax_sync();
+        // ---- C: probabilities -> P^T (bf16, swizzled); this thread's partial row sums
         {
           // Slots past the regular region that no query sees may hold anything (stale
           // draft views, the next sequence, never-written memory).  Their P is 0, but
           // 0 * NaN would still poison O, so their V rows are zeroed before the PV MMA.
           if (!FP8 && (t + 1) * kKeyTile > p.max_pos && vis == 0ull && j >= p.max_pos) {
-            if (!mbar_wait(&S.v_full[vs], vph, abort_flag)) { ok = false; break; }
-            uint4* row0 = reinterpret_cast<uint4*>(S.v[vs] + r * 128);
-            uint4* row1 = reinterpret_cast<uint4*>(S.v[vs] + kTileBytes / 2 + r * 128);
+            wait(&S.v_full[vs], vph);
+            uint4* row0v = reinterpret_cast<uint4*>(S.v[vs] + r * 128);
+            uint4* row1v = reinterpret_cast<uint4*>(S.v[vs] + kTileBytes / 2 + r * 128);
 #pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              row0[i] = make_uint4(0u, 0u, 0u, 0u);
-              row1[i] = make_uint4(0u, 0u, 0u, 0u);
+            for (int k = 0; k < 8; ++k) {
+              row0v[k] = make_uint4(0u, 0u, 0u, 0u);
+              row1v[k] = make_uint4(0u, 0u, 0u, 0u);
             }
           }
           if (++vs == VST) { vs = 0; vph ^= 1u; }
           const uint32_t pb = pv_cnt & 1u, pph = (pv_cnt >> 1) & 1u;
-          // pv_cnt here counts tiles whose P has been produced; the PV that reads this
-          // buffer two tiles ago must be done
-          if (!mbar_wait(&S.p_empty[pb], pph ^ 1u, abort_flag)) { ok = false; break; }
-          uint8_t* pbuf = S.p[pb] + (r >> 6) * kQBox;
+          // the P V MMA that read this buffer two tiles ago must be done
+          wait(&S.p_empty[pb], pph ^ 1u);
+          const uint32_t pbase = smem_u32(S.p[pb] + (r >> 6) * kQBox);
           const uint32_t byte = (r & 63) * 2;
+          const float4* mu4 = reinterpret_cast<const float4*>(S.m_use);
+          const float4* al4 = reinterpret_cast<const float4*>(S.alpha[tp]);
 #pragma unroll
-          for (int q = 0; q < NQ; ++q) {
-            const float e = exp2f(s[q] - S.m_use[q]);
-            s[q] = e;
-            const __nv_bfloat16 hv = __float2bfloat16_rn(e * v_scale);
-            *reinterpret_cast<__nv_bfloat16*>(pbuf + sw128_offset(q, byte)) = hv;
+          for (int q = 0; q < NQ; q += 4) {
+            const float4 mu = mu4[q / 4];
+            const float4 al = al4[q / 4];
+            const float e0 = fast_exp2(s[q] - mu.x), e1 = fast_exp2(s[q + 1] - mu.y);
+            const float e2 = fast_exp2(s[q + 2] - mu.z), e3 = fast_exp2(s[q + 3] - mu.w);
+            l_part[q] = l_part[q] * al.x + e0;
+            l_part[q + 1] = l_part[q + 1] * al.y + e1;
+            l_part[q + 2] = l_part[q + 2] * al.z + e2;
+            l_part[q + 3] = l_part[q + 3] * al.w + e3;
+            st_bf16_pair(pbase + sw128_offset(q, byte), pbase + sw128_offset(q + 1, byte), e0 * v_scale,
+                         e1 * v_scale);
+            st_bf16_pair(pbase + sw128_offset(q + 2, byte), pbase + sw128_offset(q + 3, byte), e2 * v_scale,
+                         e3 * v_scale);
           }
           fence_proxy_async_smem();
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.p_full[pb]);
-#pragma unroll
-          for (int c = 0; c < NQ; c += 32) {
-            float tmp[32];
-#pragma unroll
-            for (int i = 0; i < 32; ++i) tmp[i] = s[c + i];
-            S.red_sum[tp][quarter][c + lane] = reduce_scatter32<false>(tmp, lane);
-          }
         }
         // ---- D: fold the previous tile's P V into the accumulators
         if (t > x.t0) {
           const uint32_t ob = (pv_cnt - 1) & 1u, oph = ((pv_cnt - 1) >> 1) & 1u;
-          if (!mbar_wait(&S.o_full[ob], oph, abort_flag)) { ok = false; break; }
+          wait(&S.o_full[ob], oph);
           tc_fence_after();
-          const float* al = S.alpha[tp ^ 1u];
+          const float4* al4 = reinterpret_cast<const float4*>(S.alpha[tp ^ 1u]);
 #pragma unroll
           for (int c = 0; c < NQ; c += 32) {
             float tmp[32];
             tmem_ld32(tmem + lane_base + 2 * NQ + ob * NQ + c, tmp);
 #pragma unroll
-            for (int i = 0; i < 32; ++i) o_acc[c + i] = o_acc[c + i] * al[c + i] + tmp[i];
+            for (int i = 0; i < 32; i += 4) {
+              const float4 al = al4[(c + i) / 4];
+              o_acc[c + i] = o_acc[c + i] * al.x + tmp[i];
+              o_acc[c + i + 1] = o_acc[c + i + 1] * al.y + tmp[i + 1];
+              o_acc[c + i + 2] = o_acc[c + i + 2] * al.z + tmp[i + 2];
+              o_acc[c + i + 3] = o_acc[c + i + 3] * al.w + tmp[i + 3];
+            }
           }
           tc_fence_before();
           __syncwarp();
@@ -485,37 +543,41 @@ __global__ void __launch_bounds__(Cfg<FP8>::kThreads, 1)
         }
         ++pv_cnt;
       }
-      if (!ok) break;
-      // ---- unit end: last tile's PV, final sums, output
+      // ---- unit end: last tile's P V, the row sums, output
       if (x.t1 > x.t0) {
         const uint32_t ob = (pv_cnt - 1) & 1u, oph = ((pv_cnt - 1) >> 1) & 1u;
-        if (!mbar_wait(&S.o_full[ob], oph, abort_flag)) { ok = false; break; }
+        wait(&S.o_full[ob], oph);
         tc_fence_after();
-        const float* al = S.alpha[(x.t1 - 1) & 1];
+        const float4* al4 = reinterpret_cast<const float4*>(S.alpha[(x.t1 - 1) & 1]);
 #pragma unroll
         for (int c = 0; c < NQ; c += 32) {
           float tmp[32];
           tmem_ld32(tmem + lane_base + 2 * NQ + ob * NQ + c, tmp);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o_acc[c + i] = o_acc[c + i] * al[c + i] + tmp[i];
+          for (int i = 0; i < 32; i += 4) {
+            const float4 al = al4[(c + i) / 4];
+            o_acc[c + i] = o_acc[c + i] * al.x + tmp[i];
+            o_acc[c + i + 1] = o_acc[c + i + 1] * al.y + tmp[i + 1];
+            o_acc[c + i + 2] = o_acc[c + i + 2] * al.z + tmp[i + 2];
+            o_acc[c + i + 3] = o_acc[c + i + 3] * al.w + tmp[i + 3];
+          }
         }
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.o_free[ob]);
       }
-      named_sync();
-      if (r < NQ && x.t1 > x.t0) {
-        const uint32_t pp = (x.t1 - 1) & 1;
-        const float ps = S.red_sum[pp][0][r] + S.red_sum[pp][1][r] + S.red_sum[pp][2][r] + S.red_sum[pp][3][r];
-        S.l_run[r] = S.l_run[r] * S.alpha[pp][r] + ps;
-      }
-      named_sync();
+      // row sums: reduce the per-key partial sums over the 128 threads
+#pragma unroll
+      for (int c = 0; c < NQ; c += 32) S.red[quarter][c + lane] = reduce_scatter32<false>(l_part + c, lane);
+      softmax_sync();
+      if (r < NQ) S.l_fin[r] = S.red[0][r] + S.red[1][r] + S.red[2][r] + S.red[3][r];
+      softmax_sync();
       if (p.n_splits == 1) {
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
-          if (q < nrows) {
-            const float l = S.l_run[q];
+          if (q < nrows && ok) {
+            const float l = S.l_fin[q];
             const float o = l > 0.0f ? o_acc[q] / l : 0.0f;
             out[static_cast<size_t>(row0 + x.qc * kQChunk + q) * p.D + x.h * kHd + r] = __float2bfloat16_rn(o);
           }
@@ -527,10 +589,10 @@ __global__ void __launch_bounds__(Cfg<FP8>::kThreads, 1)
         if (r < NQ) {
           float* wml = p.ws + static_cast<size_t>(p.units) * kQChunk * kHd + (static_cast<size_t>(u) * kQChunk + r) * 2;
           wml[0] = S.m_run[r];
-          wml[1] = S.l_run[r];
+          wml[1] = S.l_fin[r];
         }
       }
-      named_sync();  // the next unit's set-up rewrites m_run / l_run / tags
+      softmax_sync();  // the next unit's set-up rewrites the running max, sums and tags
     }
     if (!ok) {
       *abort_flag = 1;
@@ -557,8 +619,8 @@ __global__ void __launch_bounds__(Cfg<FP8>::kThreads, 1)
         const int j = t * kKeyTile + r;
         const uint32_t sw = static_cast<uint32_t>(r & 7);
         // K
-        if (!mbar_wait(&S.sk_full[ss], sph, abort_flag)) { ok = false; break; }
-        if (!mbar_wait(&S.k_empty[ko], kph ^ 1u, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_warp(&S.sk_full[ss], sph, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_warp(&S.k_empty[ko], kph ^ 1u, abort_flag)) { ok = false; break; }
         {
           const uint8_t* src = S.sk[ss] + r * 128;
           uint8_t* dst = S.k[ko] + r * 128;
@@ -581,8 +643,8 @@ __global__ void __launch_bounds__(Cfg<FP8>::kThreads, 1)
         }
         if (++ko == KST) { ko = 0; kph ^= 1u; }
         // V
-        if (!mbar_wait(&S.sv_full[ss], sph, abort_flag)) { ok = false; break; }
-        if (!mbar_wait(&S.v_empty[vo], vph ^ 1u, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_warp(&S.sv_full[ss], sph, abort_flag)) { ok = false; break; }
+        if (!mbar_wait_warp(&S.v_empty[vo], vph ^ 1u, abort_flag)) { ok = false; break; }
         {
           const uint8_t* src = S.sv[ss] + r * 128;
           uint8_t* dst = S.v[vo] + r * 128;
@@ -650,15 +712,13 @@ __global__ void __launch_bounds__(kHd) attn_combine(const AttnParams p) {
 
 }  // namespace
 
-size_t attn_tc_smem_bytes() { return sizeof(Smem<true>) + 1024; }
-
 template <int NQ, bool FP8>
 int launch_one(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, int grid, cudaStream_t s) {
-  const size_t smem = sizeof(Smem<FP8>) + 1024;
+  const size_t smem = sizeof(Smem<NQ, FP8>) + 1024;
   cudaError_t e =
       cudaFuncSetAttribute(attn_cache_tc<NQ, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return (int)e;
-  attn_cache_tc<NQ, FP8><<<grid, Cfg<FP8>::kThreads, smem, s>>>(tm_q, tm_kv, p);
+  attn_cache_tc<NQ, FP8><<<grid, Cfg<NQ, FP8>::kThreads, smem, s>>>(tm_q, tm_kv, p);
   return (int)cudaGetLastError();
 }
 

@@ -297,10 +297,19 @@ int do_project(dllm_cache* c, const StepArgs& a) {
   p.tiles_q = p.mt_q * p.nt_q;
   p.tiles_total = p.tiles_q + p.mt_kv * p.nt_kv;
   p.k_blocks = D / 64;
+  // Tiles beyond the last full round of CTAs: when they would leave at least half the
+  // SMs idle, each is done as two 128-column halves spread over those SMs.
+  p.whole_items = p.tiles_total;
+  {
+    const int rem = p.tiles_total % c->sm_count;
+    if (bn == 256 && rem > 0 && 2 * rem <= c->sm_count) p.whole_items = p.tiles_total - rem;
+  }
+  p.items_total = p.whole_items + 2 * (p.tiles_total - p.whole_items);
   p.m_fastest = ((size_t)(p.m_q + p.m_kv) * D * 2 <= ((size_t)48 << 20)) ? 1 : 0;
 
-  CUtensorMap tm_w, tm_x, tm_xkv;
+  CUtensorMap tm_w, tm_w_half, tm_x, tm_xkv;
   if (!map_2d_bf16(&tm_w, a.w_qkv, D, 3 * (uint64_t)D, 64, bn)) return DLLM_ECUDA;
+  if (!map_2d_bf16(&tm_w_half, a.w_qkv, D, 3 * (uint64_t)D, 64, 128)) return DLLM_ECUDA;
   if (p.m_q > 0) {
     if (!map_2d_bf16(&tm_x, a.x, D, p.m_q, 64, 128)) return DLLM_ECUDA;
   } else {
@@ -311,8 +320,8 @@ int do_project(dllm_cache* c, const StepArgs& a) {
   } else {
     tm_xkv = tm_w;
   }
-  const int grid = p.tiles_total < c->sm_count ? p.tiles_total : c->sm_count;
-  rc = launch_proj_tc(p, tm_x, tm_xkv, tm_w, bn, grid, a.s);
+  const int grid = p.items_total < c->sm_count ? p.items_total : c->sm_count;
+  rc = launch_proj_tc(p, tm_x, tm_xkv, tm_w, tm_w_half, bn, grid, a.s);
   return rc ? from_cuda((cudaError_t)rc) : DLLM_OK;
 }
 

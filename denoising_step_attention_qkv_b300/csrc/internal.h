@@ -41,6 +41,8 @@ struct ProjParams {
   int mt_q, mt_kv;    // 128-row tiles
   int nt_q, nt_kv;    // column tiles per row tile (3D/BN, 2D/BN)
   int tiles_q, tiles_total;
+  int whole_items;    // tiles computed whole (the first ones)
+  int items_total;    // whole_items + 2 * (tiles_total - whole_items): the rest in 128-column halves
   int k_blocks;       // D / 64
   int m_fastest;      // tile raster: row tiles vary fastest
   const int32_t* positions;
@@ -77,7 +79,7 @@ struct AttnParams {
 
 // Launchers (return a cudaError_t cast to int, 0 on success).
 int launch_proj_tc(const ProjParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_xkv,
-                   const CUtensorMap& tm_w, int bn, int grid, cudaStream_t s);
+                   const CUtensorMap& tm_w, const CUtensorMap& tm_w_half, int bn, int grid, cudaStream_t s);
 int launch_attn_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, int grid,
                    cudaStream_t s);
 int launch_attn_combine(const AttnParams& p, cudaStream_t s);

@@ -14,7 +14,9 @@
 // so both halves (i, i+64) of every rotary pair are in its own registers.  It rotates
 // Q and K in fp32 with the per-position cos/sin table, rounds to bf16 (or quantises a
 // head to e4m3 with scale amax/448) and writes 16-byte vectors straight to the token's
-// cache slot, its probe row or the Q scratch.
+// cache slot, its probe row or the Q scratch.  The tiles left over after the last full
+// round of CTAs are cut into two 128-column halves (one head each) when that keeps
+// more SMs busy in the last round; a half uses N = 128 and loads half of the W tile.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -61,6 +63,26 @@ DEVI TileCoord decode_tile(const ProjParams& p, int tile, int BN) {
   }
   c.m0 = mt * BM;
   return c;
+}
+
+// A work item is a whole tile (items [0, whole_items)) or one 128-column half of one of
+// the remaining tiles.
+struct Item {
+  int tile;
+  int half;  // -1: whole tile; 0 or 1: which 128-column half
+};
+
+DEVI Item decode_item(const ProjParams& p, int item) {
+  Item it;
+  if (item < p.whole_items) {
+    it.tile = item;
+    it.half = -1;
+  } else {
+    const int i = item - p.whole_items;
+    it.tile = p.whole_items + (i >> 1);
+    it.half = i & 1;
+  }
+  return it;
 }
 
 DEVI void raise_status(int* status, int bits) { atomicOr(status, bits); }
@@ -119,7 +141,8 @@ DEVI void rotate32(float (&lo)[32], float (&hi)[32], const float2* __restrict__ 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     proj_rope_store_tc(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xkv,
-                       const __grid_constant__ CUtensorMap tm_w, const ProjParams p) {
+                       const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_w_half,
+                       const ProjParams p) {
   using C = Cfg<BN>;
   constexpr int STAGES = C::STAGES;
   extern __shared__ uint8_t smem_raw[];
@@ -153,6 +176,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tm_x);
     prefetch_tmap(&tm_xkv);
     prefetch_tmap(&tm_w);
+    prefetch_tmap(&tm_w_half);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, C::kTmemCols);
@@ -170,14 +194,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < p.tiles_total && ok; tile += gridDim.x) {
-      const TileCoord c = decode_tile(p, tile, BN);
+    for (int item = blockIdx.x; item < p.items_total && ok; item += gridDim.x) {
+      const Item it = decode_item(p, item);
+      const TileCoord c = decode_tile(p, it.tile, BN);
       const CUtensorMap* am = c.grp ? &tm_xkv : &tm_x;
+      const bool half = it.half >= 0;
+      const int n0 = half ? c.n0 + it.half * kHd : c.n0;
+      const uint32_t bytes = half ? kABytes + kHd * BK * 2 : C::kStageBytes;
       for (int kb = 0; kb < p.k_blocks; ++kb) {
         if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
-        mbar_arrive_expect_tx(&full[stage], C::kStageBytes);
+        mbar_arrive_expect_tx(&full[stage], bytes);
         tma_load_2d(sA + stage * kABytes, am, &full[stage], kb * BK, c.m0, pol_x);
-        tma_load_2d(sB + stage * C::kBBytes, &tm_w, &full[stage], kb * BK, c.n0, pol_w);
+        tma_load_2d(sB + stage * C::kBBytes, half ? &tm_w_half : &tm_w, &full[stage], kb * BK, n0, pol_w);
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
@@ -194,13 +222,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------ MMA issuer
-    constexpr uint32_t idesc = idesc_bf16(BM, BN, false, false);
+    constexpr uint32_t idesc_whole = idesc_bf16(BM, BN, false, false);
+    constexpr uint32_t idesc_half = idesc_bf16(BM, kHd, false, false);
     int stage = 0;
     uint32_t phase = 0;
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int tile = blockIdx.x; tile < p.tiles_total && ok; tile += gridDim.x) {
+    for (int item = blockIdx.x; item < p.items_total && ok; item += gridDim.x) {
+      const uint32_t idesc = decode_item(p, item).half >= 0 ? idesc_half : idesc_whole;
       if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
@@ -238,12 +268,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     const int hd = kHd;
-    for (int tile = blockIdx.x; tile < p.tiles_total; tile += gridDim.x) {
-      const TileCoord c = decode_tile(p, tile, BN);
-      if (!mbar_wait(&tfull[acc], acc_phase, abort_flag)) {
+    bool ok = true;  // a failed wait is recorded; the item sequence continues without stores
+    for (int item = blockIdx.x; item < p.items_total; item += gridDim.x) {
+      const Item it = decode_item(p, item);
+      TileCoord c = decode_tile(p, it.tile, BN);
+      if (it.half >= 0) c.n0 += it.half * kHd;
+      const int heads = it.half >= 0 ? 1 : BN / kHd;
+      if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag)) {
+        ok = false;
         *abort_flag = 1;
-        raise_status(p.status, DLLM_DEV_TIMEOUT);
-        break;
       }
       tc_fence_after();
 
@@ -283,12 +316,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (c.n0 == (c.grp ? p.D : 0)) raise_status(p.status, DLLM_DEV_BAD_POSITION);
         valid = false;
       }
+      valid = valid && ok;
 
       const int part = c.n0 / p.D;  // 0 Q, 1 K, 2 V
       const bool rope = part < 2;
       const float2* cs_row = p.rope + static_cast<size_t>(valid ? pos : 0) * (hd / 2);
 #pragma unroll 1
-      for (int hh = 0; hh < BN / kHd; ++hh) {
+      for (int hh = 0; hh < heads; ++hh) {
         const int h = (c.n0 - part * p.D) / kHd + hh;
         const uint32_t tcol = tmem_base + lane_base + acc * BN + hh * kHd;
         // destination of this row's 128 values
@@ -348,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       acc ^= 1;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (!ok) raise_status(p.status, DLLM_DEV_TIMEOUT);
   }
 
   tc_fence_before();
@@ -363,18 +398,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 size_t proj_tc_smem_bytes(int bn) { return bn == 256 ? Cfg<256>::kSmem : Cfg<128>::kSmem; }
 
 int launch_proj_tc(const ProjParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_xkv,
-                   const CUtensorMap& tm_w, int bn, int grid, cudaStream_t s) {
+                   const CUtensorMap& tm_w, const CUtensorMap& tm_w_half, int bn, int grid, cudaStream_t s) {
   cudaError_t e;
   if (bn == 256) {
     auto k = proj_rope_store_tc<256>;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<256>::kSmem);
     if (e != cudaSuccess) return (int)e;
-    k<<<grid, kThreads, Cfg<256>::kSmem, s>>>(tm_x, tm_xkv, tm_w, p);
+    k<<<grid, kThreads, Cfg<256>::kSmem, s>>>(tm_x, tm_xkv, tm_w, tm_w_half, p);
   } else {
     auto k = proj_rope_store_tc<128>;
     e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<128>::kSmem);
     if (e != cudaSuccess) return (int)e;
-    k<<<grid, kThreads, Cfg<128>::kSmem, s>>>(tm_x, tm_xkv, tm_w, p);
+    k<<<grid, kThreads, Cfg<128>::kSmem, s>>>(tm_x, tm_xkv, tm_w, tm_w_half, p);
   }
   return (int)cudaGetLastError();
 }

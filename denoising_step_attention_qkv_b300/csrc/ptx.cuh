@@ -42,6 +42,19 @@ DEVI bool mbar_test(uint32_t addr, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
+// Non-blocking probe of the same condition (test_wait returns at once; try_wait may
+// suspend the thread for a while), for a thread that polls several barriers in turn.
+DEVI bool mbar_poll(uint32_t addr, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n.reg .pred p;\n"
+      "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      "selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(addr), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
 // Wait for the phase with parity `parity` to complete.  Returns false (without
 // completing) when the shared abort flag is raised or the wall-clock limit passes.
 DEVI bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
@@ -55,6 +68,14 @@ DEVI bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
       if (globaltimer() - t0 > kWaitLimitNs) return false;
     }
   }
+}
+
+// mbar_wait called by all 32 lanes of a warp, with one answer for the whole warp (a
+// lane that saw the phase complete just after another lane gave up still reports
+// failure), so that the warp never splits around a later warp-wide operation.
+DEVI bool mbar_wait_warp(uint64_t* bar, uint32_t parity, volatile int* abort_flag) {
+  const bool ok = mbar_wait(bar, parity, abort_flag);
+  return __all_sync(0xffffffffu, ok);
 }
 
 // ------------------------------------------------------------------------------- TMA

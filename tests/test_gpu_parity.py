@@ -51,6 +51,8 @@ SMALL_BF16 = [
     dict(batch=40, d_model=512, max_pos=200, block=16, gen_lo=128),
     # more than one 64-query chunk
     dict(batch=2, d_model=256, max_pos=400, block=100, gen_lo=200),
+    # 156 tiles of 128 x 256 on 148 SMs: the 8 left over run as 128-column halves
+    dict(batch=52, d_model=1024, max_pos=160, block=32, gen_lo=128),
 ]
 
 
