@@ -72,6 +72,9 @@ struct Smem {
   float m_use[NQ];
   float alpha[2][NQ];
   float l_fin[NQ];
+  float inv_l[NQ];
+  float fin_alpha[2][NQ];  // per unit parity: the last tile's rescale factor and running max
+  float fin_m[2][NQ];
   uint32_t mask_bits[kMaxBitmapWords];
   uint32_t draft_qmask[2];
   int n_draft;
@@ -377,7 +380,75 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     };
     const int mask_words = (p.max_pos + 31) >> 5;
 
-    for (int u = blockIdx.x; u < p.units; u += gridDim.x) {
+    // Finishing a unit (fold its last P V, reduce the row sums, write the output or the
+    // split partials) waits for that P V MMA.  With 32 bf16 queries the finish is
+    // deferred into the next unit's first tile, whose P V fold slot is empty, so the
+    // wait hides behind that tile's softmax.
+    constexpr bool kDefer = (NQ == 32) && !FP8;
+    auto finish = [&](float (&o)[NQ], float (&l)[NQ], const Unit& fx, int fu, int fuu, uint32_t fpv) {
+      const uint32_t ob = fpv & 1u, oph = (fpv >> 1) & 1u;  // the unit's last P V
+      wait(&S.o_full[ob], oph);
+      tc_fence_after();
+      const float4* al4 = reinterpret_cast<const float4*>(S.fin_alpha[fuu & 1]);
+#pragma unroll
+      for (int c = 0; c < NQ; c += 32) {
+        float tmp[32];
+        tmem_ld32(tmem + lane_base + 2 * NQ + ob * NQ + c, tmp);
+#pragma unroll
+        for (int i = 0; i < 32; i += 4) {
+          const float4 al = al4[(c + i) / 4];
+          o[c + i] = o[c + i] * al.x + tmp[i];
+          o[c + i + 1] = o[c + i + 1] * al.y + tmp[i + 1];
+          o[c + i + 2] = o[c + i + 2] * al.z + tmp[i + 2];
+          o[c + i + 3] = o[c + i + 3] * al.w + tmp[i + 3];
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&S.o_free[ob]);
+      // row sums: reduce the per-key partial sums over the 128 threads
+#pragma unroll
+      for (int c = 0; c < NQ; c += 32) S.red[quarter][c + lane] = reduce_scatter32<false>(l + c, lane);
+      softmax_sync();
+      if (r < NQ) {
+        const float lt = S.red[0][r] + S.red[1][r] + S.red[2][r] + S.red[3][r];
+        S.l_fin[r] = lt;
+        S.inv_l[r] = lt > 0.0f ? 1.0f / lt : 0.0f;
+      }
+      softmax_sync();
+      const int frow0 = fx.b * p.n_tok + fx.qc * kQChunk;
+      const int fnrows = min(kQChunk, p.n_tok - fx.qc * kQChunk);
+      if (p.n_splits == 1) {
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(frow0) * p.D + fx.h * kHd + r;
+        const float4* il4 = reinterpret_cast<const float4*>(S.inv_l);
+#pragma unroll
+        for (int q = 0; q < NQ; q += 4) {
+          const float4 il = il4[q / 4];
+          if (ok && q < fnrows) out[static_cast<size_t>(q) * p.D] = __float2bfloat16_rn(o[q] * il.x);
+          if (ok && q + 1 < fnrows) out[static_cast<size_t>(q + 1) * p.D] = __float2bfloat16_rn(o[q + 1] * il.y);
+          if (ok && q + 2 < fnrows) out[static_cast<size_t>(q + 2) * p.D] = __float2bfloat16_rn(o[q + 2] * il.z);
+          if (ok && q + 3 < fnrows) out[static_cast<size_t>(q + 3) * p.D] = __float2bfloat16_rn(o[q + 3] * il.w);
+        }
+      } else {
+        float* wo = p.ws + static_cast<size_t>(fu) * kQChunk * kHd;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) wo[q * kHd + r] = o[q];
+        if (r < NQ) {
+          float* wml = p.ws + static_cast<size_t>(p.units) * kQChunk * kHd + (static_cast<size_t>(fu) * kQChunk + r) * 2;
+          wml[0] = S.fin_m[fuu & 1][r];
+          wml[1] = S.l_fin[r];
+        }
+      }
+    };
+
+    float o_prev[NQ], l_prev[NQ];  // the unit waiting to be finished (deferred finish only)
+    Unit px{};
+    int pu = 0, puu = 0;
+    uint32_t ppv = 0;
+    bool pending = false;
+    int uu = 0;  // units started by this CTA (parity selects the finish buffers)
+
+    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++uu) {
       const Unit x = decode_unit(p, u);
       const int row0 = x.b * p.n_tok;  // first row of the sequence
       const int nrows = min(kQChunk, p.n_tok - x.qc * kQChunk);  // valid columns of this chunk
@@ -471,9 +542,14 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
           const float m_old = S.m_run[r];
           const float m_new = fmaxf(m_old, mt);
           const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
+          const float a = fast_exp2(m_old - m_use);
           S.m_run[r] = m_new;
           S.m_use[r] = m_use;
-          S.alpha[tp][r] = fast_exp2(m_old - m_use);
+          S.alpha[tp][r] = a;
+          if (t == x.t1 - 1) {  // the unit's last tile: what its finish needs
+            S.fin_alpha[uu & 1][r] = a;
+            S.fin_m[uu & 1][r] = m_new;
+          }
         }
         softmax_sync();
         // ---- C: probabilities -> P^T (bf16, swizzled); this thread's partial row sums
@@ -518,7 +594,12 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
           __syncwarp();
           if (lane == 0) mbar_arrive(&S.p_full[pb]);
         }
-        // ---- D: fold the previous tile's P V into the accumulators
+        // ---- D: fold the previous tile's P V into the accumulators (in a unit's first
+        // tile: finish the previous unit instead, when that was deferred)
+        if (kDefer && t == x.t0 && pending) {
+          finish(o_prev, l_prev, px, pu, puu, ppv);
+          pending = false;
+        }
         if (t > x.t0) {
           const uint32_t ob = (pv_cnt - 1) & 1u, oph = ((pv_cnt - 1) >> 1) & 1u;
           wait(&S.o_full[ob], oph);
@@ -543,56 +624,25 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         }
         ++pv_cnt;
       }
-      // ---- unit end: last tile's P V, the row sums, output
-      if (x.t1 > x.t0) {
-        const uint32_t ob = (pv_cnt - 1) & 1u, oph = ((pv_cnt - 1) >> 1) & 1u;
-        wait(&S.o_full[ob], oph);
-        tc_fence_after();
-        const float4* al4 = reinterpret_cast<const float4*>(S.alpha[(x.t1 - 1) & 1]);
-#pragma unroll
-        for (int c = 0; c < NQ; c += 32) {
-          float tmp[32];
-          tmem_ld32(tmem + lane_base + 2 * NQ + ob * NQ + c, tmp);
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 al = al4[(c + i) / 4];
-            o_acc[c + i] = o_acc[c + i] * al.x + tmp[i];
-            o_acc[c + i + 1] = o_acc[c + i + 1] * al.y + tmp[i + 1];
-            o_acc[c + i + 2] = o_acc[c + i + 2] * al.z + tmp[i + 2];
-            o_acc[c + i + 3] = o_acc[c + i + 3] * al.w + tmp[i + 3];
-          }
-        }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&S.o_free[ob]);
-      }
-      // row sums: reduce the per-key partial sums over the 128 threads
-#pragma unroll
-      for (int c = 0; c < NQ; c += 32) S.red[quarter][c + lane] = reduce_scatter32<false>(l_part + c, lane);
-      softmax_sync();
-      if (r < NQ) S.l_fin[r] = S.red[0][r] + S.red[1][r] + S.red[2][r] + S.red[3][r];
-      softmax_sync();
-      if (p.n_splits == 1) {
-        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out);
+      // ---- unit end: finish now, or hand the state to the next unit's first tile
+      if constexpr (kDefer) {
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
-          if (q < nrows && ok) {
-            const float l = S.l_fin[q];
-            const float o = l > 0.0f ? o_acc[q] / l : 0.0f;
-            out[static_cast<size_t>(row0 + x.qc * kQChunk + q) * p.D + x.h * kHd + r] = __float2bfloat16_rn(o);
-          }
+          o_prev[q] = o_acc[q];
+          l_prev[q] = l_part[q];
         }
+        px = x;
+        pu = u;
+        puu = uu;
+        ppv = pv_cnt - 1;
+        pending = true;
       } else {
-        float* wo = p.ws + static_cast<size_t>(u) * kQChunk * kHd;
-#pragma unroll
-        for (int q = 0; q < NQ; ++q) wo[q * kHd + r] = o_acc[q];
-        if (r < NQ) {
-          float* wml = p.ws + static_cast<size_t>(p.units) * kQChunk * kHd + (static_cast<size_t>(u) * kQChunk + r) * 2;
-          wml[0] = S.m_run[r];
-          wml[1] = S.l_fin[r];
-        }
+        finish(o_acc, l_part, x, u, uu, pv_cnt - 1);
       }
-      softmax_sync();  // the next unit's set-up rewrites the running max, sums and tags
+      softmax_sync();  // the next unit's set-up rewrites the running max and tags
+    }
+    if constexpr (kDefer) {
+      if (pending) finish(o_prev, l_prev, px, pu, puu, ppv);
     }
     if (!ok) {
       *abort_flag = 1;
