@@ -131,6 +131,13 @@ int dllm_cache_alloc(const dllm_cache_desc* desc, dllm_cache** out) {
   if (e != cudaSuccess) return fail(from_cuda(e));
   e = cudaDeviceGetAttribute(&c->sm_count, cudaDevAttrMultiProcessorCount, c->device);
   if (e != cudaSuccess) return fail(from_cuda(e));
+  if (desc->kv_dtype != DLLM_F32) {
+    // CTA pairs the projection can keep resident at once (0: use single-CTA tiles)
+    int clusters = 0;
+    if (proj_pair_max_clusters(&clusters) != 0) clusters = 0;
+    (void)cudaGetLastError();
+    c->pair_clusters = clusters < c->sm_count / 2 ? clusters : c->sm_count / 2;
+  }
 
   if (desc->external_buf) {
     c->kv = desc->external_buf;
@@ -159,6 +166,10 @@ int dllm_cache_alloc(const dllm_cache_desc* desc, dllm_cache** out) {
   if (e != cudaSuccess) return fail(from_cuda(e));
   e = cudaMemset(c->status, 0, sizeof(int));
   if (e != cudaSuccess) return fail(from_cuda(e));
+  e = cudaMalloc(&c->drift_cnt, (size_t)desc->batch * sizeof(int));
+  if (e != cudaSuccess) return fail(from_cuda(e));
+  e = cudaMemset(c->drift_cnt, 0, (size_t)desc->batch * sizeof(int));
+  if (e != cudaSuccess) return fail(from_cuda(e));
 
   // split-KV partials: at most 2 * (2 * SMs) units of kQChunk rows
   if (desc->kv_dtype != DLLM_F32) {
@@ -176,6 +187,7 @@ int dllm_cache_free(dllm_cache* c) {
   if (c->owns_kv && c->kv) cudaFree(c->kv);
   if (c->rope) cudaFree(c->rope);
   if (c->status) cudaFree(c->status);
+  if (c->drift_cnt) cudaFree(c->drift_cnt);
   if (c->ws) cudaFree(c->ws);
   delete c;
   return DLLM_OK;
@@ -290,36 +302,54 @@ int do_project(dllm_cache* c, const StepArgs& a) {
     return (long long)ceil_div(p.m_q, 128) * (3 * D / bnv) + (long long)ceil_div(p.m_kv, 128) * (2 * D / bnv);
   };
   if (bn == 256 && tiles_for(256) < c->sm_count) bn = 128;
+  p.k_blocks = D / 64;
+  p.m_fastest = ((size_t)(p.m_q + p.m_kv) * D * 2 <= ((size_t)48 << 20)) ? 1 : 0;
+
+  // Tiles beyond the last full round: when they would leave at least half the workers
+  // (CTAs, or CTA pairs) idle, each is done as two 128-column halves spread over them.
+  auto split_tail = [&](int tiles, int workers) {
+    p.tiles_total = tiles;
+    p.whole_items = tiles;
+    const int rem = tiles % workers;
+    if (rem > 0 && 2 * rem <= workers) p.whole_items = tiles - rem;
+    p.items_total = p.whole_items + 2 * (tiles - p.whole_items);
+  };
+
+  CUtensorMap tm_w, tm_w_half, tm_x, tm_xkv;
+  if (p.m_q > 0) {
+    if (!map_2d_bf16(&tm_x, a.x, D, p.m_q, 64, 128)) return DLLM_ECUDA;
+  }
+  if (p.m_kv > 0) {
+    if (!map_2d_bf16(&tm_xkv, a.kv_x, D, p.m_kv, 64, 128)) return DLLM_ECUDA;
+  }
+  if (bn == 256 && c->pair_clusters >= 1) {
+    // 256 x 256 tiles on CTA pairs (cta_group::2); each CTA loads 128 (or 64) W rows
+    if (!map_2d_bf16(&tm_w, a.w_qkv, D, 3 * (uint64_t)D, 64, 128)) return DLLM_ECUDA;
+    if (!map_2d_bf16(&tm_w_half, a.w_qkv, D, 3 * (uint64_t)D, 64, 64)) return DLLM_ECUDA;
+    if (p.m_q == 0) tm_x = tm_w;
+    if (p.m_kv == 0) tm_xkv = tm_w;
+    p.pmt_q = ceil_div(p.m_q, 256);
+    p.pmt_kv = ceil_div(p.m_kv, 256);
+    const int pairs = c->pair_clusters;
+    split_tail(p.pmt_q * (3 * D / 256) + p.pmt_kv * (2 * D / 256), pairs);
+    const int grid = 2 * (p.items_total < pairs ? p.items_total : pairs);
+    rc = launch_proj_pair(p, tm_x, tm_xkv, tm_w, tm_w_half, grid, a.s);
+    return rc ? from_cuda((cudaError_t)rc) : DLLM_OK;
+  }
   p.mt_q = ceil_div(p.m_q, 128);
   p.mt_kv = ceil_div(p.m_kv, 128);
   p.nt_q = 3 * D / bn;
   p.nt_kv = 2 * D / bn;
   p.tiles_q = p.mt_q * p.nt_q;
-  p.tiles_total = p.tiles_q + p.mt_kv * p.nt_kv;
-  p.k_blocks = D / 64;
-  // Tiles beyond the last full round of CTAs: when they would leave at least half the
-  // SMs idle, each is done as two 128-column halves spread over those SMs.
-  p.whole_items = p.tiles_total;
-  {
-    const int rem = p.tiles_total % c->sm_count;
-    if (bn == 256 && rem > 0 && 2 * rem <= c->sm_count) p.whole_items = p.tiles_total - rem;
+  split_tail(p.tiles_q + p.mt_kv * p.nt_kv, c->sm_count);
+  if (bn != 256) {  // 128-wide tiles have no halves
+    p.whole_items = p.tiles_total;
+    p.items_total = p.tiles_total;
   }
-  p.items_total = p.whole_items + 2 * (p.tiles_total - p.whole_items);
-  p.m_fastest = ((size_t)(p.m_q + p.m_kv) * D * 2 <= ((size_t)48 << 20)) ? 1 : 0;
-
-  CUtensorMap tm_w, tm_w_half, tm_x, tm_xkv;
   if (!map_2d_bf16(&tm_w, a.w_qkv, D, 3 * (uint64_t)D, 64, bn)) return DLLM_ECUDA;
   if (!map_2d_bf16(&tm_w_half, a.w_qkv, D, 3 * (uint64_t)D, 64, 128)) return DLLM_ECUDA;
-  if (p.m_q > 0) {
-    if (!map_2d_bf16(&tm_x, a.x, D, p.m_q, 64, 128)) return DLLM_ECUDA;
-  } else {
-    tm_x = tm_w;
-  }
-  if (p.m_kv > 0) {
-    if (!map_2d_bf16(&tm_xkv, a.kv_x, D, p.m_kv, 64, 128)) return DLLM_ECUDA;
-  } else {
-    tm_xkv = tm_w;
-  }
+  if (p.m_q == 0) tm_x = tm_w;
+  if (p.m_kv == 0) tm_xkv = tm_w;
   const int grid = p.items_total < c->sm_count ? p.items_total : c->sm_count;
   rc = launch_proj_tc(p, tm_x, tm_xkv, tm_w, tm_w_half, bn, grid, a.s);
   return rc ? from_cuda((cudaError_t)rc) : DLLM_OK;
@@ -432,8 +462,8 @@ int dllm_kv_drift(const dllm_cache* c, int layer, const int32_t* idx, int k, con
   const void* kvl = reinterpret_cast<const uint8_t*>(c->kv) + (size_t)layer * c->layer_elems * c->elem_bytes;
   const float* scl = c->scale ? c->scale + (size_t)layer * c->layer_scales : nullptr;
   return from_cuda((cudaError_t)launch_drift(kvl, scl, d.kv_dtype, d.batch, c->slots, d.max_pos, d.n_heads, d.head_dim,
-                                             idx, k, probe_kv, gamma, cos, refresh, c->status,
-                                             reinterpret_cast<cudaStream_t>(stream)));
+                                             idx, k, probe_kv, gamma, cos, refresh, c->drift_cnt, c->sm_count,
+                                             c->status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 int dllm_cache_status(dllm_cache* c, int* device_bits) {

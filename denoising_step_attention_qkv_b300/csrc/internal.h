@@ -13,6 +13,8 @@ struct dllm_cache {
   dllm_cache_desc desc;
   int device;
   int sm_count;
+  int pair_clusters;  // clusters of two projection CTAs resident at once (0 = none)
+  int* drift_cnt;     // [batch] block arrivals of dllm_kv_drift; zero between calls
   void* kv;
   float* scale;
   bool owns_kv;
@@ -43,6 +45,7 @@ struct ProjParams {
   int tiles_q, tiles_total;
   int whole_items;    // tiles computed whole (the first ones)
   int items_total;    // whole_items + 2 * (tiles_total - whole_items): the rest in 128-column halves
+  int pmt_q, pmt_kv;  // CTA-pair kernel: 256-row tiles of the query rows, of the K/V-only rows
   int k_blocks;       // D / 64
   int m_fastest;      // tile raster: row tiles vary fastest
   const int32_t* positions;
@@ -80,6 +83,11 @@ struct AttnParams {
 // Launchers (return a cudaError_t cast to int, 0 on success).
 int launch_proj_tc(const ProjParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_xkv,
                    const CUtensorMap& tm_w, const CUtensorMap& tm_w_half, int bn, int grid, cudaStream_t s);
+// CTA-pair variant (256 x 256 output tiles on two SMs, cta_group::2); grid = 2 x pairs.
+// tm_w / tm_w_half: W boxes of 128 / 64 rows (each CTA's half of a 256 / 128-wide tile).
+int launch_proj_pair(const ProjParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_xkv,
+                     const CUtensorMap& tm_w, const CUtensorMap& tm_w_half, int grid, cudaStream_t s);
+int proj_pair_max_clusters(int* clusters);
 int launch_attn_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, int grid,
                    cudaStream_t s);
 int launch_attn_combine(const AttnParams& p, cudaStream_t s);
@@ -92,7 +100,7 @@ int launch_topk(const float* mass, int batch, int n_pos, const int32_t* block_lo
                 int32_t* idx, cudaStream_t s);
 int launch_drift(const void* kv_layer, const float* scale_layer, int kv_dtype, int B, int slots, int max_pos,
                  int H, int hd, const int32_t* idx, int k, const void* probe, float gamma, float* cos,
-                 int32_t* refresh, int* status, cudaStream_t s);
+                 int32_t* refresh, int* counters, int sm_count, int* status, cudaStream_t s);
 
 size_t proj_tc_smem_bytes(int bn);
 size_t attn_tc_smem_bytes();

@@ -49,16 +49,36 @@ struct TileCoord {
 DEVI TileCoord decode_tile(const ProjParams& p, int tile, int BN) {
   TileCoord c;
   int mt, nt;
+  if (p.m_fastest) {
+    // column-major over the output features; a K or V column tile is followed by both
+    // row groups, so the CTAs in flight share each W tile in L2 (W is read from DRAM once)
+    const int q_cols = p.D / BN;  // column tiles of the Q features (query rows only)
+    const int q_tiles = q_cols * p.mt_q;
+    if (tile < q_tiles) {
+      c.grp = 0;
+      c.n0 = (tile / p.mt_q) * BN;
+      c.m0 = (tile % p.mt_q) * BM;
+    } else {
+      const int t = tile - q_tiles;
+      const int per = p.mt_q + p.mt_kv;
+      const int i = t % per;
+      c.n0 = p.D + (t / per) * BN;
+      c.grp = i < p.mt_q ? 0 : 1;
+      c.m0 = (c.grp ? i - p.mt_q : i) * BM;
+    }
+    return c;
+  }
+  // row-major (large activations): query-row tiles, then K/V-only row tiles
   if (tile < p.tiles_q) {
     c.grp = 0;
-    if (p.m_fastest) { mt = tile % p.mt_q; nt = tile / p.mt_q; }
-    else { nt = tile % p.nt_q; mt = tile / p.nt_q; }
+    nt = tile % p.nt_q;
+    mt = tile / p.nt_q;
     c.n0 = nt * BN;
   } else {
     c.grp = 1;
     const int t = tile - p.tiles_q;
-    if (p.m_fastest) { mt = t % p.mt_kv; nt = t / p.mt_kv; }
-    else { nt = t % p.nt_kv; mt = t / p.nt_kv; }
+    nt = t % p.nt_kv;
+    mt = t / p.nt_kv;
     c.n0 = p.D + nt * BN;
   }
   c.m0 = mt * BM;
@@ -135,6 +155,112 @@ DEVI void rotate32(float (&lo)[32], float (&hi)[32], const float2* __restrict__ 
       lo[2 * i + 1] = a * t.z - b * t.w;
       hi[2 * i + 1] = b * t.z + a * t.w;
     }
+  }
+}
+
+// The epilogue of one accumulator tile for this thread's row c.m0 + r: `heads` heads
+// starting at output feature c.n0, read from TMEM columns tacc ...  It rotates Q and K,
+// rounds to bf16 (or quantises each head to e4m3 with scale amax/448) and stores the
+// row's 128-value runs to the Q rows, the probe rows or the row's cache slot.  Nothing
+// is stored for rows outside the matrix, rows with out-of-range positions or view tags
+// (which raise a status bit), or when `ok` is false.
+DEVI void store_rows(const ProjParams& p, const TileCoord& c, int heads, uint32_t tacc, int r, bool ok) {
+  const int hd = kHd;
+  // ---- this thread's row
+  const int m = c.m0 + r;
+  bool valid;
+  int b = 0, pos = 0, slot = 0;
+  if (c.grp == 0) {
+    valid = m < p.m_q;
+    if (valid) {
+      b = m / p.n_tok;
+      pos = __ldg(p.positions + m);
+      slot = pos;
+      const int v = p.view ? static_cast<int>(__ldg(p.view + m)) : DLLM_VIEW_BASE;
+      if (v > DLLM_VIEW_MASK) {
+        if (c.n0 == 0) raise_status(p.status, DLLM_DEV_BAD_VIEW);
+        valid = false;
+      } else if (v == DLLM_VIEW_DRAFT) {
+        int rank = 0;
+        for (int t = b * p.n_tok; t < m; ++t) rank += (__ldg(p.view + t) == DLLM_VIEW_DRAFT);
+        if (rank >= p.tail) {
+          if (c.n0 == 0) raise_status(p.status, DLLM_DEV_TAIL_FULL);
+          valid = false;
+        }
+        slot = p.max_pos + rank;
+      }
+    }
+  } else {
+    valid = m < p.m_kv;
+    if (valid) {
+      b = m / p.n_kv;
+      pos = __ldg(p.kv_positions + m);
+      slot = pos;
+    }
+  }
+  if (valid && (pos < 0 || pos >= p.max_pos)) {
+    if (c.n0 == (c.grp ? p.D : 0)) raise_status(p.status, DLLM_DEV_BAD_POSITION);
+    valid = false;
+  }
+  valid = valid && ok;
+
+  const int part = c.n0 / p.D;  // 0 Q, 1 K, 2 V
+  const bool rope = part < 2;
+  const float2* cs_row = p.rope + static_cast<size_t>(valid ? pos : 0) * (hd / 2);
+#pragma unroll 1
+  for (int hh = 0; hh < heads; ++hh) {
+    const int h = (c.n0 - part * p.D) / kHd + hh;
+    const uint32_t tcol = tacc + hh * kHd;
+    // destination of this row's 128 values
+    uint8_t* dst = nullptr;
+    float* sdst = nullptr;
+    const bool to_probe = (c.grp == 1) && (p.probe != nullptr);
+    if (part == 0) {
+      dst = reinterpret_cast<uint8_t*>(p.q_out) + (static_cast<size_t>(m) * p.D + h * hd) * 2;
+    } else if (to_probe) {
+      dst = reinterpret_cast<uint8_t*>(p.probe) +
+            ((static_cast<size_t>(m) * 2 + (part - 1)) * p.D + h * hd) * 2;
+    } else {
+      const size_t row = (static_cast<size_t>(b) * p.slots + slot) * 2 + (part - 1);
+      if (p.kv_dtype == DLLM_E4M3) {
+        dst = reinterpret_cast<uint8_t*>(p.cache_kv) + row * p.D + h * hd;
+        sdst = p.cache_scale + row * p.H + h;
+      } else {
+        dst = reinterpret_cast<uint8_t*>(p.cache_kv) + (row * p.D + h * hd) * 2;
+      }
+    }
+    const bool fp8 = (sdst != nullptr);
+    float scale = 1.0f;
+    if (fp8) {
+      float amax = 0.0f;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        float lo[32], hi[32];
+        tmem_ld32(tcol + half * 32, lo);
+        tmem_ld32(tcol + 64 + half * 32, hi);
+        if (rope) rotate32(lo, hi, cs_row + half * 32);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fmaxf(fabsf(lo[i]), fabsf(hi[i])));
+      }
+      scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+    }
+#pragma unroll 1
+    for (int half = 0; half < 2; ++half) {
+      float lo[32], hi[32];
+      tmem_ld32(tcol + half * 32, lo);
+      tmem_ld32(tcol + 64 + half * 32, hi);
+      if (rope) rotate32(lo, hi, cs_row + half * 32);
+      if (valid) {
+        if (fp8) {
+          store_e4m3x32(dst + half * 32, lo, scale);
+          store_e4m3x32(dst + 64 + half * 32, hi, scale);
+        } else {
+          store_bf16x32(dst + half * 64, lo);
+          store_bf16x32(dst + 128 + half * 64, hi);
+        }
+      }
+    }
+    if (fp8 && valid) *sdst = scale;
   }
 }
 
@@ -267,7 +393,6 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     int acc = 0;
     uint32_t acc_phase = 0;
-    const int hd = kHd;
     bool ok = true;  // a failed wait is recorded; the item sequence continues without stores
     for (int item = blockIdx.x; item < p.items_total; item += gridDim.x) {
       const Item it = decode_item(p, item);
@@ -280,102 +405,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
 
-      // ---- this thread's row
-      const int m = c.m0 + r;
-      bool valid;
-      int b = 0, pos = 0, slot = 0;
-      if (c.grp == 0) {
-        valid = m < p.m_q;
-        if (valid) {
-          b = m / p.n_tok;
-          pos = __ldg(p.positions + m);
-          slot = pos;
-          const int v = p.view ? static_cast<int>(__ldg(p.view + m)) : DLLM_VIEW_BASE;
-          if (v > DLLM_VIEW_MASK) {
-            if (c.n0 == 0) raise_status(p.status, DLLM_DEV_BAD_VIEW);
-            valid = false;
-          } else if (v == DLLM_VIEW_DRAFT) {
-            int rank = 0;
-            for (int t = b * p.n_tok; t < m; ++t) rank += (__ldg(p.view + t) == DLLM_VIEW_DRAFT);
-            if (rank >= p.tail) {
-              if (c.n0 == 0) raise_status(p.status, DLLM_DEV_TAIL_FULL);
-              valid = false;
-            }
-            slot = p.max_pos + rank;
-          }
-        }
-      } else {
-        valid = m < p.m_kv;
-        if (valid) {
-          b = m / p.n_kv;
-          pos = __ldg(p.kv_positions + m);
-          slot = pos;
-        }
-      }
-      if (valid && (pos < 0 || pos >= p.max_pos)) {
-        if (c.n0 == (c.grp ? p.D : 0)) raise_status(p.status, DLLM_DEV_BAD_POSITION);
-        valid = false;
-      }
-      valid = valid && ok;
-
-      const int part = c.n0 / p.D;  // 0 Q, 1 K, 2 V
-      const bool rope = part < 2;
-      const float2* cs_row = p.rope + static_cast<size_t>(valid ? pos : 0) * (hd / 2);
-#pragma unroll 1
-      for (int hh = 0; hh < heads; ++hh) {
-        const int h = (c.n0 - part * p.D) / kHd + hh;
-        const uint32_t tcol = tmem_base + lane_base + acc * BN + hh * kHd;
-        // destination of this row's 128 values
-        uint8_t* dst = nullptr;
-        float* sdst = nullptr;
-        const bool to_probe = (c.grp == 1) && (p.probe != nullptr);
-        if (part == 0) {
-          dst = reinterpret_cast<uint8_t*>(p.q_out) + (static_cast<size_t>(m) * p.D + h * hd) * 2;
-        } else if (to_probe) {
-          dst = reinterpret_cast<uint8_t*>(p.probe) +
-                ((static_cast<size_t>(m) * 2 + (part - 1)) * p.D + h * hd) * 2;
-        } else {
-          const size_t row = (static_cast<size_t>(b) * p.slots + slot) * 2 + (part - 1);
-          if (p.kv_dtype == DLLM_E4M3) {
-            dst = reinterpret_cast<uint8_t*>(p.cache_kv) + row * p.D + h * hd;
-            sdst = p.cache_scale + row * p.H + h;
-          } else {
-            dst = reinterpret_cast<uint8_t*>(p.cache_kv) + (row * p.D + h * hd) * 2;
-          }
-        }
-        const bool fp8 = (sdst != nullptr);
-        float scale = 1.0f;
-        if (fp8) {
-          float amax = 0.0f;
-#pragma unroll 1
-          for (int half = 0; half < 2; ++half) {
-            float lo[32], hi[32];
-            tmem_ld32(tcol + half * 32, lo);
-            tmem_ld32(tcol + 64 + half * 32, hi);
-            if (rope) rotate32(lo, hi, cs_row + half * 32);
-#pragma unroll
-            for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fmaxf(fabsf(lo[i]), fabsf(hi[i])));
-          }
-          scale = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
-        }
-#pragma unroll 1
-        for (int half = 0; half < 2; ++half) {
-          float lo[32], hi[32];
-          tmem_ld32(tcol + half * 32, lo);
-          tmem_ld32(tcol + 64 + half * 32, hi);
-          if (rope) rotate32(lo, hi, cs_row + half * 32);
-          if (valid) {
-            if (fp8) {
-              store_e4m3x32(dst + half * 32, lo, scale);
-              store_e4m3x32(dst + 64 + half * 32, hi, scale);
-            } else {
-              store_bf16x32(dst + half * 64, lo);
-              store_bf16x32(dst + 128 + half * 64, hi);
-            }
-          }
-        }
-        if (fp8 && valid) *sdst = scale;
-      }
+      store_rows(p, c, heads, tmem_base + lane_base + acc * BN, r, ok);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(&tempty[acc]);
@@ -390,6 +420,231 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem_base, C::kTmemCols);
+  }
+}
+
+// ------------------------------------------------------------------------------------
+// CTA-pair kernel.  Two CTAs of a cluster compute one 256 x 256 output tile with
+// tcgen05.mma.cta_group::2 (M = 256, N = 256, K = 16): each CTA stages its 128 rows of x
+// and its 128 rows of W per k-block (32 KB a stage instead of 48 KB), so a 6-deep ring
+// fits and the loads run further ahead of the tensor core.  Rank 0 issues the MMAs and
+// commits to the barriers of both CTAs; each CTA's epilogue drains its own TMEM rows.
+// Tiles left over after the last full round of pairs run as 128-column halves.
+// ------------------------------------------------------------------------------------
+constexpr int kPairStages = 6;
+constexpr uint32_t kPairBBytes = 128 * BK * 2;  // 16 KB: this CTA's half of a W k-block
+constexpr uint32_t kPairStageBytes = kABytes + kPairBBytes;
+constexpr size_t kPairSmem = 1024 + kPairStages * kPairStageBytes + 256;
+
+struct PairItem {
+  int grp, pm0, n0;  // row group, first row of the 256-row pair tile, first output feature
+  bool half;         // a 128-column half (n0 already offset)
+};
+
+DEVI PairItem decode_pair_item(const ProjParams& p, int item) {
+  int tile = item, hf = -1;
+  if (item >= p.whole_items) {
+    const int i = item - p.whole_items;
+    tile = p.whole_items + (i >> 1);
+    hf = i & 1;
+  }
+  PairItem it;
+  if (p.m_fastest) {
+    // column-major: a K or V column tile is followed by both row groups (W read once)
+    const int q_cols = p.D / 256;
+    const int q_tiles = q_cols * p.pmt_q;
+    if (tile < q_tiles) {
+      it.grp = 0;
+      it.n0 = (tile / p.pmt_q) * 256;
+      it.pm0 = (tile % p.pmt_q) * 256;
+    } else {
+      const int t = tile - q_tiles;
+      const int per = p.pmt_q + p.pmt_kv;
+      const int i = t % per;
+      it.n0 = p.D + (t / per) * 256;
+      it.grp = i < p.pmt_q ? 0 : 1;
+      it.pm0 = (it.grp ? i - p.pmt_q : i) * 256;
+    }
+  } else {
+    const int nq = 3 * p.D / 256, nkv = 2 * p.D / 256;
+    const int q_tiles = p.pmt_q * nq;
+    if (tile < q_tiles) {
+      it.grp = 0;
+      it.n0 = (tile % nq) * 256;
+      it.pm0 = (tile / nq) * 256;
+    } else {
+      const int t = tile - q_tiles;
+      it.grp = 1;
+      it.n0 = p.D + (t % nkv) * 256;
+      it.pm0 = (t / nkv) * 256;
+    }
+  }
+  it.half = hf >= 0;
+  if (it.half) it.n0 += hf * kHd;
+  return it;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+    proj_rope_store_pair(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_xkv,
+                         const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_w_half,
+                         const ProjParams p) {
+  constexpr int STAGES = kPairStages;
+  constexpr uint32_t kTmemCols = 512;  // two 256-column accumulators
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * kABytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(smem + STAGES * kPairStageBytes);
+  uint64_t* full = bars;                  // rank 0's: both CTAs' copies complete here
+  uint64_t* empty = bars + STAGES;        // each CTA's: rank 0's MMAs done with the stage
+  uint64_t* tfull = bars + 2 * STAGES;    // each CTA's: accumulator ready
+  uint64_t* tempty = bars + 2 * STAGES + 2;  // rank 0's: both CTAs' epilogues drained it
+  uint64_t* drain = bars + 2 * STAGES + 4;
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + 2 * STAGES + 5);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();
+  const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full[s], 1);
+      mbar_init(&empty[s], 1);
+    }
+    for (int a = 0; a < 2; ++a) {
+      mbar_init(&tfull[a], 1);
+      mbar_init(&tempty[a], 8);  // four epilogue warps in each CTA
+    }
+    mbar_init(drain, 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+    prefetch_tmap(&tm_x);
+    prefetch_tmap(&tm_xkv);
+    prefetch_tmap(&tm_w);
+    prefetch_tmap(&tm_w_half);
+  }
+  if (warp == 1) {
+    tmem_alloc_pair(tmem_slot, kTmemCols);
+    tmem_relinquish_pair();
+  }
+  tc_fence_before();
+  cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
+  tc_fence_after();
+  const uint32_t tmem_base = *tmem_slot;
+
+  if (warp == 0 && lane == 0) {
+    // ------------------------------------------------------------ TMA producer (both CTAs)
+    const uint64_t pol_x = p.m_fastest ? policy_evict_last() : policy_evict_first();
+    const uint64_t pol_w = p.m_fastest ? policy_evict_first() : policy_evict_last();
+    int stage = 0;
+    uint32_t phase = 0;
+    bool ok = true;
+    for (int item = pair; item < p.items_total && ok; item += n_pairs) {
+      const PairItem it = decode_pair_item(p, item);
+      const CUtensorMap* am = it.grp ? &tm_xkv : &tm_x;
+      const int b_rows = it.half ? 64 : 128;
+      const CUtensorMap* bm = it.half ? &tm_w_half : &tm_w;
+      const int m0 = it.pm0 + static_cast<int>(rank) * 128;
+      const int n0 = it.n0 + static_cast<int>(rank) * b_rows;
+      const uint32_t bytes = 2 * (kABytes + b_rows * BK * 2);  // both CTAs' copies
+      for (int kb = 0; kb < p.k_blocks; ++kb) {
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+        if (rank == 0) mbar_arrive_expect_tx(&full[stage], bytes);
+        const uint32_t fb = map_to_rank(smem_u32(&full[stage]), 0);
+        tma_load_2d_pair(sA + stage * kABytes, am, fb, kb * BK, m0, pol_x);
+        tma_load_2d_pair(sB + stage * kPairBBytes, bm, fb, kb * BK, n0, pol_w);
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      raise_status(p.status, DLLM_DEV_TIMEOUT);
+    }
+    if (rank == 0) {
+      // every copy of both CTAs lands on these barriers: wait for the last phase of each
+      for (int s = 0; s < STAGES; ++s) {
+        const uint32_t par = (s < stage) ? phase : (phase ^ 1u);
+        volatile int never = 0;
+        mbar_wait(&full[s], par, &never);
+      }
+    }
+  } else if (warp == 1 && lane == 0 && rank == 0) {
+    // ------------------------------------------------------------ MMA issuer (rank 0)
+    constexpr uint32_t idesc_whole = idesc_bf16(256, 256, false, false);
+    constexpr uint32_t idesc_half = idesc_bf16(256, 128, false, false);
+    int stage = 0;
+    uint32_t phase = 0;
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;
+    for (int item = pair; item < p.items_total && ok; item += n_pairs) {
+      const uint32_t idesc = decode_pair_item(p, item).half ? idesc_half : idesc_whole;
+      if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; break; }
+      tc_fence_after();
+      const uint32_t d_tmem = tmem_base + acc * 256;
+      for (int kb = 0; kb < p.k_blocks; ++kb) {
+        if (!mbar_wait(&full[stage], phase, abort_flag)) { ok = false; break; }
+        tc_fence_after();
+        const uint32_t a0 = smem_u32(sA + stage * kABytes);
+        const uint32_t b0 = smem_u32(sB + stage * kPairBBytes);
+#pragma unroll
+        for (int k = 0; k < BK / 16; ++k) {
+          tc_mma_f16_pair(d_tmem, sdesc_sw128(a0 + k * 32, 16, 1024), sdesc_sw128(b0 + k * 32, 16, 1024), idesc,
+                          (kb | k) != 0);
+        }
+        tc_commit_pair(&empty[stage]);
+        if (++stage == STAGES) { stage = 0; phase ^= 1u; }
+      }
+      if (!ok) break;
+      tc_commit_pair(&tfull[acc]);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok) {
+      *abort_flag = 1;
+      raise_status(p.status, DLLM_DEV_TIMEOUT);
+    }
+    // Drain: every MMA issued here (into both CTAs' TMEM) finishes before TMEM is freed.
+    tc_commit_pair_local(drain);
+    volatile int never = 0;
+    mbar_wait(drain, 0, &never);
+  } else if (warp >= 2) {
+    // ------------------------------------------------------------ epilogue (both CTAs)
+    const int quarter = warp & 3;
+    const int r = quarter * 32 + lane;
+    const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
+    const uint32_t tempty0 = map_to_rank(smem_u32(&tempty[0]), 0);
+    int acc = 0;
+    uint32_t acc_phase = 0;
+    bool ok = true;  // a failed wait is recorded; the item sequence continues without stores
+    for (int item = pair; item < p.items_total; item += n_pairs) {
+      const PairItem it = decode_pair_item(p, item);
+      if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag)) {
+        ok = false;
+        *abort_flag = 1;
+      }
+      tc_fence_after();
+      TileCoord c;
+      c.grp = it.grp;
+      c.m0 = it.pm0 + static_cast<int>(rank) * 128;
+      c.n0 = it.n0;
+      store_rows(p, c, it.half ? 1 : 2, tmem_base + lane_base + acc * 256, r, ok);
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive_cluster(tempty0 + acc * 8);
+      acc ^= 1;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+    if (!ok) raise_status(p.status, DLLM_DEV_TIMEOUT);
+  }
+
+  tc_fence_before();
+  cluster_sync();  // no CTA leaves while its pair may still touch its memory
+  if (warp == 1) {
+    tc_fence_after();
+    tmem_dealloc_pair(tmem_base, kTmemCols);
   }
 }
 
@@ -412,6 +667,47 @@ int launch_proj_tc(const ProjParams& p, const CUtensorMap& tm_x, const CUtensorM
     k<<<grid, kThreads, Cfg<128>::kSmem, s>>>(tm_x, tm_xkv, tm_w, tm_w_half, p);
   }
   return (int)cudaGetLastError();
+}
+
+int launch_proj_pair(const ProjParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_xkv,
+                     const CUtensorMap& tm_w, const CUtensorMap& tm_w_half, int grid, cudaStream_t s) {
+  cudaError_t e = cudaFuncSetAttribute(proj_rope_store_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kPairSmem);
+  if (e != cudaSuccess) return (int)e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kPairSmem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, proj_rope_store_pair, tm_x, tm_xkv, tm_w, tm_w_half, p);
+  if (e != cudaSuccess) return (int)e;
+  return (int)cudaGetLastError();
+}
+
+// Clusters of two CTAs of the pair kernel that the device can hold at once.
+int proj_pair_max_clusters(int* clusters) {
+  cudaError_t e = cudaFuncSetAttribute(proj_rope_store_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)kPairSmem);
+  if (e != cudaSuccess) return (int)e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(2);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = kPairSmem;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return (int)cudaOccupancyMaxActiveClusters(clusters, proj_rope_store_pair, &cfg);
 }
 
 }  // namespace dllm

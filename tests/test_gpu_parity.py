@@ -122,6 +122,60 @@ def test_topk_bit_exact_with_ties():
     np.testing.assert_array_equal(_topk_gpu(wl), O.kv_topk(wl.mass, wl.block_lo, wl.block_len, wl.drift_k))
 
 
+@pytest.mark.parametrize("k,n_pos", [(7, 5000), (32, 4100), (40, 700), (1, 33)])
+def test_topk_sizes_bit_exact(k, n_pos):
+    # k <= 32 merges per-warp top-32 lists (several rounds per warp above 1024
+    # positions); larger k sorts every candidate
+    wl = W.make(3, batch=4, d_model=256, head_dim=128, max_pos=n_pos, block=min(32, n_pos - k - 1),
+                gen_lo=0, drift_k=k)
+    wl.mass[0, ::3] = wl.mass[0, 1]  # many ties
+    np.testing.assert_array_equal(_topk_gpu(wl), O.kv_topk(wl.mass, wl.block_lo, wl.block_len, wl.drift_k))
+
+
+DRIFT_CASES = [
+    ("bf16", dict(d_model=512, head_dim=128, act="bf16", kv="bf16")),
+    ("f32", dict(d_model=192, head_dim=64, act="f32", kv="f32")),
+    ("e4m3", dict(d_model=512, head_dim=128, act="bf16", kv="e4m3")),
+]
+
+
+@pytest.mark.parametrize("name,kw", DRIFT_CASES, ids=[c[0] for c in DRIFT_CASES])
+def test_drift_cache_types(name, kw):
+    wl = W.make(3, batch=5, max_pos=300, block=16, gen_lo=200, drift_k=24, **kw)
+    idx = _topk_gpu(wl)
+    cache, out, probe, ocache, o_probe = _check_step(wl, probe_idx=idx)
+    ptype = torch.float32 if kw["act"] == "f32" else torch.bfloat16
+    cos = torch.empty((wl.shape.batch, wl.drift_k, 2), dtype=torch.float32, device="cuda")
+    refresh = torch.full((wl.shape.batch,), 7, dtype=torch.int32, device="cuda")
+    pk = torch.from_numpy(probe).to(ptype).cuda()
+    for _ in range(2):  # the per-sequence arrival counters reset themselves
+        capi.dllm_kv_drift(cache.handle, 0, G.idev(idx), pk, 0.9, cos, refresh)
+        o_cos = O.kv_drift(ocache, idx, o_probe)
+        G.assert_close(cos.double().cpu().numpy(), o_cos, G.TOL[kw["kv"]], f"drift cos ({name})")
+        g_min = cos.cpu().numpy().reshape(wl.shape.batch, -1).min(1)
+        np.testing.assert_array_equal(refresh.cpu().numpy(), (g_min < np.float32(0.9)).astype(np.int32))
+
+
+def test_drift_refresh_flags_both_ways():
+    # sequence 0 probes equal their cached tokens (cos = 1, no refresh); sequence 1 gets
+    # unrelated probes (cos near 0, refresh)
+    wl = W.make(3, batch=2, d_model=256, head_dim=128, max_pos=200, block=16, gen_lo=128, drift_k=8)
+    idx = _topk_gpu(wl)
+    cache, out, probe, ocache, o_probe = _check_step(wl, probe_idx=idx)
+    kv = G.gpu_kv(cache)  # [B][slots][2][H][hd]
+    probe = probe.copy()
+    for j in range(wl.drift_k):
+        probe[0, j] = kv[0, idx[0, j]].reshape(2, -1)
+    probe[1] = np.random.default_rng(5).standard_normal(probe[1].shape)
+    pk = torch.from_numpy(probe).to(torch.bfloat16).cuda()
+    cos = torch.empty((2, wl.drift_k, 2), dtype=torch.float32, device="cuda")
+    refresh = torch.empty(2, dtype=torch.int32, device="cuda")
+    capi.dllm_kv_drift(cache.handle, 0, G.idev(idx), pk, 0.9, cos, refresh)
+    c = cos.cpu().numpy()
+    assert np.all(np.abs(c[0] - 1.0) < 1e-3) and np.all(np.abs(c[1]) < 0.2)
+    np.testing.assert_array_equal(refresh.cpu().numpy(), [0, 1])
+
+
 def test_drift_small():
     wl = W.make(3, batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200, drift_k=8)
     idx = _topk_gpu(wl)
