@@ -23,7 +23,8 @@ DLLM_VIEW_BASE, DLLM_VIEW_DRAFT, DLLM_VIEW_MASK = 0, 1, 2
 DEV_BAD_POSITION, DEV_BAD_VIEW, DEV_TAIL_FULL, DEV_TIMEOUT, DEV_BAD_INDEX = 0x1, 0x2, 0x4, 0x8, 0x10
 
 EXPORTS = ("dllm_cache_bytes", "dllm_cache_alloc", "dllm_cache_free", "dllm_cache_get_layout", "dllm_cache_step",
-           "dllm_cache_project", "dllm_cache_attend", "dllm_cache_attend_noalloc", "dllm_kv_topk", "dllm_kv_drift", "dllm_cache_status", "dllm_strerror")
+           "dllm_cache_project", "dllm_cache_attend", "dllm_cache_attend_noalloc", "dllm_unfused_workspace_bytes",
+           "dllm_cache_step_unfused", "dllm_kv_topk", "dllm_kv_drift", "dllm_cache_status", "dllm_strerror")
 
 
 class dllm_cache_desc(ctypes.Structure):
@@ -63,13 +64,17 @@ def lib() -> ctypes.CDLL:
         L.dllm_cache_project.argtypes = L.dllm_cache_step.argtypes
         L.dllm_cache_attend.argtypes = [c_void_p, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p]
         L.dllm_cache_attend_noalloc.argtypes = L.dllm_cache_attend.argtypes
+        L.dllm_unfused_workspace_bytes.argtypes = [c_void_p, c_int, c_int]
+        L.dllm_unfused_workspace_bytes.restype = c_size_t
+        L.dllm_cache_step_unfused.argtypes = [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p,
+                                              c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_size_t, c_void_p]
         L.dllm_kv_topk.argtypes = [c_void_p, c_int, c_int, c_void_p, c_int, c_int, c_void_p, c_void_p]
         L.dllm_kv_drift.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_float, c_void_p, c_void_p, c_void_p]
         L.dllm_cache_status.argtypes = [c_void_p, POINTER(c_int)]
         L.dllm_strerror.argtypes = [c_int]
         L.dllm_strerror.restype = ctypes.c_char_p
         for name in EXPORTS:
-            if name not in ("dllm_cache_bytes", "dllm_strerror"):
+            if name not in ("dllm_cache_bytes", "dllm_strerror", "dllm_unfused_workspace_bytes"):
                 getattr(L, name).restype = c_int
         _lib = L
     return _lib
@@ -151,6 +156,24 @@ def dllm_cache_attend_noalloc(handle, layer: int, positions: torch.Tensor, view:
     """dllm_cache_attend with its scratch in a fixed static device array (no allocation)."""
     _check("dllm_cache_attend_noalloc", lib().dllm_cache_attend_noalloc(
         handle, int(layer), _ptr(positions), _ptr(view), int(positions.shape[-1]), _ptr(out), _stream(stream)))
+
+
+def dllm_unfused_workspace_bytes(handle, n_tok: int, n_kv: int) -> int:
+    return int(lib().dllm_unfused_workspace_bytes(handle, int(n_tok), int(n_kv)))
+
+
+def dllm_cache_step_unfused(handle, layer: int, x: Optional[torch.Tensor], w_qkv: torch.Tensor,
+                            positions: Optional[torch.Tensor], view: Optional[torch.Tensor], out: Optional[torch.Tensor],
+                            workspace: torch.Tensor, kv_x: Optional[torch.Tensor] = None,
+                            kv_positions: Optional[torch.Tensor] = None, probe_kv: Optional[torch.Tensor] = None,
+                            stream=None) -> None:
+    """The four-kernel pipeline (projection, rotary, cache write, attention) for comparison."""
+    n_tok = 0 if positions is None else int(positions.shape[-1])
+    n_kv = 0 if kv_positions is None else int(kv_positions.shape[-1])
+    _check("dllm_cache_step_unfused", lib().dllm_cache_step_unfused(
+        handle, int(layer), _ptr(x), _ptr(w_qkv), _ptr(positions), _ptr(view), n_tok, _ptr(out),
+        _ptr(kv_x), _ptr(kv_positions), n_kv, _ptr(probe_kv), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream)))
 
 
 def dllm_kv_topk(mass: torch.Tensor, block_lo: torch.Tensor, block_len: int, k: int, idx: torch.Tensor,

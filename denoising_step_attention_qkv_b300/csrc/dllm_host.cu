@@ -287,10 +287,12 @@ ProjParams make_proj(dllm_cache* c, const StepArgs& a) {
   return p;
 }
 
-int do_project(dllm_cache* c, const StepArgs& a) {
+int do_project(dllm_cache* c, const StepArgs& a, __nv_bfloat16* raw_q = nullptr, __nv_bfloat16* raw_kv = nullptr) {
   if (a.n_tok == 0 && a.n_kv == 0) return DLLM_OK;
   const dllm_cache_desc& d = c->desc;
   ProjParams p = make_proj(c, a);
+  p.raw_q = raw_q;
+  p.raw_kv = raw_kv;
   const int D = p.D;
   int rc;
   if (d.kv_dtype == DLLM_F32) {
@@ -442,6 +444,48 @@ int dllm_cache_step(dllm_cache* c, int layer, const void* x, const void* w_qkv, 
   }
   rc = do_project(c, a);
   if (rc) return rc;
+  return do_attend(c, layer, positions, view, n_tok, out, a.s);
+}
+
+size_t dllm_unfused_workspace_bytes(const dllm_cache* c, int n_tok, int n_kv) {
+  if (!c || n_tok < 0 || n_kv < 0) return 0;
+  const size_t D = (size_t)c->desc.n_heads * c->desc.head_dim;
+  const size_t q_bytes = (size_t)c->desc.batch * n_tok * 3 * D * 2;
+  const size_t kv_bytes = (size_t)c->desc.batch * n_kv * 2 * D * 2;
+  return ((q_bytes + 255) / 256) * 256 + kv_bytes;
+}
+
+int dllm_cache_step_unfused(dllm_cache* c, int layer, const void* x, const void* w_qkv, const int32_t* positions,
+                            const uint8_t* view, int n_tok, void* out, const void* kv_x, const int32_t* kv_positions,
+                            int n_kv, void* probe_kv, void* workspace, size_t workspace_bytes, void* stream) {
+  StepArgs a{layer, x, w_qkv, positions, view, n_tok, out, kv_x, kv_positions, n_kv, probe_kv,
+             reinterpret_cast<cudaStream_t>(stream)};
+  int rc = check_project(c, a);
+  if (rc) return rc;
+  if (c->desc.kv_dtype == DLLM_F32) return DLLM_EUNSUPPORTED;
+  if (n_tok > 0) {
+    rc = check_attend(c, layer, n_tok, positions, view, out);
+    if (rc) return rc;
+  }
+  const size_t need = dllm_unfused_workspace_bytes(c, n_tok, n_kv);
+  if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return DLLM_EINVAL;
+  if (n_tok == 0 && n_kv == 0) return DLLM_OK;
+  const size_t D = (size_t)c->desc.n_heads * c->desc.head_dim;
+  __nv_bfloat16* raw_q = reinterpret_cast<__nv_bfloat16*>(workspace);
+  __nv_bfloat16* raw_kv = reinterpret_cast<__nv_bfloat16*>(
+      reinterpret_cast<uint8_t*>(workspace) + (((size_t)c->desc.batch * n_tok * 3 * D * 2 + 255) / 256) * 256);
+  // 1. projection GEMM, plain bf16 output to the workspace
+  rc = do_project(c, a, raw_q, raw_kv);
+  if (rc) return rc;
+  // 2. rotary embedding (Q into `out`, K in place), 3. cache (or probe) write
+  ProjParams p = make_proj(c, a);
+  p.raw_q = raw_q;
+  p.raw_kv = raw_kv;
+  rc = launch_rope_rows(p, a.s);
+  if (rc) return from_cuda((cudaError_t)rc);
+  rc = launch_cache_write(p, a.s);
+  if (rc) return from_cuda((cudaError_t)rc);
+  // 4. attention
   return do_attend(c, layer, positions, view, n_tok, out, a.s);
 }
 

@@ -59,6 +59,10 @@ struct ProjParams {
   int max_pos, tail, slots;
   const float2* rope;
   int* status;
+  // Unfused pipeline only (else null): the GEMM stores its plain bf16 output here,
+  // [m_q][3D] for query rows and [m_kv][2D] (K|V) for K/V-only rows, with no rotation.
+  __nv_bfloat16* raw_q;
+  __nv_bfloat16* raw_kv;
 };
 
 // ------------------------------------------------------------------------ attention
@@ -101,6 +105,11 @@ int launch_topk(const float* mass, int batch, int n_pos, const int32_t* block_lo
 int launch_drift(const void* kv_layer, const float* scale_layer, int kv_dtype, int B, int slots, int max_pos,
                  int H, int hd, const int32_t* idx, int k, const void* probe, float gamma, float* cos,
                  int32_t* refresh, int* counters, int sm_count, int* status, cudaStream_t s);
+
+// The conventional pipeline's separate stages (unfused comparison): rotate Q (into
+// q_out) and K (in place) of the raw GEMM output, then write K/V to their slots.
+int launch_rope_rows(const ProjParams& p, cudaStream_t s);
+int launch_cache_write(const ProjParams& p, cudaStream_t s);
 
 size_t proj_tc_smem_bytes(int bn);
 size_t attn_tc_smem_bytes();

@@ -166,6 +166,20 @@ DEVI void rotate32(float (&lo)[32], float (&hi)[32], const float2* __restrict__ 
 // (which raise a status bit), or when `ok` is false.
 DEVI void store_rows(const ProjParams& p, const TileCoord& c, int heads, uint32_t tacc, int r, bool ok) {
   const int hd = kHd;
+  if (p.raw_q != nullptr || p.raw_kv != nullptr) {
+    // unfused pipeline: the plain projection output, rounded to bf16, no rotation
+    const int m = c.m0 + r;
+    const bool exists = ok && (c.grp == 0 ? m < p.m_q : m < p.m_kv);
+    __nv_bfloat16* dst = c.grp == 0 ? p.raw_q + static_cast<size_t>(m) * 3 * p.D + c.n0
+                                    : p.raw_kv + static_cast<size_t>(m) * 2 * p.D + (c.n0 - p.D);
+#pragma unroll 1
+    for (int col = 0; col < heads * kHd; col += 32) {
+      float v[32];
+      tmem_ld32(tacc + col, v);
+      if (exists) store_bf16x32(dst + col, v);
+    }
+    return;
+  }
   // ---- this thread's row
   const int m = c.m0 + r;
   bool valid;

@@ -20,7 +20,9 @@
  *   - D = n_heads * head_dim.  "act" is the activation type: fp32 for a DLLM_F32
  *     cache, bf16 for DLLM_BF16 and DLLM_E4M3 caches.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
- *     stream) and never synchronise, except dllm_cache_alloc/free/status.
+ *     stream) and never synchronise, except dllm_cache_alloc/free/status.  A cache
+ *     owns small workspaces (split-KV partials, drift arrival counters), so calls on
+ *     one cache must be ordered (one stream, or events between streams).
  *   - Every call returns a dllm_status.  Argument errors are detected on the host
  *     before anything is launched and leave all buffers untouched.  Range errors in
  *     device-resident index data (a position outside [0, max_pos), too many draft
@@ -184,6 +186,27 @@ int dllm_cache_project(dllm_cache* cache, int layer,
 int dllm_cache_attend(dllm_cache* cache, int layer,
                       const int32_t* positions, const uint8_t* view, int n_tok,
                       void* out, void* stream);
+
+/* The conventional pipeline, for comparison with the fused step ("Flash-dLLM ...",
+ * paragraph 2: QKV projection, rotary embedding, cache write and attention as four
+ * kernels, each writing its intermediates to HBM for the next one).  Same arguments and
+ * effects as dllm_cache_step, plus a caller-owned device workspace that receives the
+ * projection output: bf16 [batch][n_tok][3D] for the query rows, then (at the next
+ * 256-byte boundary) bf16 [batch][n_kv][2D] for the K/V-only rows.  The projection
+ * output is rounded to bf16 before the rotation and the cache store, so results differ
+ * from dllm_cache_step by that extra rounding.
+ *
+ *   workspace        device buffer of >= dllm_unfused_workspace_bytes() bytes, 256-byte
+ *                    aligned (DLLM_EINVAL otherwise)
+ * Returns DLLM_EUNSUPPORTED for DLLM_F32 caches. */
+size_t dllm_unfused_workspace_bytes(const dllm_cache* cache, int n_tok, int n_kv);
+int dllm_cache_step_unfused(dllm_cache* cache, int layer,
+                            const void* x, const void* w_qkv,
+                            const int32_t* positions, const uint8_t* view, int n_tok,
+                            void* out,
+                            const void* kv_x, const int32_t* kv_positions, int n_kv,
+                            void* probe_kv, void* workspace, size_t workspace_bytes,
+                            void* stream);
 
 /* Top-k most-attended positions ("Flash-dLLM ...", paragraph 4: a fixed budget of the
  * top 32 most-attended tokens; "Elastic-Cache", Core idea: the previous step's
