@@ -24,7 +24,9 @@ DEV_BAD_POSITION, DEV_BAD_VIEW, DEV_TAIL_FULL, DEV_TIMEOUT, DEV_BAD_INDEX = 0x1,
 
 EXPORTS = ("dllm_cache_bytes", "dllm_cache_alloc", "dllm_cache_free", "dllm_cache_get_layout", "dllm_cache_step",
            "dllm_cache_project", "dllm_cache_attend", "dllm_cache_attend_noalloc", "dllm_unfused_workspace_bytes",
-           "dllm_cache_step_unfused", "dllm_kv_topk", "dllm_kv_drift", "dllm_cache_status", "dllm_strerror")
+           "dllm_cache_step_unfused", "dllm_attention_mass", "dllm_kv_topk", "dllm_kv_drift",
+           "dllm_selftest_wait_timeout",
+           "dllm_cache_status", "dllm_strerror")
 
 
 class dllm_cache_desc(ctypes.Structure):
@@ -70,6 +72,8 @@ def lib() -> ctypes.CDLL:
                                               c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_size_t, c_void_p]
         L.dllm_kv_topk.argtypes = [c_void_p, c_int, c_int, c_void_p, c_int, c_int, c_void_p, c_void_p]
         L.dllm_kv_drift.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_float, c_void_p, c_void_p, c_void_p]
+        L.dllm_selftest_wait_timeout.argtypes = [c_void_p, c_void_p]
+        L.dllm_attention_mass.argtypes = [c_void_p, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p]
         L.dllm_cache_status.argtypes = [c_void_p, POINTER(c_int)]
         L.dllm_strerror.argtypes = [c_int]
         L.dllm_strerror.restype = ctypes.c_char_p
@@ -158,6 +162,14 @@ def dllm_cache_attend_noalloc(handle, layer: int, positions: torch.Tensor, view:
         handle, int(layer), _ptr(positions), _ptr(view), int(positions.shape[-1]), _ptr(out), _stream(stream)))
 
 
+def dllm_attention_mass(handle, layer: int, positions: torch.Tensor, view: Optional[torch.Tensor], q: torch.Tensor,
+                        mass: torch.Tensor, stream=None) -> None:
+    """Per-position attention mass of the step (needs the rotated Q from dllm_cache_project)."""
+    _check("dllm_attention_mass", lib().dllm_attention_mass(handle, int(layer), _ptr(positions), _ptr(view),
+                                                            int(positions.shape[-1]), _ptr(q), _ptr(mass),
+                                                            _stream(stream)))
+
+
 def dllm_unfused_workspace_bytes(handle, n_tok: int, n_kv: int) -> int:
     return int(lib().dllm_unfused_workspace_bytes(handle, int(n_tok), int(n_kv)))
 
@@ -188,6 +200,11 @@ def dllm_kv_drift(handle, layer: int, idx: torch.Tensor, probe_kv: torch.Tensor,
     k = int(idx.shape[-1])
     _check("dllm_kv_drift", lib().dllm_kv_drift(handle, int(layer), _ptr(idx), k, _ptr(probe_kv), float(gamma),
                                                 _ptr(cos), _ptr(refresh), _stream(stream)))
+
+
+def dllm_selftest_wait_timeout(handle, stream=None) -> None:
+    """Launch the bounded-wait self-test (sets DEV_TIMEOUT in the status word after ~1 s)."""
+    _check("dllm_selftest_wait_timeout", lib().dllm_selftest_wait_timeout(handle, _stream(stream)))
 
 
 def dllm_cache_status(handle):

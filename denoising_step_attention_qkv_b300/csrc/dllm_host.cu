@@ -447,6 +447,45 @@ int dllm_cache_step(dllm_cache* c, int layer, const void* x, const void* w_qkv, 
   return do_attend(c, layer, positions, view, n_tok, out, a.s);
 }
 
+int dllm_attention_mass(dllm_cache* c, int layer, const int32_t* positions, const uint8_t* view, int n_tok,
+                        const void* q, float* mass, void* stream) {
+  int rc = check_attend(c, layer, n_tok, positions, view, const_cast<void*>(q));
+  if (rc) return rc;
+  if (!mass) return DLLM_EINVAL;
+  if (c->desc.kv_dtype != DLLM_BF16) return DLLM_EUNSUPPORTED;
+  const dllm_cache_desc& d = c->desc;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  cudaError_t e = cudaMemsetAsync(mass, 0, (size_t)d.batch * d.max_pos * sizeof(float), s);
+  if (e != cudaSuccess) return from_cuda(e);
+  if (n_tok == 0) return DLLM_OK;
+  const int B = d.batch, H = d.n_heads, hd = d.head_dim, D = H * hd;
+  AttnParams a{};
+  a.B = B;
+  a.H = H;
+  a.D = D;
+  a.n_tok = n_tok;
+  a.max_pos = d.max_pos;
+  a.tail = d.tail_slots;
+  a.slots = c->slots;
+  a.view = view;
+  a.positions = positions;
+  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)hd));
+  a.kv_dtype = d.kv_dtype;
+  a.status = c->status;
+  a.nq_pad = n_tok <= 32 ? 32 : 64;
+  a.n_qchunks = ceil_div(n_tok, kQChunk);
+  a.key_tiles = ceil_div(d.max_pos + (view ? d.tail_slots : 0), kKeyTile);
+  a.n_splits = 1;
+  a.tiles_per_split = a.key_tiles;
+  a.units = B * H * a.n_qchunks;
+  CUtensorMap tm_q, tm_kv;
+  if (!map_2d_bf16(&tm_q, q, D, (uint64_t)B * n_tok, 64, a.nq_pad)) return DLLM_ECUDA;
+  if (!map_cache(&tm_kv, layer_kv(c, layer), d.kv_dtype, hd, H, (uint64_t)B * c->slots)) return DLLM_ECUDA;
+  const int grid = a.units < c->sm_count ? a.units : c->sm_count;
+  rc = launch_attn_mass(a, tm_q, tm_kv, mass, grid, s);
+  return rc ? from_cuda((cudaError_t)rc) : DLLM_OK;
+}
+
 size_t dllm_unfused_workspace_bytes(const dllm_cache* c, int n_tok, int n_kv) {
   if (!c || n_tok < 0 || n_kv < 0) return 0;
   const size_t D = (size_t)c->desc.n_heads * c->desc.head_dim;

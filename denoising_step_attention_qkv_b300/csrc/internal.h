@@ -95,6 +95,8 @@ int proj_pair_max_clusters(int* clusters);
 int launch_attn_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, int grid,
                    cudaStream_t s);
 int launch_attn_combine(const AttnParams& p, cudaStream_t s);
+int launch_attn_mass(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, float* mass, int grid,
+                     cudaStream_t s);
 
 int launch_proj_f32(const ProjParams& p, const float* x, const float* xkv, const float* w, int hd,
                     cudaStream_t s);

@@ -187,6 +187,23 @@ int dllm_cache_attend(dllm_cache* cache, int layer,
                       const int32_t* positions, const uint8_t* view, int n_tok,
                       void* out, void* stream);
 
+/* Attention mass of this step per cached position ("Flash-dLLM ...", paragraph 4 tracks
+ * the most-attended tokens; "Elastic-Cache", Core idea tests the previous step's
+ * most-attended tokens).  For sequence b and regular slot j < max_pos:
+ *   mass[b][j] = sum over heads h and query rows t of softmax_j(q_{t,h} . k_{j,h} / sqrt(hd)),
+ * with the same visibility rule as the attention (Flash-Verify views included; weights
+ * of draft-view tail slots count in each softmax but are not reported).  The result is
+ * what dllm_kv_topk reads in the next step.
+ *
+ *   q         bf16 [batch][n_tok][D]: the rotated Q that dllm_cache_project leaves in its
+ *             `out` (call this before dllm_cache_attend overwrites it)
+ *   mass      fp32 [batch][max_pos] out (zeroed and filled by the call)
+ * Other arguments as for dllm_cache_attend.  DLLM_BF16 caches only (else
+ * DLLM_EUNSUPPORTED).  Reads the layer's K twice per (sequence, head) unit; the second
+ * read mostly hits L2. */
+int dllm_attention_mass(dllm_cache* cache, int layer, const int32_t* positions, const uint8_t* view, int n_tok,
+                        const void* q, float* mass, void* stream);
+
 /* The conventional pipeline, for comparison with the fused step ("Flash-dLLM ...",
  * paragraph 2: QKV projection, rotary embedding, cache write and attention as four
  * kernels, each writing its intermediates to HBM for the next one).  Same arguments and
@@ -262,6 +279,13 @@ int dllm_kv_drift(const dllm_cache* cache, int layer, const int32_t* idx, int k,
 int dllm_cache_attend_noalloc(dllm_cache* cache, int layer,
                               const int32_t* positions, const uint8_t* view, int n_tok,
                               void* out, void* stream);
+
+/* Self-test of the failure handling: launches one CTA that waits, with the library's
+ * bounded wait, on an mbarrier that nothing arrives at.  The wait gives up after its
+ * time limit (about one second), the kernel sets DLLM_DEV_TIMEOUT in the cache's status
+ * word and ends; dllm_cache_status() then returns DLLM_EDEVICE with that bit and clears
+ * it, and the context stays usable.  Not part of the pages' method. */
+int dllm_selftest_wait_timeout(dllm_cache* cache, void* stream);
 
 /* Synchronise the device, read the cache's device status word into *device_bits (may
  * be NULL) and clear it.  Returns DLLM_EDEVICE if any bit was set, else DLLM_OK. */

@@ -56,7 +56,7 @@ import numpy as np
 __all__ = [
     "VIEW_BASE", "VIEW_DRAFT", "VIEW_MASK", "KVIEW_SHARED", "KVIEW_MASK", "KVIEW_DRAFT", "KVIEW_NONE",
     "rope_inv_freq", "rope", "project_qkv", "project_head", "row_slots", "key_views", "visible", "attention",
-    "OracleCache", "write_rows", "step", "kv_topk", "cosine", "kv_drift",
+    "OracleCache", "write_rows", "step", "kv_topk", "cosine", "kv_drift", "attention_weights", "attention_mass",
     "e4m3_decode", "e4m3_table", "e4m3_quantize", "fp8_group_quantize",
 ]
 
@@ -197,6 +197,18 @@ def attention(q: np.ndarray, K: np.ndarray, V: np.ndarray, vis: Optional[np.ndar
     return np.einsum("hqk,khd->qhd", p, V)
 
 
+def attention_weights(q: np.ndarray, K: np.ndarray, vis: Optional[np.ndarray] = None) -> np.ndarray:
+    """softmax(q K^T / sqrt(hd)) per head, masked by vis: [H][nq][nk] fp64 (rows sum to 1)."""
+    q = np.asarray(q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    s = np.einsum("qhd,khd->hqk", q, K) / math.sqrt(q.shape[-1])
+    if vis is not None:
+        s = np.where(np.asarray(vis, bool)[None, :, :], s, -np.inf)
+    s = s - s.max(axis=-1, keepdims=True)
+    e = np.exp(s)
+    return e / e.sum(axis=-1, keepdims=True)
+
+
 # ------------------------------------------------------------------------------------
 # The flat per-layer cache and one step ([Flash-dLLM] paragraphs 2 and 5).
 # ------------------------------------------------------------------------------------
@@ -292,6 +304,24 @@ def step(cache: OracleCache, w: np.ndarray, theta: float, x: np.ndarray, positio
             raise ValueError("a visible slot was never written")
         out[b] = attention(q[b], cache.K[b], cache.V[b], vis).reshape(n, D)
     return out, probe_kv
+
+
+def attention_mass(cache: OracleCache, q: np.ndarray, positions: np.ndarray,
+                   view: Optional[np.ndarray] = None) -> np.ndarray:
+    """Attention mass each cached position receives in this step: for sequence b and
+    regular slot j, the sum over heads and query rows of the softmax weight of key j
+    ([Flash-dLLM] paragraph 4 and [Elastic-Cache] Core idea track the most-attended
+    tokens).  q: rotated queries [B][n][H][hd] (as ``write_rows`` returns them), read
+    against the cache after the step's writes.  Returns [B][max_pos] fp64."""
+    B, n = positions.shape
+    mass = np.zeros((B, cache.S))
+    for b in range(B):
+        vb = None if view is None else view[b]
+        kview = key_views(positions[b], vb, cache.S, cache.S + cache.T)
+        qview = np.zeros(n, np.int64) if vb is None else np.asarray(vb, np.int64)
+        p = attention_weights(q[b], cache.K[b], visible(qview, kview))
+        mass[b] = p.sum(axis=(0, 1))[:cache.S]
+    return mass
 
 
 # ------------------------------------------------------------------------------------

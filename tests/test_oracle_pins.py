@@ -382,3 +382,44 @@ def test_fp8_cache_stores_group_quantised_values():
             scale = np.max(np.abs(v[t, h])) / 448.0
             codes = c.V[0, s, h] / scale
             np.testing.assert_allclose(O.e4m3_quantize(codes), codes, rtol=1e-12)
+
+
+# ------------------------------------------------------------------ attention mass
+def test_attention_weights_rows_sum_to_one_and_match_attention():
+    r = _rng(20)
+    q, K, V = r.standard_normal((5, 2, 8)), r.standard_normal((9, 2, 8)), r.standard_normal((9, 2, 8))
+    p = O.attention_weights(q, K)
+    np.testing.assert_allclose(p.sum(-1), 1.0, rtol=1e-13)
+    # weights applied to V reproduce the attention output (an independent contraction)
+    np.testing.assert_allclose(np.einsum("hqk,khd->qhd", p, V), O.attention(q, K, V), rtol=1e-12)
+
+
+def test_attention_mass_totals_uniform_keys_and_views():
+    r = _rng(21)
+    S, H, hd, n = 12, 3, 8, 4
+    cache = O.OracleCache(1, S, 0, H, hd)
+    cache.K[0] = r.standard_normal((S, H, hd))
+    q = r.standard_normal((1, n, H, hd))
+    pos = np.array([[2, 5, 7, 9]])
+    m = O.attention_mass(cache, q, pos)
+    assert m.shape == (1, S)
+    np.testing.assert_allclose(m.sum(), H * n, rtol=1e-13)  # every query's weights sum to 1
+    cache.K[0] = 1.0  # identical keys: every slot gets the same share
+    np.testing.assert_allclose(O.attention_mass(cache, q, pos), np.full((1, S), H * n / S), rtol=1e-12)
+    # brute force on one (head, query): a hand-written softmax
+    cache.K[0] = r.standard_normal((S, H, hd))
+    m = O.attention_mass(cache, q[:, :1], pos[:, :1])
+    ref = np.zeros(S)
+    for h in range(H):
+        sc = [float(np.dot(q[0, 0, h], cache.K[0, j, h])) / math.sqrt(hd) for j in range(S)]
+        mx = max(sc)
+        e = [math.exp(v - mx) for v in sc]
+        ref += np.array(e) / sum(e)
+    np.testing.assert_allclose(m[0], ref, rtol=1e-12)
+    # a DRAFT query sees the tail slot, whose mass is not a position's: totals drop
+    cache2 = O.OracleCache(1, S, 2, H, hd)
+    cache2.K[0] = r.standard_normal((S + 2, H, hd))
+    view = np.array([[O.VIEW_BASE, O.VIEW_MASK, O.VIEW_BASE, O.VIEW_DRAFT]])
+    pos2 = np.array([[2, 5, 7, 5]])
+    m2 = O.attention_mass(cache2, q, pos2, view)
+    assert m2.sum() < H * n - 1e-9
