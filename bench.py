@@ -334,6 +334,17 @@ def run_ours(args, rank, world, local):
             return statistics.mean(a_.elapsed_time(b_) for a_, b_ in evs2) * 1e3
 
         t_fused, t_unfused = timed(fused_pair), timed(unfused)
+        # the per-position attention mass that the next step's top-k reads (optional
+        # output; the workload's mass input stands in for it in the timed step)
+        mass_out = torch.empty((B, S), dtype=torch.float32, device=dev)
+
+        def with_mass():
+            capi.dllm_cache_project(cache.handle, 0, x, w, pos, None, out, kv_x=x_probe, kv_positions=idx,
+                                    probe_kv=probe, stream=stream)
+            capi.dllm_attention_mass(cache.handle, 0, pos, None, out, mass_out, stream=stream)
+            capi.dllm_cache_attend(cache.handle, 0, pos, None, out, stream=stream)
+
+        t_mass = timed(with_mass) - t_fused
         attend_us = statistics.mean(per["attend"]) * 1e3
         fvu = {"steps": n_cmp, "fused_project_attend_us": t_fused, "unfused_us": t_unfused,
                "ratio": t_unfused / t_fused,
@@ -341,13 +352,17 @@ def run_ours(args, rank, world, local):
                                    "unfused_us": t_unfused - attend_us,
                                    "ratio": (t_unfused - attend_us) / (statistics.mean(per["project"]) * 1e3)},
                "note": "unfused = projection GEMM to a bf16 workspace, rotary kernel, cache-write kernel, "
-                       "attention; the pages quote 1.37x for the fused kernel alone on an RTX 3090"}
+                       "attention; the pages quote 1.37x for the fused kernel alone on an RTX 3090",
+               "attention_mass_us": t_mass}
 
     # ---- end to end through the C ABI with host buffers (copies inside the timed region).
-    # Each step copies its inputs from pinned host memory and reads its results back; the
-    # copies of one step overlap the compute of its neighbours (copy-in stream, compute
-    # stream, copy-out stream, double-buffered device buffers).  No L2 flush here: every
-    # step streams the whole cache, which is larger than L2.
+    # Every step copies its inputs from pinned host memory and reads its results back.
+    # Steady state is one CUDA graph per step with three independent branches: the
+    # copy-in of step i+1, the four kernels of step i and the read-back of step i-1, on
+    # double-buffered device tensors, so a step costs the slowest branch.  The timed
+    # region is the copy-in of step 0, K graph launches and the read-back of step K-1
+    # (the graphs also copy in one step too many and read back one too many: counted).
+    # No L2 flush here: every step streams the whole cache, which is larger than L2.
     e2e = None
     if not args.no_e2e:
         h_in = [t.cpu().pin_memory() for t in (x, x_probe, pos, mass, block_lo)]
@@ -358,50 +373,60 @@ def run_ours(args, rank, world, local):
         d_probe = [probe, torch.empty_like(probe)]
         h2d = sum(t.numel() * t.element_size() for t in h_in)
         d2h = sum(t.numel() * t.element_size() for t in h_out[0])
-        s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-        ev_in = [torch.cuda.Event() for _ in range(2)]
-        ev_comp = [torch.cuda.Event() for _ in range(2)]
-        ev_out = [torch.cuda.Event() for _ in range(2)]
+        s_cp_in, s_cp_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
 
-        def e2e_run(n):
-            for i in range(n):
-                j = i & 1
-                xi, xpi, posi, massi, loi = d_in[j]
-                outi, cosi, refi = d_out[j]
-                with torch.cuda.stream(s_in):
-                    if i >= 2:
-                        s_in.wait_event(ev_comp[j])  # step i-2 has finished reading these inputs
-                    for d_, h_ in zip(d_in[j], h_in):
-                        d_.copy_(h_, non_blocking=True)
-                    ev_in[j].record(s_in)
-                stream.wait_event(ev_in[j])
-                if i >= 2:
-                    stream.wait_event(ev_out[j])  # step i-2's results have been read back
-                capi.dllm_kv_topk(massi, loi, wl.block_len, k, d_idx[j], stream)
-                capi.dllm_cache_project(cache.handle, 0, xi, w, posi, None, outi, kv_x=xpi, kv_positions=d_idx[j],
-                                        probe_kv=d_probe[j], stream=stream)
-                capi.dllm_cache_attend(cache.handle, 0, posi, None, outi, stream=stream)
-                capi.dllm_kv_drift(cache.handle, 0, d_idx[j], d_probe[j], wl.gamma, cosi, refi, stream=stream)
-                ev_comp[j].record(stream)
-                with torch.cuda.stream(s_out):
-                    s_out.wait_event(ev_comp[j])
-                    for h_, d_ in zip(h_out[j], d_out[j]):
-                        h_.copy_(d_, non_blocking=True)
-                    ev_out[j].record(s_out)
+        def copy_in(j):
+            for d_, h_ in zip(d_in[j], h_in):
+                d_.copy_(h_, non_blocking=True)
 
-        e2e_run(4)
+        def compute(j):
+            xi, xpi, posi, massi, loi = d_in[j]
+            outi, cosi, refi = d_out[j]
+            capi.dllm_kv_topk(massi, loi, wl.block_len, k, d_idx[j])
+            capi.dllm_cache_project(cache.handle, 0, xi, w, posi, None, outi, kv_x=xpi, kv_positions=d_idx[j],
+                                    probe_kv=d_probe[j])
+            capi.dllm_cache_attend(cache.handle, 0, posi, None, outi)
+            capi.dllm_kv_drift(cache.handle, 0, d_idx[j], d_probe[j], wl.gamma, cosi, refi)
+
+        def copy_out(j):
+            for h_, d_ in zip(h_out[j], d_out[j]):
+                h_.copy_(d_, non_blocking=True)
+
+        def capture(j):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                cap = torch.cuda.current_stream()
+                s_cp_in.wait_stream(cap)
+                s_cp_out.wait_stream(cap)
+                with torch.cuda.stream(s_cp_in):
+                    copy_in(j ^ 1)  # the next step's inputs
+                with torch.cuda.stream(s_cp_out):
+                    copy_out(j ^ 1)  # the previous step's results
+                compute(j)
+                cap.wait_stream(s_cp_in)
+                cap.wait_stream(s_cp_out)
+            return g
+
+        graphs = [capture(0), capture(1)]
+        # warm-up: two steps through the graphs
+        copy_in(0)
+        for i in range(4):
+            graphs[i & 1].replay()
         torch.cuda.synchronize(dev)
         if world > 1:
             torch.distributed.barrier()
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(s_in)
-        e2e_run(args.steps)
-        e1.record(s_out)  # after the last read-back, which follows every step's work
+        e0.record(stream)
+        copy_in(0)
+        for i in range(args.steps):
+            graphs[i & 1].replay()
+        copy_out((args.steps - 1) & 1)
+        e1.record(stream)
         torch.cuda.synchronize(dev)
         _, e2e_value = job_rate(e0.elapsed_time(e1), args.steps, world, dev)
         e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h}
+               "d2h_bytes_per_step": d2h, "graphs": "one CUDA graph per step: copy-in(i+1) | step(i) | read-back(i-1)"}
         np.testing.assert_array_equal(h_out[(args.steps - 1) & 1][2].numpy(), refresh.cpu().numpy())
 
     rc, bits = cache.status()

@@ -765,8 +765,7 @@ __global__ void __launch_bounds__(kHd) attn_combine(const AttnParams p) {
 template <int NQ, bool FP8>
 int launch_one(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, int grid, cudaStream_t s) {
   const size_t smem = sizeof(Smem<NQ, FP8>) + 1024;
-  cudaError_t e =
-      cudaFuncSetAttribute(attn_cache_tc<NQ, FP8>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(attn_cache_tc<NQ, FP8>), (int)smem);
   if (e != cudaSuccess) return (int)e;
   attn_cache_tc<NQ, FP8><<<grid, Cfg<NQ, FP8>::kThreads, smem, s>>>(tm_q, tm_kv, p);
   return (int)cudaGetLastError();

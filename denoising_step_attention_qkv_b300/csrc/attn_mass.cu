@@ -337,7 +337,7 @@ template <int NQ>
 int launch_mass_one(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, float* mass, int grid,
                     cudaStream_t s) {
   const size_t smem = sizeof(MassSmem<NQ>) + 1024;
-  cudaError_t e = cudaFuncSetAttribute(attn_mass_tc<NQ>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(attn_mass_tc<NQ>), (int)(smem));
   if (e != cudaSuccess) return (int)e;
   attn_mass_tc<NQ><<<grid, 192, smem, s>>>(tm_q, tm_kv, p, mass);
   return (int)cudaGetLastError();

@@ -13,6 +13,35 @@
 
 using namespace dllm;
 
+namespace dllm {
+
+cudaError_t ensure_smem_limit(const void* kernel, int bytes) {
+  struct Entry {
+    int device;
+    const void* kernel;
+    int bytes;
+  };
+  static std::mutex mu;
+  static std::vector<Entry> table;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  for (Entry& en : table) {
+    if (en.device == dev && en.kernel == kernel) {
+      if (en.bytes >= bytes) return cudaSuccess;
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+      if (e == cudaSuccess) en.bytes = bytes;
+      return e;
+    }
+  }
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess) table.push_back(Entry{dev, kernel, bytes});
+  return e;
+}
+
+}  // namespace dllm
+
 namespace {
 
 int from_cuda(cudaError_t e) {

@@ -31,6 +31,11 @@ struct dllm_cache {
 
 namespace dllm {
 
+// Raise `kernel`'s dynamic shared-memory limit to at least `bytes` on the current
+// device, calling the driver only the first time (per device and kernel) a larger size
+// is needed, so that launches (and stream capture) do no extra driver work.
+cudaError_t ensure_smem_limit(const void* kernel, int bytes);
+
 constexpr int kHd = 128;         // head_dim of the tensor-core path
 constexpr int kQChunk = 64;      // query rows per attention work unit (tensor-core path)
 constexpr int kKeyTile = 128;    // keys per attention tile

@@ -671,12 +671,12 @@ int launch_proj_tc(const ProjParams& p, const CUtensorMap& tm_x, const CUtensorM
   cudaError_t e;
   if (bn == 256) {
     auto k = proj_rope_store_tc<256>;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<256>::kSmem);
+    e = ensure_smem_limit(reinterpret_cast<const void*>(k), (int)(Cfg<256>::kSmem));
     if (e != cudaSuccess) return (int)e;
     k<<<grid, kThreads, Cfg<256>::kSmem, s>>>(tm_x, tm_xkv, tm_w, tm_w_half, p);
   } else {
     auto k = proj_rope_store_tc<128>;
-    e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)Cfg<128>::kSmem);
+    e = ensure_smem_limit(reinterpret_cast<const void*>(k), (int)(Cfg<128>::kSmem));
     if (e != cudaSuccess) return (int)e;
     k<<<grid, kThreads, Cfg<128>::kSmem, s>>>(tm_x, tm_xkv, tm_w, tm_w_half, p);
   }
@@ -685,8 +685,7 @@ int launch_proj_tc(const ProjParams& p, const CUtensorMap& tm_x, const CUtensorM
 
 int launch_proj_pair(const ProjParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_xkv,
                      const CUtensorMap& tm_w, const CUtensorMap& tm_w_half, int grid, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(proj_rope_store_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kPairSmem);
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(proj_rope_store_pair), (int)(kPairSmem));
   if (e != cudaSuccess) return (int)e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(grid);
@@ -707,8 +706,7 @@ int launch_proj_pair(const ProjParams& p, const CUtensorMap& tm_x, const CUtenso
 
 // Clusters of two CTAs of the pair kernel that the device can hold at once.
 int proj_pair_max_clusters(int* clusters) {
-  cudaError_t e = cudaFuncSetAttribute(proj_rope_store_pair, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)kPairSmem);
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(proj_rope_store_pair), (int)(kPairSmem));
   if (e != cudaSuccess) return (int)e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(2);

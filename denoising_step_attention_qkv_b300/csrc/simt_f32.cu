@@ -184,7 +184,7 @@ int launch_attn_f32(const AttnParams& p, const float* kv_layer, int hd, cudaStre
   const int n_keys = p.max_pos + (p.view ? p.tail : 0);
   const size_t smem = (static_cast<size_t>(hd) + n_keys + 32) * sizeof(float);
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(attn_f32, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(attn_f32), (int)(smem));
     if (e != cudaSuccess) return (int)e;
   }
   dim3 grid(p.B * p.n_tok, p.H);

@@ -302,7 +302,7 @@ int launch_topk(const float* mass, int batch, int n_pos, const int32_t* block_lo
   while (n < n_pos) n <<= 1;
   const size_t smem = static_cast<size_t>(n) * 8;
   if (smem > 48 * 1024) {
-    cudaError_t e = cudaFuncSetAttribute(kv_topk_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(kv_topk_kernel), (int)(smem));
     if (e != cudaSuccess) return (int)e;
   }
   const int threads = n < 1024 ? (n < 32 ? 32 : n) : 1024;
