@@ -24,7 +24,8 @@ DEV_BAD_POSITION, DEV_BAD_VIEW, DEV_TAIL_FULL, DEV_TIMEOUT, DEV_BAD_INDEX = 0x1,
 
 EXPORTS = ("dllm_cache_bytes", "dllm_cache_alloc", "dllm_cache_free", "dllm_cache_get_layout", "dllm_cache_step",
            "dllm_cache_project", "dllm_cache_attend", "dllm_cache_attend_noalloc", "dllm_unfused_workspace_bytes",
-           "dllm_cache_step_unfused", "dllm_attention_mass", "dllm_kv_topk", "dllm_kv_drift",
+           "dllm_cache_step_unfused", "dllm_attention_mass", "dllm_cache_attend_ragged", "dllm_cache_attend_partial",
+           "dllm_attend_merge", "dllm_kv_topk", "dllm_kv_drift",
            "dllm_selftest_wait_timeout",
            "dllm_cache_status", "dllm_strerror")
 
@@ -74,6 +75,10 @@ def lib() -> ctypes.CDLL:
         L.dllm_kv_drift.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_float, c_void_p, c_void_p, c_void_p]
         L.dllm_selftest_wait_timeout.argtypes = [c_void_p, c_void_p]
         L.dllm_attention_mass.argtypes = [c_void_p, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p]
+        L.dllm_cache_attend_ragged.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_void_p, c_void_p]
+        L.dllm_cache_attend_partial.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_int, c_int, c_void_p,
+                                                c_void_p]
+        L.dllm_attend_merge.argtypes = [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]
         L.dllm_cache_status.argtypes = [c_void_p, POINTER(c_int)]
         L.dllm_strerror.argtypes = [c_int]
         L.dllm_strerror.restype = ctypes.c_char_p
@@ -168,6 +173,29 @@ def dllm_attention_mass(handle, layer: int, positions: torch.Tensor, view: Optio
     _check("dllm_attention_mass", lib().dllm_attention_mass(handle, int(layer), _ptr(positions), _ptr(view),
                                                             int(positions.shape[-1]), _ptr(q), _ptr(mass),
                                                             _stream(stream)))
+
+
+def dllm_cache_attend_ragged(handle, layer: int, positions: torch.Tensor, key_len: torch.Tensor, out: torch.Tensor,
+                             stream=None) -> None:
+    """Attention of sequence b over its first key_len[b] slots only."""
+    _check("dllm_cache_attend_ragged", lib().dllm_cache_attend_ragged(
+        handle, int(layer), _ptr(positions), int(positions.shape[-1]), _ptr(key_len), _ptr(out), _stream(stream)))
+
+
+def dllm_cache_attend_partial(handle, layer: int, positions: torch.Tensor, q: torch.Tensor, slot_lo: int,
+                              slot_hi: int, state: torch.Tensor, stream=None) -> None:
+    """Partial softmax state (O, m, l) of the query rows over slots [slot_lo, slot_hi)."""
+    _check("dllm_cache_attend_partial", lib().dllm_cache_attend_partial(
+        handle, int(layer), _ptr(positions), int(positions.shape[-1]), _ptr(q), int(slot_lo), int(slot_hi),
+        _ptr(state), _stream(stream)))
+
+
+def dllm_attend_merge(state_a: torch.Tensor, state_b: torch.Tensor, out: Optional[torch.Tensor] = None,
+                      state_out: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Combine two partial states ([B][n][H][hd+2]) into an output and/or a state."""
+    B, n, H, w = state_a.shape
+    _check("dllm_attend_merge", lib().dllm_attend_merge(_ptr(state_a), _ptr(state_b), int(B), int(n), int(H),
+                                                        int(w - 2), _ptr(out), _ptr(state_out), _stream(stream)))
 
 
 def dllm_unfused_workspace_bytes(handle, n_tok: int, n_kv: int) -> int:

@@ -122,9 +122,20 @@ DEVI Unit decode_unit(const AttnParams& p, int u) {
   u /= p.n_qchunks;
   x.h = u % p.H;
   x.b = u / p.H;
-  x.t0 = x.split * p.tiles_per_split;
-  x.t1 = min(p.key_tiles, x.t0 + p.tiles_per_split);
+  x.t0 = p.tile_lo + x.split * p.tiles_per_split;
+  x.t1 = min(p.tile_lo + p.key_tiles, x.t0 + p.tiles_per_split);
+  if (p.key_len) {  // ragged batch: nothing past this sequence's length
+    const int len = min(max(p.key_len[x.b], 0), p.max_pos);
+    x.t1 = min(x.t1, (len + kKeyTile - 1) / kKeyTile);
+  }
+  if (x.t0 > x.t1) x.t0 = x.t1;  // a unit may be empty
   return x;
+}
+
+// End (exclusive) of the regular slots sequence b attends to.
+DEVI int key_end(const AttnParams& p, int b) {
+  const int len = p.key_len ? min(max(p.key_len[b], 0), p.max_pos) : p.max_pos;
+  return min(p.key_hi, len);
 }
 
 // Barrier among the four softmax warps.
@@ -386,26 +397,29 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     // wait hides behind that tile's softmax.
     constexpr bool kDefer = (NQ == 32) && !FP8;
     auto finish = [&](float (&o)[NQ], float (&l)[NQ], const Unit& fx, int fu, int fuu, uint32_t fpv) {
-      const uint32_t ob = fpv & 1u, oph = (fpv >> 1) & 1u;  // the unit's last P V
-      wait(&S.o_full[ob], oph);
-      tc_fence_after();
-      const float4* al4 = reinterpret_cast<const float4*>(S.fin_alpha[fuu & 1]);
+      const bool has_pv = fx.t1 > fx.t0;  // an empty unit (ragged batch, key range) has none
+      if (has_pv) {
+        const uint32_t ob = fpv & 1u, oph = (fpv >> 1) & 1u;  // the unit's last P V
+        wait(&S.o_full[ob], oph);
+        tc_fence_after();
+        const float4* al4 = reinterpret_cast<const float4*>(S.fin_alpha[fuu & 1]);
 #pragma unroll
-      for (int c = 0; c < NQ; c += 32) {
-        float tmp[32];
-        tmem_ld32(tmem + lane_base + 2 * NQ + ob * NQ + c, tmp);
+        for (int c = 0; c < NQ; c += 32) {
+          float tmp[32];
+          tmem_ld32(tmem + lane_base + 2 * NQ + ob * NQ + c, tmp);
 #pragma unroll
-        for (int i = 0; i < 32; i += 4) {
-          const float4 al = al4[(c + i) / 4];
-          o[c + i] = o[c + i] * al.x + tmp[i];
-          o[c + i + 1] = o[c + i + 1] * al.y + tmp[i + 1];
-          o[c + i + 2] = o[c + i + 2] * al.z + tmp[i + 2];
-          o[c + i + 3] = o[c + i + 3] * al.w + tmp[i + 3];
+          for (int i = 0; i < 32; i += 4) {
+            const float4 al = al4[(c + i) / 4];
+            o[c + i] = o[c + i] * al.x + tmp[i];
+            o[c + i + 1] = o[c + i + 1] * al.y + tmp[i + 1];
+            o[c + i + 2] = o[c + i + 2] * al.z + tmp[i + 2];
+            o[c + i + 3] = o[c + i + 3] * al.w + tmp[i + 3];
+          }
         }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.o_free[ob]);
       }
-      tc_fence_before();
-      __syncwarp();
-      if (lane == 0) mbar_arrive(&S.o_free[ob]);
       // row sums: reduce the per-key partial sums over the 128 threads
 #pragma unroll
       for (int c = 0; c < NQ; c += 32) S.red[quarter][c + lane] = reduce_scatter32<false>(l + c, lane);
@@ -418,7 +432,17 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       softmax_sync();
       const int frow0 = fx.b * p.n_tok + fx.qc * kQChunk;
       const int fnrows = min(kQChunk, p.n_tok - fx.qc * kQChunk);
-      if (p.n_splits == 1) {
+      if (p.state != nullptr) {  // partial softmax state of the key range
+        constexpr int kSt = kHd + 2;
+        float* st = p.state + (static_cast<size_t>(frow0) * p.H + fx.h) * kSt;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q)
+          if (ok && q < fnrows) st[static_cast<size_t>(q) * p.H * kSt + r] = o[q];
+        if (ok && r < NQ && r < fnrows) {
+          st[static_cast<size_t>(r) * p.H * kSt + kHd] = has_pv ? S.fin_m[fuu & 1][r] : -INFINITY;
+          st[static_cast<size_t>(r) * p.H * kSt + kHd + 1] = S.l_fin[r];
+        }
+      } else if (p.n_splits == 1) {
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(frow0) * p.D + fx.h * kHd + r;
         const float4* il4 = reinterpret_cast<const float4*>(S.inv_l);
 #pragma unroll
@@ -435,7 +459,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         for (int q = 0; q < NQ; ++q) wo[q * kHd + r] = o[q];
         if (r < NQ) {
           float* wml = p.ws + static_cast<size_t>(p.units) * kQChunk * kHd + (static_cast<size_t>(fu) * kQChunk + r) * 2;
-          wml[0] = S.fin_m[fuu & 1][r];
+          wml[0] = has_pv ? S.fin_m[fuu & 1][r] : -INFINITY;
           wml[1] = S.l_fin[r];
         }
       }
@@ -452,6 +476,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       const Unit x = decode_unit(p, u);
       const int row0 = x.b * p.n_tok;  // first row of the sequence
       const int nrows = min(kQChunk, p.n_tok - x.qc * kQChunk);  // valid columns of this chunk
+      const int kend = key_end(p, x.b);  // regular slots past this are not attended
       // ---- per-unit set-up: running max and Flash-Verify tags
       if (r < NQ) S.m_run[r] = -INFINITY;
       if (has_view) {
@@ -509,6 +534,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         } else {
           vis = (j < p.max_pos + n_draft) ? dmask : 0ull;
         }
+        if (p.ranged && (j < p.key_lo || j >= kend)) vis = 0ull;
         float k_scale = 1.0f, v_scale = 1.0f;
         if (FP8 && vis) {
           const size_t srow = (static_cast<size_t>(x.b) * p.slots + j) * 2;
@@ -557,7 +583,8 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
           // Slots past the regular region that no query sees may hold anything (stale
           // draft views, the next sequence, never-written memory).  Their P is 0, but
           // 0 * NaN would still poison O, so their V rows are zeroed before the PV MMA.
-          if (!FP8 && (t + 1) * kKeyTile > p.max_pos && vis == 0ull && j >= p.max_pos) {
+          if (!FP8 && (p.ranged || (t + 1) * kKeyTile > p.max_pos) && vis == 0ull &&
+              (p.ranged || j >= p.max_pos)) {
             wait(&S.v_full[vs], vph);
             uint4* row0v = reinterpret_cast<uint4*>(S.v[vs] + r * 128);
             uint4* row1v = reinterpret_cast<uint4*>(S.v[vs] + kTileBytes / 2 + r * 128);
@@ -626,6 +653,10 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       }
       // ---- unit end: finish now, or hand the state to the next unit's first tile
       if constexpr (kDefer) {
+        if (pending) {  // this unit had no tile to finish the previous one in
+          finish(o_prev, l_prev, px, pu, puu, ppv);
+          pending = false;
+        }
 #pragma unroll
         for (int q = 0; q < NQ; ++q) {
           o_prev[q] = o_acc[q];
@@ -664,7 +695,8 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         for (int t = 0; t < p.n_tok; ++t) n_draft += (p.view[x.b * p.n_tok + t] == DLLM_VIEW_DRAFT);
         n_draft = min(n_draft, p.tail);
       }
-      const int kend = p.max_pos + n_draft;
+      const int tail_end = p.max_pos + n_draft;
+      const int kend = key_end(p, x.b);
       for (int t = x.t0; t < x.t1; ++t) {
         const int j = t * kKeyTile + r;
         const uint32_t sw = static_cast<uint32_t>(r & 7);
@@ -698,7 +730,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         {
           const uint8_t* src = S.sv[ss] + r * 128;
           uint8_t* dst = S.v[vo] + r * 128;
-          const bool zero = j >= kend;
+          const bool zero = j < p.max_pos ? (p.ranged && (j < p.key_lo || j >= kend)) : j >= tail_end;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
@@ -760,7 +792,42 @@ __global__ void __launch_bounds__(kHd) attn_combine(const AttnParams p) {
       __float2bfloat16_rn(L > 0.0f ? O / L : 0.0f);
 }
 
+// Merge two partial states of the same rows (FACache-style: a cached state of keys that
+// did not change and a fresh state of keys that did).  m in base-2 units:
+//   M = max(m_a, m_b), O = 2^(m_a - M) O_a + 2^(m_b - M) O_b, l likewise.
+__global__ void __launch_bounds__(kHd) state_merge(const float* __restrict__ a, const float* __restrict__ b,
+                                                   int H, __nv_bfloat16* out, float* state_out) {
+  constexpr int kSt = kHd + 2;
+  const size_t rh = static_cast<size_t>(blockIdx.x) * H + blockIdx.y;  // (row, head)
+  const int i = threadIdx.x;
+  const float* sa = a + rh * kSt;
+  const float* sb = b + rh * kSt;
+  const float ma = sa[kHd], mb = sb[kHd];
+  const float M = fmaxf(ma, mb);
+  float O = 0.0f, L = 0.0f;
+  if (M != -INFINITY) {
+    const float wa = ma == -INFINITY ? 0.0f : exp2f(ma - M);
+    const float wb = mb == -INFINITY ? 0.0f : exp2f(mb - M);
+    O = sa[i] * wa + sb[i] * wb;
+    L = sa[kHd + 1] * wa + sb[kHd + 1] * wb;
+  }
+  if (out) out[static_cast<size_t>(blockIdx.x) * H * kHd + blockIdx.y * kHd + i] = __float2bfloat16_rn(L > 0.0f ? O / L : 0.0f);
+  if (state_out) {
+    float* so = state_out + rh * kSt;
+    so[i] = O;
+    if (i == 0) {
+      so[kHd] = M;
+      so[kHd + 1] = L;
+    }
+  }
+}
+
 }  // namespace
+
+int launch_state_merge(const float* a, const float* b, int rows, int H, void* out, float* state_out, cudaStream_t s) {
+  state_merge<<<dim3(rows, H), kHd, 0, s>>>(a, b, H, reinterpret_cast<__nv_bfloat16*>(out), state_out);
+  return (int)cudaGetLastError();
+}
 
 template <int NQ, bool FP8>
 int launch_one(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, int grid, cudaStream_t s) {

@@ -386,8 +386,17 @@ int do_project(dllm_cache* c, const StepArgs& a, __nv_bfloat16* raw_q = nullptr,
   return rc ? from_cuda((cudaError_t)rc) : DLLM_OK;
 }
 
+// Key range of an attention launch: regular slots [lo, hi) of every sequence, further
+// limited to the first key_len[b] slots of sequence b when key_len is given; state
+// (partial softmax state per row and head) replaces the normalised output when given.
+struct KeyRange {
+  int lo = 0, hi = -1;  // hi < 0: every slot (and the Flash-Verify tail)
+  const int32_t* key_len = nullptr;
+  float* state = nullptr;
+};
+
 int do_attend(dllm_cache* c, int layer, const int32_t* positions, const uint8_t* view, int n_tok, void* out,
-              cudaStream_t s) {
+              cudaStream_t s, const KeyRange& kr = KeyRange()) {
   if (n_tok == 0) return DLLM_OK;
   const dllm_cache_desc& d = c->desc;
   const int B = d.batch, H = d.n_heads, hd = d.head_dim, D = H * hd;
@@ -407,17 +416,30 @@ int do_attend(dllm_cache* c, int layer, const int32_t* positions, const uint8_t*
   a.kv_scale = layer_scale(c, layer);
   a.kv_dtype = d.kv_dtype;
   a.status = c->status;
+  a.key_lo = 0;
+  a.key_hi = d.max_pos;
+  a.tile_lo = 0;
+  a.key_len = kr.key_len;
+  a.state = kr.state;
+  a.ranged = kr.hi >= 0 || kr.key_len != nullptr;
+  if (kr.hi >= 0) {
+    a.key_lo = kr.lo;
+    a.key_hi = kr.hi;
+    a.tile_lo = kr.lo / kKeyTile;
+  }
   int rc;
   if (d.kv_dtype == DLLM_F32) {
+    if (a.ranged || a.state) return DLLM_EUNSUPPORTED;
     rc = launch_attn_f32(a, (const float*)layer_kv(c, layer), hd, s);
     return rc ? from_cuda((cudaError_t)rc) : DLLM_OK;
   }
   a.nq_pad = n_tok <= 32 ? 32 : 64;
   a.n_qchunks = ceil_div(n_tok, kQChunk);
-  a.key_tiles = ceil_div(d.max_pos + (view ? d.tail_slots : 0), kKeyTile);
+  a.key_tiles = kr.hi >= 0 ? ceil_div(a.key_hi, kKeyTile) - a.tile_lo
+                           : ceil_div(d.max_pos + (view ? d.tail_slots : 0), kKeyTile);
   const int base = B * H * a.n_qchunks;
   int splits = 1;
-  if (base < c->sm_count) {
+  if (base < c->sm_count && !a.state) {  // a partial state is written by one unit per row
     splits = ceil_div(c->sm_count, base);
     if (splits > a.key_tiles) splits = a.key_tiles;
   }
@@ -474,6 +496,40 @@ int dllm_cache_step(dllm_cache* c, int layer, const void* x, const void* w_qkv, 
   rc = do_project(c, a);
   if (rc) return rc;
   return do_attend(c, layer, positions, view, n_tok, out, a.s);
+}
+
+int dllm_cache_attend_ragged(dllm_cache* c, int layer, const int32_t* positions, int n_tok, const int32_t* key_len,
+                             void* out, void* stream) {
+  int rc = check_attend(c, layer, n_tok, positions, nullptr, out);
+  if (rc) return rc;
+  if (!key_len) return DLLM_EINVAL;
+  KeyRange kr;
+  kr.key_len = key_len;
+  return do_attend(c, layer, positions, nullptr, n_tok, out, reinterpret_cast<cudaStream_t>(stream), kr);
+}
+
+int dllm_cache_attend_partial(dllm_cache* c, int layer, const int32_t* positions, int n_tok, const void* q,
+                              int slot_lo, int slot_hi, float* state, void* stream) {
+  int rc = check_attend(c, layer, n_tok, positions, nullptr, const_cast<void*>(q));
+  if (rc) return rc;
+  if (!state || !aligned16(state) || slot_lo < 0 || slot_hi <= slot_lo || slot_hi > c->desc.max_pos)
+    return DLLM_EINVAL;
+  KeyRange kr;
+  kr.lo = slot_lo;
+  kr.hi = slot_hi;
+  kr.state = state;
+  return do_attend(c, layer, positions, nullptr, n_tok, const_cast<void*>(q), reinterpret_cast<cudaStream_t>(stream),
+                   kr);
+}
+
+int dllm_attend_merge(const float* state_a, const float* state_b, int batch, int n_tok, int n_heads, int head_dim,
+                      void* out, float* state_out, void* stream) {
+  if (!state_a || !state_b || (!out && !state_out) || batch < 1 || n_tok < 0 || n_heads < 1) return DLLM_EINVAL;
+  if (head_dim != kHd) return DLLM_EUNSUPPORTED;
+  if (n_tok == 0) return DLLM_OK;
+  const int rc = launch_state_merge(state_a, state_b, batch * n_tok, n_heads, out, state_out,
+                                    reinterpret_cast<cudaStream_t>(stream));
+  return rc ? from_cuda((cudaError_t)rc) : DLLM_OK;
 }
 
 int dllm_attention_mass(dllm_cache* c, int layer, const int32_t* positions, const uint8_t* view, int n_tok,

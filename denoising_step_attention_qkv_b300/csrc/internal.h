@@ -86,6 +86,15 @@ struct AttnParams {
   float scale_log2;  // log2(e) / sqrt(hd)
   const float* kv_scale;  // this layer, e4m3 only
   int kv_dtype;
+  // Key range (regular slots only; the defaults cover every slot): keys j with
+  // key_lo <= j < min(key_hi, key_len[b]) are attended.  tile_lo = key_lo / 128; the
+  // units cover key_tiles tiles from there.  key_len (device, [B]) or null.
+  int key_lo, key_hi, tile_lo;
+  const int32_t* key_len;
+  bool ranged;       // key_lo > 0, key_hi < max_pos or key_len given
+  // Partial-state output instead of `out` (no key splits then):
+  // fp32 [B][n_tok][H][hd + 2] = (unnormalised O, m, l), m in base-2 units.
+  float* state;
   int* status;
 };
 
@@ -100,6 +109,9 @@ int proj_pair_max_clusters(int* clusters);
 int launch_attn_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, int grid,
                    cudaStream_t s);
 int launch_attn_combine(const AttnParams& p, cudaStream_t s);
+// Merge two partial softmax states (rows x heads, [hd + 2] each) into a normalised bf16
+// output and/or a merged state.
+int launch_state_merge(const float* a, const float* b, int rows, int H, void* out, float* state_out, cudaStream_t s);
 int launch_attn_mass(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, float* mass, int grid,
                      cudaStream_t s);
 

@@ -187,6 +187,43 @@ int dllm_cache_attend(dllm_cache* cache, int layer,
                       const int32_t* positions, const uint8_t* view, int n_tok,
                       void* out, void* stream);
 
+/* Attention over a ragged batch ("Elastic-Cache", Deployment notes: a batch built from
+ * sequences of different lengths): as dllm_cache_attend without Flash-Verify views, but
+ * sequence b attends only to its first key_len[b] slots (clamped to [0, max_pos]); cache
+ * tiles past that length are not read.  A row whose sequence has key_len 0 gets zeros.
+ *
+ *   key_len   int32 [batch], device
+ * DLLM_BF16 and DLLM_E4M3 caches (DLLM_EUNSUPPORTED for DLLM_F32). */
+int dllm_cache_attend_ragged(dllm_cache* cache, int layer, const int32_t* positions, int n_tok,
+                             const int32_t* key_len, void* out, void* stream);
+
+/* Partial attention state over a slot range ("LaCache ...", Methodology 1, FACache: the
+ * running maximum m, the normaliser l and the unnormalised accumulator O of online
+ * softmax are cached for key blocks that do not change and combined with those of the
+ * blocks that do, instead of re-reading the unchanged keys).  For every query row t,
+ * head h and the keys j in [slot_lo, slot_hi):
+ *   s_j = (q . k_j) / sqrt(hd) * log2(e),  m = max_j s_j,  l = sum_j 2^(s_j - m),
+ *   O[i] = sum_j 2^(s_j - m) v_j[i]
+ * (m = -inf, l = 0, O = 0 when the range holds no key).
+ *
+ *   q         bf16 [batch][n_tok][D]: rotated Q (dllm_cache_project's `out`); not modified,
+ *             so several ranges can be evaluated from the same q
+ *   state     fp32 [batch][n_tok][n_heads][head_dim + 2] out: O, then m, then l; 16-byte
+ *             aligned
+ *   0 <= slot_lo < slot_hi <= max_pos (regular slots; no Flash-Verify views)
+ * DLLM_BF16 and DLLM_E4M3 caches. */
+int dllm_cache_attend_partial(dllm_cache* cache, int layer, const int32_t* positions, int n_tok, const void* q,
+                              int slot_lo, int slot_hi, float* state, void* stream);
+
+/* Combine two partial states of the same rows (the key ranges must not overlap):
+ *   M = max(m_a, m_b), w_a = 2^(m_a - M), w_b = 2^(m_b - M),
+ *   O = w_a O_a + w_b O_b, l = w_a l_a + w_b l_b,
+ * and write the attention output out = O / l (bf16 [batch][n_tok][n_heads * head_dim],
+ * 0 where l = 0) and/or the combined state (same layout as the inputs; may alias
+ * neither input).  Either output may be NULL, not both.  head_dim must be 128. */
+int dllm_attend_merge(const float* state_a, const float* state_b, int batch, int n_tok, int n_heads, int head_dim,
+                      void* out, float* state_out, void* stream);
+
 /* Attention mass of this step per cached position ("Flash-dLLM ...", paragraph 4 tracks
  * the most-attended tokens; "Elastic-Cache", Core idea tests the previous step's
  * most-attended tokens).  For sequence b and regular slot j < max_pos:

@@ -57,6 +57,7 @@ __all__ = [
     "VIEW_BASE", "VIEW_DRAFT", "VIEW_MASK", "KVIEW_SHARED", "KVIEW_MASK", "KVIEW_DRAFT", "KVIEW_NONE",
     "rope_inv_freq", "rope", "project_qkv", "project_head", "row_slots", "key_views", "visible", "attention",
     "OracleCache", "write_rows", "step", "kv_topk", "cosine", "kv_drift", "attention_weights", "attention_mass",
+    "attention_partial", "merge_states", "state_output", "range_visible",
     "e4m3_decode", "e4m3_table", "e4m3_quantize", "fp8_group_quantize",
 ]
 
@@ -207,6 +208,55 @@ def attention_weights(q: np.ndarray, K: np.ndarray, vis: Optional[np.ndarray] = 
     s = s - s.max(axis=-1, keepdims=True)
     e = np.exp(s)
     return e / e.sum(axis=-1, keepdims=True)
+
+
+# ------------------------------------------------------------------------------------
+# Partial softmax states ([LaCache] Methodology 1, FACache: the running maximum m, the
+# normaliser l and the unnormalised accumulator O of online softmax, kept for key blocks
+# that do not change and combined with the blocks that do).  Base-2 units, as the
+# kernels keep them: s = q.k / sqrt(hd) * log2(e).
+# ------------------------------------------------------------------------------------
+
+LOG2E = 1.0 / math.log(2.0)
+
+
+def range_visible(n_q: int, n_keys: int, lo: int, hi: int) -> np.ndarray:
+    """Boolean [n_q][n_keys]: keys lo <= j < hi visible to every query."""
+    v = np.zeros((n_q, n_keys), bool)
+    v[:, max(lo, 0):max(min(hi, n_keys), 0)] = True
+    return v
+
+
+def attention_partial(q: np.ndarray, K: np.ndarray, V: np.ndarray, vis: Optional[np.ndarray] = None):
+    """State of q [nq][H][hd] over keys K, V [nk][H][hd] (masked by vis [nq][nk]):
+    m = max_j s_j, l = sum_j 2^(s_j - m), O = sum_j 2^(s_j - m) v_j.
+    Returns (O [nq][H][hd], m [nq][H], l [nq][H]); m = -inf, l = 0, O = 0 without keys."""
+    q = np.asarray(q, dtype=np.float64)
+    K = np.asarray(K, dtype=np.float64)
+    V = np.asarray(V, dtype=np.float64)
+    s = np.einsum("qhd,khd->qhk", q, K) / math.sqrt(q.shape[-1]) * LOG2E
+    if vis is not None:
+        s = np.where(np.asarray(vis, bool)[:, None, :], s, -np.inf)
+    m = s.max(axis=-1) if s.shape[-1] else np.full(s.shape[:2], -np.inf)
+    w = np.where(np.isfinite(m)[..., None], np.exp2(s - np.where(np.isfinite(m), m, 0.0)[..., None]), 0.0)
+    return np.einsum("qhk,khd->qhd", w, V), m, w.sum(axis=-1)
+
+
+def merge_states(a, b):
+    """Combine two states of the same rows over disjoint key sets."""
+    Oa, ma, la = a
+    Ob, mb, lb = b
+    M = np.maximum(ma, mb)
+    Mu = np.where(np.isfinite(M), M, 0.0)
+    wa = np.where(np.isfinite(ma), np.exp2(ma - Mu), 0.0)
+    wb = np.where(np.isfinite(mb), np.exp2(mb - Mu), 0.0)
+    return Oa * wa[..., None] + Ob * wb[..., None], M, la * wa + lb * wb
+
+
+def state_output(st) -> np.ndarray:
+    """Normalised attention output O / l (0 where l = 0)."""
+    O, _, l = st
+    return np.where(l[..., None] > 0, O / np.where(l > 0, l, 1.0)[..., None], 0.0)
 
 
 # ------------------------------------------------------------------------------------

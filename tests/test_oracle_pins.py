@@ -423,3 +423,40 @@ def test_attention_mass_totals_uniform_keys_and_views():
     pos2 = np.array([[2, 5, 7, 5]])
     m2 = O.attention_mass(cache2, q, pos2, view)
     assert m2.sum() < H * n - 1e-9
+
+
+# -------------------------------------------------------------- partial softmax states
+def test_partial_states_merge_to_full_attention():
+    r = _rng(30)
+    q, K, V = r.standard_normal((4, 2, 16)), r.standard_normal((20, 2, 16)), r.standard_normal((20, 2, 16))
+    full = O.attention(q, K, V)
+    for cut in (1, 7, 19):
+        a = O.attention_partial(q, K[:cut], V[:cut])
+        b = O.attention_partial(q, K[cut:], V[cut:])
+        np.testing.assert_allclose(O.state_output(O.merge_states(a, b)), full, rtol=1e-12, atol=1e-14)
+        np.testing.assert_allclose(O.state_output(O.merge_states(b, a)), full, rtol=1e-12, atol=1e-14)
+    # the same through visibility masks over the whole key set
+    va = O.range_visible(4, 20, 0, 11)
+    vb = O.range_visible(4, 20, 11, 20)
+    st = O.merge_states(O.attention_partial(q, K, V, va), O.attention_partial(q, K, V, vb))
+    np.testing.assert_allclose(O.state_output(st), full, rtol=1e-12, atol=1e-14)
+
+
+def test_partial_state_closed_forms():
+    r = _rng(31)
+    q, K, V = r.standard_normal((3, 1, 8)), r.standard_normal((5, 1, 8)), r.standard_normal((5, 1, 8))
+    O1, m1, l1 = O.attention_partial(q, K[2:3], V[2:3])  # one key: l = 1, O = v, m = its score
+    np.testing.assert_allclose(l1, 1.0, rtol=0)
+    np.testing.assert_allclose(O1[:, 0], np.broadcast_to(V[2, 0], (3, 8)), rtol=1e-15)
+    np.testing.assert_allclose(m1[:, 0], q[:, 0] @ K[2, 0] / math.sqrt(8) / math.log(2.0), rtol=1e-13)
+    Oe, me, le = O.attention_partial(q, K, V, O.range_visible(3, 5, 2, 2))  # empty range
+    assert np.all(me == -np.inf) and np.all(le == 0) and np.all(Oe == 0)
+    # m + log2(l) is the base-2 log-sum-exp of the scores
+    _, m, l = O.attention_partial(q, K, V)
+    sc = np.einsum("qhd,khd->qhk", q, K) / math.sqrt(8) / math.log(2.0)
+    np.testing.assert_allclose(m + np.log2(l), np.logaddexp2.reduce(sc, axis=-1), rtol=1e-12)
+    # merging with an empty state changes nothing
+    st = O.attention_partial(q, K, V)
+    mg = O.merge_states(st, (Oe, me, le))
+    for x, y in zip(mg, st):
+        np.testing.assert_allclose(x, y, rtol=1e-15)
