@@ -301,6 +301,21 @@ def run_ours(args, rank, world, local):
         per["drift"].append(ev[3].elapsed_time(ev[4]))
     ms_per_step, value = job_rate(sum(per["step"]), args.steps, world, dev)
 
+    def timed_us(fn, n):
+        """Mean device time of fn in microseconds over n calls, L2 flushed before each."""
+        for _ in range(3):
+            fn()
+        evs2 = []
+        for _ in range(n):
+            flush.zero_()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            fn()
+            b_.record(stream)
+            evs2.append((a_, b_))
+        torch.cuda.synchronize(dev)
+        return statistics.mean(a_.elapsed_time(b_) for a_, b_ in evs2) * 1e3
+
     # ---- fused vs the conventional four-kernel pipeline (projection GEMM, rotary, cache
     # write, attention as separate kernels with intermediates in HBM), same inputs and
     # L2 flush; the projection part of the unfused step is its total minus the attention
@@ -320,18 +335,7 @@ def run_ours(args, rank, world, local):
                                          kv_positions=idx, probe_kv=probe, stream=stream)
 
         def timed(fn):
-            for _ in range(3):
-                fn()
-            evs2 = []
-            for _ in range(n_cmp):
-                flush.zero_()
-                a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-                a_.record(stream)
-                fn()
-                b_.record(stream)
-                evs2.append((a_, b_))
-            torch.cuda.synchronize(dev)
-            return statistics.mean(a_.elapsed_time(b_) for a_, b_ in evs2) * 1e3
+            return timed_us(fn, n_cmp)
 
         t_fused, t_unfused = timed(fused_pair), timed(unfused)
         # the per-position attention mass that the next step's top-k reads (optional
@@ -354,6 +358,44 @@ def run_ours(args, rank, world, local):
                "note": "unfused = projection GEMM to a bf16 workspace, rotary kernel, cache-write kernel, "
                        "attention; the pages quote 1.37x for the fused kernel alone on an RTX 3090",
                "attention_mass_us": t_mass}
+
+    # ---- ragged batches and partial softmax states over slot ranges, on this step's
+    # rotated queries: ragged attention with seeded per-sequence key lengths, a partial
+    # state over the last quarter of the slots, and the merge of two states.  Bytes are
+    # algorithmic (keys and values read once, queries read, outputs written).
+    nxt = None
+    if not args.no_unfused:
+        n_nx = min(args.steps, 200)
+        n_tok = wl.x.shape[1]
+        H, hd = s.n_heads, s.head_dim
+        q_rows = torch.empty_like(out)
+        capi.dllm_cache_project(cache.handle, 0, x, w, pos, None, q_rows, stream=stream)
+        scratch = q_rows.clone()  # holds queries on entry; each call overwrites it with its output
+        lens = np.random.default_rng(1234).integers(128, S + 1, size=B).astype(np.int32)
+        key_len = torch.from_numpy(lens).to(dev)
+        t_rag = timed_us(lambda: capi.dllm_cache_attend_ragged(cache.handle, 0, pos, key_len, scratch, stream=stream),
+                         n_nx)
+        rag_bytes = float(lens.sum()) * H * hd * 2 * 2 + 2 * B * n_tok * D * 2
+        st_shape = (B, n_tok, H, hd + 2)
+        st_a = torch.empty(st_shape, dtype=torch.float32, device=dev)
+        st_b = torch.empty_like(st_a)
+        lo = S - S // 4
+        t_part = timed_us(lambda: capi.dllm_cache_attend_partial(cache.handle, 0, pos, q_rows, lo, S, st_a,
+                                                                 stream=stream), n_nx)
+        part_bytes = float(B) * (S - lo) * H * hd * 2 * 2 + B * n_tok * D * 2 + st_a.numel() * 4
+        capi.dllm_cache_attend_partial(cache.handle, 0, pos, q_rows, 0, lo, st_b, stream=stream)
+        t_merge = timed_us(lambda: capi.dllm_attend_merge(st_a, st_b, out=scratch, stream=stream), n_nx)
+        merge_bytes = 2.0 * st_a.numel() * 4 + B * n_tok * D * 2
+        hbm = peaks()["hbm_gbs"]
+
+        def row(us, nbytes, **kw):
+            gbs = nbytes / (us * 1e-6) / 1e9
+            return dict(us=us, algorithmic_bytes=nbytes, achieved_gbs=gbs, frac=gbs / hbm, **kw)
+
+        nxt = {"steps": n_nx,
+               "ragged": row(t_rag, rag_bytes, key_len="seeded uniform [128, %d], mean %.0f" % (S, lens.mean())),
+               "partial_state": row(t_part, part_bytes, slots=[lo, S]),
+               "merge": row(t_merge, merge_bytes)}
 
     # ---- end to end through the C ABI with host buffers (copies inside the timed region).
     # Every step copies its inputs from pinned host memory and reads its results back.
@@ -464,7 +506,7 @@ def run_ours(args, rank, world, local):
                    "l2": "value: flushed between steps (256 MiB write); e2e: no flush, every step streams the 512 MiB cache (larger than L2)",
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": value * B * wl.block_len,
-        "roofline": roofline, "kernels": kernels, "fused_vs_unfused": fvu, "e2e": e2e, "clocks": clk,
+        "roofline": roofline, "kernels": kernels, "fused_vs_unfused": fvu, "next_rows": nxt, "e2e": e2e, "clocks": clk,
         "gpu_launches": n_launch_per_step * args.steps, "wall_s_timed": t_wall,
     }
     if world > 1:
