@@ -9,4 +9,5 @@ from .capi import (  # noqa: F401
     dllm_cache_status, dllm_cache_step, dllm_cache_project, dllm_cache_attend, dllm_cache_attend_noalloc,
     dllm_cache_step_unfused, dllm_unfused_workspace_bytes, dllm_attention_mass, dllm_selftest_wait_timeout,
     dllm_cache_attend_ragged, dllm_cache_attend_partial, dllm_attend_merge, dllm_kv_drift, dllm_kv_topk, dllm_strerror,
+    dllm_elastic_workspace_bytes, dllm_elastic_step,
 )

@@ -10,7 +10,7 @@ from __future__ import annotations
 import ctypes
 import os
 from ctypes import POINTER, c_double, c_float, c_int, c_size_t, c_void_p
-from typing import Optional
+from typing import Optional, Sequence
 
 import torch
 
@@ -25,7 +25,7 @@ DEV_BAD_POSITION, DEV_BAD_VIEW, DEV_TAIL_FULL, DEV_TIMEOUT, DEV_BAD_INDEX = 0x1,
 EXPORTS = ("dllm_cache_bytes", "dllm_cache_alloc", "dllm_cache_free", "dllm_cache_get_layout", "dllm_cache_step",
            "dllm_cache_project", "dllm_cache_attend", "dllm_cache_attend_noalloc", "dllm_unfused_workspace_bytes",
            "dllm_cache_step_unfused", "dllm_attention_mass", "dllm_cache_attend_ragged", "dllm_cache_attend_partial",
-           "dllm_attend_merge", "dllm_kv_topk", "dllm_kv_drift",
+           "dllm_attend_merge", "dllm_kv_topk", "dllm_kv_drift", "dllm_elastic_workspace_bytes", "dllm_elastic_step",
            "dllm_selftest_wait_timeout",
            "dllm_cache_status", "dllm_strerror")
 
@@ -79,11 +79,16 @@ def lib() -> ctypes.CDLL:
         L.dllm_cache_attend_partial.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_int, c_int, c_void_p,
                                                 c_void_p]
         L.dllm_attend_merge.argtypes = [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]
+        L.dllm_elastic_workspace_bytes.argtypes = [c_void_p, c_int, c_int]
+        L.dllm_elastic_workspace_bytes.restype = c_size_t
+        L.dllm_elastic_step.argtypes = [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_int, c_void_p, c_int, c_float,
+                                        c_void_p, c_void_p, c_void_p, c_void_p, c_void_p, c_size_t, c_void_p]
         L.dllm_cache_status.argtypes = [c_void_p, POINTER(c_int)]
         L.dllm_strerror.argtypes = [c_int]
         L.dllm_strerror.restype = ctypes.c_char_p
         for name in EXPORTS:
-            if name not in ("dllm_cache_bytes", "dllm_strerror", "dllm_unfused_workspace_bytes"):
+            if name not in ("dllm_cache_bytes", "dllm_strerror", "dllm_unfused_workspace_bytes",
+                            "dllm_elastic_workspace_bytes"):
                 getattr(L, name).restype = c_int
         _lib = L
     return _lib
@@ -228,6 +233,26 @@ def dllm_kv_drift(handle, layer: int, idx: torch.Tensor, probe_kv: torch.Tensor,
     k = int(idx.shape[-1])
     _check("dllm_kv_drift", lib().dllm_kv_drift(handle, int(layer), _ptr(idx), k, _ptr(probe_kv), float(gamma),
                                                 _ptr(cos), _ptr(refresh), _stream(stream)))
+
+
+def dllm_elastic_workspace_bytes(handle, beta: int, k: int) -> int:
+    return int(lib().dllm_elastic_workspace_bytes(handle, int(beta), int(k)))
+
+
+def dllm_elastic_step(handle, x_all: Sequence[torch.Tensor], w_qkv: Sequence[torch.Tensor], win_lo: torch.Tensor,
+                      beta: int, mass: torch.Tensor, k: int, gamma: float, out: torch.Tensor, cos: torch.Tensor,
+                      flags: torch.Tensor, workspace: torch.Tensor, mass_out: Optional[torch.Tensor] = None,
+                      stream=None) -> None:
+    """One denoising step over len(x_all) layers with the depth-wise drift refresh."""
+    n = len(x_all)
+    if len(w_qkv) != n:
+        raise ValueError("x_all and w_qkv must have one entry per layer")
+    xs = (c_void_p * n)(*[_ptr(t) for t in x_all])
+    ws = (c_void_p * n)(*[_ptr(t) for t in w_qkv])
+    _check("dllm_elastic_step", lib().dllm_elastic_step(
+        handle, n, xs, ws, _ptr(win_lo), int(beta), _ptr(mass), int(k), float(gamma), _ptr(out), _ptr(cos),
+        _ptr(flags), _ptr(mass_out), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
+        _stream(stream)))
 
 
 def dllm_selftest_wait_timeout(handle, stream=None) -> None:

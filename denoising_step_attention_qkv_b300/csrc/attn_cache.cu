@@ -43,6 +43,7 @@ namespace {
 constexpr uint32_t kTileBytes = kKeyTile * kHd * 2;  // 32 KB (bf16 K or V tile)
 constexpr uint32_t kTile8Bytes = kKeyTile * kHd;     // 16 KB (e4m3 tile)
 constexpr int kMaxBitmapWords = 512;                 // MASK-slot bitmap: max_pos <= 16384
+constexpr int kMaxOrder = 256;                       // ragged batches: sequences ranked by length
 
 // Per (query columns, cache type): MMA-operand rings for K and V, e4m3 staging rings,
 // thread count.
@@ -76,6 +77,7 @@ struct Smem {
   float fin_alpha[2][NQ];  // per unit parity: the last tile's rescale factor and running max
   float fin_m[2][NQ];
   uint32_t mask_bits[kMaxBitmapWords];
+  int seq_order[kMaxOrder];  // ragged batches: sequences by key length, longest first
   uint32_t draft_qmask[2];
   int n_draft;
   uint64_t q_full[2], q_empty[2];
@@ -114,7 +116,9 @@ struct Unit {
   int b, h, qc, split, t0, t1;
 };
 
-DEVI Unit decode_unit(const AttnParams& p, int u) {
+// Unit u -> (sequence, head, query chunk, key split).  With `order` (ragged batches) the
+// sequence part of u is a rank in order of decreasing key length.
+DEVI Unit decode_unit(const AttnParams& p, int u, const int* order) {
   Unit x;
   x.split = u % p.n_splits;
   u /= p.n_splits;
@@ -122,6 +126,7 @@ DEVI Unit decode_unit(const AttnParams& p, int u) {
   u /= p.n_qchunks;
   x.h = u % p.H;
   x.b = u / p.H;
+  if (order) x.b = order[x.b];
   x.t0 = p.tile_lo + x.split * p.tiles_per_split;
   x.t1 = min(p.tile_lo + p.key_tiles, x.t0 + p.tiles_per_split);
   if (p.key_len) {  // ragged batch: nothing past this sequence's length
@@ -130,6 +135,15 @@ DEVI Unit decode_unit(const AttnParams& p, int u) {
   }
   if (x.t0 > x.t1) x.t0 = x.t1;  // a unit may be empty
   return x;
+}
+
+// The r-th unit this CTA processes.  Round-robin over the CTAs; for ragged batches, whose
+// units are numbered longest first, a snake (CTA c takes the c-th unit of even rounds and
+// the (P-1-c)-th of odd ones), so that long units pair with short ones across rounds.
+// Increasing in r for every CTA.
+DEVI int cta_unit(const AttnParams& p, int r) {
+  const int c = (p.key_len && (r & 1)) ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
+  return r * static_cast<int>(gridDim.x) + c;
 }
 
 // End (exclusive) of the regular slots sequence b attends to.
@@ -234,6 +248,20 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     tmem_alloc(&S.tmem_base, kTmemCols);
     tmem_relinquish();
   }
+  // Ragged batch: rank the sequences by key length (longest first, ties by index).
+  const int* order = nullptr;
+  if (p.key_len && p.B <= kMaxOrder) {
+    for (int b = threadIdx.x; b < p.B; b += blockDim.x) {
+      const int lb = min(max(__ldg(p.key_len + b), 0), p.max_pos);
+      int rank = 0;
+      for (int o = 0; o < p.B; ++o) {
+        const int lo = min(max(__ldg(p.key_len + o), 0), p.max_pos);
+        rank += (lo > lb) || (lo == lb && o < b);
+      }
+      S.seq_order[rank] = b;
+    }
+    order = S.seq_order;
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -246,8 +274,8 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     int ks = 0, vs = 0, uu = 0;
     uint32_t kph = 0, vph = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uu) {
-      const Unit x = decode_unit(p, u);
+    for (int r = 0, u = cta_unit(p, 0); u < p.units && ok; u = cta_unit(p, ++r), ++uu) {
+      const Unit x = decode_unit(p, u, order);
       const int qb = uu & 1;
       if (!mbar_wait(&S.q_empty[qb], ((uu >> 1) & 1) ^ 1u, abort_flag)) { ok = false; break; }
       mbar_arrive_expect_tx(&S.q_full[qb], 2 * kQBox);
@@ -333,8 +361,8 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       return true;
     };
 
-    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x, ++uu) {
-      const Unit x = decode_unit(p, u);
+    for (int r = 0, u = cta_unit(p, 0); u < p.units && ok; u = cta_unit(p, ++r), ++uu) {
+      const Unit x = decode_unit(p, u, order);
       const int qb = uu & 1;
       if (!mbar_wait(&S.q_full[qb], (uu >> 1) & 1u, abort_flag)) { ok = false; break; }
       tc_fence_after();
@@ -396,7 +424,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     // deferred into the next unit's first tile, whose P V fold slot is empty, so the
     // wait hides behind that tile's softmax.
     constexpr bool kDefer = (NQ == 32) && !FP8;
-    auto finish = [&](float (&o)[NQ], float (&l)[NQ], const Unit& fx, int fu, int fuu, uint32_t fpv) {
+    auto finish = [&](float (&o)[NQ], float (&l)[NQ], const Unit& fx, int fuu, uint32_t fpv) {
       const bool has_pv = fx.t1 > fx.t0;  // an empty unit (ragged batch, key range) has none
       if (has_pv) {
         const uint32_t ob = fpv & 1u, oph = (fpv >> 1) & 1u;  // the unit's last P V
@@ -454,11 +482,14 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
           if (ok && q + 3 < fnrows) out[static_cast<size_t>(q + 3) * p.D] = __float2bfloat16_rn(o[q + 3] * il.w);
         }
       } else {
-        float* wo = p.ws + static_cast<size_t>(fu) * kQChunk * kHd;
+        // split partials are stored by the unit's canonical number (sequence-major, the
+        // combine's indexing), whatever order the units ran in
+        const size_t cu = ((static_cast<size_t>(fx.b) * p.H + fx.h) * p.n_qchunks + fx.qc) * p.n_splits + fx.split;
+        float* wo = p.ws + cu * kQChunk * kHd;
 #pragma unroll
         for (int q = 0; q < NQ; ++q) wo[q * kHd + r] = o[q];
         if (r < NQ) {
-          float* wml = p.ws + static_cast<size_t>(p.units) * kQChunk * kHd + (static_cast<size_t>(fu) * kQChunk + r) * 2;
+          float* wml = p.ws + static_cast<size_t>(p.units) * kQChunk * kHd + (cu * kQChunk + r) * 2;
           wml[0] = has_pv ? S.fin_m[fuu & 1][r] : -INFINITY;
           wml[1] = S.l_fin[r];
         }
@@ -467,13 +498,13 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
 
     float o_prev[NQ], l_prev[NQ];  // the unit waiting to be finished (deferred finish only)
     Unit px{};
-    int pu = 0, puu = 0;
+    int puu = 0;
     uint32_t ppv = 0;
     bool pending = false;
     int uu = 0;  // units started by this CTA (parity selects the finish buffers)
 
-    for (int u = blockIdx.x; u < p.units; u += gridDim.x, ++uu) {
-      const Unit x = decode_unit(p, u);
+    for (int r = 0, u = cta_unit(p, 0); u < p.units; u = cta_unit(p, ++r), ++uu) {
+      const Unit x = decode_unit(p, u, order);
       const int row0 = x.b * p.n_tok;  // first row of the sequence
       const int nrows = min(kQChunk, p.n_tok - x.qc * kQChunk);  // valid columns of this chunk
       const int kend = key_end(p, x.b);  // regular slots past this are not attended
@@ -624,7 +655,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         // ---- D: fold the previous tile's P V into the accumulators (in a unit's first
         // tile: finish the previous unit instead, when that was deferred)
         if (kDefer && t == x.t0 && pending) {
-          finish(o_prev, l_prev, px, pu, puu, ppv);
+          finish(o_prev, l_prev, px, puu, ppv);
           pending = false;
         }
         if (t > x.t0) {
@@ -654,7 +685,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       // ---- unit end: finish now, or hand the state to the next unit's first tile
       if constexpr (kDefer) {
         if (pending) {  // this unit had no tile to finish the previous one in
-          finish(o_prev, l_prev, px, pu, puu, ppv);
+          finish(o_prev, l_prev, px, puu, ppv);
           pending = false;
         }
 #pragma unroll
@@ -663,17 +694,16 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
           l_prev[q] = l_part[q];
         }
         px = x;
-        pu = u;
         puu = uu;
         ppv = pv_cnt - 1;
         pending = true;
       } else {
-        finish(o_acc, l_part, x, u, uu, pv_cnt - 1);
+        finish(o_acc, l_part, x, uu, pv_cnt - 1);
       }
       softmax_sync();  // the next unit's set-up rewrites the running max and tags
     }
     if constexpr (kDefer) {
-      if (pending) finish(o_prev, l_prev, px, pu, puu, ppv);
+      if (pending) finish(o_prev, l_prev, px, puu, ppv);
     }
     if (!ok) {
       *abort_flag = 1;
@@ -688,8 +718,8 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     int ss = 0, ko = 0, vo = 0;
     uint32_t sph = 0, kph = 0, vph = 0;
     bool ok = true;
-    for (int u = blockIdx.x; u < p.units && ok; u += gridDim.x) {
-      const Unit x = decode_unit(p, u);
+    for (int r = 0, u = cta_unit(p, 0); u < p.units && ok; u = cta_unit(p, ++r)) {
+      const Unit x = decode_unit(p, u, order);
       int n_draft = 0;
       if (p.view) {
         for (int t = 0; t < p.n_tok; ++t) n_draft += (p.view[x.b * p.n_tok + t] == DLLM_VIEW_DRAFT);
@@ -795,37 +825,53 @@ __global__ void __launch_bounds__(kHd) attn_combine(const AttnParams p) {
 // Merge two partial states of the same rows (FACache-style: a cached state of keys that
 // did not change and a fresh state of keys that did).  m in base-2 units:
 //   M = max(m_a, m_b), O = 2^(m_a - M) O_a + 2^(m_b - M) O_b, l likewise.
-__global__ void __launch_bounds__(kHd) state_merge(const float* __restrict__ a, const float* __restrict__ b,
-                                                   int H, __nv_bfloat16* out, float* state_out) {
+// One warp per (row, head).  A state is 130 floats (8-byte aligned), so each lane moves
+// float2 pairs: elements 2*lane, 2*lane+1 and 64+2*lane, 64+2*lane+1 of O; (m, l) is the
+// 65th pair.
+constexpr int kMergeWarps = 8;
+__global__ void __launch_bounds__(kMergeWarps * 32) state_merge(const float* __restrict__ a,
+                                                                const float* __restrict__ b, long long n_rh,
+                                                                __nv_bfloat16* out, float* state_out) {
   constexpr int kSt = kHd + 2;
-  const size_t rh = static_cast<size_t>(blockIdx.x) * H + blockIdx.y;  // (row, head)
-  const int i = threadIdx.x;
-  const float* sa = a + rh * kSt;
-  const float* sb = b + rh * kSt;
-  const float ma = sa[kHd], mb = sb[kHd];
-  const float M = fmaxf(ma, mb);
-  float O = 0.0f, L = 0.0f;
+  const long long rh = static_cast<long long>(blockIdx.x) * kMergeWarps + (threadIdx.x >> 5);
+  const int lane = threadIdx.x & 31;
+  if (rh >= n_rh) return;
+  const float2* pa = reinterpret_cast<const float2*>(a + rh * kSt);
+  const float2* pb = reinterpret_cast<const float2*>(b + rh * kSt);
+  const float2 mla = __ldg(pa + kHd / 2), mlb = __ldg(pb + kHd / 2);
+  const float2 a0 = __ldg(pa + lane), a1 = __ldg(pa + 32 + lane);
+  const float2 b0 = __ldg(pb + lane), b1 = __ldg(pb + 32 + lane);
+  const float M = fmaxf(mla.x, mlb.x);
+  float wa = 0.0f, wb = 0.0f;
   if (M != -INFINITY) {
-    const float wa = ma == -INFINITY ? 0.0f : exp2f(ma - M);
-    const float wb = mb == -INFINITY ? 0.0f : exp2f(mb - M);
-    O = sa[i] * wa + sb[i] * wb;
-    L = sa[kHd + 1] * wa + sb[kHd + 1] * wb;
+    wa = mla.x == -INFINITY ? 0.0f : exp2f(mla.x - M);
+    wb = mlb.x == -INFINITY ? 0.0f : exp2f(mlb.x - M);
   }
-  if (out) out[static_cast<size_t>(blockIdx.x) * H * kHd + blockIdx.y * kHd + i] = __float2bfloat16_rn(L > 0.0f ? O / L : 0.0f);
+  const float2 o0 = make_float2(a0.x * wa + b0.x * wb, a0.y * wa + b0.y * wb);
+  const float2 o1 = make_float2(a1.x * wa + b1.x * wb, a1.y * wa + b1.y * wb);
+  const float L = mla.y * wa + mlb.y * wb;
+  if (out) {
+    const float inv = L > 0.0f ? 1.0f / L : 0.0f;
+    __nv_bfloat162* po = reinterpret_cast<__nv_bfloat162*>(out + rh * kHd);
+    po[lane] = __floats2bfloat162_rn(o0.x * inv, o0.y * inv);
+    po[32 + lane] = __floats2bfloat162_rn(o1.x * inv, o1.y * inv);
+  }
   if (state_out) {
-    float* so = state_out + rh * kSt;
-    so[i] = O;
-    if (i == 0) {
-      so[kHd] = M;
-      so[kHd + 1] = L;
-    }
+    float2* so = reinterpret_cast<float2*>(state_out + rh * kSt);
+    so[lane] = o0;
+    so[32 + lane] = o1;
+    if (lane == 0) so[kHd / 2] = make_float2(M, L);
   }
 }
 
 }  // namespace
 
 int launch_state_merge(const float* a, const float* b, int rows, int H, void* out, float* state_out, cudaStream_t s) {
-  state_merge<<<dim3(rows, H), kHd, 0, s>>>(a, b, H, reinterpret_cast<__nv_bfloat16*>(out), state_out);
+  const long long n_rh = static_cast<long long>(rows) * H;
+  if (n_rh == 0) return 0;
+  const long long blocks = (n_rh + kMergeWarps - 1) / kMergeWarps;
+  state_merge<<<static_cast<unsigned>(blocks), kMergeWarps * 32, 0, s>>>(
+      a, b, n_rh, reinterpret_cast<__nv_bfloat16*>(out), state_out);
   return (int)cudaGetLastError();
 }
 

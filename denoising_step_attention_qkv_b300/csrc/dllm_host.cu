@@ -251,6 +251,9 @@ struct StepArgs {
   int n_kv;
   void* probe_kv;
   cudaStream_t s;
+  // K/V-only rows of sequence b only where one of flags[j][b], j < n_flag_sets, is set
+  const int32_t* kv_seq_flags = nullptr;
+  int n_flag_sets = 0;
 };
 
 void* layer_kv(dllm_cache* c, int layer) {
@@ -303,6 +306,9 @@ ProjParams make_proj(dllm_cache* c, const StepArgs& a) {
   p.positions = a.positions;
   p.view = a.view;
   p.kv_positions = a.kv_positions;
+  p.kv_seq_flags = a.kv_seq_flags;
+  p.n_flag_sets = a.n_flag_sets;
+  p.batch = d.batch;
   p.q_out = a.out;
   p.cache_kv = layer_kv(c, a.layer);
   p.cache_scale = layer_scale(c, a.layer);
@@ -632,6 +638,93 @@ int dllm_kv_drift(const dllm_cache* c, int layer, const int32_t* idx, int k, con
   return from_cuda((cudaError_t)launch_drift(kvl, scl, d.kv_dtype, d.batch, c->slots, d.max_pos, d.n_heads, d.head_dim,
                                              idx, k, probe_kv, gamma, cos, refresh, c->drift_cnt, c->sm_count,
                                              c->status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// Multi-layer refresh step: workspace layout (each part at a 256-byte boundary).
+struct ElasticWs {
+  void *x_win, *x_trk, *probe;
+  int32_t *pos_win, *idx;
+  size_t bytes;
+};
+
+static ElasticWs elastic_ws(const dllm_cache* c, int beta, int k, void* base) {
+  const size_t B = c->desc.batch, D = (size_t)c->desc.n_heads * c->desc.head_dim;
+  auto up = [](size_t v) { return (v + 255) / 256 * 256; };
+  size_t off = 0;
+  ElasticWs w{};
+  uint8_t* p = static_cast<uint8_t*>(base);
+  w.x_win = p ? p + off : nullptr;
+  off += up(B * beta * D * 2);
+  w.x_trk = p ? p + off : nullptr;
+  off += up(B * k * D * 2);
+  w.probe = p ? p + off : nullptr;
+  off += up(B * k * 2 * D * 2);
+  w.pos_win = p ? reinterpret_cast<int32_t*>(p + off) : nullptr;
+  off += up(B * beta * 4);
+  w.idx = p ? reinterpret_cast<int32_t*>(p + off) : nullptr;
+  off += up(B * k * 4);
+  w.bytes = off;
+  return w;
+}
+
+size_t dllm_elastic_workspace_bytes(const dllm_cache* c, int beta, int k) {
+  if (!c || beta < 1 || k < 1) return 0;
+  return elastic_ws(c, beta, k, nullptr).bytes;
+}
+
+int dllm_elastic_step(dllm_cache* c, int n_layers, const void* const* x_all, const void* const* w_qkv,
+                      const int32_t* win_lo, int beta, const float* mass, int k, float gamma, void* out, float* cos,
+                      int32_t* flags, float* mass_out, void* workspace, size_t workspace_bytes, void* stream) {
+  if (!c || n_layers < 1 || n_layers > c->desc.n_layers || !x_all || !w_qkv || !win_lo || !mass || !out || !cos ||
+      !flags || !workspace)
+    return DLLM_EINVAL;
+  const dllm_cache_desc& d = c->desc;
+  const int B = d.batch, S = d.max_pos, D = d.n_heads * d.head_dim;
+  if (beta < 1 || beta > S || k < 1 || k > S - beta || S > 16384) return DLLM_EINVAL;
+  if (d.kv_dtype == DLLM_F32 || D % kHd != 0) return DLLM_EUNSUPPORTED;
+  if (mass_out && d.kv_dtype != DLLM_BF16) return DLLM_EUNSUPPORTED;
+  if (!aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DLLM_EINVAL;
+  const ElasticWs ws = elastic_ws(c, beta, k, workspace);
+  if (workspace_bytes < ws.bytes) return DLLM_EINVAL;
+  for (int l = 0; l < n_layers; ++l)
+    if (!x_all[l] || !w_qkv[l] || !aligned16(x_all[l]) || !aligned16(w_qkv[l])) return DLLM_EINVAL;
+  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  const size_t out_layer = (size_t)B * beta * D * 2;
+  int rc;
+  for (int l = 0; l < n_layers; ++l) {
+    void* out_l = static_cast<uint8_t*>(out) + l * out_layer;
+    // 1. recompute every slot of this layer for the sequences whose drift test failed in
+    //    a layer above (flags of layers 0 .. l-1, written by the launches before this one)
+    if (l > 0) {
+      StepArgs r{l, nullptr, w_qkv[l], nullptr, nullptr, 0, nullptr, x_all[l], nullptr, S, nullptr, s};
+      r.kv_seq_flags = flags;
+      r.n_flag_sets = l;
+      rc = do_project(c, r);
+      if (rc) return rc;
+    }
+    // 2. the tracked tokens: top-k of the previous step's mass outside the window
+    rc = from_cuda((cudaError_t)launch_topk(mass + (size_t)l * B * S, B, S, win_lo, beta, k, ws.idx, s));
+    if (rc) return rc;
+    // 3. the rows the projection reads
+    rc = from_cuda((cudaError_t)launch_gather_rows(x_all[l], B, S, D, win_lo, beta, ws.idx, k, ws.x_win, ws.x_trk,
+                                                   ws.pos_win, c->status, s));
+    if (rc) return rc;
+    // 4. window rows -> cache slots and Q; tracked rows -> probe K/V
+    StepArgs a{l, ws.x_win, w_qkv[l], ws.pos_win, nullptr, beta, out_l, ws.x_trk, ws.idx, k, ws.probe, s};
+    rc = do_project(c, a);
+    if (rc) return rc;
+    // 5. this step's attention mass (the next step's top-k input), then the attention
+    if (mass_out) {
+      rc = dllm_attention_mass(c, l, ws.pos_win, nullptr, beta, out_l, mass_out + (size_t)l * B * S, stream);
+      if (rc) return rc;
+    }
+    rc = do_attend(c, l, ws.pos_win, nullptr, beta, out_l, s);
+    if (rc) return rc;
+    // 6. drift of the tracked tokens and this layer's refresh flags
+    rc = dllm_kv_drift(c, l, ws.idx, k, ws.probe, gamma, cos + (size_t)l * B * k * 2, flags + (size_t)l * B, stream);
+    if (rc) return rc;
+  }
+  return DLLM_OK;
 }
 
 int dllm_cache_status(dllm_cache* c, int* device_bits) {

@@ -55,7 +55,12 @@ struct ProjParams {
   int m_fastest;      // tile raster: row tiles vary fastest
   const int32_t* positions;
   const uint8_t* view;
-  const int32_t* kv_positions;
+  const int32_t* kv_positions;  // [m_kv], or null: row i of a sequence is position i
+  // Optional selection of the K/V-only rows by sequence: rows of sequence b are computed
+  // and stored only when kv_seq_flags[j * batch + b] != 0 for some j < n_flag_sets
+  // (device flags, e.g. the drift test's refresh flags of the layers above).
+  const int32_t* kv_seq_flags;
+  int n_flag_sets, batch;
   void* q_out;        // act [m_q][D]
   void* cache_kv;     // this layer: [B][slots][2][H][hd]
   float* cache_scale; // this layer: [B][slots][2][H] (e4m3)
@@ -129,6 +134,11 @@ int launch_drift(const void* kv_layer, const float* scale_layer, int kv_dtype, i
 // q_out) and K (in place) of the raw GEMM output, then write K/V to their slots.
 int launch_rope_rows(const ProjParams& p, cudaStream_t s);
 int launch_cache_write(const ProjParams& p, cudaStream_t s);
+
+// Multi-layer refresh step: gather one layer's window rows (and their positions) and
+// tracked rows from its hidden states x_all [B][S][D] (bf16).
+int launch_gather_rows(const void* x_all, int B, int S, int D, const int32_t* win_lo, int beta, const int32_t* idx,
+                       int k, void* x_win, void* x_trk, int32_t* pos_win, int* status, cudaStream_t s);
 
 size_t proj_tc_smem_bytes(int bn);
 size_t attn_tc_smem_bytes();

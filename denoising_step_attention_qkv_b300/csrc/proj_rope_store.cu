@@ -158,6 +158,25 @@ DEVI void rotate32(float (&lo)[32], float (&hi)[32], const float2* __restrict__ 
   }
 }
 
+// Whether sequence b's K/V-only rows are selected (always, without flags).
+DEVI bool kv_seq_selected(const ProjParams& p, int b) {
+  if (p.kv_seq_flags == nullptr) return true;
+  for (int j = 0; j < p.n_flag_sets; ++j)
+    if (__ldg(p.kv_seq_flags + j * p.batch + b) != 0) return true;
+  return false;
+}
+
+// A tile of K/V-only rows [m0, m0 + rows) none of whose sequences is selected: every
+// role of the kernel skips it (the flags do not change while the kernel runs, so all
+// roles decide alike).
+DEVI bool kv_tile_skipped(const ProjParams& p, int grp, int m0, int rows) {
+  if (grp == 0 || p.kv_seq_flags == nullptr) return false;
+  const int m_end = min(m0 + rows, p.m_kv);
+  for (int b = m0 / p.n_kv; b <= (m_end - 1) / p.n_kv; ++b)
+    if (kv_seq_selected(p, b)) return false;
+  return true;
+}
+
 // The epilogue of one accumulator tile for this thread's row c.m0 + r: `heads` heads
 // starting at output feature c.n0, read from TMEM columns tacc ...  It rotates Q and K,
 // rounds to bf16 (or quantises each head to e4m3 with scale amax/448) and stores the
@@ -208,8 +227,9 @@ DEVI void store_rows(const ProjParams& p, const TileCoord& c, int heads, uint32_
     valid = m < p.m_kv;
     if (valid) {
       b = m / p.n_kv;
-      pos = __ldg(p.kv_positions + m);
+      pos = p.kv_positions ? __ldg(p.kv_positions + m) : m - b * p.n_kv;
       slot = pos;
+      valid = kv_seq_selected(p, b);
     }
   }
   if (valid && (pos < 0 || pos >= p.max_pos)) {
@@ -337,6 +357,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int item = blockIdx.x; item < p.items_total && ok; item += gridDim.x) {
       const Item it = decode_item(p, item);
       const TileCoord c = decode_tile(p, it.tile, BN);
+      if (kv_tile_skipped(p, c.grp, c.m0, BM)) continue;
       const CUtensorMap* am = c.grp ? &tm_xkv : &tm_x;
       const bool half = it.half >= 0;
       const int n0 = half ? c.n0 + it.half * kHd : c.n0;
@@ -370,7 +391,10 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int item = blockIdx.x; item < p.items_total && ok; item += gridDim.x) {
-      const uint32_t idesc = decode_item(p, item).half >= 0 ? idesc_half : idesc_whole;
+      const Item itm = decode_item(p, item);
+      const TileCoord ct = decode_tile(p, itm.tile, BN);
+      if (kv_tile_skipped(p, ct.grp, ct.m0, BM)) continue;
+      const uint32_t idesc = itm.half >= 0 ? idesc_half : idesc_whole;
       if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * BN;
@@ -411,6 +435,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int item = blockIdx.x; item < p.items_total; item += gridDim.x) {
       const Item it = decode_item(p, item);
       TileCoord c = decode_tile(p, it.tile, BN);
+      if (kv_tile_skipped(p, c.grp, c.m0, BM)) continue;
       if (it.half >= 0) c.n0 += it.half * kHd;
       const int heads = it.half >= 0 ? 1 : BN / kHd;
       if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag)) {
@@ -557,6 +582,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;
     for (int item = pair; item < p.items_total && ok; item += n_pairs) {
       const PairItem it = decode_pair_item(p, item);
+      if (kv_tile_skipped(p, it.grp, it.pm0, 256)) continue;
       const CUtensorMap* am = it.grp ? &tm_xkv : &tm_x;
       const int b_rows = it.half ? 64 : 128;
       const CUtensorMap* bm = it.half ? &tm_w_half : &tm_w;
@@ -594,7 +620,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t acc_phase = 0;
     bool ok = true;
     for (int item = pair; item < p.items_total && ok; item += n_pairs) {
-      const uint32_t idesc = decode_pair_item(p, item).half ? idesc_half : idesc_whole;
+      const PairItem itm = decode_pair_item(p, item);
+      if (kv_tile_skipped(p, itm.grp, itm.pm0, 256)) continue;
+      const uint32_t idesc = itm.half ? idesc_half : idesc_whole;
       if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const uint32_t d_tmem = tmem_base + acc * 256;
@@ -635,6 +663,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     bool ok = true;  // a failed wait is recorded; the item sequence continues without stores
     for (int item = pair; item < p.items_total; item += n_pairs) {
       const PairItem it = decode_pair_item(p, item);
+      if (kv_tile_skipped(p, it.grp, it.pm0, 256)) continue;
       if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag)) {
         ok = false;
         *abort_flag = 1;

@@ -288,6 +288,46 @@ int dllm_kv_topk(const float* mass, int batch, int n_pos, const int32_t* block_l
 int dllm_kv_drift(const dllm_cache* cache, int layer, const int32_t* idx, int k,
                   const void* probe_kv, float gamma, float* cos, int32_t* refresh, void* stream);
 
+/* One denoising step over layers 0 .. n_layers-1 of the cache with the depth-wise
+ * refresh of "Elastic-Cache ..." (Core idea: when the drift test of the most-attended
+ * tokens fails at layer l, the layers after l are recomputed, shallow layers keep their
+ * caches; Algorithm knobs: threshold gamma, window size beta).  Per layer l, in order,
+ * on one stream and without host synchronisation:
+ *   1. (l > 0) for every sequence b with flags[j][b] set for some j < l: K and V of
+ *      every regular slot 0 .. max_pos-1 are recomputed from x_all[l] (fused
+ *      projection, rotary embedding, cache store); other sequences' slots are untouched;
+ *   2. idx = the k most-attended positions of mass[l] outside the window (dllm_kv_topk);
+ *   3. the window rows win_lo[b] .. win_lo[b]+beta-1 of x_all[l] are projected (Q, K, V)
+ *      and their K/V written to their slots; the tracked rows x_all[l][b][idx] are
+ *      projected to probe K/V (dllm_cache_project);
+ *   4. (mass_out != NULL) the window's attention mass per slot -> mass_out[l]
+ *      (dllm_attention_mass), the next step's mass input;
+ *   5. the window attends over the cache -> out[l] (dllm_cache_attend);
+ *   6. the drift test of the tracked tokens -> cos[l], flags[l] (dllm_kv_drift).
+ * A layer whose own test fails is not recomputed in this step; the layers after it are.
+ *
+ *   x_all       host array of n_layers device pointers, each bf16 [batch][max_pos][D]:
+ *               this step's hidden states of every position at that layer
+ *   w_qkv       host array of n_layers device pointers, bf16 [3D][D] each
+ *   win_lo      int32 [batch] device: first position of each sequence's window;
+ *               0 <= win_lo[b] <= max_pos - beta (else the window's rows are zero and
+ *               DLLM_DEV_BAD_POSITION is raised)
+ *   mass        fp32 [n_layers][batch][max_pos] device: previous step's attention mass
+ *   k, gamma    tracked tokens per sequence (1 <= k <= max_pos - beta), drift threshold
+ *   out         bf16 [n_layers][batch][beta][D] device out: attention output per layer
+ *   cos         fp32 [n_layers][batch][k][2] device out
+ *   flags       int32 [n_layers][batch] device out: the drift test's refresh flags
+ *   mass_out    fp32 [n_layers][batch][max_pos] device out, or NULL (DLLM_BF16 caches
+ *               only, else DLLM_EUNSUPPORTED)
+ *   workspace   device, 256-byte aligned, >= dllm_elastic_workspace_bytes(cache, beta, k)
+ * Uses the cache's own workspaces: calls on one cache must be ordered.  DLLM_F32 caches:
+ * DLLM_EUNSUPPORTED.  max_pos <= 16384. */
+size_t dllm_elastic_workspace_bytes(const dllm_cache* cache, int beta, int k);
+int dllm_elastic_step(dllm_cache* cache, int n_layers, const void* const* x_all, const void* const* w_qkv,
+                      const int32_t* win_lo, int beta, const float* mass, int k, float gamma,
+                      void* out, float* cos, int32_t* flags, float* mass_out,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
 /* Scratch capacity of dllm_cache_attend_noalloc, in bytes (8 MiB). */
 #define DLLM_NOALLOC_SCRATCH_BYTES (8u << 20)
 

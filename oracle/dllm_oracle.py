@@ -58,6 +58,7 @@ __all__ = [
     "rope_inv_freq", "rope", "project_qkv", "project_head", "row_slots", "key_views", "visible", "attention",
     "OracleCache", "write_rows", "step", "kv_topk", "cosine", "kv_drift", "attention_weights", "attention_mass",
     "attention_partial", "merge_states", "state_output", "range_visible",
+    "refresh_due", "refresh_sequence", "elastic_step",
     "e4m3_decode", "e4m3_table", "e4m3_quantize", "fp8_group_quantize",
 ]
 
@@ -413,6 +414,77 @@ def kv_drift(cache: OracleCache, idx: np.ndarray, probe_kv: np.ndarray) -> np.nd
             cos[b, j, 0] = cosine(cache.K[b, s].reshape(D), probe_kv[b, j, 0])
             cos[b, j, 1] = cosine(cache.V[b, s].reshape(D), probe_kv[b, j, 1])
     return cos
+
+
+# ------------------------------------------------------------------------------------
+# Depth-wise refresh over the layers of one step ([Elastic-Cache] Core idea: when the
+# drift test of the most-attended tokens fails at layer l, the layers after l are
+# recomputed; shallow layers keep their caches.  Algorithm knobs: threshold gamma,
+# sliding window of beta active tokens).
+# ------------------------------------------------------------------------------------
+
+def refresh_due(flags: np.ndarray, layer: int) -> np.ndarray:
+    """Sequences whose cache of ``layer`` is recomputed this step: those whose drift
+    test failed in some layer before it.  flags: [n_layers][B] (rows >= layer unused)."""
+    flags = np.asarray(flags)
+    if layer == 0:
+        return np.zeros(flags.shape[1], bool)
+    return flags[:layer].astype(bool).any(axis=0)
+
+
+def refresh_sequence(cache: OracleCache, w: np.ndarray, x_seq: np.ndarray, b: int, theta: float):
+    """Recompute K/V of every regular slot of sequence b from its hidden states
+    x_seq [max_pos][D] (the full-sequence recompute of a refreshed layer)."""
+    _, k, v = project_qkv(x_seq, w, cache.H)
+    pos = np.arange(cache.S)
+    k = rope(k, pos, theta)
+    for s in range(cache.S):
+        for h in range(cache.H):
+            cache.K[b, s, h] = cache.stored(k[s, h])
+            cache.V[b, s, h] = cache.stored(v[s, h])
+        cache.written[b, s] = True
+
+
+def elastic_step(caches, ws, theta: float, x_all, win_lo: np.ndarray, beta: int, masses, k: int, gamma: float,
+                 with_mass: bool = False):
+    """One denoising step over the layers in order.  Per layer l:
+
+    1. sequences due for refresh (``refresh_due``) get every regular slot of layer l
+       recomputed from ``x_all[l]``;
+    2. the tracked tokens are the top-k of ``masses[l]`` outside the window
+       ``[win_lo[b], win_lo[b] + beta)``;
+    3. the window rows of ``x_all[l]`` are projected, written and attend over the cache
+       (``step``); the tracked rows are projected as probes;
+    4. the drift test compares the cached and probe K/V of the tracked tokens; the
+       sequence's flag is ``min cos < gamma``.
+
+    caches: one OracleCache per layer (modified in place); ws: weights per layer;
+    x_all: per layer [B][max_pos][D]; masses: per layer [B][max_pos].
+    Returns (out [L][B][beta][D], cos [L][B][k][2], flags [L][B] int32, mass [L][B][max_pos]
+    or None): the mass each slot receives from the window's queries after the step's
+    writes (``attention_mass``)."""
+    L = len(caches)
+    B = x_all[0].shape[0]
+    positions = (np.asarray(win_lo)[:, None] + np.arange(beta)[None, :]).astype(np.int32)
+    flags = np.zeros((L, B), np.int32)
+    outs, coss, mass_out = [], [], []
+    for l in range(L):
+        c = caches[l]
+        due = refresh_due(flags, l)
+        for b in np.nonzero(due)[0]:
+            refresh_sequence(c, ws[l], x_all[l][b], int(b), theta)
+        idx = kv_topk(masses[l], win_lo, beta, k)
+        x_win = np.stack([x_all[l][b][positions[b]] for b in range(B)])
+        x_trk = np.stack([x_all[l][b][idx[b]] for b in range(B)])
+        out, probe = step(c, ws[l], theta, x_win, positions, kv_x=x_trk, kv_pos=idx, probe=True)
+        if with_mass:
+            q = np.stack([rope(project_qkv(x_win[b], ws[l], c.H)[0], positions[b], theta) for b in range(B)])
+            mass_out.append(attention_mass(c, q, positions))
+        cos = kv_drift(c, idx, probe)
+        flags[l] = (cos.min(axis=(1, 2)) < gamma).astype(np.int32)
+        outs.append(out)
+        coss.append(cos)
+    return np.stack(outs), np.stack(coss), flags, (np.stack(mass_out) if with_mass else None)
 
 
 # ------------------------------------------------------------------------------------

@@ -117,3 +117,31 @@ def test_planted_mistake_is_caught(monkeypatch, name, bad, pins):
         except (AssertionError, ValueError, FloatingPointError):
             caught += 1
     assert caught == len(pins), f"planted mistake in {name} slipped past {pins}"
+
+
+def _refresh_due_late(flags, layer):
+    flags = np.asarray(flags)
+    if layer <= 1:
+        return np.zeros(flags.shape[1], bool)
+    return flags[:layer - 1].astype(bool).any(axis=0)
+
+
+def _refresh_due_every_sequence(flags, layer):
+    flags = np.asarray(flags)
+    any_failed = bool(flags[:layer].any()) if layer > 0 else False
+    return np.full(flags.shape[1], any_failed)
+
+
+REFRESH_CASES = [
+    (_refresh_due_late, P.test_elastic_refresh_starts_after_the_failing_layer_and_only_there),
+    (_refresh_due_every_sequence, P.test_elastic_refresh_starts_after_the_failing_layer_and_only_there),
+    (_refresh_due_late, P.test_elastic_failing_first_layer_recomputes_every_deeper_layer),
+]
+
+
+@pytest.mark.parametrize("bad,pin", REFRESH_CASES, ids=[f"{c[0].__name__}-{c[1].__name__}" for c in REFRESH_CASES])
+def test_planted_refresh_mistake_is_caught(monkeypatch, bad, pin):
+    monkeypatch.setattr(OD, "refresh_due", bad)
+    monkeypatch.setattr(O, "refresh_due", bad)
+    with pytest.raises(AssertionError):
+        pin()

@@ -460,3 +460,83 @@ def test_partial_state_closed_forms():
     mg = O.merge_states(st, (Oe, me, le))
     for x, y in zip(mg, st):
         np.testing.assert_allclose(x, y, rtol=1e-15)
+
+
+# -------------------------------------------------------------- depth-wise refresh
+def _elastic_setup(sigma, gamma, **kw):
+    import workloads as W
+    kw = dict(dict(batch=3, d_model=16, head_dim=8, max_pos=24, beta=4, gen_lo=8, k=3, act="f32"), **kw)
+    wl = W.make_elastic(np.asarray(sigma, np.float32), seed=5, gamma=gamma, **kw)
+    s = wl.shape
+    caches = []
+    for l in range(wl.n_layers):
+        c = O.OracleCache(s.batch, s.max_pos, 0, s.n_heads, s.head_dim)
+        O.write_rows(c, wl.w[l], wl.x_prev[l], np.tile(np.arange(s.max_pos, dtype=np.int32), (s.batch, 1)),
+                     s.rope_theta)
+        caches.append(c)
+    return wl, caches
+
+
+def _prefilled(wl, xs, l):
+    """A fresh cache of layer l holding K/V of every slot computed from xs[l]."""
+    s = wl.shape
+    c = O.OracleCache(s.batch, s.max_pos, 0, s.n_heads, s.head_dim)
+    O.write_rows(c, wl.w[l], xs[l], np.tile(np.arange(s.max_pos, dtype=np.int32), (s.batch, 1)), s.rope_theta)
+    return c
+
+
+def _outside_window(wl, b):
+    keep = np.ones(wl.shape.max_pos, bool)
+    keep[wl.win_lo[b]:wl.win_lo[b] + wl.beta] = False
+    return keep
+
+
+def test_elastic_never_refreshes_when_gamma_below_minus_one():
+    wl, caches = _elastic_setup(np.full((3, 3), 2.0), gamma=-2.0)
+    out, cos, flags, _ = O.elastic_step(caches, wl.w, wl.shape.rope_theta, wl.x_all, wl.win_lo, wl.beta, wl.mass,
+                                        wl.k, wl.gamma)
+    assert not flags.any()
+    assert np.all(cos >= -1.0 - 1e-12) and np.all(cos <= 1.0 + 1e-12)
+    for l in range(3):
+        old, new = _prefilled(wl, wl.x_prev, l), _prefilled(wl, wl.x_all, l)
+        for b in range(3):
+            keep = _outside_window(wl, b)
+            np.testing.assert_array_equal(caches[l].K[b][keep], old.K[b][keep])  # untouched
+            np.testing.assert_allclose(caches[l].K[b][~keep], new.K[b][~keep], rtol=1e-13, atol=1e-15)  # window rows
+            np.testing.assert_allclose(caches[l].V[b][~keep], new.V[b][~keep], rtol=1e-13, atol=1e-15)
+
+
+def test_elastic_failing_first_layer_recomputes_every_deeper_layer():
+    wl, caches = _elastic_setup(np.full((3, 3), 0.3), gamma=2.0)  # cos <= 1 < gamma: every test fails
+    out, cos, flags, _ = O.elastic_step(caches, wl.w, wl.shape.rope_theta, wl.x_all, wl.win_lo, wl.beta, wl.mass,
+                                        wl.k, wl.gamma)
+    assert flags.all()
+    old0 = _prefilled(wl, wl.x_prev, 0)
+    for b in range(3):  # the failing layer itself keeps its cache outside the window
+        keep = _outside_window(wl, b)
+        np.testing.assert_array_equal(caches[0].K[b][keep], old0.K[b][keep])
+    assert np.all(cos[0] < 0.999)
+    for l in (1, 2):  # deeper layers: every slot from this step's states, so the probes match the cache
+        new = _prefilled(wl, wl.x_all, l)
+        np.testing.assert_allclose(caches[l].K, new.K, rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(caches[l].V, new.V, rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(cos[l], 1.0, atol=1e-12)
+
+
+def test_elastic_refresh_starts_after_the_failing_layer_and_only_there():
+    # sequence 0 barely drifts; sequence 1 drifts from layer 1 on; sequence 2 from layer 0 on
+    sigma = np.array([[0.05, 0.05, 3.0], [0.05, 3.0, 3.0], [0.05, 3.0, 3.0]])
+    wl, caches = _elastic_setup(sigma, gamma=0.9)
+    out, cos, flags, _ = O.elastic_step(caches, wl.w, wl.shape.rope_theta, wl.x_all, wl.win_lo, wl.beta, wl.mass,
+                                        wl.k, wl.gamma)
+    # a recomputed layer matches its probes, so only the first failing layer flags
+    np.testing.assert_array_equal(flags, [[0, 0, 1], [0, 1, 0], [0, 0, 0]])
+    for l in range(3):
+        old, new = _prefilled(wl, wl.x_prev, l), _prefilled(wl, wl.x_all, l)
+        for b in range(3):
+            keep = _outside_window(wl, b)
+            refreshed = (b == 2 and l >= 1) or (b == 1 and l >= 2)
+            ref = new if refreshed else old
+            np.testing.assert_allclose(caches[l].K[b][keep], ref.K[b][keep], rtol=1e-12, atol=1e-15)
+            np.testing.assert_allclose(caches[l].V[b][keep], ref.V[b][keep], rtol=1e-12, atol=1e-15)
+    assert np.all(cos[1, 2] > 1 - 1e-12) and np.all(cos[2, 1:] > 1 - 1e-12)

@@ -25,6 +25,11 @@ Workload recipe (shapes are those of a LLaDA-8B attention layer where stated):
   N(0, 1) "mask embedding" row;
 * drift probes: the current hidden state of a tracked token is its prefill row
   plus ``0.1 * N(0, 1)`` noise.
+* multi-layer steps (``make_elastic``): per layer, weights as above, the hidden
+  states the cache was built from ``x_prev ~ N(0, 1)`` at every position, and this
+  step's states ``x_all = x_prev + sigma[l][b] * N(0, 1)``: ``sigma`` sets how far
+  each (layer, sequence) drifts; a window of ``beta`` positions per sequence at a
+  seeded block-aligned offset; previous-step mass ~ Dirichlet(0.1) per layer.
 """
 from __future__ import annotations
 
@@ -48,6 +53,8 @@ _S_NOISE = 6
 _S_OFFSET = 7
 _S_SEARCH = 8
 _S_MASS = 9
+_S_LAYER_PREV = 10
+_S_LAYER_NOISE = 11
 
 
 def round_bf16(a: np.ndarray) -> np.ndarray:
@@ -288,3 +295,60 @@ def make(config: int, seed: int = 0, **overrides) -> Workload:
         wl.x, wl.positions, wl.view = x, pos, view
         return wl
     raise ValueError(kind)
+
+
+# ----------------------------------------------------------------------------------
+# Multi-layer step with the depth-wise refresh.
+# ----------------------------------------------------------------------------------
+
+@dataclasses.dataclass
+class ElasticWorkload:
+    """One denoising step over ``n_layers`` layers.
+
+    ``x_prev[l]``: hidden states every cache slot of layer l was built from (an earlier
+    step); ``x_all[l]``: this step's hidden states of every position; ``w[l]``: weights;
+    ``mass[l]``: previous-step attention mass; ``win_lo``/``beta``: the active window.
+    """
+
+    name: str
+    shape: Shape
+    seed: int
+    n_layers: int
+    w: list  # [3D][D] per layer
+    x_prev: list  # [B][S][D] per layer
+    x_all: list  # [B][S][D] per layer
+    mass: np.ndarray  # float32 [L][B][S]
+    win_lo: np.ndarray  # int32 [B]
+    beta: int
+    k: int
+    gamma: float
+    sigma: np.ndarray  # [L][B]
+
+
+def make_elastic(sigma, seed: int = 0, batch: int = 4, d_model: int = 256, head_dim: int = 128,
+                 max_pos: int = 384, beta: int = 32, gen_lo: int = 128, k: int = 8, gamma: float = 0.9,
+                 rope_theta: float = 5e5, act: str = "bf16", kv: str = "bf16") -> ElasticWorkload:
+    """``sigma`` [n_layers][batch]: drift scale of each layer and sequence."""
+    sigma = np.asarray(sigma, np.float32)
+    L = sigma.shape[0]
+    if sigma.shape != (L, batch):
+        raise ValueError("sigma must be [n_layers][batch]")
+    shape = Shape(batch=batch, d_model=d_model, n_heads=d_model // head_dim, head_dim=head_dim, max_pos=max_pos,
+                  tail_slots=0, rope_theta=rope_theta, act=act, kv=kv)
+    S, D = max_pos, shape.D
+    ws, xp, xa = [], [], []
+    for l in range(L):
+        w = _rng(seed, _S_WEIGHT, l).standard_normal((3 * D, D), dtype=np.float32) * np.float32(0.02)
+        ws.append(_store(w, act))
+        prev = np.empty((batch, S, D), np.float32)
+        cur = np.empty((batch, S, D), np.float32)
+        for b in range(batch):
+            prev[b] = _rng(seed, _S_LAYER_PREV, l, b).standard_normal((S, D), dtype=np.float32)
+            noise = _rng(seed, _S_LAYER_NOISE, l, b).standard_normal((S, D), dtype=np.float32)
+            cur[b] = prev[b] + sigma[l, b] * noise
+        xp.append(_store(prev, act))
+        xa.append(_store(cur, act))
+    mass = np.stack([_rng(seed, _S_MASS, l).dirichlet(np.full(S, 0.1), size=batch) for l in range(L)]).astype(np.float32)
+    win_lo = _block_offsets(seed, batch, min(gen_lo, S - beta), S, beta, None)
+    return ElasticWorkload(name=f"elastic-L{L}-b{batch}", shape=shape, seed=seed, n_layers=L, w=ws, x_prev=xp,
+                           x_all=xa, mass=mass, win_lo=win_lo, beta=beta, k=k, gamma=gamma, sigma=sigma)
