@@ -47,6 +47,8 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused", action="store_true", help="skip the fused-vs-unfused comparison")
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
+    ap.add_argument("--no-elastic", action="store_true", help="skip the multi-layer refresh step")
+    ap.add_argument("--elastic-layers", type=int, default=32)
     return ap.parse_args()
 
 
@@ -213,6 +215,77 @@ def algorithmic(wl):
     drift_bytes = B * k * 2 * D * 2 * 2
     return dict(proj_flops=proj_flops, proj_bytes=proj_bytes, attn_bytes=attn_bytes, attn_flops=attn_flops,
                 drift_bytes=drift_bytes)
+
+
+def elastic_leg(args, dev, B, S, D, H, hd, theta, beta, k, gamma, flush):
+    """One denoising step over L layers with the depth-wise drift refresh
+    (dllm_elastic_step), LLaDA-8B layer shapes.  Inputs are drawn on the device from a
+    seeded generator: per layer the hidden states the cache was built from, x_prev ~
+    N(0, 1), and this step's x_all = x_prev + sigma[l][b] * N(0, 1) with
+    sigma[l][b] = 0.6 * (l + 1) / L * s_b, s_b ~ U(0.3, 1.2): drift grows with depth and
+    some sequences fail the test in deep layers.  The step is stationary (the failing
+    layer keeps its cache, so every repetition refreshes the same sequence-layers).
+    Also timed: gamma = -2 (never refresh) and gamma = 2 (every sequence recomputes
+    layers 1..L-1), the two ends of the threshold."""
+    import torch
+    from denoising_step_attention_qkv_b300 import capi
+    L = args.elastic_layers
+    g = torch.Generator(device=dev)
+    g.manual_seed(2024)
+    cache = capi.Cache(L, B, S, H, hd, capi.DLLM_BF16, theta, 0, device=dev)
+    all_pos = torch.arange(S, dtype=torch.int32, device=dev).repeat(B, 1)
+    s_b = 0.3 + 0.9 * torch.rand(B, generator=g, device=dev)
+    ws, xs = [], []
+    for l in range(L):
+        w = (torch.randn((3 * D, D), generator=g, device=dev) * 0.02).to(torch.bfloat16)
+        x_prev = torch.randn((B, S, D), generator=g, device=dev)
+        capi.dllm_cache_step(cache.handle, l, None, w, None, None, None, kv_x=x_prev.to(torch.bfloat16),
+                             kv_positions=all_pos)
+        sig = (0.6 * (l + 1) / L) * s_b
+        x_prev += sig[:, None, None] * torch.randn((B, S, D), generator=g, device=dev)
+        ws.append(w)
+        xs.append(x_prev.to(torch.bfloat16))
+        del x_prev
+    mass = torch.distributions.Dirichlet(torch.full((S,), 0.1, device=dev)).sample((L, B)).float().contiguous()
+    win_lo = (512 + beta * torch.randint(0, (S - 512) // beta, (B,), generator=g, device=dev)).to(torch.int32)
+    out = torch.empty((L, B, beta, D), dtype=torch.bfloat16, device=dev)
+    cos = torch.empty((L, B, k, 2), dtype=torch.float32, device=dev)
+    flags = torch.empty((L, B), dtype=torch.int32, device=dev)
+    work = torch.empty(capi.dllm_elastic_workspace_bytes(cache.handle, beta, k), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    n = max(3, min(args.steps, 10))
+
+    def run(gm):
+        step = lambda: capi.dllm_elastic_step(cache.handle, xs, ws, win_lo, beta, mass, k, gm, out, cos, flags, work,
+                                              stream=stream)
+        for _ in range(2):
+            step()
+        evs = []
+        for _ in range(n):
+            flush.zero_()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            step()
+            b_.record(stream)
+            evs.append((a_, b_))
+        torch.cuda.synchronize(dev)
+        ms = statistics.mean(a_.elapsed_time(b_) for a_, b_ in evs)
+        f = flags.cpu().numpy()
+        failed = np.cumsum(f, axis=0) > 0  # failed at or above each layer
+        refreshed = int(failed[:-1].sum())  # sequence-layers recomputed in the next layer down
+        return {"gamma": gm, "ms_per_step": ms, "layer_steps_per_s": L * 1e3 / ms,
+                "refreshed_sequence_layers": refreshed, "of": B * L,
+                "first_failing_layer": [int(np.argmax(f[:, b])) if f[:, b].any() else None for b in range(B)]}
+
+    res = {"layers": L, "batch": B, "window": beta, "tracked": k, "steps": n, "runs": [run(gamma), run(-2.0), run(2.0)],
+           "inputs": "device-generated, seeded: x_prev ~ N(0,1); x_all = x_prev + sigma[l][b] N(0,1), "
+                     "sigma = 0.6 (l+1)/L s_b, s_b ~ U(0.3, 1.2); mass ~ Dirichlet(0.1); L2 flushed between steps"}
+    rc, bits = cache.status()
+    if rc != capi.DLLM_OK:
+        raise RuntimeError(f"device status {bits:#x} in the multi-layer step")
+    del cache, xs, ws
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_ours(args, rank, world, local):
@@ -396,6 +469,10 @@ def run_ours(args, rank, world, local):
                "ragged": row(t_rag, rag_bytes, key_len="seeded uniform [128, %d], mean %.0f" % (S, lens.mean())),
                "partial_state": row(t_part, part_bytes, slots=[lo, S]),
                "merge": row(t_merge, merge_bytes)}
+
+    if nxt is not None and not args.no_elastic:
+        nxt["elastic"] = elastic_leg(args, dev, B, S, D, s.n_heads, s.head_dim, s.rope_theta, wl.block_len, k,
+                                     wl.gamma, flush)
 
     # ---- end to end through the C ABI with host buffers (copies inside the timed region).
     # Every step copies its inputs from pinned host memory and reads its results back.

@@ -274,7 +274,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     int ks = 0, vs = 0, uu = 0;
     uint32_t kph = 0, vph = 0;
     bool ok = true;
-    for (int r = 0, u = cta_unit(p, 0); u < p.units && ok; u = cta_unit(p, ++r), ++uu) {
+    for (int rnd = 0, u = cta_unit(p, 0); u < p.units && ok; u = cta_unit(p, ++rnd), ++uu) {
       const Unit x = decode_unit(p, u, order);
       const int qb = uu & 1;
       if (!mbar_wait(&S.q_empty[qb], ((uu >> 1) & 1) ^ 1u, abort_flag)) { ok = false; break; }
@@ -361,7 +361,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       return true;
     };
 
-    for (int r = 0, u = cta_unit(p, 0); u < p.units && ok; u = cta_unit(p, ++r), ++uu) {
+    for (int rnd = 0, u = cta_unit(p, 0); u < p.units && ok; u = cta_unit(p, ++rnd), ++uu) {
       const Unit x = decode_unit(p, u, order);
       const int qb = uu & 1;
       if (!mbar_wait(&S.q_full[qb], (uu >> 1) & 1u, abort_flag)) { ok = false; break; }
@@ -503,7 +503,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     bool pending = false;
     int uu = 0;  // units started by this CTA (parity selects the finish buffers)
 
-    for (int r = 0, u = cta_unit(p, 0); u < p.units; u = cta_unit(p, ++r), ++uu) {
+    for (int rnd = 0, u = cta_unit(p, 0); u < p.units; u = cta_unit(p, ++rnd), ++uu) {
       const Unit x = decode_unit(p, u, order);
       const int row0 = x.b * p.n_tok;  // first row of the sequence
       const int nrows = min(kQChunk, p.n_tok - x.qc * kQChunk);  // valid columns of this chunk
@@ -718,7 +718,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     int ss = 0, ko = 0, vo = 0;
     uint32_t sph = 0, kph = 0, vph = 0;
     bool ok = true;
-    for (int r = 0, u = cta_unit(p, 0); u < p.units && ok; u = cta_unit(p, ++r)) {
+    for (int rnd = 0, u = cta_unit(p, 0); u < p.units && ok; u = cta_unit(p, ++rnd)) {
       const Unit x = decode_unit(p, u, order);
       int n_draft = 0;
       if (p.view) {
