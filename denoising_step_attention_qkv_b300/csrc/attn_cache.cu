@@ -248,6 +248,9 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     tmem_alloc(&S.tmem_base, kTmemCols);
     tmem_relinquish();
   }
+  // Everything below may read what the previous kernel on the stream wrote.
+  grid_dep_launch();
+  grid_dep_wait();
   // Ragged batch: rank the sequences by key length (longest first, ties by index).
   const int* order = nullptr;
   if (p.key_len && p.B <= kMaxOrder) {
@@ -797,6 +800,8 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
 
 // Merge split-KV partial states: O = sum_s 2^(m_s - M) O_s / sum_s 2^(m_s - M) l_s.
 __global__ void __launch_bounds__(kHd) attn_combine(const AttnParams p) {
+  grid_dep_launch();
+  grid_dep_wait();
   const int row = blockIdx.x;  // global query row b * n_tok + t
   const int h = blockIdx.y;
   const int i = threadIdx.x;
@@ -880,8 +885,7 @@ int launch_one(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& 
   const size_t smem = sizeof(Smem<NQ, FP8>) + 1024;
   cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(attn_cache_tc<NQ, FP8>), (int)smem);
   if (e != cudaSuccess) return (int)e;
-  attn_cache_tc<NQ, FP8><<<grid, Cfg<NQ, FP8>::kThreads, smem, s>>>(tm_q, tm_kv, p);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(attn_cache_tc<NQ, FP8>, dim3(grid), dim3(Cfg<NQ, FP8>::kThreads), smem, s, tm_q, tm_kv, p);
 }
 
 int launch_attn_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, int grid,
@@ -893,8 +897,7 @@ int launch_attn_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorM
 
 int launch_attn_combine(const AttnParams& p, cudaStream_t s) {
   dim3 grid(p.B * p.n_tok, p.H);
-  attn_combine<<<grid, kHd, 0, s>>>(p);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(attn_combine, grid, dim3(kHd), 0, s, p);
 }
 
 }  // namespace dllm

@@ -5,6 +5,7 @@
 // get their positions) and the tracked rows chosen by the top-k.  A pure copy: 16-byte
 // loads and stores, one block per row.
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dllm {
 namespace {
@@ -20,6 +21,8 @@ __global__ void __launch_bounds__(256) gather_rows_kernel(const uint4* __restric
                                                            const int32_t* __restrict__ idx, int k, int B,
                                                            uint4* __restrict__ x_win, uint4* __restrict__ x_trk,
                                                            int32_t* __restrict__ pos_win, int* status) {
+  grid_dep_launch();
+  grid_dep_wait();
   const int r = blockIdx.x;
   int b, pos, bad_bit;
   uint4* dst;
@@ -49,9 +52,9 @@ int launch_gather_rows(const void* x_all, int B, int S, int D, const int32_t* wi
                        int k, void* x_win, void* x_trk, int32_t* pos_win, int* status, cudaStream_t s) {
   const int rows = B * (beta + k);
   if (rows == 0) return 0;
-  gather_rows_kernel<<<rows, 256, 0, s>>>(static_cast<const uint4*>(x_all), S, D * 2 / 16, win_lo, beta, idx, k, B,
-                                          static_cast<uint4*>(x_win), static_cast<uint4*>(x_trk), pos_win, status);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(gather_rows_kernel, dim3(rows), dim3(256), 0, s, static_cast<const uint4*>(x_all), S,
+                         D * 2 / 16, win_lo, beta, idx, k, B, static_cast<uint4*>(x_win), static_cast<uint4*>(x_trk),
+                         pos_win, status);
 }
 
 }  // namespace dllm

@@ -6,6 +6,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <utility>
 
 #include "../../include/dllm_cache.h"
 
@@ -35,6 +36,29 @@ namespace dllm {
 // device, calling the driver only the first time (per device and kernel) a larger size
 // is needed, so that launches (and stream capture) do no extra driver work.
 cudaError_t ensure_smem_limit(const void* kernel, int bytes);
+
+// Programmatic dependent launch.  A kernel launched this way may start (its prologue:
+// barrier setup, TMEM allocation, descriptor prefetch) while the previous kernel on the
+// stream is still running; each such kernel lets its own dependents launch early
+// (griddepcontrol.launch_dependents) and, in every thread, waits for the previous grid
+// to complete (griddepcontrol.wait) before it reads or writes anything that grid may
+// touch.  Since every CTA passes that wait before it exits, completion stays ordered
+// along the stream.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                       Args&&... args) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 constexpr int kHd = 128;         // head_dim of the tensor-core path
 constexpr int kQChunk = 64;      // query rows per attention work unit (tensor-core path)

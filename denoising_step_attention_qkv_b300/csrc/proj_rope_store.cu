@@ -158,12 +158,37 @@ DEVI void rotate32(float (&lo)[32], float (&hi)[32], const float2* __restrict__ 
   }
 }
 
-// Whether sequence b's K/V-only rows are selected (always, without flags).
-DEVI bool kv_seq_selected(const ProjParams& p, int b) {
-  if (p.kv_seq_flags == nullptr) return true;
+// Selection of the K/V-only rows by sequence, one bit per sequence, built once per CTA
+// (select_init) from the device flags; batches larger than the table read the flags.
+constexpr int kSelWords = 64;  // up to 2048 sequences
+__shared__ uint32_t s_kv_sel[kSelWords];
+static_assert(Cfg<256>::kSmem + sizeof(s_kv_sel) <= 232448 && Cfg<128>::kSmem + sizeof(s_kv_sel) <= 232448,
+              "shared memory budget of the single-CTA projection");
+
+DEVI bool kv_seq_selected_flags(const ProjParams& p, int b) {
   for (int j = 0; j < p.n_flag_sets; ++j)
     if (__ldg(p.kv_seq_flags + j * p.batch + b) != 0) return true;
   return false;
+}
+
+// Whether sequence b's K/V-only rows are selected (always, without flags).
+DEVI bool kv_seq_selected(const ProjParams& p, int b) {
+  if (p.kv_seq_flags == nullptr) return true;
+  if (p.batch <= kSelWords * 32) return (s_kv_sel[b >> 5] >> (b & 31)) & 1u;
+  return kv_seq_selected_flags(p, b);
+}
+
+// Every thread of the CTA calls this after the dependency wait; a barrier follows
+// before the first kv_seq_selected.
+DEVI void select_init(const ProjParams& p) {
+  if (p.kv_seq_flags == nullptr || p.batch > kSelWords * 32) return;
+  const int words = (p.batch + 31) / 32;
+  for (int w = threadIdx.x; w < words; w += blockDim.x) {
+    uint32_t bits = 0u;
+    for (int i = 0; i < 32 && w * 32 + i < p.batch; ++i)
+      if (kv_seq_selected_flags(p, w * 32 + i)) bits |= 1u << i;
+    s_kv_sel[w] = bits;
+  }
 }
 
 // A tile of K/V-only rows [m0, m0 + rows) none of whose sequences is selected: every
@@ -346,6 +371,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dep_launch();
+  grid_dep_wait();  // x, positions, indices and flags may come from the previous kernel
+  select_init(p);
+  __syncthreads();
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -572,6 +601,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   cluster_sync();  // barriers of both CTAs initialised, TMEM allocated
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
+  grid_dep_launch();
+  grid_dep_wait();  // x, positions, indices and flags may come from the previous kernel
+  select_init(p);
+  __syncthreads();
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -702,12 +735,14 @@ int launch_proj_tc(const ProjParams& p, const CUtensorMap& tm_x, const CUtensorM
     auto k = proj_rope_store_tc<256>;
     e = ensure_smem_limit(reinterpret_cast<const void*>(k), (int)(Cfg<256>::kSmem));
     if (e != cudaSuccess) return (int)e;
-    k<<<grid, kThreads, Cfg<256>::kSmem, s>>>(tm_x, tm_xkv, tm_w, tm_w_half, p);
+    e = launch_pdl(k, dim3(grid), dim3(kThreads), Cfg<256>::kSmem, s, tm_x, tm_xkv, tm_w, tm_w_half, p);
+    if (e != cudaSuccess) return (int)e;
   } else {
     auto k = proj_rope_store_tc<128>;
     e = ensure_smem_limit(reinterpret_cast<const void*>(k), (int)(Cfg<128>::kSmem));
     if (e != cudaSuccess) return (int)e;
-    k<<<grid, kThreads, Cfg<128>::kSmem, s>>>(tm_x, tm_xkv, tm_w, tm_w_half, p);
+    e = launch_pdl(k, dim3(grid), dim3(kThreads), Cfg<128>::kSmem, s, tm_x, tm_xkv, tm_w, tm_w_half, p);
+    if (e != cudaSuccess) return (int)e;
   }
   return (int)cudaGetLastError();
 }
@@ -721,13 +756,15 @@ int launch_proj_pair(const ProjParams& p, const CUtensorMap& tm_x, const CUtenso
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = kPairSmem;
   cfg.stream = s;
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // see launch_pdl
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   e = cudaLaunchKernelEx(&cfg, proj_rope_store_pair, tm_x, tm_xkv, tm_w, tm_w_half, p);
   if (e != cudaSuccess) return (int)e;
   return (int)cudaGetLastError();

@@ -23,6 +23,12 @@ DEVI uint64_t globaltimer() {
 DEVI void mbar_init(uint64_t* bar, uint32_t count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
 }
+// Programmatic dependent launch (see launch_pdl): let the next kernel on the stream
+// start its prologue; wait until the previous kernel has completed and its writes are
+// visible (returns at once when there is no such dependency).
+DEVI void grid_dep_launch() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+DEVI void grid_dep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 DEVI void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory"); }
 DEVI void mbar_arrive(uint64_t* bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");

@@ -9,6 +9,7 @@
 #include <cuda_fp8.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace dllm {
 namespace {
@@ -66,6 +67,8 @@ __global__ void __launch_bounds__(1024) kv_topk32_kernel(const float* __restrict
                                                          const int32_t* __restrict__ block_lo, int block_len, int k,
                                                          int32_t* __restrict__ idx) {
   __shared__ unsigned long long lists[32][32];
+  grid_dep_launch();
+  grid_dep_wait();
   const int b = blockIdx.x;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int lo = block_lo[b];
@@ -98,6 +101,8 @@ __global__ void __launch_bounds__(1024) kv_topk_kernel(const float* __restrict__
                                                        const int32_t* __restrict__ block_lo, int block_len, int k,
                                                        int n, int32_t* __restrict__ idx) {
   extern __shared__ unsigned long long keys[];
+  grid_dep_launch();
+  grid_dep_wait();
   const int b = blockIdx.x;
   const int lo = block_lo[b];
   for (int i = threadIdx.x; i < n; i += blockDim.x) {
@@ -209,6 +214,8 @@ __global__ void __launch_bounds__(kDriftWarps * 32) kv_drift_kernel(
     const void* __restrict__ kv, const float* __restrict__ scale, int slots, int max_pos, int H, int hd, int D,
     const int32_t* __restrict__ idx, int k, const void* __restrict__ probe, float gamma, float* __restrict__ cos,
     int32_t* __restrict__ refresh, int* __restrict__ counters, int* status) {
+  grid_dep_launch();
+  grid_dep_wait();
   const int b = blockIdx.y;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int eb = KV == DLLM_F32 ? 4 : (KV == DLLM_BF16 ? 2 : 1);
@@ -295,8 +302,7 @@ __global__ void __launch_bounds__(kDriftWarps * 32) kv_drift_kernel(
 int launch_topk(const float* mass, int batch, int n_pos, const int32_t* block_lo, int block_len, int k, int32_t* idx,
                 cudaStream_t s) {
   if (k <= 32) {
-    kv_topk32_kernel<<<batch, 1024, 0, s>>>(mass, n_pos, block_lo, block_len, k, idx);
-    return (int)cudaGetLastError();
+    return (int)launch_pdl(kv_topk32_kernel, dim3(batch), dim3(1024), 0, s, mass, n_pos, block_lo, block_len, k, idx);
   }
   int n = 1;
   while (n < n_pos) n <<= 1;
@@ -306,8 +312,8 @@ int launch_topk(const float* mass, int batch, int n_pos, const int32_t* block_lo
     if (e != cudaSuccess) return (int)e;
   }
   const int threads = n < 1024 ? (n < 32 ? 32 : n) : 1024;
-  kv_topk_kernel<<<batch, threads, smem, s>>>(mass, n_pos, block_lo, block_len, k, n, idx);
-  return (int)cudaGetLastError();
+  return (int)launch_pdl(kv_topk_kernel, dim3(batch), dim3(threads), smem, s, mass, n_pos, block_lo, block_len, k, n,
+                         idx);
 }
 
 int launch_drift(const void* kv_layer, const float* scale_layer, int kv_dtype, int B, int slots, int max_pos, int H,
@@ -321,16 +327,11 @@ int launch_drift(const void* kv_layer, const float* scale_layer, int kv_dtype, i
   if (per_seq < 1) per_seq = 1;
   dim3 grid(per_seq, B);
   constexpr int threads = kDriftWarps * 32;
-  if (kv_dtype == DLLM_BF16)
-    kv_drift_kernel<DLLM_BF16><<<grid, threads, 0, s>>>(kv_layer, scale_layer, slots, max_pos, H, hd, D, idx, k,
-                                                        probe, gamma, cos, refresh, counters, status);
-  else if (kv_dtype == DLLM_E4M3)
-    kv_drift_kernel<DLLM_E4M3><<<grid, threads, 0, s>>>(kv_layer, scale_layer, slots, max_pos, H, hd, D, idx, k,
-                                                        probe, gamma, cos, refresh, counters, status);
-  else
-    kv_drift_kernel<DLLM_F32><<<grid, threads, 0, s>>>(kv_layer, scale_layer, slots, max_pos, H, hd, D, idx, k,
-                                                       probe, gamma, cos, refresh, counters, status);
-  return (int)cudaGetLastError();
+  auto kern = kv_drift_kernel<DLLM_F32>;
+  if (kv_dtype == DLLM_BF16) kern = kv_drift_kernel<DLLM_BF16>;
+  else if (kv_dtype == DLLM_E4M3) kern = kv_drift_kernel<DLLM_E4M3>;
+  return (int)launch_pdl(kern, grid, dim3(threads), 0, s, kv_layer, scale_layer, slots, max_pos, H, hd, D, idx, k,
+                         probe, gamma, cos, refresh, counters, status);
 }
 
 }  // namespace dllm
