@@ -412,6 +412,80 @@ def run_ours(args, rank, world, local):
         torch.cuda.synchronize(dev)
         return statistics.mean(a_.elapsed_time(b_) for a_, b_ in evs2) * 1e3
 
+    # ---- end to end through the C ABI with host buffers (copies inside the timed region).
+    # Every step copies its inputs from pinned host memory and reads its results back.
+    # Steady state is one CUDA graph per step with three independent branches: the
+    # copy-in of step i+1, the four kernels of step i and the read-back of step i-1, on
+    # double-buffered device tensors, so a step costs the slowest branch.  The timed
+    # region is the copy-in of step 0, K graph launches and the read-back of step K-1
+    # (the graphs also copy in one step too many and read back one too many: counted).
+    # No L2 flush here: every step streams the whole cache, which is larger than L2.
+    e2e = None
+    if not args.no_e2e:
+        h_in = [t.cpu().pin_memory() for t in (x, x_probe, pos, mass, block_lo)]
+        d_in = [[x, x_probe, pos, mass, block_lo], [t.clone() for t in (x, x_probe, pos, mass, block_lo)]]
+        d_out = [[out, cos, refresh], [torch.empty_like(t) for t in (out, cos, refresh)]]
+        h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (out, cos, refresh)] for _ in range(2)]
+        d_idx = [idx, torch.empty_like(idx)]
+        d_probe = [probe, torch.empty_like(probe)]
+        h2d = sum(t.numel() * t.element_size() for t in h_in)
+        d2h = sum(t.numel() * t.element_size() for t in h_out[0])
+        s_cp_in, s_cp_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+
+        def copy_in(j):
+            for d_, h_ in zip(d_in[j], h_in):
+                d_.copy_(h_, non_blocking=True)
+
+        def compute(j):
+            xi, xpi, posi, massi, loi = d_in[j]
+            outi, cosi, refi = d_out[j]
+            capi.dllm_kv_topk(massi, loi, wl.block_len, k, d_idx[j])
+            capi.dllm_cache_project(cache.handle, 0, xi, w, posi, None, outi, kv_x=xpi, kv_positions=d_idx[j],
+                                    probe_kv=d_probe[j])
+            capi.dllm_cache_attend(cache.handle, 0, posi, None, outi)
+            capi.dllm_kv_drift(cache.handle, 0, d_idx[j], d_probe[j], wl.gamma, cosi, refi)
+
+        def copy_out(j):
+            for h_, d_ in zip(h_out[j], d_out[j]):
+                h_.copy_(d_, non_blocking=True)
+
+        def capture(j):
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g):
+                cap = torch.cuda.current_stream()
+                s_cp_in.wait_stream(cap)
+                s_cp_out.wait_stream(cap)
+                with torch.cuda.stream(s_cp_in):
+                    copy_in(j ^ 1)  # the next step's inputs
+                with torch.cuda.stream(s_cp_out):
+                    copy_out(j ^ 1)  # the previous step's results
+                compute(j)
+                cap.wait_stream(s_cp_in)
+                cap.wait_stream(s_cp_out)
+            return g
+
+        graphs = [capture(0), capture(1)]
+        # warm-up: two steps through the graphs
+        copy_in(0)
+        for i in range(4):
+            graphs[i & 1].replay()
+        torch.cuda.synchronize(dev)
+        if world > 1:
+            torch.distributed.barrier()
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        copy_in(0)
+        for i in range(args.steps):
+            graphs[i & 1].replay()
+        copy_out((args.steps - 1) & 1)
+        e1.record(stream)
+        torch.cuda.synchronize(dev)
+        _, e2e_value = job_rate(e0.elapsed_time(e1), args.steps, world, dev)
+        e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "graphs": "one CUDA graph per step: copy-in(i+1) | step(i) | read-back(i-1)"}
+        np.testing.assert_array_equal(h_out[(args.steps - 1) & 1][2].numpy(), refresh.cpu().numpy())
+
     # ---- fused vs the conventional four-kernel pipeline (projection GEMM, rotary, cache
     # write, attention as separate kernels with intermediates in HBM), same inputs and
     # L2 flush; the projection part of the unfused step is its total minus the attention
@@ -496,80 +570,6 @@ def run_ours(args, rank, world, local):
     if nxt is not None and not args.no_elastic:
         nxt["elastic"] = elastic_leg(args, dev, B, S, D, s.n_heads, s.head_dim, s.rope_theta, wl.block_len, k,
                                      wl.gamma, flush)
-
-    # ---- end to end through the C ABI with host buffers (copies inside the timed region).
-    # Every step copies its inputs from pinned host memory and reads its results back.
-    # Steady state is one CUDA graph per step with three independent branches: the
-    # copy-in of step i+1, the four kernels of step i and the read-back of step i-1, on
-    # double-buffered device tensors, so a step costs the slowest branch.  The timed
-    # region is the copy-in of step 0, K graph launches and the read-back of step K-1
-    # (the graphs also copy in one step too many and read back one too many: counted).
-    # No L2 flush here: every step streams the whole cache, which is larger than L2.
-    e2e = None
-    if not args.no_e2e:
-        h_in = [t.cpu().pin_memory() for t in (x, x_probe, pos, mass, block_lo)]
-        d_in = [[x, x_probe, pos, mass, block_lo], [t.clone() for t in (x, x_probe, pos, mass, block_lo)]]
-        d_out = [[out, cos, refresh], [torch.empty_like(t) for t in (out, cos, refresh)]]
-        h_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (out, cos, refresh)] for _ in range(2)]
-        d_idx = [idx, torch.empty_like(idx)]
-        d_probe = [probe, torch.empty_like(probe)]
-        h2d = sum(t.numel() * t.element_size() for t in h_in)
-        d2h = sum(t.numel() * t.element_size() for t in h_out[0])
-        s_cp_in, s_cp_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-
-        def copy_in(j):
-            for d_, h_ in zip(d_in[j], h_in):
-                d_.copy_(h_, non_blocking=True)
-
-        def compute(j):
-            xi, xpi, posi, massi, loi = d_in[j]
-            outi, cosi, refi = d_out[j]
-            capi.dllm_kv_topk(massi, loi, wl.block_len, k, d_idx[j])
-            capi.dllm_cache_project(cache.handle, 0, xi, w, posi, None, outi, kv_x=xpi, kv_positions=d_idx[j],
-                                    probe_kv=d_probe[j])
-            capi.dllm_cache_attend(cache.handle, 0, posi, None, outi)
-            capi.dllm_kv_drift(cache.handle, 0, d_idx[j], d_probe[j], wl.gamma, cosi, refi)
-
-        def copy_out(j):
-            for h_, d_ in zip(h_out[j], d_out[j]):
-                h_.copy_(d_, non_blocking=True)
-
-        def capture(j):
-            g = torch.cuda.CUDAGraph()
-            with torch.cuda.graph(g):
-                cap = torch.cuda.current_stream()
-                s_cp_in.wait_stream(cap)
-                s_cp_out.wait_stream(cap)
-                with torch.cuda.stream(s_cp_in):
-                    copy_in(j ^ 1)  # the next step's inputs
-                with torch.cuda.stream(s_cp_out):
-                    copy_out(j ^ 1)  # the previous step's results
-                compute(j)
-                cap.wait_stream(s_cp_in)
-                cap.wait_stream(s_cp_out)
-            return g
-
-        graphs = [capture(0), capture(1)]
-        # warm-up: two steps through the graphs
-        copy_in(0)
-        for i in range(4):
-            graphs[i & 1].replay()
-        torch.cuda.synchronize(dev)
-        if world > 1:
-            torch.distributed.barrier()
-        e0 = torch.cuda.Event(enable_timing=True)
-        e1 = torch.cuda.Event(enable_timing=True)
-        e0.record(stream)
-        copy_in(0)
-        for i in range(args.steps):
-            graphs[i & 1].replay()
-        copy_out((args.steps - 1) & 1)
-        e1.record(stream)
-        torch.cuda.synchronize(dev)
-        _, e2e_value = job_rate(e0.elapsed_time(e1), args.steps, world, dev)
-        e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-               "d2h_bytes_per_step": d2h, "graphs": "one CUDA graph per step: copy-in(i+1) | step(i) | read-back(i-1)"}
-        np.testing.assert_array_equal(h_out[(args.steps - 1) & 1][2].numpy(), refresh.cpu().numpy())
 
     rc, bits = cache.status()
     if rc != capi.DLLM_OK:

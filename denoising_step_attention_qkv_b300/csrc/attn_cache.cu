@@ -364,9 +364,17 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       return true;
     };
 
+    // The P V of a unit's last tile stays pending until the next unit's first S MMA has
+    // been issued (or an empty unit, or the end), so at unit boundaries too the softmax
+    // finds its next S ready.
+    bool pv_pending = false;
     for (int rnd = 0, u = cta_unit(p, 0); u < p.units && ok; u = cta_unit(p, ++rnd), ++uu) {
       const Unit x = decode_unit(p, u, order);
       const int qb = uu & 1;
+      if (x.t1 == x.t0 && pv_pending) {
+        if (!issue_pv()) { ok = false; break; }
+        pv_pending = false;
+      }
       if (!mbar_wait(&S.q_full[qb], (uu >> 1) & 1u, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const uint32_t q0 = smem_u32(S.q[qb]);
@@ -387,12 +395,13 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         tc_commit(&S.s_full[sb]);
         if (++ks == KST) { ks = 0; kph ^= 1u; }
         ++s_cnt;
-        if (t > x.t0 && !issue_pv()) { ok = false; break; }
+        if (pv_pending && !issue_pv()) { ok = false; break; }
+        pv_pending = true;
       }
       if (!ok) break;
       tc_commit(&S.q_empty[qb]);
-      if (x.t1 > x.t0 && !issue_pv()) { ok = false; break; }
     }
+    if (ok && pv_pending && !issue_pv()) ok = false;
     if (!ok) {
       *abort_flag = 1;
       atomicOr(p.status, DLLM_DEV_TIMEOUT);

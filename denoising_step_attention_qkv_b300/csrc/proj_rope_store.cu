@@ -178,6 +178,16 @@ DEVI bool kv_seq_selected(const ProjParams& p, int b) {
   return kv_seq_selected_flags(p, b);
 }
 
+// Whether this launch has nothing to do: only K/V-only rows, selected by flags, and no
+// sequence selected (the usual case of a refresh launch).  Read after the barrier that
+// follows select_init; every thread gets the same answer.
+DEVI bool nothing_selected(const ProjParams& p) {
+  if (p.kv_seq_flags == nullptr || p.m_q > 0 || p.batch > kSelWords * 32) return false;
+  uint32_t any = 0u;
+  for (int w = 0; w < (p.batch + 31) / 32; ++w) any |= s_kv_sel[w];
+  return any == 0u;
+}
+
 // Every thread of the CTA calls this after the dependency wait; a barrier follows
 // before the first kv_seq_selected.
 DEVI void select_init(const ProjParams& p) {
@@ -375,6 +385,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dep_wait();  // x, positions, indices and flags may come from the previous kernel
   select_init(p);
   __syncthreads();
+  const int items_end = nothing_selected(p) ? 0 : p.items_total;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer
@@ -383,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < p.items_total && ok; item += gridDim.x) {
+    for (int item = blockIdx.x; item < items_end && ok; item += gridDim.x) {
       const Item it = decode_item(p, item);
       const TileCoord c = decode_tile(p, it.tile, BN);
       if (kv_tile_skipped(p, c.grp, c.m0, BM)) continue;
@@ -419,7 +430,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int item = blockIdx.x; item < p.items_total && ok; item += gridDim.x) {
+    for (int item = blockIdx.x; item < items_end && ok; item += gridDim.x) {
       const Item itm = decode_item(p, item);
       const TileCoord ct = decode_tile(p, itm.tile, BN);
       if (kv_tile_skipped(p, ct.grp, ct.m0, BM)) continue;
@@ -461,7 +472,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;  // a failed wait is recorded; the item sequence continues without stores
-    for (int item = blockIdx.x; item < p.items_total; item += gridDim.x) {
+    for (int item = blockIdx.x; item < items_end; item += gridDim.x) {
       const Item it = decode_item(p, item);
       TileCoord c = decode_tile(p, it.tile, BN);
       if (kv_tile_skipped(p, c.grp, c.m0, BM)) continue;
@@ -605,6 +616,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   grid_dep_wait();  // x, positions, indices and flags may come from the previous kernel
   select_init(p);
   __syncthreads();
+  const int items_end = nothing_selected(p) ? 0 : p.items_total;
 
   if (warp == 0 && lane == 0) {
     // ------------------------------------------------------------ TMA producer (both CTAs)
@@ -613,7 +625,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int stage = 0;
     uint32_t phase = 0;
     bool ok = true;
-    for (int item = pair; item < p.items_total && ok; item += n_pairs) {
+    for (int item = pair; item < items_end && ok; item += n_pairs) {
       const PairItem it = decode_pair_item(p, item);
       if (kv_tile_skipped(p, it.grp, it.pm0, 256)) continue;
       const CUtensorMap* am = it.grp ? &tm_xkv : &tm_x;
@@ -652,7 +664,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;
-    for (int item = pair; item < p.items_total && ok; item += n_pairs) {
+    for (int item = pair; item < items_end && ok; item += n_pairs) {
       const PairItem itm = decode_pair_item(p, item);
       if (kv_tile_skipped(p, itm.grp, itm.pm0, 256)) continue;
       const uint32_t idesc = itm.half ? idesc_half : idesc_whole;
@@ -694,7 +706,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int acc = 0;
     uint32_t acc_phase = 0;
     bool ok = true;  // a failed wait is recorded; the item sequence continues without stores
-    for (int item = pair; item < p.items_total; item += n_pairs) {
+    for (int item = pair; item < items_end; item += n_pairs) {
       const PairItem it = decode_pair_item(p, item);
       if (kv_tile_skipped(p, it.grp, it.pm0, 256)) continue;
       if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag)) {
