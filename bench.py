@@ -288,6 +288,96 @@ def elastic_leg(args, dev, B, S, D, H, hd, theta, beta, k, gamma, flush):
     return res
 
 
+def other_configs(dev, flush, n_iter=30):
+    """Projection and attention of the other workloads against their rooflines: the
+    LLaDA-8B layer at batch 1 (eager and replayed as one CUDA graph, which shows the
+    launch overhead), the batch-16 Flash-Verify step (48 rows per sequence, 16 tail
+    slots) and the batch-8 full refresh into an e4m3 cache (every non-block position
+    K/V, then the 32-row block).  Per-call CUDA events, L2 flushed before each call."""
+    import torch
+    import workloads as W
+    from denoising_step_attention_qkv_b300 import capi
+    pk = peaks()
+    stream = torch.cuda.current_stream(dev)
+    kvt = {"bf16": capi.DLLM_BF16, "e4m3": capi.DLLM_E4M3}
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).to(dev)
+
+    def timed(fn):
+        for _ in range(3):
+            fn()
+        evs = []
+        for _ in range(n_iter):
+            flush.zero_()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            fn()
+            b_.record(stream)
+            evs.append((a_, b_))
+        torch.cuda.synchronize(dev)
+        return statistics.median(a_.elapsed_time(b_) for a_, b_ in evs) * 1e3
+
+    res = {}
+    for cfg in (2, 4, 5):
+        wl = W.make(cfg)
+        s = wl.shape
+        B, D, H, hd, S, T = s.batch, s.D, s.n_heads, s.head_dim, s.max_pos, s.tail_slots
+        cache = capi.Cache(1, B, S, H, hd, kvt[s.kv], s.rope_theta, T, device=dev)
+        w = bf(wl.w)
+        if wl.pre_x is not None:
+            capi.dllm_cache_step(cache.handle, 0, None, w, None, None, None, kv_x=bf(wl.pre_x),
+                                 kv_positions=torch.from_numpy(wl.pre_pos).to(dev))
+        x = bf(wl.x)
+        pos = torch.from_numpy(wl.positions).to(dev)
+        view = torch.from_numpy(wl.view).to(dev) if wl.view is not None else None
+        kv_x = bf(wl.kv_x) if wl.kv_x is not None else None
+        kv_pos = torch.from_numpy(wl.kv_pos).to(dev) if wl.kv_pos is not None else None
+        out = torch.empty_like(x)
+        n = x.shape[1]
+        n_kv = 0 if kv_x is None else kv_x.shape[1]
+
+        def project():
+            capi.dllm_cache_project(cache.handle, 0, x, w, pos, view, out, kv_x=kv_x, kv_positions=kv_pos,
+                                    stream=stream)
+
+        def attend():
+            capi.dllm_cache_attend(cache.handle, 0, pos, view, out, stream=stream)
+
+        t_p = timed(project)
+        t_a = timed(lambda: (project(), attend())) - t_p
+        flops = 2.0 * B * (n * 3 * D + n_kv * 2 * D) * D
+        elt = 1 if s.kv == "e4m3" else 2
+        slots = S + (T if view is not None else 0)
+        a_bytes = B * slots * 2 * D * elt + (B * slots * 2 * H * 4 if s.kv == "e4m3" else 0) + 2 * B * n * D * 2
+        r = {"workload": wl.name, "rows_per_seq": n, "refresh_rows_per_seq": n_kv, "kv": s.kv,
+             "project_us": t_p, "project_tflops": flops / (t_p * 1e-6) / 1e12,
+             "project_frac": flops / (t_p * 1e-6) / 1e12 / pk["bf16_tflops"],
+             "attend_us": t_a, "attend_gbs": a_bytes / (t_a * 1e-6) / 1e9,
+             "attend_frac": a_bytes / (t_a * 1e-6) / 1e9 / pk["hbm_gbs"],
+             "algorithmic_flops": flops, "attend_bytes": a_bytes}
+        if cfg == 2:  # the same two calls replayed from one CUDA graph: no launch cost
+            g = torch.cuda.CUDAGraph()
+            s_cap = torch.cuda.Stream(dev)
+            s_cap.wait_stream(stream)
+            with torch.cuda.stream(s_cap):
+                for _ in range(2):
+                    capi.dllm_cache_project(cache.handle, 0, x, w, pos, view, out, stream=s_cap)
+                    capi.dllm_cache_attend(cache.handle, 0, pos, view, out, stream=s_cap)
+                with torch.cuda.graph(g, stream=s_cap):
+                    capi.dllm_cache_project(cache.handle, 0, x, w, pos, view, out, stream=s_cap)
+                    capi.dllm_cache_attend(cache.handle, 0, pos, view, out, stream=s_cap)
+            stream.wait_stream(s_cap)
+            r["project_attend_graph_us"] = timed(g.replay)
+            r["project_attend_eager_us"] = timed(lambda: (project(), attend()))
+        rc, bits = cache.status()
+        if rc != capi.DLLM_OK:
+            raise RuntimeError(f"device status {bits:#x} in {wl.name}")
+        res[wl.name] = r
+        del cache
+    return res
+
+
 def run_ours(args, rank, world, local):
     import torch
     import workloads as W
@@ -567,6 +657,10 @@ def run_ours(args, rank, world, local):
                "partial_state": row(t_part, part_bytes, slots=[lo, S]),
                "merge": row(t_merge, merge_bytes)}
 
+    others = None
+    if not args.no_unfused and not args.no_elastic and rank == 0:
+        others = other_configs(dev, flush)
+
     if nxt is not None and not args.no_elastic:
         nxt["elastic"] = elastic_leg(args, dev, B, S, D, s.n_heads, s.head_dim, s.rope_theta, wl.block_len, k,
                                      wl.gamma, flush)
@@ -608,7 +702,7 @@ def run_ours(args, rank, world, local):
                              "min(K, 300) steps with an event between every two kernels",
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": value * B * wl.block_len,
-        "roofline": roofline, "kernels": kernels, "fused_vs_unfused": fvu, "next_rows": nxt, "e2e": e2e, "clocks": clk,
+        "roofline": roofline, "kernels": kernels, "fused_vs_unfused": fvu, "next_rows": nxt, "other_configs": others, "e2e": e2e, "clocks": clk,
         "gpu_launches": n_launch_per_step * args.steps, "wall_s_timed": t_wall,
     }
     if world > 1:
