@@ -27,10 +27,12 @@
 //
 // FP8-e4m3 cache ("LaCache ...", Methodology 2: per-group FP8; one group here = one
 // head of one token, K or V, with an fp32 scale): TMA stages the e4m3 tiles (half the
-// bytes of bf16) in a 2- or 3-deep ring and four converter warps widen them to bf16 in the
-// MMA operand layout (exact: every e4m3 value is a bf16 value).  The K scale of a key
-// multiplies that key's scores in fp32, and the V scale multiplies its probabilities
-// before they are rounded for the PV MMA, so dequantisation adds no rounding step.
+// bytes of bf16) in a 2-deep ring and four converter warps dequantise them into the MMA
+// operand layout as f16: the code (exact in f16, one conversion per pair) times the
+// group's scale (one f16 multiply per pair), a single f16 rounding of relative size
+// 2^-11, far below the e4m3 step of 2^-4.  The MMAs of this path take f16 throughout:
+// the converters also turn each unit's Q chunk from bf16 to f16 in place, and the
+// softmax writes P as f16.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -49,9 +51,12 @@ constexpr int kMaxOrder = 256;                       // ragged batches: sequence
 // thread count.
 template <int NQ, bool FP8>
 struct Cfg {
+  // e4m3: the staging ring (TMA -> converters) and the V operand ring are 2 deep and the
+  // K operand ring 1 deep with 32 queries (measured best of the splits that fit); with
+  // 64 queries only the staging ring is doubled
   static constexpr int KST = FP8 ? 1 : (NQ == 32 ? 3 : 2);
-  static constexpr int VST = FP8 ? 1 : 2;
-  static constexpr int SST = FP8 ? (NQ == 32 ? 3 : 2) : 1;
+  static constexpr int VST = FP8 ? (NQ == 32 ? 2 : 1) : 2;
+  static constexpr int SST = FP8 ? 2 : 1;
   static constexpr uint32_t kStageBytes = FP8 ? kTile8Bytes : 1024;
   static constexpr uint32_t kQBytes = NQ * kHd * 2;       // one Q chunk (two 64-column boxes)
   static constexpr uint32_t kPBytes = NQ * kKeyTile * 2;  // one P^T tile (two 64-key halves)
@@ -81,6 +86,7 @@ struct Smem {
   uint32_t draft_qmask[2];
   int n_draft;
   uint64_t q_full[2], q_empty[2];
+  uint64_t q_conv[2];  // e4m3 caches: the Q chunk has been converted to f16 in place
   uint64_t k_full[C::KST], k_empty[C::KST];
   uint64_t v_full[C::VST], v_empty[C::VST];
   uint64_t sk_full[C::SST], sk_empty[C::SST];
@@ -97,19 +103,30 @@ static_assert(sizeof(Smem<64, false>) + 1024 <= 232448, "shared memory budget (b
 static_assert(sizeof(Smem<32, true>) + 1024 <= 232448, "shared memory budget (e4m3, 32 queries)");
 static_assert(sizeof(Smem<64, true>) + 1024 <= 232448, "shared memory budget (e4m3, 64 queries)");
 
-// Widen 16 e4m3 codes to 16 bf16 values (exact).
-DEVI void widen16(const uint4 in, uint4& lo, uint4& hi) {
+// Dequantise 16 e4m3 codes of one group to f16: code (exact in f16) times the group's
+// scale, one f16 rounding.
+DEVI void dequant16_f16(const uint4 in, __half2 scale, uint4& lo, uint4& hi) {
   const __nv_fp8x2_storage_t* pr = reinterpret_cast<const __nv_fp8x2_storage_t*>(&in);
   uint32_t w[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const __half2 h(__nv_cvt_fp8x2_to_halfraw2(pr[i], __NV_E4M3));
-    const float2 f = __half22float2(h);
-    const __nv_bfloat162 b = __floats2bfloat162_rn(f.x, f.y);
-    w[i] = *reinterpret_cast<const uint32_t*>(&b);
+    const __half2 h = __hmul2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr[i], __NV_E4M3)), scale);
+    w[i] = *reinterpret_cast<const uint32_t*>(&h);
   }
   lo = make_uint4(w[0], w[1], w[2], w[3]);
   hi = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// bf16 -> f16 of 8 values in place (a Q chunk of the e4m3 path).
+DEVI uint4 bf16x8_to_f16x8(uint4 v) {
+  uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
+    const __half2 h = __floats2half2_rn(lo, hi);
+    w[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  return v;
 }
 
 struct Unit {
@@ -170,10 +187,15 @@ DEVI float fast_exp2(float x) {
   return y;
 }
 
-// Round (a, b) to bf16 and store a at byte address pa, b at pb (shared memory).
+// Round (a, b) to bf16 (F16: to f16) and store a at byte address pa, b at pb (shared
+// memory).
+template <bool F16 = false>
 DEVI void st_bf16_pair(uint32_t pa, uint32_t pb, float a, float b) {
   uint32_t packed;
-  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed) : "f"(b), "f"(a));  // hi = b, lo = a
+  if constexpr (F16)
+    asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(packed) : "f"(b), "f"(a));  // hi = b, lo = a
+  else
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed) : "f"(b), "f"(a));
   asm volatile(
       "{\n.reg .b16 lo, hi;\n"
       "mov.b32 {lo, hi}, %2;\n"
@@ -220,6 +242,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S.q_full[i], 1);
       mbar_init(&S.q_empty[i], 1);
+      mbar_init(&S.q_conv[i], 4);  // the four converter warps (e4m3 caches)
     }
     // bf16: operand tiles are filled by TMA (one arrival + bytes); e4m3: by 4 converter warps
     for (int i = 0; i < KST; ++i) { mbar_init(&S.k_full[i], FP8 ? 4 : 1); mbar_init(&S.k_empty[i], 1); }
@@ -334,8 +357,9 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     // ------------------------------------------------------------------ MMA issuer
     // Per tile: S(t) = K(t) Q^T into S[t & 1], then P V of the previous tile into
     // O[(t - 1) & 1], so the softmax of tile t - 1 overlaps the S MMA of tile t.
-    constexpr uint32_t idesc_s = idesc_bf16(128, NQ, false, false);
-    constexpr uint32_t idesc_o = idesc_bf16(128, NQ, true, false);
+    // e4m3 caches: every operand (dequantised K and V, Q, P) is f16
+    constexpr uint32_t idesc_s = FP8 ? idesc_f16(128, NQ, false, false) : idesc_bf16(128, NQ, false, false);
+    constexpr uint32_t idesc_o = FP8 ? idesc_f16(128, NQ, true, false) : idesc_bf16(128, NQ, true, false);
     int ks = 0, vs = 0, uu = 0;
     uint32_t kph = 0, vph = 0;
     uint32_t s_cnt = 0, pv_cnt = 0;
@@ -375,7 +399,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         if (!issue_pv()) { ok = false; break; }
         pv_pending = false;
       }
-      if (!mbar_wait(&S.q_full[qb], (uu >> 1) & 1u, abort_flag)) { ok = false; break; }
+      if (!mbar_wait(FP8 ? &S.q_conv[qb] : &S.q_full[qb], (uu >> 1) & 1u, abort_flag)) { ok = false; break; }
       tc_fence_after();
       const uint32_t q0 = smem_u32(S.q[qb]);
       for (int t = x.t0; t < x.t1 && ok; ++t) {
@@ -578,13 +602,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
           vis = (j < p.max_pos + n_draft) ? dmask : 0ull;
         }
         if (p.ranged && (j < p.key_lo || j >= kend)) vis = 0ull;
-        float k_scale = 1.0f, v_scale = 1.0f;
-        if (FP8 && vis) {
-          const size_t srow = (static_cast<size_t>(x.b) * p.slots + j) * 2;
-          k_scale = __ldg(p.kv_scale + srow * p.H + x.h);
-          v_scale = __ldg(p.kv_scale + (srow + 1) * p.H + x.h);
-        }
-        const float sc = p.scale_log2 * k_scale;
+        const float sc = p.scale_log2;  // e4m3: the K scale is already in the f16 operand
         if (vis == ~0ull) {
 #pragma unroll
           for (int q = 0; q < NQ; ++q) s[q] *= sc;
@@ -655,10 +673,8 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
             l_part[q + 1] = l_part[q + 1] * al.y + e1;
             l_part[q + 2] = l_part[q + 2] * al.z + e2;
             l_part[q + 3] = l_part[q + 3] * al.w + e3;
-            st_bf16_pair(pbase + sw128_offset(q, byte), pbase + sw128_offset(q + 1, byte), e0 * v_scale,
-                         e1 * v_scale);
-            st_bf16_pair(pbase + sw128_offset(q + 2, byte), pbase + sw128_offset(q + 3, byte), e2 * v_scale,
-                         e3 * v_scale);
+            st_bf16_pair<FP8>(pbase + sw128_offset(q, byte), pbase + sw128_offset(q + 1, byte), e0, e1);
+            st_bf16_pair<FP8>(pbase + sw128_offset(q + 2, byte), pbase + sw128_offset(q + 3, byte), e2, e3);
           }
           fence_proxy_async_smem();
           __syncwarp();
@@ -722,16 +738,27 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       atomicOr(p.status, DLLM_DEV_TIMEOUT);
     }
   } else if (FP8 && warp >= 6) {
-    // ------------------------------------------------------------------ e4m3 -> bf16 converters
-    // Thread r widens key row r of each staged tile into both 64-column halves of the
-    // operand tile, keeping the 128-byte swizzle.  V rows of slots that no query can
-    // see are written as zeros (their probability is 0, and 0 * NaN must not reach O).
+    // ------------------------------------------------------------------ e4m3 -> f16 converters
+    // Per unit: the Q chunk, bf16 -> f16 in place (the MMAs of this path take f16).  Per
+    // tile: thread r dequantises key row r of the staged K and V codes (code times the
+    // key's group scale, one f16 rounding) into both 64-column halves of the operand
+    // tiles, keeping the 128-byte swizzle.  V rows of slots that no query can see are
+    // written as zeros (their probability is 0, and 0 * NaN must not reach O).
     const int r = (warp & 3) * 32 + lane;
-    int ss = 0, ko = 0, vo = 0;
+    int ss = 0, ko = 0, vo = 0, uu = 0;
     uint32_t sph = 0, kph = 0, vph = 0;
     bool ok = true;
-    for (int rnd = 0, u = cta_unit(p, 0); u < p.units && ok; u = cta_unit(p, ++rnd)) {
+    for (int rnd = 0, u = cta_unit(p, 0); u < p.units && ok; u = cta_unit(p, ++rnd), ++uu) {
       const Unit x = decode_unit(p, u, order);
+      {
+        const int qb = uu & 1;
+        if (!mbar_wait_warp(&S.q_full[qb], (uu >> 1) & 1u, abort_flag)) { ok = false; break; }
+        uint4* qv = reinterpret_cast<uint4*>(S.q[qb]);
+        for (int i = r; i < static_cast<int>(C::kQBytes / 16); i += 128) qv[i] = bf16x8_to_f16x8(qv[i]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&S.q_conv[qb]);
+      }
       int n_draft = 0;
       if (p.view) {
         for (int t = 0; t < p.n_tok; ++t) n_draft += (p.view[x.b * p.n_tok + t] == DLLM_VIEW_DRAFT);
@@ -742,17 +769,25 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       for (int t = x.t0; t < x.t1; ++t) {
         const int j = t * kKeyTile + r;
         const uint32_t sw = static_cast<uint32_t>(r & 7);
+        // this key's group scales, fetched before waiting for its codes
+        float ksc = 0.0f, vsc = 0.0f;
+        if (j < p.slots) {
+          const size_t srow = (static_cast<size_t>(x.b) * p.slots + j) * 2;
+          ksc = __ldg(p.kv_scale + srow * p.H + x.h);
+          vsc = __ldg(p.kv_scale + (srow + 1) * p.H + x.h);
+        }
         // K
         if (!mbar_wait_warp(&S.sk_full[ss], sph, abort_flag)) { ok = false; break; }
         if (!mbar_wait_warp(&S.k_empty[ko], kph ^ 1u, abort_flag)) { ok = false; break; }
         {
+          const __half2 sc2 = __float2half2_rn(ksc);
           const uint8_t* src = S.sk[ss] + r * 128;
           uint8_t* dst = S.k[ko] + r * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint4 in = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
             uint4 lo, hi;
-            widen16(in, lo, hi);
+            dequant16_f16(in, sc2, lo, hi);
             uint8_t* half = dst + (c >> 2) * (kTileBytes / 2);
             const uint32_t c0 = (c & 3) * 2;
             *reinterpret_cast<uint4*>(half + ((c0 ^ sw) << 4)) = lo;
@@ -770,13 +805,14 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         if (!mbar_wait_warp(&S.sv_full[ss], sph, abort_flag)) { ok = false; break; }
         if (!mbar_wait_warp(&S.v_empty[vo], vph ^ 1u, abort_flag)) { ok = false; break; }
         {
+          const __half2 sc2 = __float2half2_rn(vsc);
           const uint8_t* src = S.sv[ss] + r * 128;
           uint8_t* dst = S.v[vo] + r * 128;
           const bool zero = j < p.max_pos ? (p.ranged && (j < p.key_lo || j >= kend)) : j >= tail_end;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             uint4 lo = make_uint4(0u, 0u, 0u, 0u), hi = lo;
-            if (!zero) widen16(*reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4)), lo, hi);
+            if (!zero) dequant16_f16(*reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4)), sc2, lo, hi);
             uint8_t* half = dst + (c >> 2) * (kTileBytes / 2);
             const uint32_t c0 = (c & 3) * 2;
             *reinterpret_cast<uint4*>(half + ((c0 ^ sw) << 4)) = lo;

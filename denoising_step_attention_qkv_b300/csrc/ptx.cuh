@@ -202,6 +202,12 @@ __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool 
          (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
+// The same with f16 A and B (both operands always share one type).
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool a_mn, bool b_mn) {
+  return (1u << 4) | ((a_mn ? 1u : 0u) << 15) | ((b_mn ? 1u : 0u) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
 // Byte offset of element (row, byte) inside a 128-byte-swizzled tile whose rows are
 // 128 bytes and whose base is 1024-byte aligned.
 DEVI uint32_t sw128_offset(uint32_t row, uint32_t byte_in_row) {
