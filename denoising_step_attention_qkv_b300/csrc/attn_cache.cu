@@ -54,7 +54,7 @@ struct Cfg {
   // e4m3: the staging ring (TMA -> converters) and the V operand ring are 2 deep and the
   // K operand ring 1 deep with 32 queries (measured best of the splits that fit); with
   // 64 queries only the staging ring is doubled
-  static constexpr int KST = FP8 ? 1 : (NQ == 32 ? 3 : 2);
+  static constexpr int KST = FP8 ? 1 : (NQ <= 48 ? 3 : 2);
   static constexpr int VST = FP8 ? (NQ == 32 ? 2 : 1) : 2;
   static constexpr int SST = FP8 ? 2 : 1;
   static constexpr uint32_t kStageBytes = FP8 ? kTile8Bytes : 1024;
@@ -100,6 +100,8 @@ struct Smem {
 };
 static_assert(sizeof(Smem<32, false>) + 1024 <= 232448, "shared memory budget (bf16, 32 queries)");
 static_assert(sizeof(Smem<64, false>) + 1024 <= 232448, "shared memory budget (bf16, 64 queries)");
+static_assert(sizeof(Smem<48, false>) + 1024 <= 232448, "shared memory budget (bf16, 48 queries)");
+static_assert(sizeof(Smem<48, true>) + 1024 <= 232448, "shared memory budget (e4m3, 48 queries)");
 static_assert(sizeof(Smem<32, true>) + 1024 <= 232448, "shared memory budget (e4m3, 32 queries)");
 static_assert(sizeof(Smem<64, true>) + 1024 <= 232448, "shared memory budget (e4m3, 64 queries)");
 
@@ -223,6 +225,37 @@ DEVI float reduce_scatter32(float* v, int lane) {
   return v[0];
 }
 
+// The same for 16 columns: afterwards lanes i and i + 16 hold the reduction of column i.
+template <bool MAX>
+DEVI float reduce_scatter16(float* v, int lane) {
+#pragma unroll
+  for (int w = 8; w >= 1; w >>= 1) {
+    const bool upper = (lane & w) != 0;
+#pragma unroll
+    for (int i = 0; i < w; ++i) {
+      const float send = upper ? v[i] : v[i + w];
+      const float keep = upper ? v[i + w] : v[i];
+      const float recv = __shfl_xor_sync(0xffffffffu, send, w);
+      v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
+    }
+  }
+  const float other = __shfl_xor_sync(0xffffffffu, v[0], 16);
+  return MAX ? fmaxf(v[0], other) : v[0] + other;
+}
+
+// Load NQ TMEM columns of this warp's lanes in chunks of 32 (of 16 when NQ is not a
+// multiple of 32).
+template <int NQ>
+DEVI void tmem_ld_cols(uint32_t taddr, float (&v)[NQ]) {
+  if constexpr (NQ % 32 == 0) {
+#pragma unroll
+    for (int c = 0; c < NQ; c += 32) tmem_ld32(taddr + c, *reinterpret_cast<float(*)[32]>(v + c));
+  } else {
+#pragma unroll
+    for (int c = 0; c < NQ; c += 16) tmem_ld16(taddr + c, *reinterpret_cast<float(*)[16]>(v + c));
+  }
+}
+
 template <int NQ, bool FP8>
 __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     attn_cache_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
@@ -235,7 +268,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
   volatile int* abort_flag = &S.abort_flag;
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  constexpr uint32_t kTmemCols = 4 * NQ;  // S[2] then O[2]
+  constexpr uint32_t kTmemCols = 4 * NQ <= 128 ? 128 : (4 * NQ <= 256 ? 256 : 512);  // S[2] then O[2]
   constexpr uint32_t kQBox = NQ * 128;    // bytes of one 64-column Q box / one 64-key P half
 
   if (threadIdx.x == 0) {
@@ -467,17 +500,16 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         wait(&S.o_full[ob], oph);
         tc_fence_after();
         const float4* al4 = reinterpret_cast<const float4*>(S.fin_alpha[fuu & 1]);
+        {
+          float tmp[NQ];
+          tmem_ld_cols<NQ>(tmem + lane_base + 2 * NQ + ob * NQ, tmp);
 #pragma unroll
-        for (int c = 0; c < NQ; c += 32) {
-          float tmp[32];
-          tmem_ld32(tmem + lane_base + 2 * NQ + ob * NQ + c, tmp);
-#pragma unroll
-          for (int i = 0; i < 32; i += 4) {
-            const float4 al = al4[(c + i) / 4];
-            o[c + i] = o[c + i] * al.x + tmp[i];
-            o[c + i + 1] = o[c + i + 1] * al.y + tmp[i + 1];
-            o[c + i + 2] = o[c + i + 2] * al.z + tmp[i + 2];
-            o[c + i + 3] = o[c + i + 3] * al.w + tmp[i + 3];
+          for (int i = 0; i < NQ; i += 4) {
+            const float4 al = al4[i / 4];
+            o[i] = o[i] * al.x + tmp[i];
+            o[i + 1] = o[i + 1] * al.y + tmp[i + 1];
+            o[i + 2] = o[i + 2] * al.z + tmp[i + 2];
+            o[i + 3] = o[i + 3] * al.w + tmp[i + 3];
           }
         }
         tc_fence_before();
@@ -486,7 +518,11 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       }
       // row sums: reduce the per-key partial sums over the 128 threads
 #pragma unroll
-      for (int c = 0; c < NQ; c += 32) S.red[quarter][c + lane] = reduce_scatter32<false>(l + c, lane);
+      for (int c = 0; c + 32 <= NQ; c += 32) S.red[quarter][c + lane] = reduce_scatter32<false>(l + c, lane);
+      if constexpr (NQ % 32 != 0) {
+        const float v16 = reduce_scatter16<false>(l + (NQ - 16), lane);
+        if (lane < 16) S.red[quarter][NQ - 16 + lane] = v16;
+      }
       softmax_sync();
       if (r < NQ) {
         const float lt = S.red[0][r] + S.red[1][r] + S.red[2][r] + S.red[3][r];
@@ -585,8 +621,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         wait(&S.s_full[sb], sph);
         tc_fence_after();
         float s[NQ];
-#pragma unroll
-        for (int c = 0; c < NQ; c += 32) tmem_ld32(tmem + lane_base + sb * NQ + c, *reinterpret_cast<float(*)[32]>(s + c));
+        tmem_ld_cols<NQ>(tmem + lane_base + sb * NQ, s);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.s_free[sb]);
@@ -691,17 +726,16 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
           wait(&S.o_full[ob], oph);
           tc_fence_after();
           const float4* al4 = reinterpret_cast<const float4*>(S.alpha[tp ^ 1u]);
+          {
+            float tmp[NQ];
+            tmem_ld_cols<NQ>(tmem + lane_base + 2 * NQ + ob * NQ, tmp);
 #pragma unroll
-          for (int c = 0; c < NQ; c += 32) {
-            float tmp[32];
-            tmem_ld32(tmem + lane_base + 2 * NQ + ob * NQ + c, tmp);
-#pragma unroll
-            for (int i = 0; i < 32; i += 4) {
-              const float4 al = al4[(c + i) / 4];
-              o_acc[c + i] = o_acc[c + i] * al.x + tmp[i];
-              o_acc[c + i + 1] = o_acc[c + i + 1] * al.y + tmp[i + 1];
-              o_acc[c + i + 2] = o_acc[c + i + 2] * al.z + tmp[i + 2];
-              o_acc[c + i + 3] = o_acc[c + i + 3] * al.w + tmp[i + 3];
+            for (int i = 0; i < NQ; i += 4) {
+              const float4 al = al4[i / 4];
+              o_acc[i] = o_acc[i] * al.x + tmp[i];
+              o_acc[i + 1] = o_acc[i + 1] * al.y + tmp[i + 1];
+              o_acc[i + 2] = o_acc[i + 2] * al.z + tmp[i + 2];
+              o_acc[i + 3] = o_acc[i + 3] * al.w + tmp[i + 3];
             }
           }
           tc_fence_before();
@@ -937,6 +971,7 @@ int launch_attn_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorM
                    cudaStream_t s) {
   const bool fp8 = p.kv_dtype == DLLM_E4M3;
   if (p.nq_pad <= 32) return fp8 ? launch_one<32, true>(p, tm_q, tm_kv, grid, s) : launch_one<32, false>(p, tm_q, tm_kv, grid, s);
+  if (p.nq_pad <= 48) return fp8 ? launch_one<48, true>(p, tm_q, tm_kv, grid, s) : launch_one<48, false>(p, tm_q, tm_kv, grid, s);
   return fp8 ? launch_one<64, true>(p, tm_q, tm_kv, grid, s) : launch_one<64, false>(p, tm_q, tm_kv, grid, s);
 }
 

@@ -439,7 +439,7 @@ int do_attend(dllm_cache* c, int layer, const int32_t* positions, const uint8_t*
     rc = launch_attn_f32(a, (const float*)layer_kv(c, layer), hd, s);
     return rc ? from_cuda((cudaError_t)rc) : DLLM_OK;
   }
-  a.nq_pad = n_tok <= 32 ? 32 : 64;
+  a.nq_pad = n_tok <= 32 ? 32 : (n_tok <= 48 ? 48 : 64);
   a.n_qchunks = ceil_div(n_tok, kQChunk);
   a.key_tiles = kr.hi >= 0 ? ceil_div(a.key_hi, kKeyTile) - a.tile_lo
                            : ceil_div(d.max_pos + (view ? d.tail_slots : 0), kKeyTile);
@@ -820,7 +820,7 @@ extern "C" int dllm_cache_attend_noalloc(dllm_cache* c, int layer, const int32_t
     return rc ? from_cuda((cudaError_t)rc) : DLLM_OK;
   }
   // same work split as dllm_cache_attend, so both produce the same result
-  a.nq_pad = n_tok <= 32 ? 32 : 64;
+  a.nq_pad = n_tok <= 32 ? 32 : (n_tok <= 48 ? 48 : 64);
   a.n_qchunks = ceil_div(n_tok, kQChunk);
   a.key_tiles = ceil_div(d.max_pos + (view ? d.tail_slots : 0), kKeyTile);
   const int base = B * H * a.n_qchunks;
