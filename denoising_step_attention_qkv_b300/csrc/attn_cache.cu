@@ -782,6 +782,30 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     int ss = 0, ko = 0, vo = 0, uu = 0;
     uint32_t sph = 0, kph = 0, vph = 0;
     bool ok = true;
+    // The group scales of key r of a tile (fetched one tile ahead: they come from HBM).
+    auto fetch_scales = [&](const Unit& y, int t, float& ks, float& vs) {
+      const int j = t * kKeyTile + r;
+      ks = 0.0f;
+      vs = 0.0f;
+      if (j < p.slots) {
+        const size_t srow = (static_cast<size_t>(y.b) * p.slots + j) * 2;
+        ks = __ldg(p.kv_scale + srow * p.H + y.h);
+        vs = __ldg(p.kv_scale + (srow + 1) * p.H + y.h);
+      }
+    };
+    // the first tile of the first non-empty unit from round `from` on
+    auto next_tile = [&](int from, Unit& y) -> bool {
+      for (int r2 = from, u2 = cta_unit(p, r2); u2 < p.units; u2 = cta_unit(p, ++r2)) {
+        y = decode_unit(p, u2, order);
+        if (y.t1 > y.t0) return true;
+      }
+      return false;
+    };
+    float nks = 0.0f, nvs = 0.0f;
+    {
+      Unit y;
+      if (next_tile(0, y)) fetch_scales(y, y.t0, nks, nvs);
+    }
     for (int rnd = 0, u = cta_unit(p, 0); u < p.units && ok; u = cta_unit(p, ++rnd), ++uu) {
       const Unit x = decode_unit(p, u, order);
       {
@@ -803,12 +827,13 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       for (int t = x.t0; t < x.t1; ++t) {
         const int j = t * kKeyTile + r;
         const uint32_t sw = static_cast<uint32_t>(r & 7);
-        // this key's group scales, fetched before waiting for its codes
-        float ksc = 0.0f, vsc = 0.0f;
-        if (j < p.slots) {
-          const size_t srow = (static_cast<size_t>(x.b) * p.slots + j) * 2;
-          ksc = __ldg(p.kv_scale + srow * p.H + x.h);
-          vsc = __ldg(p.kv_scale + (srow + 1) * p.H + x.h);
+        // this key's group scales (prefetched), and the next tile's
+        const float ksc = nks, vsc = nvs;
+        if (t + 1 < x.t1) {
+          fetch_scales(x, t + 1, nks, nvs);
+        } else {
+          Unit y;
+          if (next_tile(rnd + 1, y)) fetch_scales(y, y.t0, nks, nvs);
         }
         // K
         if (!mbar_wait_warp(&S.sk_full[ss], sph, abort_flag)) { ok = false; break; }
