@@ -684,10 +684,12 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
             wait(&S.v_full[vs], vph);
             uint4* row0v = reinterpret_cast<uint4*>(S.v[vs] + r * 128);
             uint4* row1v = reinterpret_cast<uint4*>(S.v[vs] + kTileBytes / 2 + r * 128);
+            // chunk order rotated per row (the 128-byte swizzle), so that neighbouring
+            // rows write different banks
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
-              row0v[k] = make_uint4(0u, 0u, 0u, 0u);
-              row1v[k] = make_uint4(0u, 0u, 0u, 0u);
+              row0v[k ^ (r & 7)] = make_uint4(0u, 0u, 0u, 0u);
+              row1v[k ^ (r & 7)] = make_uint4(0u, 0u, 0u, 0u);
             }
           }
           if (++vs == VST) { vs = 0; vph ^= 1u; }
