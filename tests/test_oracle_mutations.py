@@ -145,3 +145,50 @@ def test_planted_refresh_mistake_is_caught(monkeypatch, bad, pin):
     monkeypatch.setattr(O, "refresh_due", bad)
     with pytest.raises(AssertionError):
         pin()
+
+
+def _merge_states_natural_base(a, b):
+    Oa, ma, la = a
+    Ob, mb, lb = b
+    M = np.maximum(ma, mb)
+    Mu = np.where(np.isfinite(M), M, 0.0)
+    wa = np.where(np.isfinite(ma), np.exp(ma - Mu), 0.0)
+    wb = np.where(np.isfinite(mb), np.exp(mb - Mu), 0.0)
+    return Oa * wa[..., None] + Ob * wb[..., None], M, la * wa + lb * wb
+
+
+def _merge_states_sums_not_rescaled(a, b):
+    Oa, ma, la = a
+    Ob, mb, lb = b
+    M = np.maximum(ma, mb)
+    Mu = np.where(np.isfinite(M), M, 0.0)
+    wa = np.where(np.isfinite(ma), np.exp2(ma - Mu), 0.0)
+    wb = np.where(np.isfinite(mb), np.exp2(mb - Mu), 0.0)
+    return Oa * wa[..., None] + Ob * wb[..., None], M, la + lb
+
+
+def _attention_partial_natural_units(q, K, V, vis=None):
+    q = np.asarray(q, np.float64)
+    K = np.asarray(K, np.float64)
+    V = np.asarray(V, np.float64)
+    s = np.einsum("qhd,khd->qhk", q, K) / math.sqrt(q.shape[-1])
+    if vis is not None:
+        s = np.where(np.asarray(vis, bool)[:, None, :], s, -np.inf)
+    m = s.max(axis=-1) if s.shape[-1] else np.full(s.shape[:2], -np.inf)
+    w = np.where(np.isfinite(m)[..., None], np.exp(s - np.where(np.isfinite(m), m, 0.0)[..., None]), 0.0)
+    return np.einsum("qhk,khd->qhd", w, V), m, w.sum(axis=-1)
+
+
+STATE_CASES = [
+    ("merge_states", _merge_states_natural_base, P.test_partial_states_merge_to_full_attention),
+    ("merge_states", _merge_states_sums_not_rescaled, P.test_partial_states_merge_to_full_attention),
+    ("attention_partial", _attention_partial_natural_units, P.test_partial_state_closed_forms),
+]
+
+
+@pytest.mark.parametrize("name,bad,pin", STATE_CASES, ids=[f"{c[0]}-{c[1].__name__}" for c in STATE_CASES])
+def test_planted_state_mistake_is_caught(monkeypatch, name, bad, pin):
+    monkeypatch.setattr(OD, name, bad)
+    monkeypatch.setattr(O, name, bad)
+    with pytest.raises(AssertionError):
+        pin()
