@@ -613,6 +613,23 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   grid_dep_launch();
+  // W is never written by the kernels of a step, so the producer requests the W half of
+  // the first stages of its first item before the dependency wait (not with selection
+  // flags, whose values decide which items run); the x halves follow after it
+  int npre = 0;
+  if (warp == 0 && lane == 0 && p.kv_seq_flags == nullptr && pair < p.items_total) {
+    const PairItem it = decode_pair_item(p, pair);
+    const int b_rows = it.half ? 64 : 128;
+    const CUtensorMap* bm = it.half ? &tm_w_half : &tm_w;
+    const int n0 = it.n0 + static_cast<int>(rank) * b_rows;
+    const uint32_t bytes = 2 * (kABytes + b_rows * BK * 2);
+    npre = p.k_blocks < kPairStages ? p.k_blocks : kPairStages;
+    for (int s = 0; s < npre; ++s) {
+      if (rank == 0) mbar_arrive_expect_tx(&full[s], bytes);
+      tma_load_2d_pair(sB + s * kPairBBytes, bm, map_to_rank(smem_u32(&full[s]), 0), s * BK, n0,
+                       p.m_fastest ? policy_evict_first() : policy_evict_last());
+    }
+  }
   grid_dep_wait();  // x, positions, indices and flags may come from the previous kernel
   select_init(p);
   __syncthreads();
@@ -635,11 +652,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int n0 = it.n0 + static_cast<int>(rank) * b_rows;
       const uint32_t bytes = 2 * (kABytes + b_rows * BK * 2);  // both CTAs' copies
       for (int kb = 0; kb < p.k_blocks; ++kb) {
-        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
-        if (rank == 0) mbar_arrive_expect_tx(&full[stage], bytes);
         const uint32_t fb = map_to_rank(smem_u32(&full[stage]), 0);
-        tma_load_2d_pair(sA + stage * kABytes, am, fb, kb * BK, m0, pol_x);
-        tma_load_2d_pair(sB + stage * kPairBBytes, bm, fb, kb * BK, n0, pol_w);
+        if (item == pair && kb < npre) {  // W already requested: only x for this stage
+          tma_load_2d_pair(sA + stage * kABytes, am, fb, kb * BK, m0, pol_x);
+        } else {
+          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+          if (rank == 0) mbar_arrive_expect_tx(&full[stage], bytes);
+          tma_load_2d_pair(sA + stage * kABytes, am, fb, kb * BK, m0, pol_x);
+          tma_load_2d_pair(sB + stage * kPairBBytes, bm, fb, kb * BK, n0, pol_w);
+        }
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }
