@@ -675,6 +675,7 @@ def run_ours(args, rank, world, local):
 
     alg = algorithmic(wl)
     pk = peaks()
+    cache_bytes = B * S * 2 * D * 2  # the layer's K and V
     mean = {kname: statistics.mean(v) for kname, v in per.items()}
     proj_tflops = alg["proj_flops"] / (mean["project"] * 1e-3) / 1e12
     attn_gbs = alg["attn_bytes"] / (mean["attend"] * 1e-3) / 1e9
@@ -701,7 +702,9 @@ def run_ours(args, rank, world, local):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": wl.name, "batch": B, "d_model": D, "n_heads": s.n_heads, "head_dim": s.head_dim,
                    "cache_positions": S, "block": wl.block_len, "tracked_topk": k, "rope_theta": s.rope_theta,
-                   "l2": "value: flushed between steps (256 MiB write); e2e: no flush, every step streams the 512 MiB cache (larger than L2)",
+                   "l2": "value: flushed between steps (256 MiB write); e2e: no flush, every step streams the "
+                         + ("%.0f MiB cache (larger than L2)" % (cache_bytes / 2**20) if cache_bytes > L2_BYTES
+                            else "%.1f MiB cache, which fits in L2 (e2e steps run L2-warm)" % (cache_bytes / 2**20)),
                    "timing": "value: K steps with events at step boundaries only; kernels: a second pass of "
                              "min(K, 300) steps with an event between every two kernels",
                    "parallelism": f"replicas x{world}"},
