@@ -58,6 +58,9 @@ RAGGED = [
     # more units than SMs with every other sequence empty: consecutive empty units per CTA
     ("empty-runs", dict(batch=40, d_model=512, head_dim=128, max_pos=256, block=16, gen_lo=128),
      [0 if b % 2 else 70 + 4 * b for b in range(40)]),
+    # more sequences than the length ranking holds (256): units in plain order
+    ("many", dict(batch=300, d_model=256, head_dim=128, max_pos=256, block=16, gen_lo=128),
+     [(37 * b) % 257 for b in range(300)]),
 ]
 
 
