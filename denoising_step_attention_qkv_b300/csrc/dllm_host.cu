@@ -531,6 +531,8 @@ int dllm_cache_attend_partial(dllm_cache* c, int layer, const int32_t* positions
 int dllm_attend_merge(const float* state_a, const float* state_b, int batch, int n_tok, int n_heads, int head_dim,
                       void* out, float* state_out, void* stream) {
   if (!state_a || !state_b || (!out && !state_out) || batch < 1 || n_tok < 0 || n_heads < 1) return DLLM_EINVAL;
+  if (!aligned16(state_a) || !aligned16(state_b) || !aligned16(out) || !aligned16(state_out)) return DLLM_EINVAL;
+  if ((long long)batch * n_tok * n_heads >= (1ll << 31)) return DLLM_EINVAL;
   if (head_dim != kHd) return DLLM_EUNSUPPORTED;
   if (n_tok == 0) return DLLM_OK;
   const int rc = launch_state_merge(state_a, state_b, batch * n_tok, n_heads, out, state_out,

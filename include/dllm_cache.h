@@ -220,7 +220,9 @@ int dllm_cache_attend_partial(dllm_cache* cache, int layer, const int32_t* posit
  *   O = w_a O_a + w_b O_b, l = w_a l_a + w_b l_b,
  * and write the attention output out = O / l (bf16 [batch][n_tok][n_heads * head_dim],
  * 0 where l = 0) and/or the combined state (same layout as the inputs; may alias
- * neither input).  Either output may be NULL, not both.  head_dim must be 128. */
+ * neither input).  Either output may be NULL, not both.  head_dim must be 128
+ * (DLLM_EUNSUPPORTED otherwise).  States and `out` 16-byte aligned, batch * n_tok *
+ * n_heads below 2^31 (DLLM_EINVAL otherwise). */
 int dllm_attend_merge(const float* state_a, const float* state_b, int batch, int n_tok, int n_heads, int head_dim,
                       void* out, float* state_out, void* stream);
 

@@ -61,3 +61,20 @@ def test_null_handles_rejected():
     assert L.dllm_cache_status(None, None) == capi.DLLM_EINVAL
     assert L.dllm_cache_free(None) == capi.DLLM_OK
     assert capi.dllm_strerror(capi.DLLM_EUNSUPPORTED) == "unsupported configuration"
+
+
+def test_merge_and_multilayer_arguments_rejected_on_host():
+    L = capi.lib()
+    a, b, o = 0x10000, 0x20000, 0x30000  # never dereferenced: every call below fails its checks
+    assert L.dllm_attend_merge(None, b, 1, 1, 1, 128, o, None, None) == capi.DLLM_EINVAL
+    assert L.dllm_attend_merge(a, b, 1, 1, 1, 128, None, None, None) == capi.DLLM_EINVAL  # no output
+    assert L.dllm_attend_merge(a + 8, b, 1, 1, 1, 128, o, None, None) == capi.DLLM_EINVAL  # misaligned state
+    assert L.dllm_attend_merge(a, b, 1, 1, 1, 128, o + 4, None, None) == capi.DLLM_EINVAL  # misaligned out
+    assert L.dllm_attend_merge(a, b, 1 << 20, 1 << 10, 4, 128, o, None, None) == capi.DLLM_EINVAL  # rows overflow
+    assert L.dllm_attend_merge(a, b, 1, 1, 1, 64, o, None, None) == capi.DLLM_EUNSUPPORTED
+    assert L.dllm_attend_merge(a, b, 1, 0, 1, 128, o, None, None) == capi.DLLM_OK  # nothing to do
+    assert L.dllm_elastic_workspace_bytes(None, 32, 8) == 0
+    xs = (ctypes.c_void_p * 1)(a)
+    assert L.dllm_elastic_step(None, 1, xs, xs, a, 32, a, 8, 0.9, o, a, a, None, a, 1 << 20, None) == capi.DLLM_EINVAL
+    assert L.dllm_cache_attend_ragged(None, 0, a, 1, a, o, None) == capi.DLLM_EINVAL
+    assert L.dllm_cache_attend_partial(None, 0, a, 1, o, 0, 1, a, None) == capi.DLLM_EINVAL
