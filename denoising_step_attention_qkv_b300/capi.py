@@ -27,7 +27,8 @@ EXPORTS = ("dllm_cache_bytes", "dllm_cache_alloc", "dllm_cache_free", "dllm_cach
            "dllm_cache_step_unfused", "dllm_attention_mass", "dllm_cache_attend_ragged", "dllm_cache_attend_partial",
            "dllm_attend_merge", "dllm_kv_topk", "dllm_kv_drift", "dllm_elastic_workspace_bytes", "dllm_elastic_step",
            "dllm_selftest_wait_timeout",
-           "dllm_cache_status", "dllm_strerror")
+           "dllm_cache_status", "dllm_strerror", "dllm_host_alloc", "dllm_host_free",
+           "dllm_host_stage")
 
 
 class dllm_cache_desc(ctypes.Structure):
@@ -86,6 +87,9 @@ def lib() -> ctypes.CDLL:
         L.dllm_cache_status.argtypes = [c_void_p, POINTER(c_int)]
         L.dllm_strerror.argtypes = [c_int]
         L.dllm_strerror.restype = ctypes.c_char_p
+        L.dllm_host_alloc.argtypes = [c_size_t, POINTER(c_void_p)]
+        L.dllm_host_free.argtypes = [c_void_p]
+        L.dllm_host_stage.argtypes = [c_void_p, c_void_p, c_size_t]
         for name in EXPORTS:
             if name not in ("dllm_cache_bytes", "dllm_strerror", "dllm_unfused_workspace_bytes",
                             "dllm_elastic_workspace_bytes"):
@@ -267,6 +271,59 @@ def dllm_cache_status(handle):
     if rc not in (DLLM_OK, DLLM_EDEVICE):
         raise DllmError("dllm_cache_status", rc)
     return rc, bits.value
+
+
+def dllm_host_alloc(nbytes: int) -> Optional[int]:
+    """Page-locked host block of nbytes bytes; returns its address (None for 0 bytes)."""
+    p = c_void_p()
+    _check("dllm_host_alloc", lib().dllm_host_alloc(int(nbytes), ctypes.byref(p)))
+    return p.value
+
+
+def dllm_host_free(ptr: Optional[int]) -> None:
+    _check("dllm_host_free", lib().dllm_host_free(ptr))
+
+
+def dllm_host_stage(dst: torch.Tensor, src: torch.Tensor) -> torch.Tensor:
+    """Byte copy of the contiguous CPU tensor src into dst (same byte size) with
+    streaming stores; returns dst."""
+    if dst.device.type != "cpu" or src.device.type != "cpu":
+        raise ValueError("dllm_host_stage copies host tensors")
+    nbytes = dst.numel() * dst.element_size()
+    if src.numel() * src.element_size() != nbytes:
+        raise ValueError("dllm_host_stage: dst and src differ in size")
+    _check("dllm_host_stage", lib().dllm_host_stage(_ptr(dst) if nbytes else None, _ptr(src) if nbytes else None,
+                                                   nbytes))
+    return dst
+
+
+class _HostBlock:
+    """Owns one dllm_host_alloc block; freed when the last tensor viewing it is gone."""
+
+    def __init__(self, nbytes: int):
+        self.ptr = dllm_host_alloc(nbytes)
+
+    def __del__(self):
+        if self.ptr and _lib is not None:
+            _lib.dllm_host_free(self.ptr)
+            self.ptr = None
+
+
+def host_empty(shape, dtype: torch.dtype) -> torch.Tensor:
+    """Uninitialised CPU tensor over a dllm_host_alloc block (page-locked, read and
+    written by the GPU's copy engines at the link rate).  The block is released when
+    the tensor and every view of it are gone."""
+    shape = tuple(int(s) for s in (shape if isinstance(shape, (tuple, list, torch.Size)) else (shape,)))
+    numel = 1
+    for s in shape:
+        numel *= s
+    nbytes = numel * torch.empty((), dtype=dtype).element_size()
+    if nbytes == 0:
+        return torch.empty(shape, dtype=dtype)
+    blk = _HostBlock(nbytes)
+    arr = (ctypes.c_uint8 * nbytes).from_address(blk.ptr)
+    arr._owner = blk  # the tensor's storage keeps arr, and arr the block, alive
+    return torch.frombuffer(arr, dtype=torch.uint8).view(dtype).reshape(shape)
 
 
 # ------------------------------------------------------------------------------------

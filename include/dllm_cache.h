@@ -373,6 +373,37 @@ int dllm_cache_status(dllm_cache* cache, int* device_bits);
 /* Static, human-readable name of a dllm_status. */
 const char* dllm_strerror(int status);
 
+/* Page-locked HOST memory for a step's inputs and results when they live on the host
+ * (a serving loop that receives hidden states and returns outputs): `bytes` bytes
+ * from the CUDA runtime's own page-locked allocator, which the GPU's copy engines read
+ * and write directly, at the link rate, with no staging copy.  Not part of the pages'
+ * method: the end-to-end path's host-side buffers.
+ *   - *out receives the host address (16-byte aligned or better), or NULL on error or
+ *     when bytes == 0 (which returns DLLM_OK).  The contents are uninitialised.
+ *   - The caller owns the block and releases it with dllm_host_free; it stays valid for
+ *     every device and context of the process until then.
+ *   - Errors: DLLM_EINVAL if out is NULL; DLLM_EOOM if the memory cannot be locked;
+ *     DLLM_ECUDA if no CUDA device is usable.  Synchronous; launches nothing. */
+int dllm_host_alloc(size_t bytes, void** out);
+
+/* Release a block from dllm_host_alloc (NULL: no-op, DLLM_OK).  The caller first makes
+ * sure no copy that reads or writes it is still pending.  Returns DLLM_ECUDA if the
+ * runtime rejects the address (not a dllm_host_alloc block). */
+int dllm_host_free(void* ptr);
+
+/* Copy `bytes` bytes of host memory from src to dst (normally a dllm_host_alloc block
+ * that a host-to-device copy will read next) with streaming stores, which leave no
+ * dirty copies of dst in the CPU caches.  A device copy that reads host lines still
+ * dirty in those caches has to fetch each one out of them, and on the B300 hosts
+ * measured that cut host-to-device copies from about 54 GB/s to about 12 GB/s; a
+ * buffer written with this call is read at the full rate.  Not part of the pages'
+ * method: staging of the end-to-end path.
+ *   - Host pointers, any alignment; the ranges must not overlap (DLLM_EINVAL), nor
+ *     may dst or src be NULL unless bytes == 0 (which does nothing, DLLM_OK).
+ *   - Synchronous, on the calling thread; no CUDA call, no GPU needed.  The result is
+ *     a plain byte copy (memcpy semantics). */
+int dllm_host_stage(void* dst, const void* src, size_t bytes);
+
 #ifdef __cplusplus
 }
 #endif

@@ -78,3 +78,52 @@ def test_merge_and_multilayer_arguments_rejected_on_host():
     assert L.dllm_elastic_step(None, 1, xs, xs, a, 32, a, 8, 0.9, o, a, a, None, a, 1 << 20, None) == capi.DLLM_EINVAL
     assert L.dllm_cache_attend_ragged(None, 0, a, 1, a, o, None) == capi.DLLM_EINVAL
     assert L.dllm_cache_attend_partial(None, 0, a, 1, o, 0, 1, a, None) == capi.DLLM_EINVAL
+
+
+def test_host_alloc_arguments():
+    """Page-locked host blocks: a zero-byte request and a NULL free are no-ops, a NULL
+    out-pointer is rejected, and without a usable device the call fails cleanly."""
+    L = capi.lib()
+    p = ctypes.c_void_p(1234)
+    assert L.dllm_host_alloc(0, ctypes.byref(p)) == capi.DLLM_OK and p.value is None
+    assert L.dllm_host_alloc(16, None) == capi.DLLM_EINVAL
+    assert L.dllm_host_free(None) == capi.DLLM_OK
+    assert capi.host_empty((0, 3), capi.torch.bfloat16).shape == (0, 3)
+    import torch
+    if not torch.cuda.is_available():
+        p = ctypes.c_void_p()
+        assert L.dllm_host_alloc(64, ctypes.byref(p)) == capi.DLLM_ECUDA and p.value is None
+
+
+@pytest.mark.parametrize("nbytes", [1, 15, 16, 17, 63, 64, 65, 1000, 4096 + 7, (1 << 20) + 3])
+@pytest.mark.parametrize("dst_off,src_off", [(0, 0), (1, 0), (0, 5), (7, 3), (15, 15)])
+def test_host_stage_is_a_byte_copy(nbytes, dst_off, src_off):
+    """The streaming-store copy writes exactly the bytes of src into dst, whatever the
+    alignment of either side and the length of the unaligned head and tail, and
+    touches nothing around the destination range."""
+    import numpy as np
+    rng = np.random.default_rng(nbytes * 31 + dst_off * 7 + src_off)
+    src = np.frombuffer(rng.bytes(nbytes + 32), dtype=np.uint8).copy()
+    dst = np.full(nbytes + 32, 0xA5, dtype=np.uint8)
+    rc = capi.lib().dllm_host_stage(dst.ctypes.data + dst_off, src.ctypes.data + src_off, nbytes)
+    assert rc == capi.DLLM_OK
+    assert np.array_equal(dst[dst_off:dst_off + nbytes], src[src_off:src_off + nbytes])
+    assert (dst[:dst_off] == 0xA5).all() and (dst[dst_off + nbytes:] == 0xA5).all()
+
+
+def test_host_stage_arguments():
+    import numpy as np
+    import torch
+    L = capi.lib()
+    buf = np.zeros(256, dtype=np.uint8)
+    p = buf.ctypes.data
+    assert L.dllm_host_stage(None, None, 0) == capi.DLLM_OK
+    assert L.dllm_host_stage(None, p, 16) == capi.DLLM_EINVAL
+    assert L.dllm_host_stage(p, None, 16) == capi.DLLM_EINVAL
+    assert L.dllm_host_stage(p, p + 64, 65) == capi.DLLM_EINVAL  # overlapping ranges
+    assert L.dllm_host_stage(p + 64, p, 65) == capi.DLLM_EINVAL
+    assert L.dllm_host_stage(p, p + 64, 64) == capi.DLLM_OK  # adjacent is fine
+    a, b = torch.arange(100, dtype=torch.int32), torch.empty(100, dtype=torch.int32)
+    assert torch.equal(capi.dllm_host_stage(b, a), a)
+    with pytest.raises(ValueError):
+        capi.dllm_host_stage(b[:50], a)

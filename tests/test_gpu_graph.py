@@ -104,3 +104,35 @@ def test_multilayer_step_graph_replay_matches_eager():
     for key in ("out", "cos", "flags", "mass_out"):
         assert torch.equal(a[key], b[key]), key
     assert torch.equal(a["cache"].kv(), b["cache"].kv())
+
+
+def test_host_staged_step_matches_device_inputs():
+    """The end-to-end form of a step: inputs staged in dllm_host_alloc blocks, copied
+    in on a side stream, results copied back into host blocks; the same bits as the
+    step on device-resident inputs."""
+    wl = W.make(3, batch=6, d_model=512, head_dim=128, max_pos=300, gen_lo=128, drift_k=8)
+    ref, staged = _step_state(wl), _step_state(wl)
+    st = torch.cuda.current_stream()
+    _run_step(wl, ref, st)
+    keys_in, keys_out = ("x", "xp", "pos", "mass", "lo"), ("out", "cos", "ref", "idx")
+    h_in = {k: capi.host_empty(staged[k].shape, staged[k].dtype) for k in keys_in}
+    h_out = {k: capi.host_empty(staged[k].shape, staged[k].dtype) for k in keys_out}
+    for k in keys_in:
+        capi.dllm_host_stage(h_in[k], staged[k].cpu())
+        assert h_in[k].is_pinned() and h_in[k].data_ptr() % 16 == 0
+        staged[k].fill_(0)
+    copy = torch.cuda.Stream()
+    copy.wait_stream(st)
+    with torch.cuda.stream(copy):
+        for k in keys_in:
+            staged[k].copy_(h_in[k], non_blocking=True)
+    st.wait_stream(copy)
+    _run_step(wl, staged, st)
+    for k in keys_out:
+        h_out[k].copy_(staged[k], non_blocking=True)
+    torch.cuda.synchronize()
+    for k in keys_out:
+        assert torch.equal(h_out[k], ref[k].cpu()), k
+    view = h_out["out"][1:3]
+    del h_out
+    assert torch.equal(view, ref["out"][1:3].cpu())  # a view keeps its block alive
