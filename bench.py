@@ -217,7 +217,7 @@ def algorithmic(wl):
                 drift_bytes=drift_bytes)
 
 
-def elastic_leg(args, dev, B, S, D, H, hd, theta, beta, k, gamma, flush):
+def elastic_leg(args, dev, B, S, D, H, hd, theta, beta, k, gamma, flush, kv_dtype=None):
     """One denoising step over L layers with the depth-wise drift refresh
     (dllm_elastic_step), LLaDA-8B layer shapes.  Inputs are drawn on the device from a
     seeded generator: per layer the hidden states the cache was built from, x_prev ~
@@ -226,13 +226,16 @@ def elastic_leg(args, dev, B, S, D, H, hd, theta, beta, k, gamma, flush):
     some sequences fail the test in deep layers.  The step is stationary (the failing
     layer keeps its cache, so every repetition refreshes the same sequence-layers).
     Also timed: gamma = -2 (never refresh) and gamma = 2 (every sequence recomputes
-    layers 1..L-1), the two ends of the threshold."""
+    layers 1..L-1), the two ends of the threshold.  kv_dtype: the cache's storage type
+    (bf16 by default; e4m3 refreshes into the FP8 cache with its per-group scales)."""
     import torch
     from denoising_step_attention_qkv_b300 import capi
+    if kv_dtype is None:
+        kv_dtype = capi.DLLM_BF16
     L = args.elastic_layers
     g = torch.Generator(device=dev)
     g.manual_seed(2024)
-    cache = capi.Cache(L, B, S, H, hd, capi.DLLM_BF16, theta, 0, device=dev)
+    cache = capi.Cache(L, B, S, H, hd, kv_dtype, theta, 0, device=dev)
     all_pos = torch.arange(S, dtype=torch.int32, device=dev).repeat(B, 1)
     s_b = 0.3 + 0.9 * torch.rand(B, generator=g, device=dev)
     ws, xs = [], []
@@ -277,7 +280,8 @@ def elastic_leg(args, dev, B, S, D, H, hd, theta, beta, k, gamma, flush):
                 "refreshed_sequence_layers": refreshed, "of": B * L,
                 "first_failing_layer": [int(np.argmax(f[:, b])) if f[:, b].any() else None for b in range(B)]}
 
-    res = {"layers": L, "batch": B, "window": beta, "tracked": k, "steps": n, "runs": [run(gamma), run(-2.0), run(2.0)],
+    res = {"layers": L, "batch": B, "window": beta, "tracked": k, "steps": n,
+           "kv": "e4m3" if kv_dtype == capi.DLLM_E4M3 else "bf16", "runs": [run(gamma), run(-2.0), run(2.0)],
            "inputs": "device-generated, seeded: x_prev ~ N(0,1); x_all = x_prev + sigma[l][b] N(0,1), "
                      "sigma = 0.6 (l+1)/L s_b, s_b ~ U(0.3, 1.2); mass ~ Dirichlet(0.1); L2 flushed between steps"}
     rc, bits = cache.status()
@@ -701,6 +705,8 @@ def run_ours(args, rank, world, local):
     if nxt is not None and not args.no_elastic:
         nxt["elastic"] = elastic_leg(args, dev, B, S, D, s.n_heads, s.head_dim, s.rope_theta, wl.block_len, k,
                                      wl.gamma, flush)
+        nxt["elastic_fp8"] = elastic_leg(args, dev, B, S, D, s.n_heads, s.head_dim, s.rope_theta, wl.block_len, k,
+                                         wl.gamma, flush, kv_dtype=capi.DLLM_E4M3)
 
     rc, bits = cache.status()
     if rc != capi.DLLM_OK:
