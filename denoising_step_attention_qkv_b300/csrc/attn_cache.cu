@@ -27,8 +27,10 @@
 //
 // FP8-e4m3 cache ("LaCache ...", Methodology 2: per-group FP8; one group here = one
 // head of one token, K or V, with an fp32 scale): TMA stages the e4m3 tiles (half the
-// bytes of bf16) in a 2-deep ring and four converter warps dequantise them into the MMA
-// operand layout as f16: the code (exact in f16, one conversion per pair) times the
+// bytes of bf16) in a 2-deep ring and four converter warps turn them into the MMA
+// operand layout as f16 (one conversion per pair of codes).  K keeps the bare code,
+// exact in f16: a key's K scale is constant along its row of the score tile, so the
+// softmax folds it into that row's logit scale (in fp32).  V is the code times the
 // group's scale (one f16 multiply per pair), a single f16 rounding of relative size
 // 2^-11, far below the e4m3 step of 2^-4.  The MMAs of this path take f16 throughout:
 // the converters also turn each unit's Q chunk from bf16 to f16 in place, and the
@@ -113,6 +115,19 @@ DEVI void dequant16_f16(const uint4 in, __half2 scale, uint4& lo, uint4& hi) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
     const __half2 h = __hmul2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr[i], __NV_E4M3)), scale);
+    w[i] = *reinterpret_cast<const uint32_t*>(&h);
+  }
+  lo = make_uint4(w[0], w[1], w[2], w[3]);
+  hi = make_uint4(w[4], w[5], w[6], w[7]);
+}
+
+// 16 e4m3 codes to f16, unscaled (exact: every e4m3 value is an f16 value).
+DEVI void cvt16_f16(const uint4 in, uint4& lo, uint4& hi) {
+  const __nv_fp8x2_storage_t* pr = reinterpret_cast<const __nv_fp8x2_storage_t*>(&in);
+  uint32_t w[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    const __half2 h = __half2(__nv_cvt_fp8x2_to_halfraw2(pr[i], __NV_E4M3));
     w[i] = *reinterpret_cast<const uint32_t*>(&h);
   }
   lo = make_uint4(w[0], w[1], w[2], w[3]);
@@ -568,6 +583,25 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       }
     };
 
+    // e4m3: the K group scale of this thread's key, fetched one tile ahead (it comes
+    // from HBM); it multiplies the key's logits, the K operand holding the bare code
+    auto fetch_ks = [&](const Unit& y, int t) -> float {
+      const int jj = t * kKeyTile + r;
+      return jj < p.slots ? __ldg(p.kv_scale + (static_cast<size_t>(y.b) * p.slots + jj) * 2 * p.H + y.h) : 0.0f;
+    };
+    auto first_tile = [&](int from, Unit& y) -> bool {
+      for (int r2 = from, u2 = cta_unit(p, r2); u2 < p.units; u2 = cta_unit(p, ++r2)) {
+        y = decode_unit(p, u2, order);
+        if (y.t1 > y.t0) return true;
+      }
+      return false;
+    };
+    float ks_next = 0.0f;
+    if constexpr (FP8) {
+      Unit y;
+      if (first_tile(0, y)) ks_next = fetch_ks(y, y.t0);
+    }
+
     float o_prev[NQ], l_prev[NQ];  // the unit waiting to be finished (deferred finish only)
     Unit px{};
     int puu = 0;
@@ -617,6 +651,16 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       for (int t = x.t0; t < x.t1; ++t) {
         const uint32_t sb = s_cnt & 1u, sph = (s_cnt >> 1) & 1u;
         const uint32_t tp = t & 1;  // parity slot for alpha
+        float ks_cur = 1.0f;
+        if constexpr (FP8) {
+          ks_cur = ks_next;
+          if (t + 1 < x.t1) {
+            ks_next = fetch_ks(x, t + 1);
+          } else {
+            Unit y;
+            if (first_tile(rnd + 1, y)) ks_next = fetch_ks(y, y.t0);
+          }
+        }
         // ---- A: scores of this thread's key for every query
         wait(&S.s_full[sb], sph);
         tc_fence_after();
@@ -637,7 +681,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
           vis = (j < p.max_pos + n_draft) ? dmask : 0ull;
         }
         if (p.ranged && (j < p.key_lo || j >= kend)) vis = 0ull;
-        const float sc = p.scale_log2;  // e4m3: the K scale is already in the f16 operand
+        const float sc = p.scale_log2 * ks_cur;  // e4m3: times the key's K group scale
         if (vis == ~0ull) {
 #pragma unroll
           for (int q = 0; q < NQ; ++q) s[q] *= sc;
@@ -776,24 +820,20 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
   } else if (FP8 && warp >= 6) {
     // ------------------------------------------------------------------ e4m3 -> f16 converters
     // Per unit: the Q chunk, bf16 -> f16 in place (the MMAs of this path take f16).  Per
-    // tile: thread r dequantises key row r of the staged K and V codes (code times the
-    // key's group scale, one f16 rounding) into both 64-column halves of the operand
-    // tiles, keeping the 128-byte swizzle.  V rows of slots that no query can see are
+    // tile: thread r converts key row r of the staged codes into both 64-column halves
+    // of the operand tiles, keeping the 128-byte swizzle: K as the bare code (exact in
+    // f16; the softmax multiplies the key's logits by its K scale), V as code times the
+    // key's V scale with one f16 rounding.  V rows of slots that no query can see are
     // written as zeros (their probability is 0, and 0 * NaN must not reach O).
     const int r = (warp & 3) * 32 + lane;
     int ss = 0, ko = 0, vo = 0, uu = 0;
     uint32_t sph = 0, kph = 0, vph = 0;
     bool ok = true;
-    // The group scales of key r of a tile (fetched one tile ahead: they come from HBM).
-    auto fetch_scales = [&](const Unit& y, int t, float& ks, float& vs) {
+    // The V group scale of key r of a tile (fetched one tile ahead: it comes from HBM;
+    // the K scale multiplies the key's logits in the softmax instead).
+    auto fetch_vscale = [&](const Unit& y, int t) -> float {
       const int j = t * kKeyTile + r;
-      ks = 0.0f;
-      vs = 0.0f;
-      if (j < p.slots) {
-        const size_t srow = (static_cast<size_t>(y.b) * p.slots + j) * 2;
-        ks = __ldg(p.kv_scale + srow * p.H + y.h);
-        vs = __ldg(p.kv_scale + (srow + 1) * p.H + y.h);
-      }
+      return j < p.slots ? __ldg(p.kv_scale + ((static_cast<size_t>(y.b) * p.slots + j) * 2 + 1) * p.H + y.h) : 0.0f;
     };
     // the first tile of the first non-empty unit from round `from` on
     auto next_tile = [&](int from, Unit& y) -> bool {
@@ -803,10 +843,10 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       }
       return false;
     };
-    float nks = 0.0f, nvs = 0.0f;
+    float nvs = 0.0f;
     {
       Unit y;
-      if (next_tile(0, y)) fetch_scales(y, y.t0, nks, nvs);
+      if (next_tile(0, y)) nvs = fetch_vscale(y, y.t0);
     }
     for (int rnd = 0, u = cta_unit(p, 0); u < p.units && ok; u = cta_unit(p, ++rnd), ++uu) {
       const Unit x = decode_unit(p, u, order);
@@ -829,26 +869,25 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       for (int t = x.t0; t < x.t1; ++t) {
         const int j = t * kKeyTile + r;
         const uint32_t sw = static_cast<uint32_t>(r & 7);
-        // this key's group scales (prefetched), and the next tile's
-        const float ksc = nks, vsc = nvs;
+        // this key's V scale (prefetched), and the next tile's
+        const float vsc = nvs;
         if (t + 1 < x.t1) {
-          fetch_scales(x, t + 1, nks, nvs);
+          nvs = fetch_vscale(x, t + 1);
         } else {
           Unit y;
-          if (next_tile(rnd + 1, y)) fetch_scales(y, y.t0, nks, nvs);
+          if (next_tile(rnd + 1, y)) nvs = fetch_vscale(y, y.t0);
         }
         // K
         if (!mbar_wait_warp(&S.sk_full[ss], sph, abort_flag)) { ok = false; break; }
         if (!mbar_wait_warp(&S.k_empty[ko], kph ^ 1u, abort_flag)) { ok = false; break; }
         {
-          const __half2 sc2 = __float2half2_rn(ksc);
           const uint8_t* src = S.sk[ss] + r * 128;
           uint8_t* dst = S.k[ko] + r * 128;
 #pragma unroll
           for (int c = 0; c < 8; ++c) {
             const uint4 in = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
             uint4 lo, hi;
-            dequant16_f16(in, sc2, lo, hi);
+            cvt16_f16(in, lo, hi);
             uint8_t* half = dst + (c >> 2) * (kTileBytes / 2);
             const uint32_t c0 = (c & 3) * 2;
             *reinterpret_cast<uint4*>(half + ((c0 ^ sw) << 4)) = lo;
