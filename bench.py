@@ -609,6 +609,8 @@ def run_ours(args, rank, world, local):
         t_in, t_out, t_both = copies_us(True, False), copies_us(False, True), copies_us(True, True)
         e2e = {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "graphs": "one CUDA graph per step: copy-in(i+1) | step(i) | read-back(i-1)",
+               "host_buffers": "page-locked dllm_host_alloc blocks; the inputs written into them once, before the "
+                               "timed region, with dllm_host_stage (streaming stores)",
                "us_per_step": step_us,
                "copies_only": {"h2d_us": t_in, "h2d_gbs": h2d / t_in / 1e3, "d2h_us": t_out,
                                "d2h_gbs": d2h / t_out / 1e3, "both_us": t_both,
