@@ -192,3 +192,55 @@ def test_planted_state_mistake_is_caught(monkeypatch, name, bad, pin):
     monkeypatch.setattr(O, name, bad)
     with pytest.raises(AssertionError):
         pin()
+
+
+def _row_slots_drafts_reversed(positions, view, max_pos):
+    positions = np.asarray(positions, dtype=np.int64)
+    slots = positions.copy()
+    if view is None:
+        return slots
+    drafts = [t for t in range(len(positions)) if view[t] == O.VIEW_DRAFT]
+    for r, t in enumerate(drafts):
+        slots[t] = max_pos + len(drafts) - 1 - r
+    return slots
+
+
+def _drift_per_head_mean(cache, idx, probe_kv):
+    B, k = idx.shape
+    H, hd = cache.H, cache.hd
+    cos = np.empty((B, k, 2))
+    for b in range(B):
+        for j in range(k):
+            s = int(idx[b, j])
+            for c, X in enumerate((cache.K, cache.V)):
+                pr = np.asarray(probe_kv[b, j, c]).reshape(H, hd)
+                cos[b, j, c] = np.mean([O.cosine(X[b, s, h], pr[h]) for h in range(H)])
+    return cos
+
+
+def _drift_kv_swapped(cache, idx, probe_kv):
+    return _orig_drift(cache, idx, probe_kv)[..., ::-1]
+
+
+_orig_drift = OD.kv_drift
+
+SLOT_DRIFT_CASES = [
+    ("row_slots", _row_slots_drafts_reversed, P.test_verify_rth_draft_row_writes_tail_slot_r),
+    ("kv_drift", _drift_per_head_mean, P.test_drift_closed_form_over_the_whole_token_vector),
+    ("kv_drift", _drift_kv_swapped, P.test_drift_closed_form_over_the_whole_token_vector),
+]
+
+
+@pytest.mark.parametrize("name,bad,pin", SLOT_DRIFT_CASES, ids=[f"{c[0]}-{c[1].__name__}" for c in SLOT_DRIFT_CASES])
+def test_planted_slot_or_drift_mistake_is_caught(monkeypatch, name, bad, pin):
+    monkeypatch.setattr(OD, name, bad)
+    monkeypatch.setattr(O, name, bad)
+    with pytest.raises(AssertionError):
+        pin()
+
+
+def test_reversed_draft_slots_pass_the_written_set_pin(monkeypatch):
+    """Why the contents pin is needed: the written-set pin alone cannot see the order."""
+    monkeypatch.setattr(OD, "row_slots", _row_slots_drafts_reversed)
+    monkeypatch.setattr(O, "row_slots", _row_slots_drafts_reversed)
+    P.test_verify_draft_rows_use_tail_slots()

@@ -257,6 +257,23 @@ def test_verify_draft_rows_use_tail_slots():
     assert cache.written[0, S:S + n_draft].all() and not cache.written[0, S + n_draft:].any()
 
 
+def test_verify_rth_draft_row_writes_tail_slot_r():
+    """Flash-dLLM, paragraph 3: a DRAFT row keeps its absolute position for the rotary
+    embedding but goes to the tail; the r-th DRAFT row of a sequence (row order) fills
+    tail slot max_pos + r, which then holds that row's own K and V."""
+    wl = _verify_case()
+    _, cache = _run(wl, view=wl.view)
+    s = wl.shape
+    for b in range(s.batch):
+        drafts = [t for t in range(wl.x.shape[1]) if wl.view[b, t] == O.VIEW_DRAFT]
+        assert len(drafts) >= 2
+        for r_, t in enumerate(drafts):
+            _, k, v = O.project_qkv(wl.x[b, t:t + 1], wl.w, s.n_heads)
+            k = O.rope(k, wl.positions[b, t:t + 1], s.rope_theta)
+            np.testing.assert_allclose(cache.K[b, s.max_pos + r_], k[0], rtol=1e-12, atol=1e-12)
+            np.testing.assert_allclose(cache.V[b, s.max_pos + r_], v[0], rtol=1e-12, atol=1e-12)
+
+
 # ---------------------------------------------------------------------------- drift
 def test_cosine_special_cases():
     v = _rng(10).standard_normal(300)
@@ -311,6 +328,32 @@ def test_drift_is_one_when_probe_equals_cached_token():
                        kv_x=wl.probe_rows(idx), kv_pos=idx, probe=True)
     c2 = O.kv_drift(cache, idx, probe2)
     assert np.all(c2 < 1.0) and np.all(c2 > 0.9)
+
+
+def test_drift_closed_form_over_the_whole_token_vector():
+    """Flash-dLLM, paragraph 4: the drift of a tracked token is the cosine between its
+    cached and recomputed K (and, apart, V) over the token's whole D-vector.  Negating
+    head h of the probe K gives 1 - 2|K_h|^2 / |K|^2; a probe V of -V gives -1."""
+    r = _rng(13)
+    B, S, H, hd = 2, 16, 4, 8
+    cache = O.OracleCache(B, S, 0, H, hd)
+    cache.K[:] = r.standard_normal(cache.K.shape) * r.uniform(0.5, 2.0, size=(B, S, H, 1))
+    cache.V[:] = r.standard_normal(cache.V.shape)
+    idx = np.array([[3, 0, 9], [15, 7, 2]])
+    k, D = idx.shape[1], H * hd
+    probe = np.empty((B, k, 2, D))
+    expect = np.empty((B, k, 2))
+    for b in range(B):
+        for j in range(k):
+            Kt = cache.K[b, idx[b, j]]
+            h = (b + j) % H
+            Kp = Kt.copy()
+            Kp[h] *= -1.0
+            probe[b, j, 0] = Kp.reshape(D)
+            probe[b, j, 1] = -cache.V[b, idx[b, j]].reshape(D)
+            expect[b, j, 0] = 1.0 - 2.0 * np.sum(Kt[h] ** 2) / np.sum(Kt ** 2)
+            expect[b, j, 1] = -1.0
+    np.testing.assert_allclose(O.kv_drift(cache, idx, probe), expect, rtol=0, atol=1e-12)
 
 
 # ------------------------------------------------------------------------------ FP8
