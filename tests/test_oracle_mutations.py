@@ -244,3 +244,42 @@ def test_reversed_draft_slots_pass_the_written_set_pin(monkeypatch):
     monkeypatch.setattr(OD, "row_slots", _row_slots_drafts_reversed)
     monkeypatch.setattr(O, "row_slots", _row_slots_drafts_reversed)
     P.test_verify_draft_rows_use_tail_slots()
+
+
+def _mass_mean_over_heads(cache, q, positions, view=None):
+    return _orig_mass(cache, q, positions, view) / cache.H
+
+
+def _group_scale_fnuz_max(v):
+    v = np.asarray(v, np.float64)
+    amax = float(np.max(np.abs(v)))
+    scale = amax / 240.0 if amax > 0 else 1.0
+    return O.e4m3_quantize(v / scale) * scale, scale
+
+
+def _e4m3_decode_bias_8(code):
+    code = int(code) & 0xFF
+    sgn = -1.0 if code & 0x80 else 1.0
+    e, m = (code >> 3) & 0xF, code & 0x7
+    if e == 0xF and m == 0x7:
+        return math.nan
+    if e == 0:
+        return sgn * m * 2.0 ** -10
+    return sgn * (1.0 + m / 8.0) * 2.0 ** (e - 8)
+
+
+_orig_mass = OD.attention_mass
+
+MASS_FP8_CASES = [
+    ("attention_mass", _mass_mean_over_heads, P.test_attention_mass_totals_uniform_keys_and_views),
+    ("fp8_group_quantize", _group_scale_fnuz_max, P.test_fp8_group_quantize_scale_and_zero_group),
+    ("e4m3_decode", _e4m3_decode_bias_8, P.test_e4m3_named_values),
+]
+
+
+@pytest.mark.parametrize("name,bad,pin", MASS_FP8_CASES, ids=[f"{c[0]}-{c[1].__name__}" for c in MASS_FP8_CASES])
+def test_planted_mass_or_fp8_mistake_is_caught(monkeypatch, name, bad, pin):
+    monkeypatch.setattr(OD, name, bad)
+    monkeypatch.setattr(O, name, bad)
+    with pytest.raises(AssertionError):
+        pin()
