@@ -42,7 +42,7 @@ def parse():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--config", type=int, default=3, choices=[2, 3])
+    ap.add_argument("--workload", default="llada8b-b32-drift", choices=["llada8b-b1", "llada8b-b32-drift"])
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused", action="store_true", help="skip the fused-vs-unfused comparison")
@@ -323,8 +323,8 @@ def other_configs(dev, flush, n_iter=30):
         return statistics.median(a_.elapsed_time(b_) for a_, b_ in evs) * 1e3
 
     res = {}
-    for cfg in (2, 4, 5):
-        wl = W.make(cfg)
+    for wl_name in ("llada8b-b1", "llada8b-b16-verify", "llada8b-b8-refresh-fp8"):
+        wl = W.make(wl_name)
         s = wl.shape
         B, D, H, hd, S, T = s.batch, s.D, s.n_heads, s.head_dim, s.max_pos, s.tail_slots
         cache = capi.Cache(1, B, S, H, hd, kvt[s.kv], s.rope_theta, T, device=dev)
@@ -364,7 +364,7 @@ def other_configs(dev, flush, n_iter=30):
              "attend_us": t_a, "attend_gbs": a_bytes / (t_a * 1e-6) / 1e9,
              "attend_frac": a_bytes / (t_a * 1e-6) / 1e9 / pk["hbm_gbs"],
              "algorithmic_flops": flops, "attend_bytes": a_bytes}
-        if cfg == 2:  # the same two calls replayed from one CUDA graph: no launch cost
+        if wl_name == "llada8b-b1":  # the same two calls replayed from one CUDA graph: no launch cost
             g = torch.cuda.CUDAGraph()
             s_cap = torch.cuda.Stream(dev)
             s_cap.wait_stream(stream)
@@ -396,7 +396,7 @@ def run_ours(args, rank, world, local):
     if world > 1:
         import torch.distributed as dist
         dist.init_process_group("nccl", device_id=dev)
-    wl = _with_drift_inputs(W.make(args.config))
+    wl = _with_drift_inputs(W.make(args.workload))
     s = wl.shape
     B, D, S = s.batch, s.D, s.max_pos
     k = wl.drift_k
@@ -804,7 +804,7 @@ def main():
         if rank != 0:
             return
         import workloads as W
-        wl = _with_drift_inputs(W.make(args.config))
+        wl = _with_drift_inputs(W.make(args.workload))
         sample = OracleSample(wl)
         for _ in range(args.warmup):
             sample.rep()

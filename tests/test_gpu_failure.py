@@ -14,7 +14,7 @@ pytestmark = pytest.mark.gpu
 
 
 def test_bounded_wait_reports_timeout_and_context_survives():
-    wl = W.make(2, batch=2, d_model=256, head_dim=128, max_pos=256, block=32, gen_lo=128, fixed_lo=None)
+    wl = W.make("llada8b-b1", batch=2, d_model=256, head_dim=128, max_pos=256, block=32, gen_lo=128, fixed_lo=None)
     cache = G.make_cache(wl)
     t0 = time.perf_counter()
     capi.dllm_selftest_wait_timeout(cache.handle)
@@ -31,7 +31,7 @@ def test_bounded_wait_reports_timeout_and_context_survives():
 
 def test_device_range_errors_are_reported_not_faulted():
     # a position outside [0, max_pos) is skipped by the kernels and reported
-    wl = W.make(2, batch=2, d_model=256, head_dim=128, max_pos=256, block=32, gen_lo=128, fixed_lo=None)
+    wl = W.make("llada8b-b1", batch=2, d_model=256, head_dim=128, max_pos=256, block=32, gen_lo=128, fixed_lo=None)
     cache = G.make_cache(wl)
     w = G.tdev(wl.w, "bf16")
     x = G.tdev(wl.x, "bf16")

@@ -20,7 +20,7 @@ def _topk(wl):
 
 
 def test_config3_batch32_drift_fullsize():
-    wl = W.make(3)
+    wl = W.make("llada8b-b32-drift")
     idx = _topk(wl)
     idx_np = idx.cpu().numpy()
     np.testing.assert_array_equal(idx_np, O.kv_topk(wl.mass, wl.block_lo, wl.block_len, wl.drift_k))
@@ -50,14 +50,14 @@ def test_config3_batch32_drift_fullsize():
 
 
 def test_config4_verify_fullsize():
-    wl = W.make(4)
+    wl = W.make("llada8b-b16-verify")
     cache = G.make_cache(wl)
     out, _ = G.run_gpu(wl, cache)
     G.check_sampled(wl, cache, out, [(0, 3), (9, 20), (15, 31)])
 
 
 def test_config5_refresh_fp8_fullsize():
-    wl = W.make(5)
+    wl = W.make("llada8b-b8-refresh-fp8")
     cache = G.make_cache(wl)
     out, _ = G.run_gpu(wl, cache)
     G.check_sampled(wl, cache, out, [(0, 0), (4, 11), (7, 31)], exact_diag_tol=0.15)

@@ -39,7 +39,7 @@ def _run_step(wl, t, stream):
 
 @pytest.mark.parametrize("batch,max_pos", [(4, 300), (40, 256)])
 def test_step_graph_replay_matches_eager(batch, max_pos):
-    wl = W.make(3, batch=batch, d_model=512, head_dim=128, max_pos=max_pos, gen_lo=128, drift_k=8)
+    wl = W.make("llada8b-b32-drift", batch=batch, d_model=512, head_dim=128, max_pos=max_pos, gen_lo=128, drift_k=8)
     eager, graphed = _step_state(wl), _step_state(wl)
     st = torch.cuda.current_stream()
     _run_step(wl, eager, st)
@@ -110,7 +110,7 @@ def test_host_staged_step_matches_device_inputs():
     """The end-to-end form of a step: inputs staged in dllm_host_alloc blocks, copied
     in on a side stream, results copied back into host blocks; the same bits as the
     step on device-resident inputs."""
-    wl = W.make(3, batch=6, d_model=512, head_dim=128, max_pos=300, gen_lo=128, drift_k=8)
+    wl = W.make("llada8b-b32-drift", batch=6, d_model=512, head_dim=128, max_pos=300, gen_lo=128, drift_k=8)
     ref, staged = _step_state(wl), _step_state(wl)
     st = torch.cuda.current_stream()
     _run_step(wl, ref, st)

@@ -46,23 +46,23 @@ def _oracle_mass(wl):
 
 
 CASES = [
-    ("plain", 2, dict(batch=3, d_model=512, head_dim=128, max_pos=300, block=40, gen_lo=200, fixed_lo=None)),
-    ("two-chunks", 2, dict(batch=2, d_model=256, head_dim=128, max_pos=400, block=100, gen_lo=200, fixed_lo=None)),
-    ("verify", 4, dict(batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200, search=6,
+    ("plain", "llada8b-b1", dict(batch=3, d_model=512, head_dim=128, max_pos=300, block=40, gen_lo=200, fixed_lo=None)),
+    ("two-chunks", "llada8b-b1", dict(batch=2, d_model=256, head_dim=128, max_pos=400, block=100, gen_lo=200, fixed_lo=None)),
+    ("verify", "llada8b-b16-verify", dict(batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200, search=6,
                        tail_slots=8)),
 ]
 
 
-@pytest.mark.parametrize("name,cfg,kw", CASES, ids=[c[0] for c in CASES])
-def test_mass_matches_oracle(name, cfg, kw):
-    wl = W.make(cfg, **kw)
+@pytest.mark.parametrize("name,workload,kw", CASES, ids=[c[0] for c in CASES])
+def test_mass_matches_oracle(name, workload, kw):
+    wl = W.make(workload, **kw)
     cache = G.make_cache(wl)
     mass, _ = _gpu_mass(wl, cache)
     G.assert_close(mass, _oracle_mass(wl), G.TOL["bf16"], f"attention mass ({name})")
 
 
 def test_mass_fullsize_sampled_sequences():
-    wl = W.make(3)
+    wl = W.make("llada8b-b32-drift")
     s = wl.shape
     cache = G.make_cache(wl)
     mass, _ = _gpu_mass(wl, cache)

@@ -31,11 +31,11 @@ def _check_step(wl, probe_idx=None):
 
 # ------------------------------------------------------------------------------ fp32
 def test_config1_tiny_f32_full():
-    _check_step(W.make(1))
+    _check_step(W.make("tiny-f32"))
 
 
 def test_f32_ragged_small():
-    wl = W.make(1, batch=3, d_model=192, head_dim=64, max_pos=77, block=5, gen_lo=30, fixed_lo=None)
+    wl = W.make("tiny-f32", batch=3, d_model=192, head_dim=64, max_pos=77, block=5, gen_lo=30, fixed_lo=None)
     _check_step(wl)
 
 
@@ -58,40 +58,40 @@ SMALL_BF16 = [
 
 @pytest.mark.parametrize("kw", SMALL_BF16, ids=[f"B{k['batch']}-D{k['d_model']}-S{k['max_pos']}-n{k['block']}" for k in SMALL_BF16])
 def test_bf16_step_small(kw):
-    wl = W.make(2, head_dim=128, fixed_lo=None, **kw)
+    wl = W.make("llada8b-b1", head_dim=128, fixed_lo=None, **kw)
     _check_step(wl)
 
 
 def test_bf16_config2_full():
-    _check_step(W.make(2))
+    _check_step(W.make("llada8b-b1"))
 
 
 # ------------------------------------------------------------------------------ FP8
 def test_fp8_refresh_small():
     # full-sequence K/V refresh into an e4m3 cache, then the block attends over it
-    wl = W.make(5, batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200)
+    wl = W.make("llada8b-b8-refresh-fp8", batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200)
     _check_step(wl)
 
 
 def test_fp8_prefill_then_step_small():
-    wl = W.make(2, kv="e4m3", batch=2, d_model=256, head_dim=128, max_pos=400, block=40, gen_lo=300, fixed_lo=None)
+    wl = W.make("llada8b-b1", kv="e4m3", batch=2, d_model=256, head_dim=128, max_pos=400, block=40, gen_lo=300, fixed_lo=None)
     _check_step(wl)
 
 
 def test_fp8_verify_small():
-    wl = W.make(4, kv="e4m3", batch=3, d_model=256, head_dim=128, max_pos=300, block=16, gen_lo=200, search=6,
+    wl = W.make("llada8b-b16-verify", kv="e4m3", batch=3, d_model=256, head_dim=128, max_pos=300, block=16, gen_lo=200, search=6,
                 tail_slots=8)
     _check_step(wl)
 
 
 # ---------------------------------------------------------------------- Flash-Verify
 def test_verify_small():
-    wl = W.make(4, batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200, search=6, tail_slots=8)
+    wl = W.make("llada8b-b16-verify", batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200, search=6, tail_slots=8)
     _check_step(wl)
 
 
 def test_verify_draft_equals_mask_views_identical():
-    wl = W.make(4, batch=2, d_model=256, head_dim=128, max_pos=200, block=16, gen_lo=128, search=5, tail_slots=8)
+    wl = W.make("llada8b-b16-verify", batch=2, d_model=256, head_dim=128, max_pos=200, block=16, gen_lo=128, search=5, tail_slots=8)
     nb = wl.block_len
     for b in range(wl.shape.batch):
         for t in range(nb, wl.x.shape[1]):
@@ -115,7 +115,7 @@ def _topk_gpu(wl):
 
 
 def test_topk_bit_exact_with_ties():
-    wl = W.make(3, batch=5, d_model=256, head_dim=128, max_pos=1000, block=32, gen_lo=512, drift_k=32)
+    wl = W.make("llada8b-b32-drift", batch=5, d_model=256, head_dim=128, max_pos=1000, block=32, gen_lo=512, drift_k=32)
     wl.mass[1, 100:140] = 0.25  # ties across the cut
     wl.mass[2, :] = 0.0         # all equal
     wl.mass[3, wl.block_lo[3]:wl.block_lo[3] + 32] = 10.0  # block dominates but is excluded
@@ -126,7 +126,7 @@ def test_topk_bit_exact_with_ties():
 def test_topk_sizes_bit_exact(k, n_pos):
     # k <= 32 merges per-warp top-32 lists (several rounds per warp above 1024
     # positions); larger k sorts every candidate
-    wl = W.make(3, batch=4, d_model=256, head_dim=128, max_pos=n_pos, block=min(32, n_pos - k - 1),
+    wl = W.make("llada8b-b32-drift", batch=4, d_model=256, head_dim=128, max_pos=n_pos, block=min(32, n_pos - k - 1),
                 gen_lo=0, drift_k=k)
     wl.mass[0, ::3] = wl.mass[0, 1]  # many ties
     np.testing.assert_array_equal(_topk_gpu(wl), O.kv_topk(wl.mass, wl.block_lo, wl.block_len, wl.drift_k))
@@ -141,7 +141,7 @@ DRIFT_CASES = [
 
 @pytest.mark.parametrize("name,kw", DRIFT_CASES, ids=[c[0] for c in DRIFT_CASES])
 def test_drift_cache_types(name, kw):
-    wl = W.make(3, batch=5, max_pos=300, block=16, gen_lo=200, drift_k=24, **kw)
+    wl = W.make("llada8b-b32-drift", batch=5, max_pos=300, block=16, gen_lo=200, drift_k=24, **kw)
     idx = _topk_gpu(wl)
     cache, out, probe, ocache, o_probe = _check_step(wl, probe_idx=idx)
     ptype = torch.float32 if kw["act"] == "f32" else torch.bfloat16
@@ -159,7 +159,7 @@ def test_drift_cache_types(name, kw):
 def test_drift_refresh_flags_both_ways():
     # sequence 0 probes equal their cached tokens (cos = 1, no refresh); sequence 1 gets
     # unrelated probes (cos near 0, refresh)
-    wl = W.make(3, batch=2, d_model=256, head_dim=128, max_pos=200, block=16, gen_lo=128, drift_k=8)
+    wl = W.make("llada8b-b32-drift", batch=2, d_model=256, head_dim=128, max_pos=200, block=16, gen_lo=128, drift_k=8)
     idx = _topk_gpu(wl)
     cache, out, probe, ocache, o_probe = _check_step(wl, probe_idx=idx)
     kv = G.gpu_kv(cache)  # [B][slots][2][H][hd]
@@ -177,7 +177,7 @@ def test_drift_refresh_flags_both_ways():
 
 
 def test_drift_small():
-    wl = W.make(3, batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200, drift_k=8)
+    wl = W.make("llada8b-b32-drift", batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200, drift_k=8)
     idx = _topk_gpu(wl)
     np.testing.assert_array_equal(idx, O.kv_topk(wl.mass, wl.block_lo, wl.block_len, wl.drift_k))
     cache, out, probe, ocache, o_probe = _check_step(wl, probe_idx=idx)

@@ -66,7 +66,7 @@ RAGGED = [
 
 @pytest.mark.parametrize("name,kw,lens", RAGGED, ids=[r[0] for r in RAGGED])
 def test_ragged_matches_oracle(name, kw, lens):
-    wl = W.make(2, fixed_lo=None, **kw)
+    wl = W.make("llada8b-b1", fixed_lo=None, **kw)
     cache, pos, q = _staged(wl)
     key_len = torch.tensor(lens, dtype=torch.int32, device="cuda")
     out = q.clone()
@@ -83,7 +83,7 @@ def test_ragged_matches_oracle(name, kw, lens):
 
 @pytest.mark.parametrize("kv", ["bf16", "e4m3"])
 def test_partial_states_and_merge(kv):
-    wl = W.make(2, batch=3, d_model=512, head_dim=128, max_pos=600, block=40, gen_lo=300, fixed_lo=None, kv=kv)
+    wl = W.make("llada8b-b1", batch=3, d_model=512, head_dim=128, max_pos=600, block=40, gen_lo=300, fixed_lo=None, kv=kv)
     s = wl.shape
     cache, pos, q = _staged(wl)
     q_before = q.clone()

@@ -44,16 +44,16 @@ def _run_unfused(wl, cache, probe_idx=None):
 
 
 CASES = [
-    ("bf16", 2, dict(batch=3, d_model=512, head_dim=128, max_pos=300, block=40, gen_lo=200, fixed_lo=None)),
-    ("fp8-refresh", 5, dict(batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200)),
-    ("verify", 4, dict(batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200, search=6,
+    ("bf16", "llada8b-b1", dict(batch=3, d_model=512, head_dim=128, max_pos=300, block=40, gen_lo=200, fixed_lo=None)),
+    ("fp8-refresh", "llada8b-b8-refresh-fp8", dict(batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200)),
+    ("verify", "llada8b-b16-verify", dict(batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200, search=6,
                        tail_slots=8)),
 ]
 
 
-@pytest.mark.parametrize("name,cfg,kw", CASES, ids=[c[0] for c in CASES])
-def test_unfused_matches_oracle(name, cfg, kw):
-    wl = W.make(cfg, **kw)
+@pytest.mark.parametrize("name,workload,kw", CASES, ids=[c[0] for c in CASES])
+def test_unfused_matches_oracle(name, workload, kw):
+    wl = W.make(workload, **kw)
     cache = G.make_cache(wl)
     out, _ = _run_unfused(wl, cache)
     o_out, ocache, _ = G.run_oracle(wl)
@@ -67,7 +67,7 @@ def test_unfused_matches_oracle(name, cfg, kw):
 
 
 def test_unfused_probes_match_oracle():
-    wl = W.make(3, batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200, drift_k=8)
+    wl = W.make("llada8b-b32-drift", batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200, drift_k=8)
     idx = np.stack([np.arange(8, dtype=np.int32) * 3 for _ in range(3)])
     cache = G.make_cache(wl)
     out, probe = _run_unfused(wl, cache, probe_idx=idx)
@@ -77,7 +77,7 @@ def test_unfused_probes_match_oracle():
 
 
 def test_unfused_agrees_with_fused_at_full_size():
-    wl = W.make(3)
+    wl = W.make("llada8b-b32-drift")
     idx = np.stack([np.arange(32, dtype=np.int32) * 7 % 512 for _ in range(wl.shape.batch)])
     c1, c2 = G.make_cache(wl), G.make_cache(wl)
     out_f, probe_f = G.run_gpu(wl, c1, probe_idx=idx)

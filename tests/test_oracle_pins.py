@@ -202,7 +202,7 @@ def test_visibility_truth_table():
 def _verify_case(seed=0, **kw):
     args = dict(batch=2, d_model=256, head_dim=128, max_pos=96, block=16, gen_lo=48, search=6, tail_slots=8)
     args.update(kw)
-    return W.make(4, seed=seed, **args)
+    return W.make("llada8b-b16-verify", seed=seed, **args)
 
 
 def _run(wl, x=None, positions=None, view=None):
@@ -314,7 +314,7 @@ def test_topk_ties_take_lower_position_and_permutation_equivariance():
 
 
 def test_drift_is_one_when_probe_equals_cached_token():
-    wl = W.make(3, batch=2, d_model=256, head_dim=128, max_pos=96, gen_lo=48, block=16, drift_k=5)
+    wl = W.make("llada8b-b32-drift", batch=2, d_model=256, head_dim=128, max_pos=96, gen_lo=48, block=16, drift_k=5)
     s = wl.shape
     cache = O.OracleCache(s.batch, s.max_pos, 0, s.n_heads, s.head_dim)
     O.write_rows(cache, wl.w, wl.pre_x, wl.pre_pos, s.rope_theta)

@@ -55,24 +55,24 @@ def _noalloc(cache, pos, view, q):
 
 SPLIT_CASES = [
     # LLaDA-8B layer at batch 1: 32 (sequence, head) units, keys split three ways
-    dict(cfg=2, kw={}),
+    dict(workload="llada8b-b1", kw={}),
     # small batch, 5 key tiles, more than one query chunk, Flash-Verify tail
-    dict(cfg=4, kw=dict(batch=2, d_model=256, head_dim=128, max_pos=600, block=48, gen_lo=400, search=20,
+    dict(workload="llada8b-b16-verify", kw=dict(batch=2, d_model=256, head_dim=128, max_pos=600, block=48, gen_lo=400, search=20,
                         tail_slots=24)),
 ]
 
 
 @pytest.mark.parametrize("case", SPLIT_CASES, ids=["llada8b-b1", "verify-small"])
 def test_noalloc_matches_attend_two_calls_in_a_row(case):
-    wl = W.make(case["cfg"], **case["kw"])
+    wl = W.make(case["workload"], **case["kw"])
     cache, pos, view, q, ref = _pair(wl)
     for call in range(2):
         G.assert_close(_noalloc(cache, pos, view, q), ref, G.TOL["bf16"], f"no-alloc call {call}")
 
 
 def test_noalloc_interleaved_workloads_reuse_the_scratch():
-    a = _pair(W.make(2, batch=1, d_model=512, head_dim=128, max_pos=900, block=32, gen_lo=512, fixed_lo=None))
-    b = _pair(W.make(2, batch=3, d_model=256, head_dim=128, max_pos=333, block=20, gen_lo=200, fixed_lo=None))
+    a = _pair(W.make("llada8b-b1", batch=1, d_model=512, head_dim=128, max_pos=900, block=32, gen_lo=512, fixed_lo=None))
+    b = _pair(W.make("llada8b-b1", batch=3, d_model=256, head_dim=128, max_pos=333, block=20, gen_lo=200, fixed_lo=None))
     for first, second in ((a, b), (b, a)):
         for case in (first, second):
             cache, pos, view, q, ref = case
@@ -82,7 +82,7 @@ def test_noalloc_interleaved_workloads_reuse_the_scratch():
 def test_noalloc_rejects_requests_beyond_the_scratch():
     sm = torch.cuda.get_device_properties(0).multi_processor_count
     B = sm - 1  # one head each: just below the SM count, so the keys are split in two
-    wl = W.make(2, batch=B, d_model=128, head_dim=128, max_pos=384, block=16, gen_lo=256, fixed_lo=None)
+    wl = W.make("llada8b-b1", batch=B, d_model=128, head_dim=128, max_pos=384, block=16, gen_lo=256, fixed_lo=None)
     need = 2 * B * 64 * 130 * 4
     cache, pos, view, q = _staged(wl)
     out = q.clone()

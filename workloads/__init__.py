@@ -204,30 +204,31 @@ def _shape(d: dict) -> Shape:
     )
 
 
-CONFIGS = {
+WORKLOADS = {
     # tiny single layer-step, fp32
-    1: dict(name="tiny-f32", batch=1, d_model=256, n_heads=4, head_dim=64, max_pos=128,
+    "tiny-f32": dict(name="tiny-f32", batch=1, d_model=256, n_heads=4, head_dim=64, max_pos=128,
             rope_theta=1e4, act="f32", kv="f32", block=16, gen_lo=64, fixed_lo=64, kind="plain"),
     # LLaDA-8B layer, batch 1
-    2: dict(name="llada8b-b1", batch=1, d_model=4096, n_heads=32, head_dim=128, max_pos=768,
+    "llada8b-b1": dict(name="llada8b-b1", batch=1, d_model=4096, n_heads=32, head_dim=128, max_pos=768,
             rope_theta=5e5, act="bf16", kv="bf16", block=32, gen_lo=512, fixed_lo=512, kind="plain"),
     # LLaDA-8B layer, batch 32, random block offsets, top-32 drift
-    3: dict(name="llada8b-b32-drift", batch=32, d_model=4096, n_heads=32, head_dim=128, max_pos=1024,
+    "llada8b-b32-drift": dict(name="llada8b-b32-drift", batch=32, d_model=4096, n_heads=32, head_dim=128, max_pos=1024,
             rope_theta=5e5, act="bf16", kv="bf16", block=32, gen_lo=512, fixed_lo=None, kind="drift",
             drift_k=32),
     # Flash-Verify layout, batch 16: 16 search tokens duplicated as draft + mask views
-    4: dict(name="llada8b-b16-verify", batch=16, d_model=4096, n_heads=32, head_dim=128, max_pos=1024,
+    "llada8b-b16-verify": dict(name="llada8b-b16-verify", batch=16, d_model=4096, n_heads=32, head_dim=128, max_pos=1024,
             tail_slots=16, rope_theta=5e5, act="bf16", kv="bf16", block=32, gen_lo=512, fixed_lo=None,
             kind="verify", search=16),
     # long-context full refresh into an FP8-e4m3 cache, batch 8
-    5: dict(name="llada8b-b8-refresh-fp8", batch=8, d_model=4096, n_heads=32, head_dim=128, max_pos=3072,
+    "llada8b-b8-refresh-fp8": dict(name="llada8b-b8-refresh-fp8", batch=8, d_model=4096, n_heads=32, head_dim=128, max_pos=3072,
             rope_theta=5e5, act="bf16", kv="e4m3", block=32, gen_lo=2048, fixed_lo=None, kind="refresh"),
 }
 
 
-def make(config: int, seed: int = 0, **overrides) -> Workload:
-    """Build workload ``config`` (1..5), optionally shrunk by ``overrides``."""
-    d = dict(CONFIGS[config])
+def make(name: str, seed: int = 0, **overrides) -> Workload:
+    """Build the workload called ``name`` (a key of WORKLOADS), optionally shrunk by
+    ``overrides``."""
+    d = dict(WORKLOADS[name])
     d.update(overrides)
     if "d_model" in overrides and "n_heads" not in overrides:
         d["n_heads"] = d["d_model"] // d["head_dim"]
