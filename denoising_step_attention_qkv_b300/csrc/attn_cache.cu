@@ -405,7 +405,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     // ------------------------------------------------------------------ MMA issuer
     // Per tile: S(t) = K(t) Q^T into S[t & 1], then P V of the previous tile into
     // O[(t - 1) & 1], so the softmax of tile t - 1 overlaps the S MMA of tile t.
-    // e4m3 caches: every operand (dequantised K and V, Q, P) is f16
+    // e4m3 caches: every operand (K codes, dequantised V, Q, P) is f16
     constexpr uint32_t idesc_s = FP8 ? idesc_f16(128, NQ, false, false) : idesc_bf16(128, NQ, false, false);
     constexpr uint32_t idesc_o = FP8 ? idesc_f16(128, NQ, true, false) : idesc_bf16(128, NQ, true, false);
     int ks = 0, vs = 0, uu = 0;
