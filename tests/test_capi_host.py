@@ -127,3 +127,14 @@ def test_host_stage_arguments():
     assert torch.equal(capi.dllm_host_stage(b, a), a)
     with pytest.raises(ValueError):
         capi.dllm_host_stage(b[:50], a)
+
+
+def test_host_empty_fails_loudly_without_a_device():
+    """No silent fallback to ordinary host memory: without a usable device the binding
+    raises with the library's status."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a device is present")
+    with pytest.raises(capi.DllmError) as e:
+        capi.host_empty((4, 8), torch.bfloat16)
+    assert e.value.code == capi.DLLM_ECUDA
