@@ -67,10 +67,12 @@ def measured_traffic(kernel_key: str):
     files = {"project": ["proj_rope_store.cu", "ptx.cuh", "internal.h"],
              "attend": ["attn_cache.cu", "ptx.cuh", "internal.h"]}[kernel_key]
     try:
-        rec = json.load(open(path))["kernels"][kernel_key]
+        with open(path) as f:
+            rec = json.load(f)["kernels"][kernel_key]
         h = hashlib.sha256()
         for fn in files:
-            h.update(open(os.path.join(ROOT, "denoising_step_attention_qkv_b300", "csrc", fn), "rb").read())
+            with open(os.path.join(ROOT, "denoising_step_attention_qkv_b300", "csrc", fn), "rb") as f:
+                h.update(f.read())
         if h.hexdigest()[:16] != rec["sources_sha256_16"]:
             return None
         return rec["traffic_bytes"]
@@ -81,7 +83,8 @@ def measured_traffic(kernel_key: str):
 def peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     if os.path.exists(path):
-        d = json.load(open(path))
+        with open(path) as f:
+            d = json.load(f)
         return {"hbm_gbs": d["hbm_gbs"], "bf16_tflops": d["bf16_tflops"],
                 "bf16_tflops_sustained": d.get("bf16_tflops_sustained"), "source": "measured"}
     return {"hbm_gbs": 6400.0, "bf16_tflops": 1800.0, "bf16_tflops_sustained": 1400.0, "source": "fallback"}

@@ -301,10 +301,11 @@ class _HostBlock:
     """Owns one dllm_host_alloc block; freed when the last tensor viewing it is gone."""
 
     def __init__(self, nbytes: int):
+        self.ptr = None
         self.ptr = dllm_host_alloc(nbytes)
 
     def __del__(self):
-        if self.ptr and _lib is not None:
+        if getattr(self, "ptr", None) and _lib is not None:
             _lib.dllm_host_free(self.ptr)
             self.ptr = None
 

@@ -263,8 +263,21 @@ float* layer_scale(dllm_cache* c, int layer) {
   return c->scale ? c->scale + (size_t)layer * c->layer_scales : nullptr;
 }
 
+// The calls launch on the current device; the cache's buffers live on the device that
+// was current when it was created.  A call made with another device current would run
+// kernels against another GPU's memory, so it is rejected.
+bool on_cache_device(const dllm_cache* c) {
+  int d = -1;
+  if (cudaGetDevice(&d) != cudaSuccess) {
+    cudaGetLastError();
+    return false;
+  }
+  return d == c->device;
+}
+
 int check_common(dllm_cache* c, int layer, int n_tok, const int32_t* positions, void* out) {
   if (!c || layer < 0 || layer >= c->desc.n_layers || n_tok < 0) return DLLM_EINVAL;
+  if (!on_cache_device(c)) return DLLM_EINVAL;
   if (n_tok > 0 && (!positions || !out)) return DLLM_EINVAL;
   if (!aligned16(out)) return DLLM_EINVAL;
   if ((long long)c->desc.batch * n_tok > (1ll << 30)) return DLLM_EINVAL;
@@ -633,6 +646,7 @@ int dllm_kv_topk(const float* mass, int batch, int n_pos, const int32_t* block_l
 int dllm_kv_drift(const dllm_cache* c, int layer, const int32_t* idx, int k, const void* probe_kv, float gamma,
                   float* cos, int32_t* refresh, void* stream) {
   if (!c || layer < 0 || layer >= c->desc.n_layers || !idx || k < 1 || !probe_kv || !cos) return DLLM_EINVAL;
+  if (!on_cache_device(c)) return DLLM_EINVAL;
   if (!aligned16(probe_kv)) return DLLM_EINVAL;
   const dllm_cache_desc& d = c->desc;
   const void* kvl = reinterpret_cast<const uint8_t*>(c->kv) + (size_t)layer * c->layer_elems * c->elem_bytes;
@@ -680,6 +694,7 @@ int dllm_elastic_step(dllm_cache* c, int n_layers, const void* const* x_all, con
   if (!c || n_layers < 1 || n_layers > c->desc.n_layers || !x_all || !w_qkv || !win_lo || !mass || !out || !cos ||
       !flags || !workspace)
     return DLLM_EINVAL;
+  if (!on_cache_device(c)) return DLLM_EINVAL;
   const dllm_cache_desc& d = c->desc;
   const int B = d.batch, S = d.max_pos, D = d.n_heads * d.head_dim;
   if (beta < 1 || beta > S || k < 1 || k > S - beta || S > 16384) return DLLM_EINVAL;

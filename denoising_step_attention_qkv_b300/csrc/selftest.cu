@@ -26,6 +26,11 @@ __global__ void wait_timeout_kernel(int* status) {
 
 extern "C" int dllm_selftest_wait_timeout(dllm_cache* c, void* stream) {
   if (!c) return DLLM_EINVAL;
+  int dev = -1;  // the cache's device must be current (its status word lives there)
+  if (cudaGetDevice(&dev) != cudaSuccess || dev != c->device) {
+    cudaGetLastError();
+    return DLLM_EINVAL;
+  }
   dllm::wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(c->status);
   return cudaGetLastError() == cudaSuccess ? DLLM_OK : DLLM_ECUDA;
 }

@@ -23,6 +23,9 @@
  *     stream) and never synchronise, except dllm_cache_alloc/free/status.  A cache
  *     owns small workspaces (split-KV partials, drift arrival counters), so calls on
  *     one cache must be ordered (one stream, or events between streams).
+ *   - A cache lives on the device that was current when dllm_cache_alloc created it;
+ *     every call that launches work on it must be made with that device current,
+ *     else it returns DLLM_EINVAL and launches nothing.
  *   - Every call returns a dllm_status.  Argument errors are detected on the host
  *     before anything is launched and leave all buffers untouched.  Range errors in
  *     device-resident index data (a position outside [0, max_pos), too many draft

@@ -37,7 +37,7 @@ def _fake_root(tmp_path):
     def digest(files):
         h = hashlib.sha256()
         for fn in files:
-            h.update(open(csrc / fn, "rb").read())
+            h.update((csrc / fn).read_bytes())
         return h.hexdigest()[:16]
 
     rec = {"kernels": {
@@ -65,7 +65,8 @@ def test_measured_traffic_is_withdrawn_when_a_kernel_changes(tmp_path, monkeypat
 
 
 def test_committed_traffic_record_is_well_formed():
-    rec = json.load(open(os.path.join(ROOT, "profiles", "traffic_llada8b_b32.json")))
+    with open(os.path.join(ROOT, "profiles", "traffic_llada8b_b32.json")) as f:
+        rec = json.load(f)
     assert rec["capture"].startswith("ncu ") and "--clock-control none" in rec["capture"]
     for key in ("project", "attend"):
         k = rec["kernels"][key]

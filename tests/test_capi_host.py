@@ -12,7 +12,8 @@ HEADER = os.path.join(os.path.dirname(os.path.dirname(__file__)), "include", "dl
 
 
 def _declared():
-    text = open(HEADER).read()
+    with open(HEADER) as f:
+        text = f.read()
     text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
     return sorted(set(re.findall(r"\b(dllm_[a-z_]+)\s*\(", text)))
 

@@ -13,7 +13,8 @@ import pytest
 import oracle as O
 import workloads as W
 
-GOLD = json.load(open(os.path.join(os.path.dirname(__file__), "golden", "closed_forms.json")))
+with open(os.path.join(os.path.dirname(__file__), "golden", "closed_forms.json")) as _f:
+    GOLD = json.load(_f)
 
 
 def _rng(s=0):
