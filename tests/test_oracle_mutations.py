@@ -283,3 +283,32 @@ def test_planted_mass_or_fp8_mistake_is_caught(monkeypatch, name, bad, pin):
     monkeypatch.setattr(O, name, bad)
     with pytest.raises(AssertionError):
         pin()
+
+
+def _elastic_step_window_early(caches, ws, theta, x_all, win_lo, beta, masses, k, gamma, with_mass=False):
+    # the multi-layer step with its window one position early (positions win_lo - 1 ...)
+    L = len(caches)
+    B = x_all[0].shape[0]
+    positions = (np.asarray(win_lo)[:, None] - 1 + np.arange(beta)[None, :]).astype(np.int32)
+    flags = np.zeros((L, B), np.int32)
+    outs, coss = [], []
+    for l in range(L):
+        c = caches[l]
+        for b in np.nonzero(O.refresh_due(flags, l))[0]:
+            O.refresh_sequence(c, ws[l], x_all[l][b], int(b), theta)
+        idx = O.kv_topk(masses[l], win_lo, beta, k)
+        x_win = np.stack([x_all[l][b][positions[b]] for b in range(B)])
+        x_trk = np.stack([x_all[l][b][idx[b]] for b in range(B)])
+        out, probe = O.step(c, ws[l], theta, x_win, positions, kv_x=x_trk, kv_pos=idx, probe=True)
+        cos = O.kv_drift(c, idx, probe)
+        flags[l] = (cos.min(axis=(1, 2)) < gamma).astype(np.int32)
+        outs.append(out)
+        coss.append(cos)
+    return np.stack(outs), np.stack(coss), flags, None
+
+
+def test_planted_early_window_is_caught(monkeypatch):
+    monkeypatch.setattr(OD, "elastic_step", _elastic_step_window_early)
+    monkeypatch.setattr(O, "elastic_step", _elastic_step_window_early)
+    with pytest.raises(AssertionError):
+        P.test_elastic_never_refreshes_when_gamma_below_minus_one()
