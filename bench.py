@@ -42,7 +42,8 @@ def parse():
     ap.add_argument("--steps", type=int, default=1000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="llada8b-b32-drift", choices=["llada8b-b1", "llada8b-b32-drift"])
+    ap.add_argument("--workload", default="llada8b-b32-drift", choices=["llada8b-b1", "llada8b-b32-drift"],
+                    help="the step's workload: the LLaDA-8B layer at batch 32 with drift tracking (default) or batch 1")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-unfused", action="store_true", help="skip the fused-vs-unfused comparison")
