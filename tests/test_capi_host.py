@@ -139,3 +139,19 @@ def test_host_empty_fails_loudly_without_a_device():
     with pytest.raises(capi.DllmError) as e:
         capi.host_empty((4, 8), torch.bfloat16)
     assert e.value.code == capi.DLLM_ECUDA
+
+
+def test_binding_declares_every_signature():
+    """Every exported function has ctypes argument and result types, so no pointer or
+    size is ever passed through ctypes' default int conversion; and the argument count
+    matches the header's declaration."""
+    L = capi.lib()
+    with open(HEADER) as f:
+        text = re.sub(r"/\*.*?\*/", "", f.read(), flags=re.S)
+    for name in capi.EXPORTS:
+        fn = getattr(L, name)
+        assert fn.argtypes is not None and fn.restype is not None, name
+        m = re.search(r"\b" + name + r"\s*\(([^)]*)\)\s*;", text)
+        assert m, f"{name} not declared in the header"
+        params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
+        assert len(fn.argtypes) == len(params), (name, len(fn.argtypes), len(params))
