@@ -155,3 +155,12 @@ def test_binding_declares_every_signature():
         assert m, f"{name} not declared in the header"
         params = [p for p in m.group(1).split(",") if p.strip() and p.strip() != "void"]
         assert len(fn.argtypes) == len(params), (name, len(fn.argtypes), len(params))
+        for decl, ct in zip(params, fn.argtypes):
+            if "*" in decl:  # any pointer: an address-sized ctypes type
+                assert ct is ctypes.c_void_p or ct is ctypes.c_char_p or hasattr(ct, "_type_") and \
+                    issubclass(ct, ctypes._Pointer), (name, decl, ct)
+            else:
+                ctype = decl.split()[-2] if len(decl.split()) > 1 else decl.split()[0]
+                want = {"int": ctypes.c_int, "float": ctypes.c_float, "double": ctypes.c_double,
+                        "size_t": ctypes.c_size_t}[ctype]
+                assert ct is want, (name, decl, ct)
