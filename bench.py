@@ -780,6 +780,8 @@ class OracleSample:
             self.cores = max([i.get("num_threads", 1) for i in threadpool_info()] or [1])
         except Exception:
             self.cores = os.cpu_count()
+        self.threads = (f"up to {self.cores}: numpy's BLAS pool for the matrix products; "
+                        "the oracle's loops and einsum contractions run on one thread")
 
     def rep(self) -> float:
         O, wl, one, s = self.O, self.wl, self.one, self.wl.shape
@@ -819,7 +821,7 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": {"workload": wl.name, "batch": wl.shape.batch},
-                "cpu_baseline": {"value": value, "unit": UNIT, "cores": sample.cores, "kind": "oracle",
+                "cpu_baseline": {"value": value, "unit": UNIT, "cores": sample.cores, "kind": "oracle", "threads": sample.threads,
                                  "sample": "each step: the whole step for sequence 0 of the batch (top-k, probe "
                                            "and block projection, attention, drift); time x batch size"},
                 "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -833,7 +835,7 @@ def main():
         while sum(reps) < args.cpu_seconds or len(reps) < 2:
             reps.append(sample.rep())
         sec = statistics.mean(reps) * wl.shape.batch
-        line["cpu_baseline"] = {"value": 1.0 / sec, "unit": UNIT, "cores": sample.cores, "kind": "oracle",
+        line["cpu_baseline"] = {"value": 1.0 / sec, "unit": UNIT, "cores": sample.cores, "kind": "oracle", "threads": sample.threads,
                                 "sample": f"{len(reps)} repetitions of the whole step for sequence 0 of "
                                           f"{wl.shape.batch} (top-k, probe and block projection, attention, "
                                           f"drift); time x batch size"}
