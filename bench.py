@@ -754,7 +754,8 @@ def run_ours(args, rank, world, local):
                              "min(K, 300) steps with an event between every two kernels",
                    "parallelism": f"replicas x{world}"},
         "tokens_per_s": value * B * wl.block_len,
-        "roofline": roofline, "kernels": kernels, "fused_vs_unfused": fvu, "next_rows": nxt, "other_configs": others, "e2e": e2e, "clocks": clk,
+        "roofline": roofline, "kernels": kernels, "fused_vs_unfused": fvu, "next_rows": nxt, "other_configs": others,
+        "e2e": e2e, "clocks": clk,
         "gpu_launches": n_launch_per_step * args.steps, "wall_s_timed": t_wall,
     }
     if world > 1:
@@ -821,7 +822,8 @@ def main():
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": {"workload": wl.name, "batch": wl.shape.batch},
-                "cpu_baseline": {"value": value, "unit": UNIT, "cores": sample.cores, "kind": "oracle", "threads": sample.threads,
+                "cpu_baseline": {"value": value, "unit": UNIT, "cores": sample.cores, "kind": "oracle",
+                                 "threads": sample.threads,
                                  "sample": "each step: the whole step for sequence 0 of the batch (top-k, probe "
                                            "and block projection, attention, drift); time x batch size"},
                 "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -835,7 +837,8 @@ def main():
         while sum(reps) < args.cpu_seconds or len(reps) < 2:
             reps.append(sample.rep())
         sec = statistics.mean(reps) * wl.shape.batch
-        line["cpu_baseline"] = {"value": 1.0 / sec, "unit": UNIT, "cores": sample.cores, "kind": "oracle", "threads": sample.threads,
+        line["cpu_baseline"] = {"value": 1.0 / sec, "unit": UNIT, "cores": sample.cores, "kind": "oracle",
+                                "threads": sample.threads,
                                 "sample": f"{len(reps)} repetitions of the whole step for sequence 0 of "
                                           f"{wl.shape.batch} (top-k, probe and block projection, attention, "
                                           f"drift); time x batch size"}
