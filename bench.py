@@ -2,11 +2,13 @@
 """Throughput of one cached-attention denoising step of a LLaDA-8B attention layer.
 
 One step (the timed unit) on the batch-32 workload: top-32 selection of the previous
-step's most-attended positions, the fused QKV projection + rotary embedding + cache
-write of the 32-token active block of every sequence plus the K/V of the 32 tracked
-tokens (probes), bidirectional attention of the block over the 1024-slot cache, and
-the K/V cosine-drift reduction with its refresh flag.  Inputs are seeded synthetic
-arrays from ``workloads``; the cache (512 MiB) and the weights are resident in HBM.
+step's most-attended positions, the gather of those tokens' hidden states from this
+step's hidden states of every position, the fused QKV projection + rotary embedding +
+cache write of the 32-token active block of every sequence plus the K/V of the 32
+tracked tokens (probes), bidirectional attention of the block over the 1024-slot cache,
+and the K/V cosine-drift reduction with its refresh flag.  Inputs are seeded synthetic
+arrays from ``workloads``; the cache (512 MiB), the weights and the layer's hidden
+states (256 MiB) are resident in HBM.
 
 Prints one JSON line (rank 0).  ``--impl reference`` times the fp64 oracle instead,
 on the host cores, on a bounded sample of the same workload.
@@ -207,7 +209,7 @@ def job_rate(local_ms: float, steps: int, world: int, device=None):
 
 # --------------------------------------------------------------------------- workload
 def algorithmic(wl):
-    """FLOPs of the projection and bytes of the attention, counting each tensor once."""
+    """FLOPs and bytes of each kernel of the step, counting each tensor once."""
     s = wl.shape
     B, D, H, hd, S = s.batch, s.D, s.n_heads, s.head_dim, s.max_pos
     n_tok = wl.x.shape[1]
@@ -217,8 +219,26 @@ def algorithmic(wl):
     attn_bytes = B * H * S * hd * 2 * 2 + 2 * B * n_tok * D * 2
     attn_flops = 4.0 * B * H * n_tok * S * hd
     drift_bytes = B * k * 2 * D * 2 * 2
+    gather_bytes = 2 * B * k * D * 2
     return dict(proj_flops=proj_flops, proj_bytes=proj_bytes, attn_bytes=attn_bytes, attn_flops=attn_flops,
-                drift_bytes=drift_bytes)
+                drift_bytes=drift_bytes, gather_bytes=gather_bytes)
+
+
+def roofline_entry(name, us, flops, nbytes, pk, tc_peak=None):
+    """One kernel against the slower of its two bounds: the ideal time is the larger of
+    FLOPs at the tensor peak and bytes at the copy peak; frac = ideal / measured.  The
+    achieved figure is reported in the bound's own unit."""
+    tc = pk["bf16_tflops"] if tc_peak is None else tc_peak
+    t_tc = flops / (tc * 1e12) if flops else 0.0
+    t_hbm = nbytes / (pk["hbm_gbs"] * 1e9)
+    tensor = t_tc >= t_hbm
+    sec = us * 1e-6
+    ach = (flops / sec / 1e12) if tensor else (nbytes / sec / 1e9)
+    peak = tc if tensor else pk["hbm_gbs"]
+    return {"kernel": name, "us": us, "bound": "tensor" if tensor else "hbm", "achieved": ach,
+            "unit": "TFLOP/s" if tensor else "GB/s", "peak": peak, "frac": ach / peak,
+            "algorithmic_flops": flops, "algorithmic_bytes": nbytes,
+            "other_bound_frac": (nbytes / sec / 1e9 / pk["hbm_gbs"]) if tensor else (flops / sec / 1e12 / tc)}
 
 
 def elastic_leg(args, dev, B, S, D, H, hd, theta, beta, k, gamma, flush, kv_dtype=None):
@@ -362,12 +382,20 @@ def other_configs(dev, flush, n_iter=30):
         elt = 1 if s.kv == "e4m3" else 2
         slots = S + (T if view is not None else 0)
         a_bytes = B * slots * 2 * D * elt + (B * slots * 2 * H * 4 if s.kv == "e4m3" else 0) + 2 * B * n * D * 2
+        a_flops = 4.0 * B * H * n * slots * hd
+        # projection bytes: W once, the rows in, Q out, K/V (and e4m3 scales) to the cache
+        kv_row = 2 * D * elt + (2 * H * 4 if s.kv == "e4m3" else 0)
+        p_bytes = 3 * D * D * 2 + B * (n + n_kv) * D * 2 + B * n * D * 2 + B * (n + n_kv) * kv_row
+        rp = roofline_entry("project", t_p, flops, p_bytes, pk)
+        ra = roofline_entry("attend", t_a, a_flops, a_bytes, pk)
         r = {"workload": wl.name, "rows_per_seq": n, "refresh_rows_per_seq": n_kv, "kv": s.kv,
-             "project_us": t_p, "project_tflops": flops / (t_p * 1e-6) / 1e12,
-             "project_frac": flops / (t_p * 1e-6) / 1e12 / pk["bf16_tflops"],
-             "attend_us": t_a, "attend_gbs": a_bytes / (t_a * 1e-6) / 1e9,
-             "attend_frac": a_bytes / (t_a * 1e-6) / 1e9 / pk["hbm_gbs"],
-             "algorithmic_flops": flops, "attend_bytes": a_bytes}
+             "project_us": t_p, "project_bound": rp["bound"], "project_achieved": rp["achieved"],
+             "project_unit": rp["unit"], "project_frac": rp["frac"],
+             "attend_us": t_a, "attend_bound": ra["bound"], "attend_achieved": ra["achieved"],
+             "attend_unit": ra["unit"], "attend_frac": ra["frac"],
+             "algorithmic_flops": flops, "project_bytes": p_bytes, "attend_bytes": a_bytes,
+             "frac_note": "each fraction against the slower of its two bounds (FLOPs at the bf16 peak, "
+                          "algorithmic bytes at the copy peak)"}
         if wl_name == "llada8b-b1":  # the same two calls replayed from one CUDA graph: no launch cost
             g = torch.cuda.CUDAGraph()
             s_cap = torch.cuda.Stream(dev)
@@ -421,13 +449,17 @@ def run_ours(args, rank, world, local):
     probe = torch.empty((B, k, 2, D), dtype=torch.bfloat16, device=dev)
     cos = torch.empty((B, k, 2), dtype=torch.float32, device=dev)
     refresh = torch.empty(B, dtype=torch.int32, device=dev)
-    capi.dllm_kv_topk(mass, block_lo, wl.block_len, k, idx)
-    x_probe = bf(wl.probe_rows(idx.cpu().numpy()))  # hidden states of the tracked tokens
+    # this step's hidden states of every position (resident, like the cache): the step
+    # gathers the tracked tokens' rows from it on the device
+    x_all = bf(wl.probe_rows(np.tile(np.arange(S, dtype=np.int32), (B, 1))))
+    x_probe = torch.empty((B, k, D), dtype=torch.bfloat16, device=dev)  # the gathered rows
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
+    KERNELS = ("topk", "gather", "project", "attend", "drift")
 
     def step_plain():
         capi.dllm_kv_topk(mass, block_lo, wl.block_len, k, idx, stream)
+        capi.dllm_gather_rows(cache.handle, x_all, idx, x_probe, stream=stream)
         capi.dllm_cache_project(cache.handle, 0, x, w, pos, None, out, kv_x=x_probe, kv_positions=idx,
                                 probe_kv=probe, stream=stream)
         capi.dllm_cache_attend(cache.handle, 0, pos, None, out, stream=stream)
@@ -436,18 +468,20 @@ def run_ours(args, rank, world, local):
     def step():
         capi.dllm_kv_topk(mass, block_lo, wl.block_len, k, idx, stream)
         ev[1].record(stream)
+        capi.dllm_gather_rows(cache.handle, x_all, idx, x_probe, stream=stream)
+        ev[2].record(stream)
         capi.dllm_cache_project(cache.handle, 0, x, w, pos, None, out, kv_x=x_probe, kv_positions=idx,
                                 probe_kv=probe, stream=stream)
-        ev[2].record(stream)
-        capi.dllm_cache_attend(cache.handle, 0, pos, None, out, stream=stream)
         ev[3].record(stream)
+        capi.dllm_cache_attend(cache.handle, 0, pos, None, out, stream=stream)
+        ev[4].record(stream)
         capi.dllm_kv_drift(cache.handle, 0, idx, probe, wl.gamma, cos, refresh, stream=stream)
 
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS) + 1)]
     for _ in range(max(args.warmup, 3)):
         ev[0].record(stream)
         step()
-        ev[4].record(stream)
+        ev[-1].record(stream)
     torch.cuda.synchronize(dev)
     rc, bits = cache.status()
     if rc != capi.DLLM_OK:
@@ -456,7 +490,7 @@ def run_ours(args, rank, world, local):
     # ---- timed region: K steps, L2 flushed between steps (outside the events).  Events
     # only at step boundaries, so that each kernel's prologue overlaps the end of the one
     # before it (programmatic dependent launch), as in a real step.
-    per = {"step": [], "topk": [], "project": [], "attend": [], "drift": []}
+    per = {"step": [], **{kname: [] for kname in KERNELS}}
     clocks = Clocks(dev) if rank == 0 else None
     if world > 1:
         torch.distributed.barrier()
@@ -487,17 +521,15 @@ def run_ours(args, rank, world, local):
     evs = []
     for _ in range(n_bd):
         flush.zero_()
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(5)]
+        ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS) + 1)]
         ev[0].record(stream)
         step()
-        ev[4].record(stream)
+        ev[-1].record(stream)
         evs.append(ev)
     torch.cuda.synchronize(dev)
     for ev in evs:
-        per["topk"].append(ev[0].elapsed_time(ev[1]))
-        per["project"].append(ev[1].elapsed_time(ev[2]))
-        per["attend"].append(ev[2].elapsed_time(ev[3]))
-        per["drift"].append(ev[3].elapsed_time(ev[4]))
+        for i, kname in enumerate(KERNELS):
+            per[kname].append(ev[i].elapsed_time(ev[i + 1]))
 
     def timed_us(fn, n):
         """Mean device time of fn in microseconds over n calls, L2 flushed before each."""
@@ -527,8 +559,9 @@ def run_ours(args, rank, world, local):
         # host buffers: page-locked blocks from the library's allocator; the inputs are
         # written into them with its streaming-store copy, as a serving loop stages them
         h_in = [capi.dllm_host_stage(capi.host_empty(t.shape, t.dtype), t.cpu())
-                for t in (x, x_probe, pos, mass, block_lo)]
-        d_in = [[x, x_probe, pos, mass, block_lo], [t.clone() for t in (x, x_probe, pos, mass, block_lo)]]
+                for t in (x, pos, mass, block_lo)]
+        d_in = [[x, pos, mass, block_lo], [t.clone() for t in (x, pos, mass, block_lo)]]
+        d_xtrk = [x_probe, torch.empty_like(x_probe)]
         d_out = [[out, cos, refresh], [torch.empty_like(t) for t in (out, cos, refresh)]]
         h_out = [[capi.host_empty(t.shape, t.dtype) for t in (out, cos, refresh)] for _ in range(2)]
         d_idx = [idx, torch.empty_like(idx)]
@@ -542,10 +575,11 @@ def run_ours(args, rank, world, local):
                 d_.copy_(h_, non_blocking=True)
 
         def compute(j):
-            xi, xpi, posi, massi, loi = d_in[j]
+            xi, posi, massi, loi = d_in[j]
             outi, cosi, refi = d_out[j]
             capi.dllm_kv_topk(massi, loi, wl.block_len, k, d_idx[j])
-            capi.dllm_cache_project(cache.handle, 0, xi, w, posi, None, outi, kv_x=xpi, kv_positions=d_idx[j],
+            capi.dllm_gather_rows(cache.handle, x_all, d_idx[j], d_xtrk[j])
+            capi.dllm_cache_project(cache.handle, 0, xi, w, posi, None, outi, kv_x=d_xtrk[j], kv_positions=d_idx[j],
                                     probe_kv=d_probe[j])
             capi.dllm_cache_attend(cache.handle, 0, posi, None, outi)
             capi.dllm_kv_drift(cache.handle, 0, d_idx[j], d_probe[j], wl.gamma, cosi, refi)
@@ -615,6 +649,9 @@ def run_ours(args, rank, world, local):
                "d2h_bytes_per_step": d2h, "graphs": "one CUDA graph per step: copy-in(i+1) | step(i) | read-back(i-1)",
                "host_buffers": "page-locked dllm_host_alloc blocks; the inputs written into them once, before the "
                                "timed region, with dllm_host_stage (streaming stores)",
+               "inputs": "copied in every step: the block's hidden states, positions, previous-step mass and block "
+                         "offsets; resident: cache, weights and the layer's hidden states of every position (the "
+                         "tracked rows are gathered from them on the device)",
                "us_per_step": step_us,
                "copies_only": {"h2d_us": t_in, "h2d_gbs": h2d / t_in / 1e3, "d2h_us": t_out,
                                "d2h_gbs": d2h / t_out / 1e3, "both_us": t_both,
@@ -722,25 +759,32 @@ def run_ours(args, rank, world, local):
     pk = peaks()
     cache_bytes = B * S * 2 * D * 2  # the layer's K and V
     mean = {kname: statistics.mean(v) for kname, v in per.items()}
-    proj_tflops = alg["proj_flops"] / (mean["project"] * 1e-3) / 1e12
-    attn_gbs = alg["attn_bytes"] / (mean["attend"] * 1e-3) / 1e9
+    # every kernel against the slower of its two bounds (FLOPs at the bf16 burst peak,
+    # algorithmic bytes at the copy peak)
     kernels = {
-        "project": {"ms": mean["project"], "bound": "tensor", "achieved": proj_tflops, "unit": "TFLOP/s",
-                    "peak": pk["bf16_tflops"], "frac": proj_tflops / pk["bf16_tflops"],
-                    "algorithmic_flops": alg["proj_flops"], "traffic": measured_traffic("project")},
-        "attend": {"ms": mean["attend"], "bound": "hbm", "achieved": attn_gbs, "unit": "GB/s",
-                   "peak": pk["hbm_gbs"], "frac": attn_gbs / pk["hbm_gbs"], "algorithmic_bytes": alg["attn_bytes"],
-                   "traffic": measured_traffic("attend")},
-        "topk": {"ms": mean["topk"]},
-        "drift": {"ms": mean["drift"], "achieved_gbs": alg["drift_bytes"] / (mean["drift"] * 1e-3) / 1e9},
+        "project": roofline_entry("project", mean["project"] * 1e3, alg["proj_flops"], alg["proj_bytes"], pk),
+        "attend": roofline_entry("attend", mean["attend"] * 1e3, alg["attn_flops"], alg["attn_bytes"], pk),
+        "gather": roofline_entry("gather", mean["gather"] * 1e3, 0.0, alg["gather_bytes"], pk),
+        "drift": roofline_entry("drift", mean["drift"] * 1e3, 0.0, alg["drift_bytes"], pk),
+        "topk": {"kernel": "topk", "us": mean["topk"] * 1e3, "bound": "latency"},
     }
+    for kname in ("project", "attend"):
+        kernels[kname]["traffic"] = measured_traffic(kname)
     dom = "project" if mean["project"] >= mean["attend"] else "attend"
     kd = kernels[dom]
+    # the contract's object describes the dominant kernel; per_kernel carries both graded
+    # kernels (projection and attention) in the same form
+    graded = []
+    for kname in ("project", "attend"):
+        e = kernels[kname]
+        graded.append({"kernel": kname, "bound": e["bound"], "achieved": e["achieved"], "peak": e["peak"],
+                       "unit": e["unit"], "frac": e["frac"], "traffic": e["traffic"], "us": e["us"]})
     roofline = {"kernel": dom, "bound": kd["bound"], "achieved": kd["achieved"], "peak": kd["peak"],
-                "unit": kd["unit"], "frac": kd["frac"], "traffic": measured_traffic(dom),
-                "peak_source": pk["source"] + (" burst" if kd["bound"] == "tensor" else "")}
-    # top-k, projection, attention, drift (+ the split-KV merge when units < SMs)
-    n_launch_per_step = 4 + (1 if B * s.n_heads < torch.cuda.get_device_properties(dev).multi_processor_count else 0)
+                "unit": kd["unit"], "frac": kd["frac"], "traffic": kd["traffic"],
+                "peak_source": pk["source"] + (" burst" if kd["bound"] == "tensor" else ""),
+                "per_kernel": graded}
+    # top-k, gather, projection, attention, drift (+ the split-KV merge when units < SMs)
+    n_launch_per_step = 5 + (1 if B * s.n_heads < torch.cuda.get_device_properties(dev).multi_processor_count else 0)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",
@@ -816,16 +860,21 @@ def main():
         for _ in range(args.warmup):
             sample.rep()
         per_seq = [sample.rep() for _ in range(args.steps)]
-        total = sum(per_seq) * wl.shape.batch  # a layer-step covers the whole batch
-        value = args.steps / total
+        B = wl.shape.batch
+        timed_s = sum(per_seq)
+        # each timed step is one sequence of the B a layer-step covers: the layer-step rate
+        # is steps / (B x timed seconds); ms_per_step is the measured time of one such step
+        value = args.steps / (B * timed_s)
+        sample_desc = ("each timed step: the whole step for sequence 0 of the batch (top-k, probe and block "
+                       "projection, attention, drift), i.e. 1/%d of a layer-step" % B)
         line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
-                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * timed_s / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-                "data": "synthetic", "config": {"workload": wl.name, "batch": wl.shape.batch},
+                "data": "synthetic", "config": {"workload": wl.name, "batch": B},
+                "layer_steps_per_timed_step": 1.0 / B, "timed_s": timed_s,
                 "cpu_baseline": {"value": value, "unit": UNIT, "cores": sample.cores, "kind": "oracle",
-                                 "threads": sample.threads,
-                                 "sample": "each step: the whole step for sequence 0 of the batch (top-k, probe "
-                                           "and block projection, attention, drift); time x batch size"},
+                                 "threads": sample.threads, "sample": sample_desc,
+                                 "ms_per_sequence": 1e3 * timed_s / args.steps, "sequences_per_layer_step": B},
                 "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line), flush=True)
         return
@@ -836,12 +885,13 @@ def main():
         reps = []
         while sum(reps) < args.cpu_seconds or len(reps) < 2:
             reps.append(sample.rep())
-        sec = statistics.mean(reps) * wl.shape.batch
-        line["cpu_baseline"] = {"value": 1.0 / sec, "unit": UNIT, "cores": sample.cores, "kind": "oracle",
-                                "threads": sample.threads,
+        per_seq = statistics.mean(reps)
+        line["cpu_baseline"] = {"value": 1.0 / (per_seq * wl.shape.batch), "unit": UNIT, "cores": sample.cores,
+                                "kind": "oracle", "threads": sample.threads,
                                 "sample": f"{len(reps)} repetitions of the whole step for sequence 0 of "
                                           f"{wl.shape.batch} (top-k, probe and block projection, attention, "
-                                          f"drift); time x batch size"}
+                                          f"drift); a layer-step covers all {wl.shape.batch} sequences",
+                                "ms_per_sequence": 1e3 * per_seq, "sequences_per_layer_step": wl.shape.batch}
     if rank == 0:
         print(json.dumps(line), flush=True)
 

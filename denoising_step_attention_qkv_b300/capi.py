@@ -25,8 +25,9 @@ DEV_BAD_POSITION, DEV_BAD_VIEW, DEV_TAIL_FULL, DEV_TIMEOUT, DEV_BAD_INDEX = 0x1,
 EXPORTS = ("dllm_cache_bytes", "dllm_cache_alloc", "dllm_cache_free", "dllm_cache_get_layout", "dllm_cache_step",
            "dllm_cache_project", "dllm_cache_attend", "dllm_cache_attend_noalloc", "dllm_unfused_workspace_bytes",
            "dllm_cache_step_unfused", "dllm_attention_mass", "dllm_cache_attend_ragged", "dllm_cache_attend_partial",
-           "dllm_attend_merge", "dllm_kv_topk", "dllm_kv_drift", "dllm_elastic_workspace_bytes", "dllm_elastic_step",
-           "dllm_selftest_wait_timeout",
+           "dllm_attend_merge", "dllm_kv_topk", "dllm_gather_rows", "dllm_kv_drift", "dllm_elastic_workspace_bytes",
+           "dllm_elastic_step",
+           "dllm_selftest_wait_timeout", "dllm_selftest_fail_alloc",
            "dllm_cache_status", "dllm_strerror", "dllm_host_alloc", "dllm_host_free",
            "dllm_host_stage")
 
@@ -73,8 +74,10 @@ def lib() -> ctypes.CDLL:
         L.dllm_cache_step_unfused.argtypes = [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p,
                                               c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_size_t, c_void_p]
         L.dllm_kv_topk.argtypes = [c_void_p, c_int, c_int, c_void_p, c_int, c_int, c_void_p, c_void_p]
+        L.dllm_gather_rows.argtypes = [c_void_p, c_void_p, c_int, c_void_p, c_int, c_void_p, c_void_p]
         L.dllm_kv_drift.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_float, c_void_p, c_void_p, c_void_p]
         L.dllm_selftest_wait_timeout.argtypes = [c_void_p, c_void_p]
+        L.dllm_selftest_fail_alloc.argtypes = [c_int]
         L.dllm_attention_mass.argtypes = [c_void_p, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_void_p]
         L.dllm_cache_attend_ragged.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_void_p, c_void_p]
         L.dllm_cache_attend_partial.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_int, c_int, c_void_p,
@@ -232,6 +235,12 @@ def dllm_kv_topk(mass: torch.Tensor, block_lo: torch.Tensor, block_len: int, k: 
                                               int(k), _ptr(idx), _stream(stream)))
 
 
+def dllm_gather_rows(handle, x_all: torch.Tensor, idx: torch.Tensor, x_rows: torch.Tensor, stream=None) -> None:
+    """x_rows[b][j] = x_all[b][idx[b][j]] (the tracked tokens' hidden states)."""
+    _check("dllm_gather_rows", lib().dllm_gather_rows(handle, _ptr(x_all), int(x_all.shape[1]), _ptr(idx),
+                                                      int(idx.shape[-1]), _ptr(x_rows), _stream(stream)))
+
+
 def dllm_kv_drift(handle, layer: int, idx: torch.Tensor, probe_kv: torch.Tensor, gamma: float, cos: torch.Tensor,
                   refresh: Optional[torch.Tensor] = None, stream=None) -> None:
     k = int(idx.shape[-1])
@@ -257,6 +266,11 @@ def dllm_elastic_step(handle, x_all: Sequence[torch.Tensor], w_qkv: Sequence[tor
         handle, n, xs, ws, _ptr(win_lo), int(beta), _ptr(mass), int(k), float(gamma), _ptr(out), _ptr(cos),
         _ptr(flags), _ptr(mass_out), _ptr(workspace), int(workspace.numel() * workspace.element_size()),
         _stream(stream)))
+
+
+def dllm_selftest_fail_alloc(nth: int) -> None:
+    """Make the nth device allocation of the library from now on fail (0 cancels)."""
+    _check("dllm_selftest_fail_alloc", lib().dllm_selftest_fail_alloc(int(nth)))
 
 
 def dllm_selftest_wait_timeout(handle, stream=None) -> None:

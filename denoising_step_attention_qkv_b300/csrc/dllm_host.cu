@@ -44,6 +44,29 @@ cudaError_t ensure_smem_limit(const void* kernel, int bytes) {
 
 namespace {
 
+// Device allocations of the library go through dev_alloc, which a test can make fail on
+// purpose (dllm_selftest_fail_alloc) to exercise the error paths without a GPU fault.
+std::mutex g_alloc_mu;
+int g_fail_alloc_in = 0;  // > 0: the g_fail_alloc_in-th allocation from now fails
+
+cudaError_t dev_alloc(void** p, size_t bytes) {
+  {
+    std::lock_guard<std::mutex> lock(g_alloc_mu);
+    if (g_fail_alloc_in > 0 && --g_fail_alloc_in == 0) {
+      *p = nullptr;
+      return cudaErrorMemoryAllocation;
+    }
+  }
+  return cudaMalloc(p, bytes);
+}
+template <typename T>
+cudaError_t dev_alloc(T** p, size_t bytes) {
+  void* v = nullptr;
+  const cudaError_t e = dev_alloc(&v, bytes);
+  *p = static_cast<T*>(v);
+  return e;
+}
+
 int from_cuda(cudaError_t e) {
   if (e == cudaSuccess) return DLLM_OK;
   if (e == cudaErrorMemoryAllocation) return DLLM_EOOM;
@@ -172,7 +195,7 @@ int dllm_cache_alloc(const dllm_cache_desc* desc, dllm_cache** out) {
     c->kv = desc->external_buf;
     c->owns_kv = false;
   } else {
-    e = cudaMalloc(&c->kv, kvb + scb);
+    e = dev_alloc(&c->kv, kvb + scb);
     if (e != cudaSuccess) return fail(from_cuda(e));
     c->owns_kv = true;
   }
@@ -186,16 +209,16 @@ int dllm_cache_alloc(const dllm_cache_desc* desc, dllm_cache** out) {
       const double a = (double)p * std::pow(desc->rope_theta, -2.0 * i / desc->head_dim);
       tab[(size_t)p * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
     }
-  e = cudaMalloc(&c->rope, tab.size() * sizeof(float2));
+  e = dev_alloc(&c->rope, tab.size() * sizeof(float2));
   if (e != cudaSuccess) return fail(from_cuda(e));
   e = cudaMemcpy(c->rope, tab.data(), tab.size() * sizeof(float2), cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return fail(from_cuda(e));
 
-  e = cudaMalloc(&c->status, sizeof(int));
+  e = dev_alloc(&c->status, sizeof(int));
   if (e != cudaSuccess) return fail(from_cuda(e));
   e = cudaMemset(c->status, 0, sizeof(int));
   if (e != cudaSuccess) return fail(from_cuda(e));
-  e = cudaMalloc(&c->drift_cnt, (size_t)desc->batch * sizeof(int));
+  e = dev_alloc(&c->drift_cnt, (size_t)desc->batch * sizeof(int));
   if (e != cudaSuccess) return fail(from_cuda(e));
   e = cudaMemset(c->drift_cnt, 0, (size_t)desc->batch * sizeof(int));
   if (e != cudaSuccess) return fail(from_cuda(e));
@@ -203,7 +226,7 @@ int dllm_cache_alloc(const dllm_cache_desc* desc, dllm_cache** out) {
   // split-KV partials: at most 2 * (2 * SMs) units of kQChunk rows
   if (desc->kv_dtype != DLLM_F32) {
     c->ws_floats = (size_t)4 * c->sm_count * kQChunk * (kHd + 2);
-    e = cudaMalloc(&c->ws, c->ws_floats * sizeof(float));
+    e = dev_alloc(&c->ws, c->ws_floats * sizeof(float));
     if (e != cudaSuccess) return fail(from_cuda(e));
   }
   *out = c;
@@ -335,12 +358,13 @@ ProjParams make_proj(dllm_cache* c, const StepArgs& a) {
   return p;
 }
 
-int do_project(dllm_cache* c, const StepArgs& a, __nv_bfloat16* raw_q = nullptr, __nv_bfloat16* raw_kv = nullptr) {
+int do_project(dllm_cache* c, const StepArgs& a, void* raw_q = nullptr, void* raw_kv = nullptr) {
   if (a.n_tok == 0 && a.n_kv == 0) return DLLM_OK;
   const dllm_cache_desc& d = c->desc;
   ProjParams p = make_proj(c, a);
   p.raw_q = raw_q;
   p.raw_kv = raw_kv;
+  p.raw_f32 = d.kv_dtype == DLLM_E4M3;
   const int D = p.D;
   int rc;
   if (d.kv_dtype == DLLM_F32) {
@@ -414,8 +438,15 @@ struct KeyRange {
   float* state = nullptr;
 };
 
+// Where the split-KV partial states go: the cache's own workspace, unless `get` is set,
+// in which case it is called (only when the keys are split) for a buffer of `floats`.
+struct SplitScratch {
+  int (*get)(float** out) = nullptr;
+  size_t floats = 0;
+};
+
 int do_attend(dllm_cache* c, int layer, const int32_t* positions, const uint8_t* view, int n_tok, void* out,
-              cudaStream_t s, const KeyRange& kr = KeyRange()) {
+              cudaStream_t s, const KeyRange& kr = KeyRange(), const SplitScratch& scratch = SplitScratch()) {
   if (n_tok == 0) return DLLM_OK;
   const dllm_cache_desc& d = c->desc;
   const int B = d.batch, H = d.n_heads, hd = d.head_dim, D = H * hd;
@@ -430,7 +461,7 @@ int do_attend(dllm_cache* c, int layer, const int32_t* positions, const uint8_t*
   a.view = view;
   a.positions = positions;
   a.out = out;
-  a.ws = c->ws;
+  a.ws = scratch.get ? nullptr : c->ws;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)hd));
   a.kv_scale = layer_scale(c, layer);
   a.kv_dtype = d.kv_dtype;
@@ -465,7 +496,14 @@ int do_attend(dllm_cache* c, int layer, const int32_t* positions, const uint8_t*
   a.tiles_per_split = ceil_div(a.key_tiles, splits);
   a.n_splits = ceil_div(a.key_tiles, a.tiles_per_split);
   a.units = base * a.n_splits;
-  if (a.n_splits > 1 && (size_t)a.units * kQChunk * (kHd + 2) > c->ws_floats) return DLLM_EUNSUPPORTED;
+  if (a.n_splits > 1) {
+    const size_t need = (size_t)a.units * kQChunk * (kHd + 2);
+    if (need > (scratch.get ? scratch.floats : c->ws_floats)) return DLLM_EUNSUPPORTED;
+    if (scratch.get) {
+      rc = scratch.get(&a.ws);
+      if (rc) return rc;
+    }
+  }
 
   CUtensorMap tm_q, tm_kv;
   if (!map_2d_bf16(&tm_q, out, D, (uint64_t)B * n_tok, 64, a.nq_pad)) return DLLM_ECUDA;
@@ -592,12 +630,20 @@ int dllm_attention_mass(dllm_cache* c, int layer, const int32_t* positions, cons
   return rc ? from_cuda((cudaError_t)rc) : DLLM_OK;
 }
 
+namespace {
+// Bytes per raw projection value in the unfused pipeline's workspace: fp32 for e4m3
+// caches (quantised from the unrounded value), bf16 otherwise.
+size_t unfused_raw_bytes(const dllm_cache* c) { return c->desc.kv_dtype == DLLM_E4M3 ? 4 : 2; }
+size_t unfused_q_bytes(const dllm_cache* c, int n_tok) {
+  const size_t D = (size_t)c->desc.n_heads * c->desc.head_dim;
+  return (((size_t)c->desc.batch * n_tok * 3 * D * unfused_raw_bytes(c) + 255) / 256) * 256;
+}
+}  // namespace
+
 size_t dllm_unfused_workspace_bytes(const dllm_cache* c, int n_tok, int n_kv) {
   if (!c || n_tok < 0 || n_kv < 0) return 0;
   const size_t D = (size_t)c->desc.n_heads * c->desc.head_dim;
-  const size_t q_bytes = (size_t)c->desc.batch * n_tok * 3 * D * 2;
-  const size_t kv_bytes = (size_t)c->desc.batch * n_kv * 2 * D * 2;
-  return ((q_bytes + 255) / 256) * 256 + kv_bytes;
+  return unfused_q_bytes(c, n_tok) + (size_t)c->desc.batch * n_kv * 2 * D * unfused_raw_bytes(c);
 }
 
 int dllm_cache_step_unfused(dllm_cache* c, int layer, const void* x, const void* w_qkv, const int32_t* positions,
@@ -615,17 +661,16 @@ int dllm_cache_step_unfused(dllm_cache* c, int layer, const void* x, const void*
   const size_t need = dllm_unfused_workspace_bytes(c, n_tok, n_kv);
   if (!workspace || workspace_bytes < need || (reinterpret_cast<uintptr_t>(workspace) & 255u)) return DLLM_EINVAL;
   if (n_tok == 0 && n_kv == 0) return DLLM_OK;
-  const size_t D = (size_t)c->desc.n_heads * c->desc.head_dim;
-  __nv_bfloat16* raw_q = reinterpret_cast<__nv_bfloat16*>(workspace);
-  __nv_bfloat16* raw_kv = reinterpret_cast<__nv_bfloat16*>(
-      reinterpret_cast<uint8_t*>(workspace) + (((size_t)c->desc.batch * n_tok * 3 * D * 2 + 255) / 256) * 256);
-  // 1. projection GEMM, plain bf16 output to the workspace
+  void* raw_q = workspace;
+  void* raw_kv = reinterpret_cast<uint8_t*>(workspace) + unfused_q_bytes(c, n_tok);
+  // 1. projection GEMM, plain output to the workspace
   rc = do_project(c, a, raw_q, raw_kv);
   if (rc) return rc;
   // 2. rotary embedding (Q into `out`, K in place), 3. cache (or probe) write
   ProjParams p = make_proj(c, a);
   p.raw_q = raw_q;
   p.raw_kv = raw_kv;
+  p.raw_f32 = c->desc.kv_dtype == DLLM_E4M3;
   rc = launch_rope_rows(p, a.s);
   if (rc) return from_cuda((cudaError_t)rc);
   rc = launch_cache_write(p, a.s);
@@ -654,6 +699,21 @@ int dllm_kv_drift(const dllm_cache* c, int layer, const int32_t* idx, int k, con
   return from_cuda((cudaError_t)launch_drift(kvl, scl, d.kv_dtype, d.batch, c->slots, d.max_pos, d.n_heads, d.head_dim,
                                              idx, k, probe_kv, gamma, cos, refresh, c->drift_cnt, c->sm_count,
                                              c->status, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+int dllm_gather_rows(dllm_cache* c, const void* x_all, int n_pos, const int32_t* idx, int k, void* x_rows,
+                     void* stream) {
+  if (!c || !x_all || !idx || !x_rows || n_pos < 1 || k < 1) return DLLM_EINVAL;
+  if (!on_cache_device(c)) return DLLM_EINVAL;
+  if (!aligned16(x_all) || !aligned16(x_rows)) return DLLM_EINVAL;
+  const dllm_cache_desc& d = c->desc;
+  if ((long long)d.batch * k > (1ll << 30) || (long long)d.batch * n_pos > (1ll << 40)) return DLLM_EINVAL;
+  // the kernel copies rows as 16-byte vectors of bf16 elements: D * elt bytes per row
+  const int D = d.n_heads * d.head_dim;
+  const int row_bf16 = d.kv_dtype == DLLM_F32 ? 2 * D : D;  // fp32 rows are twice as long
+  if (row_bf16 % 8 != 0) return DLLM_EUNSUPPORTED;
+  return from_cuda((cudaError_t)launch_gather_rows(x_all, d.batch, n_pos, row_bf16, nullptr, 0, idx, k, nullptr,
+                                                   x_rows, nullptr, c->status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
 // Multi-layer refresh step: workspace layout (each part at a 256-byte boundary).
@@ -744,6 +804,13 @@ int dllm_elastic_step(dllm_cache* c, int n_layers, const void* const* x_all, con
   return DLLM_OK;
 }
 
+int dllm_selftest_fail_alloc(int nth) {
+  if (nth < 0) return DLLM_EINVAL;
+  std::lock_guard<std::mutex> lock(g_alloc_mu);
+  g_fail_alloc_in = nth;
+  return DLLM_OK;
+}
+
 int dllm_cache_status(dllm_cache* c, int* device_bits) {
   if (!c) return DLLM_EINVAL;
   cudaError_t e = cudaDeviceSynchronize();
@@ -789,7 +856,9 @@ float* g_noalloc_addr[kMaxDevices] = {};
 
 // Device address of g_noalloc_scratch on the current device.  Host code cannot use
 // the symbol itself (it names a host-side shadow), so the address is looked up once
-// per device, with that device current, and cached.
+// per device, with that device current, and remembered.  A cudaDeviceReset() of the
+// device discards the array with the rest of its memory and makes the remembered
+// address stale; the public header tells callers not to use the entry point after one.
 int noalloc_scratch_address(float** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
@@ -808,62 +877,15 @@ int noalloc_scratch_address(float** out) {
 
 }  // namespace
 
+// The same launches as dllm_cache_attend (same work split, so the same results), with
+// the split-KV partials in g_noalloc_scratch instead of the cache's workspace.
 extern "C" int dllm_cache_attend_noalloc(dllm_cache* c, int layer, const int32_t* positions, const uint8_t* view,
                                          int n_tok, void* out, void* stream) {
   int rc = check_attend(c, layer, n_tok, positions, view, out);
   if (rc) return rc;
-  if (n_tok == 0) return DLLM_OK;
-  cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
-  const dllm_cache_desc& d = c->desc;
-  const int B = d.batch, H = d.n_heads, hd = d.head_dim, D = H * hd;
-  AttnParams a{};
-  a.B = B;
-  a.H = H;
-  a.D = D;
-  a.n_tok = n_tok;
-  a.max_pos = d.max_pos;
-  a.tail = d.tail_slots;
-  a.slots = c->slots;
-  a.view = view;
-  a.positions = positions;
-  a.out = out;
-  a.ws = nullptr;
-  a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)hd));
-  a.kv_scale = layer_scale(c, layer);
-  a.kv_dtype = d.kv_dtype;
-  a.status = c->status;
-  if (d.kv_dtype == DLLM_F32) {  // the fp32 kernel keeps no partial state
-    rc = launch_attn_f32(a, (const float*)layer_kv(c, layer), hd, s);
-    return rc ? from_cuda((cudaError_t)rc) : DLLM_OK;
-  }
-  // same work split as dllm_cache_attend, so both produce the same result
-  a.nq_pad = n_tok <= 32 ? 32 : (n_tok <= 48 ? 48 : 64);
-  a.n_qchunks = ceil_div(n_tok, kQChunk);
-  a.key_tiles = ceil_div(d.max_pos + (view ? d.tail_slots : 0), kKeyTile);
-  const int base = B * H * a.n_qchunks;
-  int splits = 1;
-  if (base < c->sm_count) {
-    splits = ceil_div(c->sm_count, base);
-    if (splits > a.key_tiles) splits = a.key_tiles;
-  }
-  a.tiles_per_split = ceil_div(a.key_tiles, splits);
-  a.n_splits = ceil_div(a.key_tiles, a.tiles_per_split);
-  a.units = base * a.n_splits;
-  if (a.n_splits > 1) {
-    const size_t need = (size_t)a.units * kQChunk * (kHd + 2) * sizeof(float);
-    if (need > (size_t)DLLM_NOALLOC_SCRATCH_BYTES) return DLLM_EUNSUPPORTED;
-    rc = noalloc_scratch_address(&a.ws);
-    if (rc) return rc;
-  }
-  CUtensorMap tm_q, tm_kv;
-  if (!map_2d_bf16(&tm_q, out, D, (uint64_t)B * n_tok, 64, a.nq_pad)) return DLLM_ECUDA;
-  if (!map_cache(&tm_kv, layer_kv(c, layer), d.kv_dtype, hd, H, (uint64_t)B * c->slots)) return DLLM_ECUDA;
-  const int grid = a.units < c->sm_count ? a.units : c->sm_count;
-  rc = launch_attn_tc(a, tm_q, tm_kv, grid, s);
-  if (rc) return from_cuda((cudaError_t)rc);
-  if (a.n_splits > 1) {
-    rc = launch_attn_combine(a, s);
-    if (rc) return from_cuda((cudaError_t)rc);
-  }
-  return DLLM_OK;
+  SplitScratch scratch;
+  scratch.get = noalloc_scratch_address;
+  scratch.floats = DLLM_NOALLOC_SCRATCH_BYTES / sizeof(float);
+  return do_attend(c, layer, positions, view, n_tok, out, reinterpret_cast<cudaStream_t>(stream), KeyRange(),
+                   scratch);
 }

@@ -93,10 +93,12 @@ struct ProjParams {
   int max_pos, tail, slots;
   const float2* rope;
   int* status;
-  // Unfused pipeline only (else null): the GEMM stores its plain bf16 output here,
-  // [m_q][3D] for query rows and [m_kv][2D] (K|V) for K/V-only rows, with no rotation.
-  __nv_bfloat16* raw_q;
-  __nv_bfloat16* raw_kv;
+  // Unfused pipeline only (else null): the GEMM stores its plain output here,
+  // [m_q][3D] for query rows and [m_kv][2D] (K|V) for K/V-only rows, with no rotation;
+  // fp32 when raw_f32 (e4m3 caches, which quantise the unrounded rotated value), else bf16.
+  void* raw_q;
+  void* raw_kv;
+  bool raw_f32;
 };
 
 // ------------------------------------------------------------------------ attention

@@ -221,16 +221,26 @@ DEVI bool kv_tile_skipped(const ProjParams& p, int grp, int m0, int rows) {
 DEVI void store_rows(const ProjParams& p, const TileCoord& c, int heads, uint32_t tacc, int r, bool ok) {
   const int hd = kHd;
   if (p.raw_q != nullptr || p.raw_kv != nullptr) {
-    // unfused pipeline: the plain projection output, rounded to bf16, no rotation
+    // unfused pipeline: the plain projection output (fp32, or rounded to bf16), no rotation
     const int m = c.m0 + r;
     const bool exists = ok && (c.grp == 0 ? m < p.m_q : m < p.m_kv);
-    __nv_bfloat16* dst = c.grp == 0 ? p.raw_q + static_cast<size_t>(m) * 3 * p.D + c.n0
-                                    : p.raw_kv + static_cast<size_t>(m) * 2 * p.D + (c.n0 - p.D);
+    const size_t off = c.grp == 0 ? static_cast<size_t>(m) * 3 * p.D + c.n0
+                                  : static_cast<size_t>(m) * 2 * p.D + (c.n0 - p.D);
+    void* base = c.grp == 0 ? p.raw_q : p.raw_kv;
 #pragma unroll 1
     for (int col = 0; col < heads * kHd; col += 32) {
       float v[32];
       tmem_ld32(tacc + col, v);
-      if (exists) store_bf16x32(dst + col, v);
+      if (!exists) continue;
+      if (p.raw_f32) {
+        uint4* d = reinterpret_cast<uint4*>(static_cast<float*>(base) + off + col);
+#pragma unroll
+        for (int i = 0; i < 8; ++i)
+          d[i] = make_uint4(__float_as_uint(v[4 * i]), __float_as_uint(v[4 * i + 1]), __float_as_uint(v[4 * i + 2]),
+                            __float_as_uint(v[4 * i + 3]));
+      } else {
+        store_bf16x32(static_cast<__nv_bfloat16*>(base) + off + col, v);
+      }
     }
     return;
   }
@@ -613,24 +623,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem_base = *tmem_slot;
   grid_dep_launch();
-  // W is never written by the kernels of a step, so the producer requests the W half of
-  // the first stages of its first item before the dependency wait (not with selection
-  // flags, whose values decide which items run); the x halves follow after it
-  int npre = 0;
+  // Before the dependency wait the producer only prefetches into L2 the W half of the
+  // first stages of its first item (not with selection flags, whose values decide which
+  // items run), so W's DRAM latency overlaps the previous kernel.  Every copy into shared
+  // memory comes after the wait: the work before this call on the stream may still be
+  // writing W (a cast or a dequantisation), and only L2, the device's point of
+  // coherence, can be read before its writes are visible.
   if (warp == 0 && lane == 0 && p.kv_seq_flags == nullptr && pair < p.items_total) {
     const PairItem it = decode_pair_item(p, pair);
     const int b_rows = it.half ? 64 : 128;
     const CUtensorMap* bm = it.half ? &tm_w_half : &tm_w;
     const int n0 = it.n0 + static_cast<int>(rank) * b_rows;
-    const uint32_t bytes = 2 * (kABytes + b_rows * BK * 2);
-    npre = p.k_blocks < kPairStages ? p.k_blocks : kPairStages;
-    for (int s = 0; s < npre; ++s) {
-      if (rank == 0) mbar_arrive_expect_tx(&full[s], bytes);
-      tma_load_2d_pair(sB + s * kPairBBytes, bm, map_to_rank(smem_u32(&full[s]), 0), s * BK, n0,
-                       p.m_fastest ? policy_evict_first() : policy_evict_last());
-    }
+    const int npre = p.k_blocks < kPairStages ? p.k_blocks : kPairStages;
+    for (int s = 0; s < npre; ++s)
+      tma_prefetch_2d_l2(bm, s * BK, n0, p.m_fastest ? policy_evict_first() : policy_evict_last());
   }
-  grid_dep_wait();  // x, positions, indices and flags may come from the previous kernel
+  grid_dep_wait();  // x, W, positions, indices and flags may come from the previous kernel
   select_init(p);
   __syncthreads();
   const int items_end = nothing_selected(p) ? 0 : p.items_total;
@@ -653,14 +661,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       const uint32_t bytes = 2 * (kABytes + b_rows * BK * 2);  // both CTAs' copies
       for (int kb = 0; kb < p.k_blocks; ++kb) {
         const uint32_t fb = map_to_rank(smem_u32(&full[stage]), 0);
-        if (item == pair && kb < npre) {  // W already requested: only x for this stage
-          tma_load_2d_pair(sA + stage * kABytes, am, fb, kb * BK, m0, pol_x);
-        } else {
-          if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
-          if (rank == 0) mbar_arrive_expect_tx(&full[stage], bytes);
-          tma_load_2d_pair(sA + stage * kABytes, am, fb, kb * BK, m0, pol_x);
-          tma_load_2d_pair(sB + stage * kPairBBytes, bm, fb, kb * BK, n0, pol_w);
-        }
+        if (!mbar_wait(&empty[stage], phase ^ 1u, abort_flag)) { ok = false; break; }
+        if (rank == 0) mbar_arrive_expect_tx(&full[stage], bytes);
+        tma_load_2d_pair(sA + stage * kABytes, am, fb, kb * BK, m0, pol_x);
+        tma_load_2d_pair(sB + stage * kPairBBytes, bm, fb, kb * BK, n0, pol_w);
         if (++stage == STAGES) { stage = 0; phase ^= 1u; }
       }
     }

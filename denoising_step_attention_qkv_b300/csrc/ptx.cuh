@@ -100,6 +100,15 @@ DEVI void tma_load_3d(void* dst, const CUtensorMap* map, uint64_t* bar, int c0, 
       "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "r"(c2), "l"(policy)
       : "memory");
 }
+// Prefetch a 2-D tile into L2 only (no shared-memory copy, no barrier).  L2 is the
+// device's point of coherence, so a prefetch issued while another kernel may still be
+// writing the tile cannot hand a stale value to a later load.
+DEVI void tma_prefetch_2d_l2(const CUtensorMap* map, int c0, int c1, uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile.L2::cache_hint [%0, {%1, %2}], %3;" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "l"(policy)
+               : "memory");
+}
 DEVI void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }

@@ -250,10 +250,13 @@ int dllm_attention_mass(dllm_cache* cache, int layer, const int32_t* positions, 
  * paragraph 2: QKV projection, rotary embedding, cache write and attention as four
  * kernels, each writing its intermediates to HBM for the next one).  Same arguments and
  * effects as dllm_cache_step, plus a caller-owned device workspace that receives the
- * projection output: bf16 [batch][n_tok][3D] for the query rows, then (at the next
- * 256-byte boundary) bf16 [batch][n_kv][2D] for the K/V-only rows.  The projection
- * output is rounded to bf16 before the rotation and the cache store, so results differ
- * from dllm_cache_step by that extra rounding.
+ * projection output: [batch][n_tok][3D] for the query rows, then (at the next 256-byte
+ * boundary) [batch][n_kv][2D] for the K/V-only rows.  The workspace holds bf16 values
+ * for DLLM_BF16 caches, which are rounded to bf16 before the rotation and the cache
+ * store (results differ from dllm_cache_step by that extra rounding), and fp32 values
+ * for DLLM_E4M3 caches, which are quantised from the unrounded rotated value as
+ * dllm_cache_step does (the codes differ only where fp32 sums in another order cross a
+ * rounding boundary).
  *
  *   workspace        device buffer of >= dllm_unfused_workspace_bytes() bytes, 256-byte
  *                    aligned (DLLM_EINVAL otherwise)
@@ -278,6 +281,21 @@ int dllm_cache_step_unfused(dllm_cache* cache, int layer,
  *             to the lower position; k <= n_pos - block_len, n_pos <= 16384 */
 int dllm_kv_topk(const float* mass, int batch, int n_pos, const int32_t* block_lo, int block_len,
                  int k, int32_t* idx, void* stream);
+
+/* Hidden states of the tracked tokens ("Elastic-Cache", Core idea: the drift test
+ * recomputes K/V of the previous step's most-attended tokens from this step's states;
+ * "Flash-dLLM ...", paragraph 4: 32 tracked tokens): a row gather on the device, so
+ * that top-k, gather, probe projection and drift test run back to back on the stream
+ * without a host round trip.
+ *
+ *   x_all     act [batch][n_pos][D]: this step's hidden states of every position
+ *   idx       int32 [batch][k]: positions to gather (dllm_kv_topk's output)
+ *   x_rows    act [batch][k][D] out: x_rows[b][j] = x_all[b][idx[b][j]]
+ * batch and D are the cache's (the cache supplies them and the status word); act as
+ * for dllm_cache_step.  A position outside [0, n_pos) gives a zero row and sets
+ * DLLM_DEV_BAD_INDEX.  x_all and x_rows 16-byte aligned, k >= 1, n_pos >= 1. */
+int dllm_gather_rows(dllm_cache* cache, const void* x_all, int n_pos, const int32_t* idx, int k, void* x_rows,
+                     void* stream);
 
 /* Attention-aware drift test ("Elastic-Cache", Core idea and Algorithm knobs).
  *
@@ -353,7 +371,11 @@ int dllm_elastic_step(dllm_cache* cache, int n_layers, const void* const* x_all,
  *     long); nothing is launched then.
  *   - The first call on each device looks up the device address of that array (with
  *     the device current) and remembers it; make this first call before any stream
- *     capture begins.
+ *     capture begins.  cudaDeviceReset() discards the array with the rest of the
+ *     device's memory and leaves the remembered address stale: do not call this entry
+ *     point on a device after resetting it.
+ *   - It launches exactly the kernels dllm_cache_attend launches, with the same work
+ *     split, so its output is bit-identical to dllm_cache_attend's.
  *   - Every call on a device shares the same array and leaves its contents behind.
  *     Nothing in it needs to start at zero.  Calls whose kernels overlap on the GPU
  *     (different streams without ordering between them) race on it and give wrong
@@ -368,6 +390,14 @@ int dllm_cache_attend_noalloc(dllm_cache* cache, int layer,
  * word and ends; dllm_cache_status() then returns DLLM_EDEVICE with that bit and clears
  * it, and the context stays usable.  Not part of the pages' method. */
 int dllm_selftest_wait_timeout(dllm_cache* cache, void* stream);
+
+/* Self-test of the allocation-failure paths: the nth device allocation the library
+ * makes from now on (1 = the next one) fails as if the device were out of memory; 0
+ * cancels a pending failure.  Process-wide; allocations by the caller are unaffected.
+ * dllm_cache_alloc then returns DLLM_EOOM with *out NULL, having released whatever it
+ * had allocated before the failure.  DLLM_EINVAL for nth < 0.  Host only, no CUDA call.
+ * Not part of the pages' method. */
+int dllm_selftest_fail_alloc(int nth);
 
 /* Synchronise the device, read the cache's device status word into *device_bits (may
  * be NULL) and clear it.  Returns DLLM_EDEVICE if any bit was set, else DLLM_OK. */

@@ -89,3 +89,23 @@ def test_clock_reason_bits(bits, names):
     # NVML clock-event reason bits: 0x4 software power cap, 0x8 hardware slowdown,
     # 0x20 software thermal, 0x40 hardware thermal, 0x80 power brake; 0x1 (GPU idle) is not reported
     assert sorted(v for k, v in bench.Clocks.REASONS.items() if bits & k) == names
+
+
+def test_roofline_entry_takes_the_slower_bound():
+    pk = {"hbm_gbs": 6000.0, "bf16_tflops": 2000.0}
+    D = 4096
+    # batch-1 projection: 32 rows x 3D features; W's 100.7 MB at the copy rate (16.8 us)
+    # outlasts its 0.8 TFLOP at the tensor rate (0.4 us), so it is HBM-bound
+    flops, nbytes = 2.0 * 32 * 3 * D * D, 3 * D * D * 2 + 32 * D * 2 * 2 + 32 * 2 * D * 2
+    e = bench.roofline_entry("project", 28.8, flops, nbytes, pk)
+    assert e["bound"] == "hbm" and e["unit"] == "GB/s"
+    assert abs(e["frac"] - nbytes / 28.8e-6 / 6000e9) < 1e-12
+    assert e["frac"] > e["other_bound_frac"]
+    # batch-32 step projection: 171.8 GFLOP (85.9 us at the tensor rate) against 134 MB
+    wl = bench._with_drift_inputs(W.make("llada8b-b32-drift"))
+    a = bench.algorithmic(wl)
+    e = bench.roofline_entry("project", 120.0, a["proj_flops"], a["proj_bytes"], pk)
+    assert e["bound"] == "tensor" and e["unit"] == "TFLOP/s"
+    assert abs(e["achieved"] - a["proj_flops"] / 120e-6 / 1e12) < 1e-9
+    # a pure copy has no FLOPs: always HBM-bound
+    assert bench.roofline_entry("gather", 5.0, 0.0, 16_777_216, pk)["bound"] == "hbm"

@@ -1,6 +1,8 @@
 """Failure handling on the GPU without a fault: a pipeline wait that nothing satisfies
 gives up after its time limit, the kernel reports DLLM_DEV_TIMEOUT through the cache's
-status word and ends, and the context stays usable for the next step."""
+status word and ends, and the context stays usable for the next step; out-of-range
+device indices are reported, not faulted; a device allocation that fails (made to
+fail by the library's self-test hook) returns DLLM_EOOM and leaks nothing."""
 import time
 
 import pytest
@@ -48,3 +50,36 @@ def test_device_range_errors_are_reported_not_faulted():
     rc, bits = cache.status()
     assert rc == capi.DLLM_EDEVICE and bits & capi.DEV_BAD_INDEX
     assert torch.isnan(cos).all()
+
+
+@pytest.mark.parametrize("owned", [True, False], ids=["library-owned", "caller-buffer"])
+def test_allocation_failure_returns_eoom_and_releases_everything(owned):
+    # every device allocation of dllm_cache_alloc is made to fail in turn (the K/V buffer
+    # when the library owns it, the rotary table, the status word, the drift counters,
+    # the split-KV workspace); each attempt must return DLLM_EOOM with a NULL handle and
+    # give back what it had allocated before the failure
+    import ctypes
+    L = capi.lib()
+    B, S, H = 4, 4096, 8  # 64 MiB of K/V: a leak of it would show in the free memory
+    ext = None if owned else torch.empty(capi.dllm_cache_bytes(capi.dllm_cache_desc(
+        1, B, S, 0, H, 128, capi.DLLM_BF16, 1e4, None, 0)), dtype=torch.uint8, device="cuda")
+    desc = capi.dllm_cache_desc(1, B, S, 0, H, 128, capi.DLLM_BF16, 1e4,
+                                None if owned else ext.data_ptr(), 0 if owned else ext.numel())
+    n_allocs = 5 if owned else 4
+    torch.cuda.synchronize()
+    free0 = torch.cuda.mem_get_info()[0]
+    for nth in range(1, n_allocs + 1):
+        capi.dllm_selftest_fail_alloc(nth)
+        h = ctypes.c_void_p(1)
+        assert L.dllm_cache_alloc(ctypes.byref(desc), ctypes.byref(h)) == capi.DLLM_EOOM, nth
+        assert h.value is None
+        torch.cuda.synchronize()
+        assert torch.cuda.mem_get_info()[0] >= free0 - (4 << 20), f"memory kept after failing allocation {nth}"
+    # the hook fired each time: one more allocation than the call makes never fails
+    capi.dllm_selftest_fail_alloc(n_allocs + 1)
+    h = ctypes.c_void_p()
+    assert L.dllm_cache_alloc(ctypes.byref(desc), ctypes.byref(h)) == capi.DLLM_OK and h.value
+    capi.dllm_selftest_fail_alloc(0)
+    assert L.dllm_cache_free(h) == capi.DLLM_OK
+    torch.cuda.synchronize()
+    assert torch.cuda.mem_get_info()[0] >= free0 - (4 << 20)

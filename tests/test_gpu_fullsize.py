@@ -1,5 +1,12 @@
-"""Full-size workloads through the C ABI, checked against the fp64 oracle on sampled
-(sequence, head) pairs plus bit-exact slot sets and top-k indices."""
+"""Full-size workloads through the C ABI, in the launch configuration the bench times,
+against the fp64 oracle: the written-slot set of every sequence and the top-k indices
+bit-exactly, then every head of three sequences per workload (cache K/V, attention
+output, probes and drift cosines).
+
+The attention runs one persistent CTA per SM (148 on a B300) over units numbered
+(sequence, head) in order, round-robin, so the checked sequences are the first one
+(round 0), one that straddles the last two rounds and the last one (every unit in the
+last round)."""
 import numpy as np
 import pytest
 import torch
@@ -10,6 +17,16 @@ from tests import gpu_harness as G
 from denoising_step_attention_qkv_b300 import capi
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
+
+
+def _round_seqs(wl, n_queries):
+    """First sequence, the sequence holding the first unit of the last round, last sequence."""
+    s = wl.shape
+    sm = torch.cuda.get_device_properties(0).multi_processor_count
+    units = s.batch * s.n_heads * -(-n_queries // 64)
+    last_round = (units - 1) // sm * sm
+    mid = last_round // (s.n_heads * -(-n_queries // 64))
+    return sorted({0, min(mid, s.batch - 1), s.batch - 1})
 
 
 def _topk(wl):
@@ -26,38 +43,41 @@ def test_config3_batch32_drift_fullsize():
     np.testing.assert_array_equal(idx_np, O.kv_topk(wl.mass, wl.block_lo, wl.block_len, wl.drift_k))
     cache = G.make_cache(wl)
     out, probe = G.run_gpu(wl, cache, probe_idx=idx_np)
-    G.check_sampled(wl, cache, out, [(0, 0), (13, 7), (31, 31)], probe_gpu=probe, probe_idx=idx_np)
-    # drift for two whole sequences (the cosine spans all heads)
+    seqs = _round_seqs(wl, wl.x.shape[1])
+    assert len(seqs) == 3
+    G.check_sequences(wl, cache, out, seqs, probe_gpu=probe, probe_idx=idx_np)
+    # drift of the same sequences (the cosine spans all heads of a token)
     cos = torch.empty((wl.shape.batch, wl.drift_k, 2), dtype=torch.float32, device="cuda")
     refresh = torch.empty(wl.shape.batch, dtype=torch.int32, device="cuda")
     pk = torch.from_numpy(probe).to(torch.bfloat16).cuda()
     capi.dllm_kv_drift(cache.handle, 0, idx, pk, wl.gamma, cos, refresh)
     g_cos = cos.double().cpu().numpy()
-    for b in (5, 30):
-        s = wl.shape
-        Kc = np.zeros((wl.drift_k, s.D))
-        Vc = np.zeros((wl.drift_k, s.D))
-        Kp = np.zeros((wl.drift_k, s.D))
-        Vp = np.zeros((wl.drift_k, s.D))
-        for h in range(s.n_heads):
-            _, K, V, _, pr = G.oracle_head(wl, b, h, idx_np)
-            sl = slice(h * s.head_dim, (h + 1) * s.head_dim)
-            Kc[:, sl], Vc[:, sl] = K[idx_np[b]], V[idx_np[b]]
-            Kp[:, sl], Vp[:, sl] = pr
-        o_cos = np.array([[O.cosine(Kc[j], Kp[j]), O.cosine(Vc[j], Vp[j])] for j in range(wl.drift_k)])
+    g_ref = refresh.cpu().numpy()
+    for b in seqs:
+        _, oc, pr = G.oracle_seq(wl, b, idx_np)
+        o_cos = O.kv_drift(oc, idx_np[b:b + 1], pr[None])[0]
         G.assert_close(g_cos[b], o_cos, G.TOL["bf16"], f"drift cos b={b}")
-    assert set(np.unique(refresh.cpu().numpy())) <= {0, 1}
+        assert g_ref[b] == int(g_cos[b].min() < np.float32(wl.gamma))
+    assert set(np.unique(g_ref)) <= {0, 1}
 
 
 def test_config4_verify_fullsize():
     wl = W.make("llada8b-b16-verify")
     cache = G.make_cache(wl)
     out, _ = G.run_gpu(wl, cache)
-    G.check_sampled(wl, cache, out, [(0, 3), (9, 20), (15, 31)])
+    seqs = _round_seqs(wl, wl.x.shape[1])
+    assert len(seqs) == 3
+    G.check_sequences(wl, cache, out, seqs)
 
 
 def test_config5_refresh_fp8_fullsize():
+    # The e4m3 encoding alone (the oracle's own model of it against the unquantised
+    # oracle, no GPU) moves this workload's output by 4.3-10.2% of a sequence's
+    # max|out| and by 4.9% of the whole output's, so the output is checked as the bound
+    # states it: over the whole output tensor, every sequence computed by the oracle.
     wl = W.make("llada8b-b8-refresh-fp8")
     cache = G.make_cache(wl)
     out, _ = G.run_gpu(wl, cache)
-    G.check_sampled(wl, cache, out, [(0, 0), (4, 11), (7, 31)], exact_diag_tol=0.15)
+    seqs = _round_seqs(wl, wl.x.shape[1])
+    assert len(seqs) == 3
+    G.check_sequences(wl, cache, out, seqs, whole_output=True)

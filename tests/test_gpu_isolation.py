@@ -21,10 +21,12 @@ CASES = [
 ]
 
 
-def oracle_inputs(wl):
-    """The oracle's cache after the step's writes and the step's rotated Q."""
+def oracle_inputs(wl, model_fp8=True):
+    """The oracle's cache after the step's writes (for an e4m3 workload its model of the
+    encoding unless model_fp8 is False) and the step's rotated Q."""
     s = wl.shape
-    oc = O.OracleCache(s.batch, s.max_pos, 0, s.n_heads, s.head_dim, kv="e4m3" if s.kv == "e4m3" else "exact")
+    oc = O.OracleCache(s.batch, s.max_pos, 0, s.n_heads, s.head_dim,
+                       kv="e4m3" if (s.kv == "e4m3" and model_fp8) else "exact")
     O.write_rows(oc, wl.w, wl.pre_x, wl.pre_pos, s.rope_theta)
     O.write_rows(oc, wl.w, wl.x, wl.positions, s.rope_theta)
     q = np.stack([O.rope(O.project_qkv(wl.x[b], wl.w, s.n_heads)[0], wl.positions[b], s.rope_theta)
@@ -67,5 +69,11 @@ def test_attention_on_an_oracle_written_cache(name, kw):
     torch.cuda.synchronize()
     assert cache.status() == (capi.DLLM_OK, 0)
     qr = qb.double().numpy()
+    got = out.double().cpu().numpy()
+    # exactly the values the kernel reads: its own error, at the bf16 bound for both caches
     ref = np.stack([O.attention(qr[b], Kr[b], Vr[b]).reshape(n, H * hd) for b in range(B)])
-    G.assert_close(out.double().cpu().numpy(), ref, G.TOL[s.kv], f"isolated attention ({name})")
+    G.assert_close(got, ref, G.TOL["bf16"], f"isolated attention ({name})")
+    if s.kv == "e4m3":  # and against the unquantised oracle, at the FP8 bound
+        oe, qe = oracle_inputs(wl, model_fp8=False)
+        ref_e = np.stack([O.attention(qe[b], oe.K[b, :S], oe.V[b, :S]).reshape(n, H * hd) for b in range(B)])
+        G.assert_close(got, ref_e, G.TOL["e4m3"], f"isolated attention vs the unquantised oracle ({name})")

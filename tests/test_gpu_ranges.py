@@ -27,17 +27,19 @@ def _staged(wl):
     return cache, pos, q
 
 
-def _oracle(wl):
+def _oracle(wl, model_fp8=False):
+    """The oracle's cache after the step's writes (unquantised unless model_fp8) and the
+    step's rotated Q."""
     s = wl.shape
-    kv = "e4m3" if s.kv == "e4m3" else "exact"
+    kv = "e4m3" if (s.kv == "e4m3" and model_fp8) else "exact"
     cache = O.OracleCache(s.batch, s.max_pos, s.tail_slots, s.n_heads, s.head_dim, kv=kv)
     O.write_rows(cache, wl.w, wl.pre_x, wl.pre_pos, s.rope_theta)
     q = O.write_rows(cache, wl.w, wl.x, wl.positions, s.rope_theta)
     return cache, q
 
 
-def _ragged_reference(wl, key_len):
-    cache, q = _oracle(wl)
+def _ragged_reference(wl, key_len, model_fp8=False):
+    cache, q = _oracle(wl, model_fp8)
     n = wl.x.shape[1]
     ref = np.zeros((wl.shape.batch, n, wl.shape.D))
     for b in range(wl.shape.batch):
@@ -76,6 +78,9 @@ def test_ragged_matches_oracle(name, kw, lens):
     got = out.double().cpu().numpy()
     ref = _ragged_reference(wl, lens)
     G.assert_close(got, ref, G.TOL[wl.shape.kv], f"ragged attention ({name})")
+    if wl.shape.kv == "e4m3":
+        G.assert_close(got, _ragged_reference(wl, lens, model_fp8=True), G.FP8_MODEL_TOL,
+                       f"ragged attention vs the e4m3 model ({name})")
     for b, L in enumerate(lens):
         if L == 0:
             assert np.all(got[b] == 0.0)
@@ -101,24 +106,30 @@ def test_partial_states_and_merge(kv):
     torch.cuda.synchronize()
     assert cache.status() == (capi.DLLM_OK, 0)
     assert torch.equal(q, q_before)  # partial calls leave Q alone
-    tol = G.TOL[kv]
-    ocache, oq = _oracle(wl)
-    full_ref = np.stack([O.attention(oq[b], ocache.K[b], ocache.V[b]).reshape(n, -1) for b in range(s.batch)])
-    G.assert_close(merged.double().cpu().numpy(), full_ref, tol, "merged partial states")
-    G.assert_close(merged.double().cpu().numpy(), full.double().cpu().numpy(), tol, "merged vs one-pass")
-    # each state against the oracle's: the normalised output and the base-2 log-sum-exp
-    for st, lo, hi in ((st_a, 0, cut), (st_b, cut, s.max_pos)):
-        g = st.double().cpu().numpy()
-        for b in range(s.batch):
-            vis = O.range_visible(n, s.max_pos, lo, hi)
-            ost = O.attention_partial(oq[b], ocache.K[b], ocache.V[b], vis)
-            o_out = O.state_output(ost)
-            g_out = g[b, :, :, :s.head_dim] / g[b, :, :, s.head_dim + 1][..., None]
-            G.assert_close(g_out, o_out, tol, f"partial state output [{lo}, {hi}) b={b}")
-            lse_g = g[b, :, :, s.head_dim] + np.log2(g[b, :, :, s.head_dim + 1])
-            lse_o = ost[1] + np.log2(ost[2])
-            assert np.max(np.abs(lse_g - lse_o)) < 0.05, np.max(np.abs(lse_g - lse_o))
-    # the merged state normalises to the same output
-    g = st_ab.double().cpu().numpy()
-    G.assert_close(g[..., :s.head_dim] / g[..., s.head_dim + 1:], full_ref.reshape(g[..., :s.head_dim].shape), tol,
-                   "merged state")
+    refs = [("oracle", _oracle(wl), G.TOL[kv])]
+    if kv == "e4m3":
+        # also against the oracle's model of the encoding, which holds the values the
+        # kernel reads (up to rounding ties): the kernel's own error at the bf16 bound
+        refs.append(("e4m3 model", _oracle(wl, model_fp8=True), G.FP8_MODEL_TOL))
+    G.assert_close(merged.double().cpu().numpy(), full.double().cpu().numpy(), G.TOL["bf16"], "merged vs one-pass")
+    for ref_name, (ocache, oq), tol in refs:
+        full_ref = np.stack([O.attention(oq[b], ocache.K[b], ocache.V[b]).reshape(n, -1) for b in range(s.batch)])
+        G.assert_close(merged.double().cpu().numpy(), full_ref, tol, f"merged partial states vs {ref_name}")
+        # each state against the oracle's: the normalised output and the base-2 log-sum-exp
+        for st, lo, hi in ((st_a, 0, cut), (st_b, cut, s.max_pos)):
+            g = st.double().cpu().numpy()
+            for b in range(s.batch):
+                vis = O.range_visible(n, s.max_pos, lo, hi)
+                ost = O.attention_partial(oq[b], ocache.K[b], ocache.V[b], vis)
+                o_out = O.state_output(ost)
+                g_out = g[b, :, :, :s.head_dim] / g[b, :, :, s.head_dim + 1][..., None]
+                G.assert_close(g_out, o_out, tol, f"partial state output [{lo}, {hi}) b={b} vs {ref_name}")
+                lse_g = g[b, :, :, s.head_dim] + np.log2(g[b, :, :, s.head_dim + 1])
+                lse_o = ost[1] + np.log2(ost[2])
+                G.record(f"partial state log2-sum-exp [{lo}, {hi}) b={b} vs {ref_name} (absolute)",
+                         np.max(np.abs(lse_g - lse_o)), 0.05)
+                assert np.max(np.abs(lse_g - lse_o)) < 0.05, np.max(np.abs(lse_g - lse_o))
+        # the merged state normalises to the same output
+        g = st_ab.double().cpu().numpy()
+        G.assert_close(g[..., :s.head_dim] / g[..., s.head_dim + 1:], full_ref.reshape(g[..., :s.head_dim].shape),
+                       tol, f"merged state vs {ref_name}")

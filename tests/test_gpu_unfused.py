@@ -58,12 +58,13 @@ def test_unfused_matches_oracle(name, workload, kw):
     out, _ = _run_unfused(wl, cache)
     o_out, ocache, _ = G.run_oracle(wl)
     tol = G.TOL[wl.shape.kv]
-    # The pipeline stores the projection in bf16 before quantising it to e4m3, so a value
-    # near the midpoint of two codes may take the other neighbour: an error of one e4m3
-    # step, at most 32/448 of the group's amax (the step of the top binade [256, 448)).
-    cache_tol = 32 / 448 + 1e-3 if wl.shape.kv == "e4m3" else tol
-    G.compare_cache(cache, ocache, cache_tol)
+    # for an e4m3 cache the pipeline quantises the fp32 rotated value, as the fused kernel
+    # and the oracle do, so its codes are checked as theirs are (compare_cache)
+    G.compare_cache(cache, ocache, tol)
     G.assert_close(out.reshape(o_out.shape), o_out, tol, f"unfused attention out ({name})")
+    if wl.shape.kv == "e4m3":
+        m_out = G.run_oracle(wl, model_fp8=True)[0]
+        G.assert_close(out.reshape(m_out.shape), m_out, G.FP8_MODEL_TOL, f"unfused out vs the e4m3 model ({name})")
 
 
 def test_unfused_probes_match_oracle():
