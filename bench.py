@@ -4,9 +4,10 @@
 One step (the timed unit) on the batch-32 workload: top-32 selection of the previous
 step's most-attended positions, the gather of those tokens' hidden states from this
 step's hidden states of every position, the fused QKV projection + rotary embedding +
-cache write of the 32-token active block of every sequence plus the K/V of the 32
-tracked tokens (probes), bidirectional attention of the block over the 1024-slot cache,
-and the K/V cosine-drift reduction with its refresh flag.  Inputs are seeded synthetic
+cache write of the 32-token active block of every sequence together with the K/V of
+the 32 tracked tokens, whose cosine drift against the cache and refresh flag the same
+kernel's epilogue computes, and bidirectional attention of the block over the
+1024-slot cache.  Inputs are seeded synthetic
 arrays from ``workloads``; the cache (512 MiB), the weights and the layer's hidden
 states (256 MiB) are resident in HBM.
 
@@ -215,10 +216,12 @@ def algorithmic(wl):
     n_tok = wl.x.shape[1]
     k = wl.drift_k
     proj_flops = 2.0 * B * n_tok * 3 * D * D + 2.0 * B * k * 2 * D * D
+    # W once, the block and tracked rows in, Q and the block's K/V out, and (the fused
+    # drift test) the tracked tokens' cached K/V read
     proj_bytes = 3 * D * D * 2 + B * (n_tok + k) * D * 2 + B * n_tok * 3 * D * 2 + B * k * 2 * D * 2
     attn_bytes = B * H * S * hd * 2 * 2 + 2 * B * n_tok * D * 2
     attn_flops = 4.0 * B * H * n_tok * S * hd
-    drift_bytes = B * k * 2 * D * 2 * 2
+    drift_bytes = B * k * 2 * D * 2 * 2  # the separate drift kernel: cache rows + probe rows
     gather_bytes = 2 * B * k * D * 2
     return dict(proj_flops=proj_flops, proj_bytes=proj_bytes, attn_bytes=attn_bytes, attn_flops=attn_flops,
                 drift_bytes=drift_bytes, gather_bytes=gather_bytes)
@@ -455,27 +458,24 @@ def run_ours(args, rank, world, local):
     x_probe = torch.empty((B, k, D), dtype=torch.bfloat16, device=dev)  # the gathered rows
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    KERNELS = ("topk", "gather", "project", "attend", "drift")
+    KERNELS = ("topk", "gather", "project", "attend")
 
     def step_plain():
         capi.dllm_kv_topk(mass, block_lo, wl.block_len, k, idx, stream)
         capi.dllm_gather_rows(cache.handle, x_all, idx, x_probe, stream=stream)
-        capi.dllm_cache_project(cache.handle, 0, x, w, pos, None, out, kv_x=x_probe, kv_positions=idx,
-                                probe_kv=probe, stream=stream)
+        capi.dllm_cache_project_drift(cache.handle, 0, x, w, pos, None, out, x_probe, idx, wl.gamma, cos, refresh,
+                                      stream=stream)
         capi.dllm_cache_attend(cache.handle, 0, pos, None, out, stream=stream)
-        capi.dllm_kv_drift(cache.handle, 0, idx, probe, wl.gamma, cos, refresh, stream=stream)
 
     def step():
         capi.dllm_kv_topk(mass, block_lo, wl.block_len, k, idx, stream)
         ev[1].record(stream)
         capi.dllm_gather_rows(cache.handle, x_all, idx, x_probe, stream=stream)
         ev[2].record(stream)
-        capi.dllm_cache_project(cache.handle, 0, x, w, pos, None, out, kv_x=x_probe, kv_positions=idx,
-                                probe_kv=probe, stream=stream)
+        capi.dllm_cache_project_drift(cache.handle, 0, x, w, pos, None, out, x_probe, idx, wl.gamma, cos, refresh,
+                                      stream=stream)
         ev[3].record(stream)
         capi.dllm_cache_attend(cache.handle, 0, pos, None, out, stream=stream)
-        ev[4].record(stream)
-        capi.dllm_kv_drift(cache.handle, 0, idx, probe, wl.gamma, cos, refresh, stream=stream)
 
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS) + 1)]
     for _ in range(max(args.warmup, 3)):
@@ -565,7 +565,6 @@ def run_ours(args, rank, world, local):
         d_out = [[out, cos, refresh], [torch.empty_like(t) for t in (out, cos, refresh)]]
         h_out = [[capi.host_empty(t.shape, t.dtype) for t in (out, cos, refresh)] for _ in range(2)]
         d_idx = [idx, torch.empty_like(idx)]
-        d_probe = [probe, torch.empty_like(probe)]
         h2d = sum(t.numel() * t.element_size() for t in h_in)
         d2h = sum(t.numel() * t.element_size() for t in h_out[0])
         s_cp_in, s_cp_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
@@ -579,10 +578,9 @@ def run_ours(args, rank, world, local):
             outi, cosi, refi = d_out[j]
             capi.dllm_kv_topk(massi, loi, wl.block_len, k, d_idx[j])
             capi.dllm_gather_rows(cache.handle, x_all, d_idx[j], d_xtrk[j])
-            capi.dllm_cache_project(cache.handle, 0, xi, w, posi, None, outi, kv_x=d_xtrk[j], kv_positions=d_idx[j],
-                                    probe_kv=d_probe[j])
+            capi.dllm_cache_project_drift(cache.handle, 0, xi, w, posi, None, outi, d_xtrk[j], d_idx[j], wl.gamma,
+                                          cosi, refi)
             capi.dllm_cache_attend(cache.handle, 0, posi, None, outi)
-            capi.dllm_kv_drift(cache.handle, 0, d_idx[j], d_probe[j], wl.gamma, cosi, refi)
 
         def copy_out(j):
             for h_, d_ in zip(h_out[j], d_out[j]):
@@ -670,25 +668,32 @@ def run_ours(args, rank, world, local):
         n_cmp = min(args.steps, 200)
 
         def fused_pair():
-            capi.dllm_cache_project(cache.handle, 0, x, w, pos, None, out, kv_x=x_probe, kv_positions=idx,
-                                    probe_kv=probe, stream=stream)
+            capi.dllm_cache_project_drift(cache.handle, 0, x, w, pos, None, out, x_probe, idx, wl.gamma, cos,
+                                          refresh, stream=stream)
             capi.dllm_cache_attend(cache.handle, 0, pos, None, out, stream=stream)
 
         def unfused():
             capi.dllm_cache_step_unfused(cache.handle, 0, x, w, pos, None, out, ws, kv_x=x_probe,
                                          kv_positions=idx, probe_kv=probe, stream=stream)
+            capi.dllm_kv_drift(cache.handle, 0, idx, probe, wl.gamma, cos, refresh, stream=stream)
+
+        def separate_drift():  # the fused kernels with the drift test as its own launch
+            capi.dllm_cache_project(cache.handle, 0, x, w, pos, None, out, kv_x=x_probe, kv_positions=idx,
+                                    probe_kv=probe, stream=stream)
+            capi.dllm_cache_attend(cache.handle, 0, pos, None, out, stream=stream)
+            capi.dllm_kv_drift(cache.handle, 0, idx, probe, wl.gamma, cos, refresh, stream=stream)
 
         def timed(fn):
             return timed_us(fn, n_cmp)
 
-        t_fused, t_unfused = timed(fused_pair), timed(unfused)
+        t_fused, t_unfused, t_sep = timed(fused_pair), timed(unfused), timed(separate_drift)
         # the per-position attention mass that the next step's top-k reads (optional
         # output; the workload's mass input stands in for it in the timed step)
         mass_out = torch.empty((B, S), dtype=torch.float32, device=dev)
 
         def with_mass():
-            capi.dllm_cache_project(cache.handle, 0, x, w, pos, None, out, kv_x=x_probe, kv_positions=idx,
-                                    probe_kv=probe, stream=stream)
+            capi.dllm_cache_project_drift(cache.handle, 0, x, w, pos, None, out, x_probe, idx, wl.gamma, cos,
+                                          refresh, stream=stream)
             capi.dllm_attention_mass(cache.handle, 0, pos, None, out, mass_out, stream=stream)
             capi.dllm_cache_attend(cache.handle, 0, pos, None, out, stream=stream)
 
@@ -699,8 +704,12 @@ def run_ours(args, rank, world, local):
                "projection_part": {"fused_us": statistics.mean(per["project"]) * 1e3,
                                    "unfused_us": t_unfused - attend_us,
                                    "ratio": (t_unfused - attend_us) / (statistics.mean(per["project"]) * 1e3)},
-               "note": "unfused = projection GEMM to a bf16 workspace, rotary kernel, cache-write kernel, "
-                       "attention; the pages quote 1.37x for the fused kernel alone on an RTX 3090",
+               "drift_as_own_launch_us": t_sep,
+               "note": "fused = projection with the drift test in its epilogue, then attention; unfused = "
+                       "projection GEMM to a bf16 workspace, rotary kernel, cache-write kernel (probes to a "
+                       "buffer), attention, drift kernel; drift_as_own_launch = the fused projection storing the "
+                       "probes, attention, drift kernel.  The pages quote 1.37x for their fused kernel alone "
+                       "on an RTX 3090",
                "attention_mass_us": t_mass}
 
     # ---- ragged batches and partial softmax states over slot ranges, on this step's
@@ -730,6 +739,12 @@ def run_ours(args, rank, world, local):
         capi.dllm_cache_attend_partial(cache.handle, 0, pos, q_rows, 0, lo, st_b, stream=stream)
         t_merge = timed_us(lambda: capi.dllm_attend_merge(st_a, st_b, out=scratch, stream=stream), n_nx)
         merge_bytes = 2.0 * st_a.numel() * 4 + B * n_tok * D * 2
+        # FACache reuse as one call: attention over the last quarter (the slots a step
+        # rewrote) merged with the cached state of the rest, against one pass over all
+        t_reuse = timed_us(lambda: capi.dllm_cache_attend_with_state(cache.handle, 0, pos, q_rows, lo, S, st_b, scratch,
+                                                                     stream=stream), n_nx)
+        reuse_bytes = float(B) * (S - lo) * H * hd * 2 * 2 + B * n_tok * D * 2 * 2 + st_b.numel() * 4
+        t_onepass = timed_us(lambda: capi.dllm_cache_attend(cache.handle, 0, pos, None, scratch, stream=stream), n_nx)
         hbm = peaks()["hbm_gbs"]
 
         def row(us, nbytes, **kw):
@@ -739,7 +754,12 @@ def run_ours(args, rank, world, local):
         nxt = {"steps": n_nx,
                "ragged": row(t_rag, rag_bytes, key_len="seeded uniform [128, %d], mean %.0f" % (S, lens.mean())),
                "partial_state": row(t_part, part_bytes, slots=[lo, S]),
-               "merge": row(t_merge, merge_bytes)}
+               "merge": row(t_merge, merge_bytes),
+               "facache_reuse": row(t_reuse, reuse_bytes, slots=[lo, S], one_pass_us=t_onepass,
+                                    saving=t_onepass / t_reuse,
+                                    note="attention over the rewritten slots merged in-kernel with the cached state "
+                                         "of the others (dllm_cache_attend_with_state), against one pass over "
+                                         "every slot")}
 
     others = None
     if not args.no_unfused and not args.no_elastic and rank == 0:
@@ -765,7 +785,6 @@ def run_ours(args, rank, world, local):
         "project": roofline_entry("project", mean["project"] * 1e3, alg["proj_flops"], alg["proj_bytes"], pk),
         "attend": roofline_entry("attend", mean["attend"] * 1e3, alg["attn_flops"], alg["attn_bytes"], pk),
         "gather": roofline_entry("gather", mean["gather"] * 1e3, 0.0, alg["gather_bytes"], pk),
-        "drift": roofline_entry("drift", mean["drift"] * 1e3, 0.0, alg["drift_bytes"], pk),
         "topk": {"kernel": "topk", "us": mean["topk"] * 1e3, "bound": "latency"},
     }
     for kname in ("project", "attend"):
@@ -783,8 +802,9 @@ def run_ours(args, rank, world, local):
                 "unit": kd["unit"], "frac": kd["frac"], "traffic": kd["traffic"],
                 "peak_source": pk["source"] + (" burst" if kd["bound"] == "tensor" else ""),
                 "per_kernel": graded}
-    # top-k, gather, projection, attention, drift (+ the split-KV merge when units < SMs)
-    n_launch_per_step = 5 + (1 if B * s.n_heads < torch.cuda.get_device_properties(dev).multi_processor_count else 0)
+    # top-k, gather, projection with the drift test, attention (+ the split-KV merge when
+    # units < SMs)
+    n_launch_per_step = 4 + (1 if B * s.n_heads < torch.cuda.get_device_properties(dev).multi_processor_count else 0)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",

@@ -23,8 +23,9 @@ DLLM_VIEW_BASE, DLLM_VIEW_DRAFT, DLLM_VIEW_MASK = 0, 1, 2
 DEV_BAD_POSITION, DEV_BAD_VIEW, DEV_TAIL_FULL, DEV_TIMEOUT, DEV_BAD_INDEX = 0x1, 0x2, 0x4, 0x8, 0x10
 
 EXPORTS = ("dllm_cache_bytes", "dllm_cache_alloc", "dllm_cache_free", "dllm_cache_get_layout", "dllm_cache_step",
-           "dllm_cache_project", "dllm_cache_attend", "dllm_cache_attend_noalloc", "dllm_unfused_workspace_bytes",
+           "dllm_cache_project", "dllm_cache_project_drift", "dllm_cache_step_drift", "dllm_cache_attend", "dllm_cache_attend_noalloc", "dllm_unfused_workspace_bytes",
            "dllm_cache_step_unfused", "dllm_attention_mass", "dllm_cache_attend_ragged", "dllm_cache_attend_partial",
+           "dllm_cache_attend_with_state",
            "dllm_attend_merge", "dllm_kv_topk", "dllm_gather_rows", "dllm_kv_drift", "dllm_elastic_workspace_bytes",
            "dllm_elastic_step",
            "dllm_selftest_wait_timeout", "dllm_selftest_fail_alloc",
@@ -67,6 +68,10 @@ def lib() -> ctypes.CDLL:
         L.dllm_cache_step.argtypes = [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int, c_void_p,
                                       c_void_p, c_void_p, c_int, c_void_p, c_void_p]
         L.dllm_cache_project.argtypes = L.dllm_cache_step.argtypes
+        L.dllm_cache_project_drift.argtypes = [c_void_p, c_int, c_void_p, c_void_p, c_void_p, c_void_p, c_int,
+                                               c_void_p, c_void_p, c_void_p, c_int, c_float, c_void_p, c_void_p,
+                                               c_void_p]
+        L.dllm_cache_step_drift.argtypes = L.dllm_cache_project_drift.argtypes
         L.dllm_cache_attend.argtypes = [c_void_p, c_int, c_void_p, c_void_p, c_int, c_void_p, c_void_p]
         L.dllm_cache_attend_noalloc.argtypes = L.dllm_cache_attend.argtypes
         L.dllm_unfused_workspace_bytes.argtypes = [c_void_p, c_int, c_int]
@@ -82,6 +87,8 @@ def lib() -> ctypes.CDLL:
         L.dllm_cache_attend_ragged.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_void_p, c_void_p]
         L.dllm_cache_attend_partial.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_int, c_int, c_void_p,
                                                 c_void_p]
+        L.dllm_cache_attend_with_state.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_int, c_int,
+                                                   c_void_p, c_void_p, c_void_p]
         L.dllm_attend_merge.argtypes = [c_void_p, c_void_p, c_int, c_int, c_int, c_int, c_void_p, c_void_p, c_void_p]
         L.dllm_elastic_workspace_bytes.argtypes = [c_void_p, c_int, c_int]
         L.dllm_elastic_workspace_bytes.restype = c_size_t
@@ -166,6 +173,31 @@ def dllm_cache_project(handle, layer: int, x: Optional[torch.Tensor], w_qkv: tor
         _ptr(kv_x), _ptr(kv_positions), n_kv, _ptr(probe_kv), _stream(stream)))
 
 
+def _drift_call(fn: str, handle, layer, x, w_qkv, positions, view, out, kv_x, idx, gamma, cos, refresh, stream):
+    n_tok = 0 if positions is None else int(positions.shape[-1])
+    _check(fn, getattr(lib(), fn)(handle, int(layer), _ptr(x), _ptr(w_qkv), _ptr(positions), _ptr(view), n_tok,
+                                  _ptr(out), _ptr(kv_x), _ptr(idx), int(idx.shape[-1]), float(gamma), _ptr(cos),
+                                  _ptr(refresh), _stream(stream)))
+
+
+def dllm_cache_project_drift(handle, layer: int, x: Optional[torch.Tensor], w_qkv: torch.Tensor,
+                             positions: Optional[torch.Tensor], view: Optional[torch.Tensor],
+                             out: Optional[torch.Tensor], kv_x: torch.Tensor, idx: torch.Tensor, gamma: float,
+                             cos: torch.Tensor, refresh: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Projection with the drift test of the tracked rows fused (no probe buffer)."""
+    _drift_call("dllm_cache_project_drift", handle, layer, x, w_qkv, positions, view, out, kv_x, idx, gamma, cos,
+                refresh, stream)
+
+
+def dllm_cache_step_drift(handle, layer: int, x: Optional[torch.Tensor], w_qkv: torch.Tensor,
+                          positions: Optional[torch.Tensor], view: Optional[torch.Tensor],
+                          out: Optional[torch.Tensor], kv_x: torch.Tensor, idx: torch.Tensor, gamma: float,
+                          cos: torch.Tensor, refresh: Optional[torch.Tensor] = None, stream=None) -> None:
+    """dllm_cache_project_drift then dllm_cache_attend."""
+    _drift_call("dllm_cache_step_drift", handle, layer, x, w_qkv, positions, view, out, kv_x, idx, gamma, cos,
+                refresh, stream)
+
+
 def dllm_cache_attend(handle, layer: int, positions: torch.Tensor, view: Optional[torch.Tensor], out: torch.Tensor,
                       stream=None) -> None:
     _check("dllm_cache_attend", lib().dllm_cache_attend(handle, int(layer), _ptr(positions), _ptr(view),
@@ -200,6 +232,14 @@ def dllm_cache_attend_partial(handle, layer: int, positions: torch.Tensor, q: to
     _check("dllm_cache_attend_partial", lib().dllm_cache_attend_partial(
         handle, int(layer), _ptr(positions), int(positions.shape[-1]), _ptr(q), int(slot_lo), int(slot_hi),
         _ptr(state), _stream(stream)))
+
+
+def dllm_cache_attend_with_state(handle, layer: int, positions: torch.Tensor, q: torch.Tensor, slot_lo: int,
+                                 slot_hi: int, state: torch.Tensor, out: torch.Tensor, stream=None) -> None:
+    """Attention over [slot_lo, slot_hi) merged with a cached state of the other keys."""
+    _check("dllm_cache_attend_with_state", lib().dllm_cache_attend_with_state(
+        handle, int(layer), _ptr(positions), int(positions.shape[-1]), _ptr(q), int(slot_lo), int(slot_hi),
+        _ptr(state), _ptr(out), _stream(stream)))
 
 
 def dllm_attend_merge(state_a: torch.Tensor, state_b: torch.Tensor, out: Optional[torch.Tensor] = None,

@@ -83,6 +83,7 @@ struct Smem {
   float inv_l[NQ];
   float fin_alpha[2][NQ];  // per unit parity: the last tile's rescale factor and running max
   float fin_m[2][NQ];
+  float mrg_a[NQ], mrg_c[NQ];  // merge with a cached state: weights of this range's and the cached O
   uint32_t mask_bits[kMaxBitmapWords];
   int seq_order[kMaxOrder];  // ragged batches: sequences by key length, longest first
   uint32_t draft_qmask[2];
@@ -539,16 +540,45 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         if (lane < 16) S.red[quarter][NQ - 16 + lane] = v16;
       }
       softmax_sync();
+      const int frow0 = fx.b * p.n_tok + fx.qc * kQChunk;
+      const int fnrows = min(kQChunk, p.n_tok - fx.qc * kQChunk);
+      constexpr int kSt = kHd + 2;
       if (r < NQ) {
         const float lt = S.red[0][r] + S.red[1][r] + S.red[2][r] + S.red[3][r];
         S.l_fin[r] = lt;
-        S.inv_l[r] = lt > 0.0f ? 1.0f / lt : 0.0f;
+        if (p.state_in != nullptr) {
+          // merge with the cached state of the other keys (LaCache, FACache): M = max of
+          // both maxima, each side weighted by 2^(m - M)
+          const float ma = has_pv ? S.fin_m[fuu & 1][r] : -INFINITY;
+          float mc = -INFINITY, lc = 0.0f;
+          if (r < fnrows) {
+            const float* st = p.state_in + (static_cast<size_t>(frow0 + r) * p.H + fx.h) * kSt;
+            mc = st[kHd];
+            lc = st[kHd + 1];
+          }
+          const float M = fmaxf(ma, mc);
+          const float wa = (ma == -INFINITY) ? 0.0f : exp2f(ma - M);
+          const float wc = (mc == -INFINITY) ? 0.0f : exp2f(mc - M);
+          const float L = lt * wa + lc * wc;
+          S.mrg_a[r] = wa;
+          S.mrg_c[r] = wc;
+          S.inv_l[r] = L > 0.0f ? 1.0f / L : 0.0f;
+        } else {
+          S.inv_l[r] = lt > 0.0f ? 1.0f / lt : 0.0f;
+        }
       }
       softmax_sync();
-      const int frow0 = fx.b * p.n_tok + fx.qc * kQChunk;
-      const int fnrows = min(kQChunk, p.n_tok - fx.qc * kQChunk);
-      if (p.state != nullptr) {  // partial softmax state of the key range
-        constexpr int kSt = kHd + 2;
+      if (p.state_in != nullptr) {  // this range merged with the cached state: normalised output
+        __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(frow0) * p.D + fx.h * kHd + r;
+        const float* stc = p.state_in + static_cast<size_t>(frow0) * p.H * kSt + fx.h * kSt + r;
+#pragma unroll
+        for (int q = 0; q < NQ; ++q) {
+          if (ok && q < fnrows) {
+            const float oc = stc[static_cast<size_t>(q) * p.H * kSt];
+            out[static_cast<size_t>(q) * p.D] = __float2bfloat16_rn((o[q] * S.mrg_a[q] + oc * S.mrg_c[q]) * S.inv_l[q]);
+          }
+        }
+      } else if (p.state != nullptr) {  // partial softmax state of the key range
         float* st = p.state + (static_cast<size_t>(frow0) * p.H + fx.h) * kSt;
 #pragma unroll
         for (int q = 0; q < NQ; ++q)

@@ -222,6 +222,17 @@ int dllm_cache_alloc(const dllm_cache_desc* desc, dllm_cache** out) {
   if (e != cudaSuccess) return fail(from_cuda(e));
   e = cudaMemset(c->drift_cnt, 0, (size_t)desc->batch * sizeof(int));
   if (e != cudaSuccess) return fail(from_cuda(e));
+  {
+    // fused drift test: partial sums, row arrivals, sequence arrivals (one block, zeroed)
+    const size_t rows = (size_t)desc->batch * kMaxDriftRows;
+    const size_t bytes = rows * 6 * sizeof(float) + rows * sizeof(int) + (size_t)desc->batch * sizeof(int);
+    e = dev_alloc(&c->drift_acc, bytes);
+    if (e != cudaSuccess) return fail(from_cuda(e));
+    c->drift_rows = reinterpret_cast<int*>(c->drift_acc + rows * 6);
+    c->drift_seqs = c->drift_rows + rows;
+    e = cudaMemset(c->drift_acc, 0, bytes);
+    if (e != cudaSuccess) return fail(from_cuda(e));
+  }
 
   // split-KV partials: at most 2 * (2 * SMs) units of kQChunk rows
   if (desc->kv_dtype != DLLM_F32) {
@@ -240,6 +251,7 @@ int dllm_cache_free(dllm_cache* c) {
   if (c->rope) cudaFree(c->rope);
   if (c->status) cudaFree(c->status);
   if (c->drift_cnt) cudaFree(c->drift_cnt);
+  if (c->drift_acc) cudaFree(c->drift_acc);
   if (c->ws) cudaFree(c->ws);
   delete c;
   return DLLM_OK;
@@ -277,6 +289,10 @@ struct StepArgs {
   // K/V-only rows of sequence b only where one of flags[j][b], j < n_flag_sets, is set
   const int32_t* kv_seq_flags = nullptr;
   int n_flag_sets = 0;
+  // fused drift test: the K/V-only rows are probes compared with the cache (cos set)
+  float* drift_cos = nullptr;
+  int32_t* drift_refresh = nullptr;
+  float drift_gamma = 0.0f;
 };
 
 void* layer_kv(dllm_cache* c, int layer) {
@@ -355,6 +371,15 @@ ProjParams make_proj(dllm_cache* c, const StepArgs& a) {
   p.slots = c->slots;
   p.rope = c->rope;
   p.status = c->status;
+  if (a.drift_cos != nullptr) {
+    p.probe = nullptr;
+    p.drift_acc = c->drift_acc;
+    p.drift_rows = c->drift_rows;
+    p.drift_seqs = c->drift_seqs;
+    p.drift_cos = a.drift_cos;
+    p.drift_refresh = a.drift_refresh;
+    p.drift_gamma = a.drift_gamma;
+  }
   return p;
 }
 
@@ -436,6 +461,8 @@ struct KeyRange {
   int lo = 0, hi = -1;  // hi < 0: every slot (and the Flash-Verify tail)
   const int32_t* key_len = nullptr;
   float* state = nullptr;
+  const float* state_in = nullptr;  // cached state of the other keys, merged into the output
+  const void* q = nullptr;          // rotated Q, when it is not in `out`
 };
 
 // Where the split-KV partial states go: the cache's own workspace, unless `get` is set,
@@ -471,6 +498,7 @@ int do_attend(dllm_cache* c, int layer, const int32_t* positions, const uint8_t*
   a.tile_lo = 0;
   a.key_len = kr.key_len;
   a.state = kr.state;
+  a.state_in = kr.state_in;
   a.ranged = kr.hi >= 0 || kr.key_len != nullptr;
   if (kr.hi >= 0) {
     a.key_lo = kr.lo;
@@ -489,7 +517,7 @@ int do_attend(dllm_cache* c, int layer, const int32_t* positions, const uint8_t*
                            : ceil_div(d.max_pos + (view ? d.tail_slots : 0), kKeyTile);
   const int base = B * H * a.n_qchunks;
   int splits = 1;
-  if (base < c->sm_count && !a.state) {  // a partial state is written by one unit per row
+  if (base < c->sm_count && !a.state && !a.state_in) {  // states are per row: one unit per row
     splits = ceil_div(c->sm_count, base);
     if (splits > a.key_tiles) splits = a.key_tiles;
   }
@@ -506,7 +534,7 @@ int do_attend(dllm_cache* c, int layer, const int32_t* positions, const uint8_t*
   }
 
   CUtensorMap tm_q, tm_kv;
-  if (!map_2d_bf16(&tm_q, out, D, (uint64_t)B * n_tok, 64, a.nq_pad)) return DLLM_ECUDA;
+  if (!map_2d_bf16(&tm_q, kr.q ? kr.q : out, D, (uint64_t)B * n_tok, 64, a.nq_pad)) return DLLM_ECUDA;
   if (!map_cache(&tm_kv, layer_kv(c, layer), d.kv_dtype, hd, H, (uint64_t)B * c->slots)) return DLLM_ECUDA;
   const int grid = a.units < c->sm_count ? a.units : c->sm_count;
   rc = launch_attn_tc(a, tm_q, tm_kv, grid, s);
@@ -555,6 +583,45 @@ int dllm_cache_step(dllm_cache* c, int layer, const void* x, const void* w_qkv, 
   return do_attend(c, layer, positions, view, n_tok, out, a.s);
 }
 
+namespace {
+int project_drift_args(dllm_cache* c, StepArgs& a, int k, float gamma, float* cos, int32_t* refresh) {
+  if (!c) return DLLM_EINVAL;
+  if (k < 1 || !a.kv_x || !a.kv_positions || !cos) return DLLM_EINVAL;
+  if (c->desc.kv_dtype == DLLM_F32) return DLLM_EUNSUPPORTED;
+  if (k > kMaxDriftRows) return DLLM_EUNSUPPORTED;
+  a.drift_cos = cos;
+  a.drift_refresh = refresh;
+  a.drift_gamma = gamma;
+  return check_project(c, a);
+}
+}  // namespace
+
+int dllm_cache_project_drift(dllm_cache* c, int layer, const void* x, const void* w_qkv, const int32_t* positions,
+                             const uint8_t* view, int n_tok, void* out, const void* kv_x, const int32_t* idx, int k,
+                             float gamma, float* cos, int32_t* refresh, void* stream) {
+  StepArgs a{layer, x, w_qkv, positions, view, n_tok, out, kv_x, idx, k, nullptr,
+             reinterpret_cast<cudaStream_t>(stream)};
+  int rc = project_drift_args(c, a, k, gamma, cos, refresh);
+  if (rc) return rc;
+  return do_project(c, a);
+}
+
+int dllm_cache_step_drift(dllm_cache* c, int layer, const void* x, const void* w_qkv, const int32_t* positions,
+                          const uint8_t* view, int n_tok, void* out, const void* kv_x, const int32_t* idx, int k,
+                          float gamma, float* cos, int32_t* refresh, void* stream) {
+  StepArgs a{layer, x, w_qkv, positions, view, n_tok, out, kv_x, idx, k, nullptr,
+             reinterpret_cast<cudaStream_t>(stream)};
+  int rc = project_drift_args(c, a, k, gamma, cos, refresh);
+  if (rc) return rc;
+  if (n_tok > 0) {
+    rc = check_attend(c, layer, n_tok, positions, view, out);
+    if (rc) return rc;
+  }
+  rc = do_project(c, a);
+  if (rc) return rc;
+  return do_attend(c, layer, positions, view, n_tok, out, a.s);
+}
+
 int dllm_cache_attend_ragged(dllm_cache* c, int layer, const int32_t* positions, int n_tok, const int32_t* key_len,
                              void* out, void* stream) {
   int rc = check_attend(c, layer, n_tok, positions, nullptr, out);
@@ -579,6 +646,22 @@ int dllm_cache_attend_partial(dllm_cache* c, int layer, const int32_t* positions
                    kr);
 }
 
+int dllm_cache_attend_with_state(dllm_cache* c, int layer, const int32_t* positions, int n_tok, const void* q,
+                                 int slot_lo, int slot_hi, const float* state, void* out, void* stream) {
+  int rc = check_attend(c, layer, n_tok, positions, nullptr, out);
+  if (rc) return rc;
+  if (n_tok > 0 && (!q || !state)) return DLLM_EINVAL;
+  if (!aligned16(q) || !aligned16(state) || slot_lo < 0 || slot_hi <= slot_lo || slot_hi > c->desc.max_pos)
+    return DLLM_EINVAL;
+  if (c->desc.kv_dtype == DLLM_F32) return DLLM_EUNSUPPORTED;
+  KeyRange kr;
+  kr.lo = slot_lo;
+  kr.hi = slot_hi;
+  kr.state_in = state;
+  kr.q = q;
+  return do_attend(c, layer, positions, nullptr, n_tok, out, reinterpret_cast<cudaStream_t>(stream), kr);
+}
+
 int dllm_attend_merge(const float* state_a, const float* state_b, int batch, int n_tok, int n_heads, int head_dim,
                       void* out, float* state_out, void* stream) {
   if (!state_a || !state_b || (!out && !state_out) || batch < 1 || n_tok < 0 || n_heads < 1) return DLLM_EINVAL;
@@ -596,7 +679,7 @@ int dllm_attention_mass(dllm_cache* c, int layer, const int32_t* positions, cons
   int rc = check_attend(c, layer, n_tok, positions, view, const_cast<void*>(q));
   if (rc) return rc;
   if (!mass) return DLLM_EINVAL;
-  if (c->desc.kv_dtype != DLLM_BF16) return DLLM_EUNSUPPORTED;
+  if (c->desc.kv_dtype == DLLM_F32) return DLLM_EUNSUPPORTED;
   const dllm_cache_desc& d = c->desc;
   cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
   cudaError_t e = cudaMemsetAsync(mass, 0, (size_t)d.batch * d.max_pos * sizeof(float), s);
@@ -614,6 +697,7 @@ int dllm_attention_mass(dllm_cache* c, int layer, const int32_t* positions, cons
   a.view = view;
   a.positions = positions;
   a.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)hd));
+  a.kv_scale = layer_scale(c, layer);
   a.kv_dtype = d.kv_dtype;
   a.status = c->status;
   a.nq_pad = n_tok <= 32 ? 32 : 64;
@@ -718,7 +802,7 @@ int dllm_gather_rows(dllm_cache* c, const void* x_all, int n_pos, const int32_t*
 
 // Multi-layer refresh step: workspace layout (each part at a 256-byte boundary).
 struct ElasticWs {
-  void *x_win, *x_trk, *probe;
+  void *x_win, *x_trk;
   int32_t *pos_win, *idx;
   size_t bytes;
 };
@@ -733,8 +817,6 @@ static ElasticWs elastic_ws(const dllm_cache* c, int beta, int k, void* base) {
   off += up(B * beta * D * 2);
   w.x_trk = p ? p + off : nullptr;
   off += up(B * k * D * 2);
-  w.probe = p ? p + off : nullptr;
-  off += up(B * k * 2 * D * 2);
   w.pos_win = p ? reinterpret_cast<int32_t*>(p + off) : nullptr;
   off += up(B * beta * 4);
   w.idx = p ? reinterpret_cast<int32_t*>(p + off) : nullptr;
@@ -758,8 +840,8 @@ int dllm_elastic_step(dllm_cache* c, int n_layers, const void* const* x_all, con
   const dllm_cache_desc& d = c->desc;
   const int B = d.batch, S = d.max_pos, D = d.n_heads * d.head_dim;
   if (beta < 1 || beta > S || k < 1 || k > S - beta || S > 16384) return DLLM_EINVAL;
+  if (k > kMaxDriftRows) return DLLM_EUNSUPPORTED;
   if (d.kv_dtype == DLLM_F32 || D % kHd != 0) return DLLM_EUNSUPPORTED;
-  if (mass_out && d.kv_dtype != DLLM_BF16) return DLLM_EUNSUPPORTED;
   if (!aligned16(out) || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return DLLM_EINVAL;
   const ElasticWs ws = elastic_ws(c, beta, k, workspace);
   if (workspace_bytes < ws.bytes) return DLLM_EINVAL;
@@ -786,8 +868,12 @@ int dllm_elastic_step(dllm_cache* c, int n_layers, const void* const* x_all, con
     rc = from_cuda((cudaError_t)launch_gather_rows(x_all[l], B, S, D, win_lo, beta, ws.idx, k, ws.x_win, ws.x_trk,
                                                    ws.pos_win, c->status, s));
     if (rc) return rc;
-    // 4. window rows -> cache slots and Q; tracked rows -> probe K/V
-    StepArgs a{l, ws.x_win, w_qkv[l], ws.pos_win, nullptr, beta, out_l, ws.x_trk, ws.idx, k, ws.probe, s};
+    // 4. window rows -> cache slots and Q; tracked rows -> the drift test of this layer
+    //    (fused into the projection: cosines and refresh flags, no probe buffer)
+    StepArgs a{l, ws.x_win, w_qkv[l], ws.pos_win, nullptr, beta, out_l, ws.x_trk, ws.idx, k, nullptr, s};
+    a.drift_cos = cos + (size_t)l * B * k * 2;
+    a.drift_refresh = flags + (size_t)l * B;
+    a.drift_gamma = gamma;
     rc = do_project(c, a);
     if (rc) return rc;
     // 5. this step's attention mass (the next step's top-k input), then the attention
@@ -796,9 +882,6 @@ int dllm_elastic_step(dllm_cache* c, int n_layers, const void* const* x_all, con
       if (rc) return rc;
     }
     rc = do_attend(c, l, ws.pos_win, nullptr, beta, out_l, s);
-    if (rc) return rc;
-    // 6. drift of the tracked tokens and this layer's refresh flags
-    rc = dllm_kv_drift(c, l, ws.idx, k, ws.probe, gamma, cos + (size_t)l * B * k * 2, flags + (size_t)l * B, stream);
     if (rc) return rc;
   }
   return DLLM_OK;

@@ -16,6 +16,12 @@ struct dllm_cache {
   int sm_count;
   int pair_clusters;  // clusters of two projection CTAs resident at once (0 = none)
   int* drift_cnt;     // [batch] block arrivals of dllm_kv_drift; zero between calls
+  // Fused drift test (dllm_cache_project_drift), zero between calls: per tracked row
+  // partial sums [batch * kMaxDriftRows][2 (K,V)][3 (dot, |cache|^2, |probe|^2)], per row
+  // head arrivals [batch * kMaxDriftRows], per sequence finished rows [batch].
+  float* drift_acc;
+  int* drift_rows;
+  int* drift_seqs;
   void* kv;
   float* scale;
   bool owns_kv;
@@ -61,6 +67,7 @@ cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t s
 }
 
 constexpr int kHd = 128;         // head_dim of the tensor-core path
+constexpr int kMaxDriftRows = 256;  // tracked rows per sequence of the fused drift test
 constexpr int kQChunk = 64;      // query rows per attention work unit (tensor-core path)
 constexpr int kKeyTile = 128;    // keys per attention tile
 
@@ -99,6 +106,16 @@ struct ProjParams {
   void* raw_q;
   void* raw_kv;
   bool raw_f32;
+  // Fused drift test (else drift_acc is null): the K/V-only rows are probes, compared in
+  // the epilogue with the cached K/V at their positions instead of being stored.  The
+  // last tile to finish a row writes its cosines drift_cos[m][2] (K, V); the last row of
+  // a sequence writes drift_refresh[b] = (min cosine < drift_gamma), if not null.
+  float* drift_acc;   // [m_kv][2][3], zero on entry and on exit
+  int* drift_rows;    // [m_kv] head arrivals, zero on entry and on exit
+  int* drift_seqs;    // [batch] finished rows, zero on entry and on exit
+  float* drift_cos;
+  int32_t* drift_refresh;
+  float drift_gamma;
 };
 
 // ------------------------------------------------------------------------ attention
@@ -126,6 +143,9 @@ struct AttnParams {
   // Partial-state output instead of `out` (no key splits then):
   // fp32 [B][n_tok][H][hd + 2] = (unnormalised O, m, l), m in base-2 units.
   float* state;
+  // A cached state of the keys outside the range, same layout (no key splits then): the
+  // finish merges it with the range's and writes the normalised output to `out`.
+  const float* state_in;
   int* status;
 };
 

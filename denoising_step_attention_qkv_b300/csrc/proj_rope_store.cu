@@ -212,6 +212,89 @@ DEVI bool kv_tile_skipped(const ProjParams& p, int grp, int m0, int rows) {
   return true;
 }
 
+// ---- fused drift test ("Elastic-Cache ...", Core idea: cosine similarity between the
+// cached and the recomputed K/V of the tracked tokens; the refresh flag is set when
+// the smallest cosine of a sequence falls below gamma).
+
+// Add <cache, probe>, |cache|^2 and |probe|^2 over 32 columns of one head: probe values
+// v (fp32, after the rotation for K), cache values read from the row's slot (bf16, or
+// e4m3 codes times the group scale).
+DEVI void drift_dot32(const float (&v)[32], const void* crow, bool fp8, float scale, float& dot, float& nc,
+                      float& np) {
+  if (fp8) {
+    const uint4* src = static_cast<const uint4*>(crow);
+#pragma unroll
+    for (int i = 0; i < 2; ++i) {
+      const uint4 w = __ldg(src + i);
+      const __nv_fp8x2_storage_t* pr = reinterpret_cast<const __nv_fp8x2_storage_t*>(&w);
+#pragma unroll
+      for (int j = 0; j < 8; ++j) {
+        const float2 f = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(pr[j], __NV_E4M3)));
+        const float c0 = f.x * scale, c1 = f.y * scale;
+        const float p0 = v[16 * i + 2 * j], p1 = v[16 * i + 2 * j + 1];
+        dot = fmaf(c0, p0, fmaf(c1, p1, dot));
+        nc = fmaf(c0, c0, fmaf(c1, c1, nc));
+        np = fmaf(p0, p0, fmaf(p1, p1, np));
+      }
+    }
+  } else {
+    const uint4* src = static_cast<const uint4*>(crow);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const uint4 w = __ldg(src + i);
+      const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&w);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        const float2 f = __bfloat1622float2(pr[j]);
+        const float p0 = v[8 * i + 2 * j], p1 = v[8 * i + 2 * j + 1];
+        dot = fmaf(f.x, p0, fmaf(f.y, p1, dot));
+        nc = fmaf(f.x, f.x, fmaf(f.y, f.y, nc));
+        np = fmaf(p0, p0, fmaf(p1, p1, np));
+      }
+    }
+  }
+}
+
+// One tile's share of probe row m (the `heads` heads of K, part 0, or V, part 1, that
+// this tile covers).  The partial sums and the row's head count are device-wide
+// atomics; the contribution that completes the row (2 H heads) turns its sums into the
+// two cosines and resets them, and the row that completes its sequence (n_kv rows) sets
+// the sequence's refresh flag.  Rows with a position outside the cache still count
+// (with no sums) and get NaN cosines, which the minimum skips.
+DEVI void drift_contribute(const ProjParams& p, int m, int part, int heads, float dot, float nc, float np,
+                           bool valid) {
+  float* acc = p.drift_acc + (static_cast<size_t>(m) * 2 + part) * 3;
+  if (valid) {
+    atomicAdd(acc + 0, dot);
+    atomicAdd(acc + 1, nc);
+    atomicAdd(acc + 2, np);
+  }
+  __threadfence();
+  if (atomicAdd(p.drift_rows + m, heads) + heads != 2 * p.H) return;
+  __threadfence();
+  const int b = m / p.n_kv;
+  const int pos = p.kv_positions ? __ldg(p.kv_positions + m) : m - b * p.n_kv;
+  const bool row_ok = pos >= 0 && pos < p.max_pos;
+#pragma unroll
+  for (int q = 0; q < 2; ++q) {
+    float* a = p.drift_acc + (static_cast<size_t>(m) * 2 + q) * 3;
+    const float d = atomicExch(a, 0.0f), c = atomicExch(a + 1, 0.0f), r = atomicExch(a + 2, 0.0f);
+    const float den = sqrtf(c) * sqrtf(r);
+    p.drift_cos[static_cast<size_t>(m) * 2 + q] = !row_ok ? __int_as_float(0x7fc00000) : (den > 0.0f ? d / den : 0.0f);
+  }
+  atomicExch(p.drift_rows + m, 0);
+  __threadfence();
+  if (atomicAdd(p.drift_seqs + b, 1) + 1 != p.n_kv) return;
+  __threadfence();
+  if (p.drift_refresh != nullptr) {
+    float mn = INFINITY;
+    const float* cs = p.drift_cos + static_cast<size_t>(b) * 2 * p.n_kv;
+    for (int i = 0; i < 2 * p.n_kv; ++i) mn = fminf(mn, __ldcg(cs + i));
+    p.drift_refresh[b] = (mn < p.drift_gamma) ? 1 : 0;
+  }
+  atomicExch(p.drift_seqs + b, 0);
+}
+
 // The epilogue of one accumulator tile for this thread's row c.m0 + r: `heads` heads
 // starting at output feature c.n0, read from TMEM columns tacc ...  It rotates Q and K,
 // rounds to bf16 (or quantises each head to e4m3 with scale amax/448) and stores the
@@ -286,6 +369,34 @@ DEVI void store_rows(const ProjParams& p, const TileCoord& c, int heads, uint32_
   const int part = c.n0 / p.D;  // 0 Q, 1 K, 2 V
   const bool rope = part < 2;
   const float2* cs_row = p.rope + static_cast<size_t>(valid ? pos : 0) * (hd / 2);
+  if (c.grp == 1 && p.drift_acc != nullptr) {
+    // fused drift test: compare this probe row's K (or V) heads with the cached ones at
+    // its position; nothing is stored.  Every lane runs the TMEM loads (warp-collective),
+    // also for the rows past the last probe row, which only skip the sums and the count.
+    const bool fp8 = p.kv_dtype == DLLM_E4M3;
+    const size_t crow_i = (static_cast<size_t>(b) * p.slots + (valid ? slot : 0)) * 2 + (part - 1);
+    float dot = 0.0f, nc = 0.0f, np = 0.0f;
+#pragma unroll 1
+    for (int hh = 0; hh < heads; ++hh) {
+      const int h = (c.n0 - part * p.D) / kHd + hh;
+      const uint32_t tcol = tacc + hh * kHd;
+      const uint8_t* crow = static_cast<const uint8_t*>(p.cache_kv) + (crow_i * p.D + h * hd) * (fp8 ? 1 : 2);
+      const float sc = (fp8 && valid) ? __ldg(p.cache_scale + crow_i * p.H + h) : 1.0f;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        float lo[32], hi[32];
+        tmem_ld32(tcol + half * 32, lo);
+        tmem_ld32(tcol + 64 + half * 32, hi);
+        if (rope) rotate32(lo, hi, cs_row + half * 32);
+        if (valid) {
+          drift_dot32(lo, crow + half * 32 * (fp8 ? 1 : 2), fp8, sc, dot, nc, np);
+          drift_dot32(hi, crow + (64 + half * 32) * (fp8 ? 1 : 2), fp8, sc, dot, nc, np);
+        }
+      }
+    }
+    if (m < p.m_kv) drift_contribute(p, m, part - 1, heads, dot, nc, np, valid);
+    return;
+  }
 #pragma unroll 1
   for (int hh = 0; hh < heads; ++hh) {
     const int h = (c.n0 - part * p.D) / kHd + hh;

@@ -218,6 +218,26 @@ int dllm_cache_attend_ragged(dllm_cache* cache, int layer, const int32_t* positi
 int dllm_cache_attend_partial(dllm_cache* cache, int layer, const int32_t* positions, int n_tok, const void* q,
                               int slot_lo, int slot_hi, float* state, void* stream);
 
+/* FACache reuse in one call ("LaCache ...", Methodology 1, FACache): attention of the
+ * query rows over the slots [slot_lo, slot_hi) that changed, merged in the same kernel
+ * with a state the caller cached for all the other keys (dllm_cache_attend_partial
+ * output of an earlier call, for the same rows and the same q), written as the
+ * normalised output
+ *   out = (2^(m_r - M) O_r + 2^(m_c - M) O_c) / (2^(m_r - M) l_r + 2^(m_c - M) l_c),
+ * M = max(m_r, m_c), r = this range, c = the cached state (0 where both are empty).
+ * Only the changed slots are read: a step that rewrote a few tiles reads those tiles,
+ * not the whole cache.  The result equals the attention over both key sets when the
+ * cached state's keys and q have not changed since it was computed; the caller decides
+ * that.
+ *
+ *   q         bf16 [batch][n_tok][D]: rotated Q (not modified)
+ *   state     fp32 [batch][n_tok][n_heads][head_dim + 2], 16-byte aligned: the cached state
+ *   out       bf16 [batch][n_tok][D] out; must not alias q or state
+ *   0 <= slot_lo < slot_hi <= max_pos (regular slots; no Flash-Verify views)
+ * DLLM_BF16 and DLLM_E4M3 caches (DLLM_EUNSUPPORTED for DLLM_F32). */
+int dllm_cache_attend_with_state(dllm_cache* cache, int layer, const int32_t* positions, int n_tok, const void* q,
+                                 int slot_lo, int slot_hi, const float* state, void* out, void* stream);
+
 /* Combine two partial states of the same rows (the key ranges must not overlap):
  *   M = max(m_a, m_b), w_a = 2^(m_a - M), w_b = 2^(m_b - M),
  *   O = w_a O_a + w_b O_b, l = w_a l_a + w_b l_b,
@@ -240,9 +260,10 @@ int dllm_attend_merge(const float* state_a, const float* state_b, int batch, int
  *   q         bf16 [batch][n_tok][D]: the rotated Q that dllm_cache_project leaves in its
  *             `out` (call this before dllm_cache_attend overwrites it)
  *   mass      fp32 [batch][max_pos] out (zeroed and filled by the call)
- * Other arguments as for dllm_cache_attend.  DLLM_BF16 caches only (else
- * DLLM_EUNSUPPORTED).  Reads the layer's K twice per (sequence, head) unit; the second
- * read mostly hits L2. */
+ * Other arguments as for dllm_cache_attend.  DLLM_BF16 and DLLM_E4M3 caches (an e4m3
+ * key is its codes times its group scale, as in the attention); DLLM_EUNSUPPORTED for
+ * DLLM_F32.  Reads the layer's K twice per (sequence, head) unit; the second read
+ * mostly hits L2. */
 int dllm_attention_mass(dllm_cache* cache, int layer, const int32_t* positions, const uint8_t* view, int n_tok,
                         const void* q, float* mass, void* stream);
 
@@ -311,6 +332,37 @@ int dllm_gather_rows(dllm_cache* cache, const void* x_all, int n_pos, const int3
 int dllm_kv_drift(const dllm_cache* cache, int layer, const int32_t* idx, int k,
                   const void* probe_kv, float gamma, float* cos, int32_t* refresh, void* stream);
 
+/* The projection half with the drift test fused into it ("Elastic-Cache", Core idea and
+ * Algorithm knobs; "Flash-dLLM ...", paragraph 4).  Same effects as
+ *   dllm_cache_project(cache, layer, x, w_qkv, positions, view, n_tok, out,
+ *                      kv_x, idx, k, probe, stream)
+ *   dllm_kv_drift(cache, layer, idx, k, probe, gamma, cos, refresh, stream)
+ * without the probe buffer: the projection's epilogue compares each tracked token's
+ * recomputed K and V (fp32, before any rounding) with the cached ones at its position
+ * and writes only the cosines and the flags, so the probe K/V never go to HBM.
+ *
+ *   kv_x      act [batch][k][D]: this step's hidden states of the tracked tokens
+ *   idx       int32 [batch][k]: their positions, which are also the compared slots; they
+ *             must not be slots that this call's query rows write (dllm_kv_topk leaves
+ *             the active block out), else a cosine may see either the old or the new K/V
+ *   k         tracked tokens per sequence, 1 <= k <= 256 (DLLM_EUNSUPPORTED above)
+ *   gamma, cos, refresh   as for dllm_kv_drift
+ * Other arguments as for dllm_cache_project.  DLLM_BF16 and DLLM_E4M3 caches
+ * (DLLM_EUNSUPPORTED for DLLM_F32).  A position outside [0, max_pos) gives NaN cosines
+ * for that token (the flag's minimum skips them) and sets DLLM_DEV_BAD_POSITION.  Uses
+ * a small workspace of the cache, so calls on one cache must be ordered. */
+int dllm_cache_project_drift(dllm_cache* cache, int layer, const void* x, const void* w_qkv,
+                             const int32_t* positions, const uint8_t* view, int n_tok, void* out,
+                             const void* kv_x, const int32_t* idx, int k, float gamma,
+                             float* cos, int32_t* refresh, void* stream);
+
+/* dllm_cache_project_drift followed by dllm_cache_attend on the same stream: one
+ * denoising step of one layer with the drift test of its tracked tokens. */
+int dllm_cache_step_drift(dllm_cache* cache, int layer, const void* x, const void* w_qkv,
+                          const int32_t* positions, const uint8_t* view, int n_tok, void* out,
+                          const void* kv_x, const int32_t* idx, int k, float gamma,
+                          float* cos, int32_t* refresh, void* stream);
+
 /* One denoising step over layers 0 .. n_layers-1 of the cache with the depth-wise
  * refresh of "Elastic-Cache ..." (Core idea: when the drift test of the most-attended
  * tokens fails at layer l, the layers after l are recomputed, shallow layers keep their
@@ -322,11 +374,11 @@ int dllm_kv_drift(const dllm_cache* cache, int layer, const int32_t* idx, int k,
  *   2. idx = the k most-attended positions of mass[l] outside the window (dllm_kv_topk);
  *   3. the window rows win_lo[b] .. win_lo[b]+beta-1 of x_all[l] are projected (Q, K, V)
  *      and their K/V written to their slots; the tracked rows x_all[l][b][idx] are
- *      projected to probe K/V (dllm_cache_project);
+ *      projected and compared with their cached K/V: the drift test -> cos[l],
+ *      flags[l] (dllm_cache_project_drift);
  *   4. (mass_out != NULL) the window's attention mass per slot -> mass_out[l]
  *      (dllm_attention_mass), the next step's mass input;
- *   5. the window attends over the cache -> out[l] (dllm_cache_attend);
- *   6. the drift test of the tracked tokens -> cos[l], flags[l] (dllm_kv_drift).
+ *   5. the window attends over the cache -> out[l] (dllm_cache_attend).
  * A layer whose own test fails is not recomputed in this step; the layers after it are.
  *
  *   x_all       host array of n_layers device pointers, each bf16 [batch][max_pos][D]:
@@ -336,12 +388,12 @@ int dllm_kv_drift(const dllm_cache* cache, int layer, const int32_t* idx, int k,
  *               0 <= win_lo[b] <= max_pos - beta (else the window's rows are zero and
  *               DLLM_DEV_BAD_POSITION is raised)
  *   mass        fp32 [n_layers][batch][max_pos] device: previous step's attention mass
- *   k, gamma    tracked tokens per sequence (1 <= k <= max_pos - beta), drift threshold
+ *   k, gamma    tracked tokens per sequence (1 <= k <= max_pos - beta, k <= 256), drift
+ *               threshold
  *   out         bf16 [n_layers][batch][beta][D] device out: attention output per layer
  *   cos         fp32 [n_layers][batch][k][2] device out
  *   flags       int32 [n_layers][batch] device out: the drift test's refresh flags
- *   mass_out    fp32 [n_layers][batch][max_pos] device out, or NULL (DLLM_BF16 caches
- *               only, else DLLM_EUNSUPPORTED)
+ *   mass_out    fp32 [n_layers][batch][max_pos] device out, or NULL
  *   workspace   device, 256-byte aligned, >= dllm_elastic_workspace_bytes(cache, beta, k)
  * Uses the cache's own workspaces: calls on one cache must be ordered.  DLLM_F32 caches:
  * DLLM_EUNSUPPORTED.  max_pos <= 16384. */

@@ -303,6 +303,7 @@ def check_sequences(wl: W.Workload, cache: capi.Cache, out: np.ndarray, seqs, pr
     of the sequences ``seqs``: cache K/V at written slots, the attention output and the
     probes against the oracle of that sequence (unquantised; for an e4m3 cache also the
     codes, and the output against the oracle's model of the encoding at the bf16 bound).
+    Returns (largest error, {sequence: oracle_seq result}) for the callers' further checks.
 
     ``whole_output``: the output of every sequence is compared with the oracle's as one
     tensor, i.e. against max|oracle| over the workload's whole output, which is how the
@@ -313,11 +314,16 @@ def check_sequences(wl: W.Workload, cache: capi.Cache, out: np.ndarray, seqs, pr
     tol = TOL[s.kv]
     fp8 = s.kv == "e4m3"
     errs = []
+    oracles = {}  # the oracle of each sequence, computed once
     if whole_output:
-        o_all = np.stack([oracle_seq(wl, b, probe_idx)[0] for b in range(s.batch)])
+        for b in range(s.batch):
+            oracles[b] = oracle_seq(wl, b, probe_idx)
+        o_all = np.stack([oracles[b][0] for b in range(s.batch)])
         errs.append(assert_close(out, o_all, tol, "out (every sequence and head, one tensor)"))
     for b in seqs:
-        o, oc, pr = oracle_seq(wl, b, probe_idx)
+        if b not in oracles:
+            oracles[b] = oracle_seq(wl, b, probe_idx)
+        o, oc, pr = oracles[b]
         written = oc.written[0]
         kv = cache.kv(0)[b]
         if fp8:
@@ -337,4 +343,4 @@ def check_sequences(wl: W.Workload, cache: capi.Cache, out: np.ndarray, seqs, pr
             assert_close(out[b], om, FP8_MODEL_TOL, f"out vs the e4m3 model (b={b}, all heads)")
         if pr is not None:
             errs.append(assert_close(probe_gpu[b], pr, TOL[s.act], f"probe K/V (b={b}, all heads)"))
-    return max(errs)
+    return max(errs), oracles

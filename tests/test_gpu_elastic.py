@@ -24,7 +24,7 @@ def _sigma(B):
 
 CASES = [
     ("bf16", dict(batch=4, d_model=256, max_pos=384), True),
-    ("e4m3", dict(batch=4, d_model=256, max_pos=384, kv="e4m3"), False),
+    ("e4m3", dict(batch=4, d_model=256, max_pos=384, kv="e4m3"), True),
     # enough refresh tiles for the CTA-pair projection kernel
     ("bf16-pairs", dict(batch=8, d_model=1024, max_pos=512), True),
 ]
@@ -90,7 +90,7 @@ def test_elastic_step_matches_oracle(name, kw, with_mass):
                 exact = np.stack([caches[l].K, caches[l].V], axis=2)
                 G.fp8_code_check(codes[:, :S], scales[:, :S], exact, f"cache layer {l} e4m3 codes")
             if with_mass:
-                G.assert_close(mass_out[l].double().cpu().numpy(), o_mass[l], G.TOL["bf16"],
+                G.assert_close(mass_out[l].double().cpu().numpy(), o_mass[l], min(tol, G.TOL["bf16"]),
                                f"mass layer {l} ({name}) vs {ref}")
 
 

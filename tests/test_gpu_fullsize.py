@@ -45,7 +45,7 @@ def test_config3_batch32_drift_fullsize():
     out, probe = G.run_gpu(wl, cache, probe_idx=idx_np)
     seqs = _round_seqs(wl, wl.x.shape[1])
     assert len(seqs) == 3
-    G.check_sequences(wl, cache, out, seqs, probe_gpu=probe, probe_idx=idx_np)
+    _, oracles = G.check_sequences(wl, cache, out, seqs, probe_gpu=probe, probe_idx=idx_np)
     # drift of the same sequences (the cosine spans all heads of a token)
     cos = torch.empty((wl.shape.batch, wl.drift_k, 2), dtype=torch.float32, device="cuda")
     refresh = torch.empty(wl.shape.batch, dtype=torch.int32, device="cuda")
@@ -53,12 +53,29 @@ def test_config3_batch32_drift_fullsize():
     capi.dllm_kv_drift(cache.handle, 0, idx, pk, wl.gamma, cos, refresh)
     g_cos = cos.double().cpu().numpy()
     g_ref = refresh.cpu().numpy()
+    o_coss = {}
     for b in seqs:
-        _, oc, pr = G.oracle_seq(wl, b, idx_np)
-        o_cos = O.kv_drift(oc, idx_np[b:b + 1], pr[None])[0]
-        G.assert_close(g_cos[b], o_cos, G.TOL["bf16"], f"drift cos b={b}")
+        _, oc, pr = oracles[b]
+        o_coss[b] = O.kv_drift(oc, idx_np[b:b + 1], pr[None])[0]
+        G.assert_close(g_cos[b], o_coss[b], G.TOL["bf16"], f"drift cos b={b}")
         assert g_ref[b] == int(g_cos[b].min() < np.float32(wl.gamma))
     assert set(np.unique(g_ref)) <= {0, 1}
+    # the drift test fused into the projection (the bench's step): same tracked rows, the
+    # same cache afterwards, cosines against the oracle and flags from its own cosines
+    fcos = torch.full_like(cos, 7.0)
+    fref = torch.full_like(refresh, 7)
+    w = G.tdev(wl.w, "bf16")
+    out2 = torch.empty((wl.shape.batch, wl.x.shape[1], wl.shape.D), dtype=torch.bfloat16, device="cuda")
+    capi.dllm_cache_step_drift(cache.handle, 0, G.tdev(wl.x, "bf16"), w, G.idev(wl.positions), None, out2,
+                               G.tdev(wl.probe_rows(idx_np), "bf16"), idx, wl.gamma, fcos, fref)
+    torch.cuda.synchronize()
+    assert cache.status() == (capi.DLLM_OK, 0)
+    f_cos = fcos.double().cpu().numpy()
+    for b in seqs:
+        G.assert_close(f_cos[b], o_coss[b], G.TOL["bf16"], f"fused drift cos b={b}")
+    np.testing.assert_array_equal(fref.cpu().numpy(), (fcos.cpu().numpy().reshape(wl.shape.batch, -1).min(1)
+                                                        < np.float32(wl.gamma)).astype(np.int32))
+    np.testing.assert_array_equal(out2.double().cpu().numpy(), out)  # same step, same output
 
 
 def test_config4_verify_fullsize():

@@ -34,9 +34,12 @@ def _gpu_mass(wl, cache):
     return mass.double().cpu().numpy(), out.double().cpu().numpy()
 
 
-def _oracle_mass(wl):
+def _oracle_mass(wl, model_fp8=False):
+    """The oracle's mass over its unquantised cache, or over its model of the e4m3
+    encoding (model_fp8)."""
     s = wl.shape
-    cache = O.OracleCache(s.batch, s.max_pos, s.tail_slots, s.n_heads, s.head_dim)
+    kv = "e4m3" if (s.kv == "e4m3" and model_fp8) else "exact"
+    cache = O.OracleCache(s.batch, s.max_pos, s.tail_slots, s.n_heads, s.head_dim, kv=kv)
     if wl.pre_x is not None:
         O.write_rows(cache, wl.w, wl.pre_x, wl.pre_pos, s.rope_theta)
     slots = np.stack([O.row_slots(wl.positions[b], None if wl.view is None else wl.view[b], s.max_pos)
@@ -50,6 +53,11 @@ CASES = [
     ("two-chunks", "llada8b-b1", dict(batch=2, d_model=256, head_dim=128, max_pos=400, block=100, gen_lo=200, fixed_lo=None)),
     ("verify", "llada8b-b16-verify", dict(batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200, search=6,
                        tail_slots=8)),
+    # e4m3 caches: codes times group scales (32 and 48 query columns)
+    ("e4m3", "llada8b-b1", dict(batch=3, d_model=512, head_dim=128, max_pos=300, block=40, gen_lo=200, fixed_lo=None,
+                                kv="e4m3")),
+    ("e4m3-verify", "llada8b-b16-verify", dict(batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200,
+                                               search=6, tail_slots=8, kv="e4m3")),
 ]
 
 
@@ -58,7 +66,10 @@ def test_mass_matches_oracle(name, workload, kw):
     wl = W.make(workload, **kw)
     cache = G.make_cache(wl)
     mass, _ = _gpu_mass(wl, cache)
-    G.assert_close(mass, _oracle_mass(wl), G.TOL["bf16"], f"attention mass ({name})")
+    G.assert_close(mass, _oracle_mass(wl), G.TOL[wl.shape.kv], f"attention mass ({name})")
+    if wl.shape.kv == "e4m3":
+        G.assert_close(mass, _oracle_mass(wl, model_fp8=True), G.FP8_MODEL_TOL,
+                       f"attention mass vs the e4m3 model ({name})")
 
 
 def test_mass_fullsize_sampled_sequences():

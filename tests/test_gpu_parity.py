@@ -231,3 +231,79 @@ def test_gather_rows_bit_exact(kv):
     assert torch.count_nonzero(rows[1, 5]) == 0
     rows[1, 5] = ref[1, 5]
     assert torch.equal(rows, ref)
+
+
+# --------------------------------------------------------- drift fused into the projection
+FUSED_DRIFT = [
+    ("bf16", dict(d_model=512, head_dim=128, kv="bf16"), 24),
+    ("e4m3", dict(d_model=512, head_dim=128, kv="e4m3"), 24),
+    # 40 sequences x 37 tracked rows: 1480 probe rows over several 256-row tiles of the
+    # CTA-pair projection (enough tiles at d_model 1024), a sequence's rows straddling two
+    ("bf16-many", dict(batch=40, d_model=1024, head_dim=128, kv="bf16"), 37),
+]
+
+
+@pytest.mark.parametrize("name,kw,k", FUSED_DRIFT, ids=[c[0] for c in FUSED_DRIFT])
+def test_fused_drift_matches_oracle(name, kw, k):
+    kw = dict(kw)
+    B = kw.pop("batch", 5)
+    wl = W.make("llada8b-b32-drift", batch=B, max_pos=300, block=16, gen_lo=200, drift_k=k, **kw)
+    s = wl.shape
+    idx = _topk_gpu(wl)
+    cache = G.make_cache(wl)
+    w = G.tdev(wl.w, s.act)
+    capi.dllm_cache_step(cache.handle, 0, None, w, None, None, None,
+                         kv_x=G.tdev(wl.pre_x, s.act), kv_positions=G.idev(wl.pre_pos))
+    x = G.tdev(wl.x, s.act)
+    pos = G.idev(wl.positions)
+    out = torch.empty_like(x)
+    cos = torch.full((B, k, 2), 7.0, dtype=torch.float32, device="cuda")
+    refresh = torch.full((B,), 7, dtype=torch.int32, device="cuda")
+    xp = G.tdev(wl.probe_rows(idx), s.act)
+    o_out, ocache, o_probe = G.run_oracle(wl, probe_idx=idx)
+    o_cos = O.kv_drift(ocache, idx, o_probe)
+    for call in range(2):  # the workspace's counters and sums reset themselves
+        capi.dllm_cache_step_drift(cache.handle, 0, x, w, pos, None, out, xp, G.idev(idx), 0.9, cos, refresh)
+        torch.cuda.synchronize()
+        assert cache.status() == (capi.DLLM_OK, 0)
+        G.assert_close(out.double().cpu().numpy(), o_out, G.TOL[s.kv], f"attention out, call {call} ({name})")
+        g_cos = cos.double().cpu().numpy()
+        G.assert_close(g_cos, o_cos, G.TOL[s.kv], f"fused drift cos, call {call} ({name})")
+        if s.kv == "e4m3":
+            mcache = G.run_oracle(wl, probe_idx=idx, model_fp8=True)[1]
+            G.assert_close(g_cos, O.kv_drift(mcache, idx, o_probe), G.FP8_MODEL_TOL,
+                           f"fused drift cos vs the e4m3 model ({name})")
+        np.testing.assert_array_equal(refresh.cpu().numpy(),
+                                      (cos.cpu().numpy().reshape(B, -1).min(1) < np.float32(0.9)).astype(np.int32))
+    G.compare_cache(cache, ocache, G.TOL[s.kv])  # probes never reach the cache
+
+
+def test_fused_drift_bad_position_gives_nan_and_status():
+    wl = W.make("llada8b-b32-drift", batch=3, d_model=256, head_dim=128, max_pos=300, block=16, gen_lo=200, drift_k=8)
+    s = wl.shape
+    idx = _topk_gpu(wl)
+    cache = G.make_cache(wl, canary=False)
+    w = G.tdev(wl.w, s.act)
+    capi.dllm_cache_step(cache.handle, 0, None, w, None, None, None,
+                         kv_x=G.tdev(wl.pre_x, s.act), kv_positions=G.idev(wl.pre_pos))
+    xp = G.tdev(wl.probe_rows(idx), s.act)
+    bad = idx.copy()
+    bad[1, 2] = s.max_pos + 5
+    cos = torch.empty((3, 8, 2), dtype=torch.float32, device="cuda")
+    refresh = torch.empty(3, dtype=torch.int32, device="cuda")
+    capi.dllm_cache_project_drift(cache.handle, 0, None, w, None, None, None, xp, G.idev(bad), 0.9, cos, refresh)
+    rc, bits = cache.status()
+    assert rc == capi.DLLM_EDEVICE and bits == capi.DEV_BAD_POSITION
+    c = cos.cpu().numpy()
+    assert np.isnan(c[1, 2]).all() and np.isfinite(np.delete(c.reshape(-1, 2), 1 * 8 + 2, axis=0)).all()
+    # the next call with good indices is unaffected (every counter was reset)
+    capi.dllm_cache_project_drift(cache.handle, 0, None, w, None, None, None, xp, G.idev(idx), 0.9, cos, refresh)
+    assert cache.status() == (capi.DLLM_OK, 0)
+    ref = torch.empty_like(cos)
+    probe = torch.empty((3, 8, 2, s.D), dtype=torch.bfloat16, device="cuda")
+    capi.dllm_cache_project(cache.handle, 0, None, w, None, None, None, kv_x=xp, kv_positions=G.idev(idx),
+                            probe_kv=probe)
+    capi.dllm_kv_drift(cache.handle, 0, G.idev(idx), probe, 0.9, ref)
+    torch.cuda.synchronize()
+    # the separate path rounds the probes to bf16 first: cosines agree to that rounding
+    assert float((cos - ref).abs().max()) < 2e-3

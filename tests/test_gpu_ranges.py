@@ -133,3 +133,41 @@ def test_partial_states_and_merge(kv):
         g = st_ab.double().cpu().numpy()
         G.assert_close(g[..., :s.head_dim] / g[..., s.head_dim + 1:], full_ref.reshape(g[..., :s.head_dim].shape),
                        tol, f"merged state vs {ref_name}")
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_facache_reuse_after_a_step_rewrites_the_tail(kv):
+    # An invariant query block (q fixed) over a cache whose slots [lo, max_pos) are
+    # rewritten by the next step: the state of [0, lo) is cached once, and after the
+    # rewrite one call attends over [lo, max_pos) only and merges the cached state.
+    wl = W.make("llada8b-b1", batch=3, d_model=512, head_dim=128, max_pos=600, block=40, gen_lo=300, fixed_lo=None, kv=kv)
+    s = wl.shape
+    cache, pos, q = _staged(wl)
+    n = wl.x.shape[1]
+    lo = 300  # not a tile boundary; the block sits in the rewritten range
+    st_c = torch.empty((s.batch, n, s.n_heads, s.head_dim + 2), dtype=torch.float32, device="cuda")
+    capi.dllm_cache_attend_partial(cache.handle, 0, pos, q, 0, lo, st_c)
+    # the step rewrites every slot of [lo, max_pos) with new hidden states
+    rng = np.random.default_rng(7)
+    tail = np.arange(lo, s.max_pos, dtype=np.int32)
+    x_new = W.round_bf16(rng.standard_normal((s.batch, len(tail), s.D)).astype(np.float32))
+    w = G.tdev(wl.w, s.act)
+    capi.dllm_cache_step(cache.handle, 0, None, w, None, None, None, kv_x=G.tdev(x_new, s.act),
+                         kv_positions=G.idev(np.tile(tail, (s.batch, 1))))
+    out = torch.full_like(q, float("nan"))
+    q_before = q.clone()
+    capi.dllm_cache_attend_with_state(cache.handle, 0, pos, q, lo, s.max_pos, st_c, out)
+    full = q.clone()
+    capi.dllm_cache_attend(cache.handle, 0, pos, None, full)  # one pass over the updated cache
+    torch.cuda.synchronize()
+    assert cache.status() == (capi.DLLM_OK, 0)
+    assert torch.equal(q, q_before)
+    got = out.double().cpu().numpy()
+    # oracle: the same q over the updated cache, every slot
+    for ref_name, model_fp8, tol in [("oracle", False, G.TOL[kv])] + (
+            [("e4m3 model", True, G.FP8_MODEL_TOL)] if kv == "e4m3" else []):
+        ocache, oq = _oracle(wl, model_fp8)
+        O.write_rows(ocache, wl.w, x_new, np.tile(tail, (s.batch, 1)), s.rope_theta)
+        ref = np.stack([O.attention(oq[b], ocache.K[b], ocache.V[b]).reshape(n, -1) for b in range(s.batch)])
+        G.assert_close(got, ref, tol, f"FACache reuse vs {ref_name} ({kv})")
+    G.assert_close(got, full.double().cpu().numpy(), G.TOL["bf16"], f"FACache reuse vs one pass ({kv})")
