@@ -9,9 +9,11 @@
 // Design (sm_103a).  A work unit is (sequence b, head h, chunk of <= NQ query rows,
 // key split) and is processed by one persistent CTA.  Per 128-key tile the MMA warp
 // computes S^T = K Q^T with tcgen05 (M = 128 keys, N = NQ queries, K = hd = 128) into
-// TMEM, so a softmax thread owns one key and holds that key's scores for every query;
-// per-query maxima and sums are warp reduce-scatters plus a 4-warp exchange in shared
-// memory, and the online softmax runs in fp32 with exp2.  The thread writes its key's
+// TMEM, so a softmax thread owns one key and holds that key's scores for the queries
+// of its warpgroup (with e4m3 caches and with 48 query columns two softmax warpgroups
+// split the columns in halves and run independently); per-query maxima and sums are
+// warp reductions plus a 4-warp exchange in shared memory, and the online softmax runs
+// in fp32 with exp2.  The thread writes its key's
 // probabilities as bf16 into P^T (K-major, 128-byte swizzle) and the MMA warp computes
 // O^T = V^T P^T (M = hd, N = NQ, V read MN-major straight from the TMA-staged cache
 // tile) into TMEM, which the same threads fold into fp32 register accumulators.
@@ -27,14 +29,16 @@
 //
 // FP8-e4m3 cache ("LaCache ...", Methodology 2: per-group FP8; one group here = one
 // head of one token, K or V, with an fp32 scale): TMA stages the e4m3 tiles (half the
-// bytes of bf16) in a 2-deep ring and four converter warps turn them into the MMA
-// operand layout as f16 (one conversion per pair of codes).  K keeps the bare code,
-// exact in f16: a key's K scale is constant along its row of the score tile, so the
-// softmax folds it into that row's logit scale (in fp32).  V is the code times the
-// group's scale (one f16 multiply per pair), a single f16 rounding of relative size
-// 2^-11, far below the e4m3 step of 2^-4.  The MMAs of this path take f16 throughout:
-// the converters also turn each unit's Q chunk from bf16 to f16 in place, and the
-// softmax writes P as f16.
+// bytes of bf16) in a 3-deep ring (2 with 64 queries).  The staged K codes are the A
+// operand of an 8-bit S MMA (kind::f8f6f4) as they are: a key's K scale is constant
+// along its row of the score tile, so the softmax folds it into that row's logit scale
+// (in fp32).  The B operand is the unit's Q chunk as two e4m3 parts, Q_hi = e4m3(s q)
+// and Q_lo = e4m3(s q - Q_hi), with one scale s per chunk that takes its largest |q| to
+// 448: two MMAs give K (Q_hi + Q_lo)^T, within about 2^-9 of K (s Q)^T per term, as
+// close as bf16's rounding of Q; 1/s joins the logit scale.  Four converter warps split
+// Q once per unit and turn each V tile into an f16 operand, code times the group's
+// scale (one f16 multiply per pair, a single f16 rounding of relative size 2^-11, far
+// below the e4m3 step of 2^-4); the softmax writes P as f16 for the f16 P V MMA.
 #include <cuda_bf16.h>
 #include <cuda_fp8.h>
 
@@ -57,12 +61,16 @@ struct Cfg {
   // K operand ring 1 deep with 32 queries (measured best of the splits that fit); with
   // 64 queries only the staging ring is doubled
   static constexpr int KST = FP8 ? 1 : (NQ <= 48 ? 3 : 2);
+  static constexpr uint32_t kKBytes = FP8 ? 1024 : kTileBytes;  // e4m3: the K codes feed the MMA from staging
   static constexpr int VST = FP8 ? (NQ == 32 ? 2 : 1) : 2;
-  static constexpr int SST = FP8 ? 2 : 1;
+  static constexpr int SST = FP8 ? (NQ == 64 ? 2 : 3) : 1;
   static constexpr uint32_t kStageBytes = FP8 ? kTile8Bytes : 1024;
   static constexpr uint32_t kQBytes = NQ * kHd * 2;       // one Q chunk (two 64-column boxes)
   static constexpr uint32_t kPBytes = NQ * kKeyTile * 2;  // one P^T tile (two 64-key halves)
-  static constexpr int kThreads = 64 + 128 + (FP8 ? 128 : 0);
+  // softmax warpgroups, each owning NQ / kSmWG query columns: two where the softmax's
+  // per-tile chain bounds the kernel (e4m3 caches, 48 columns), one where HBM does
+  static constexpr int kSmWG = (FP8 || NQ == 48) ? 2 : 1;
+  static constexpr int kThreads = 64 + 128 * kSmWG + (FP8 ? 128 : 0);  // TMA + MMA, softmax, converters
 };
 
 template <int NQ, bool FP8>
@@ -70,9 +78,10 @@ struct Smem {
   using C = Cfg<NQ, FP8>;
   // all operand tiles 1024-byte aligned
   uint8_t q[2][C::kQBytes];
-  uint8_t k[C::KST][kTileBytes];
+  uint8_t k[C::KST][C::kKBytes];
   uint8_t v[C::VST][kTileBytes];
   uint8_t p[2][C::kPBytes];
+  uint8_t q8[2][2][FP8 ? NQ * 128 : 1024];  // e4m3: per Q buffer, the high and low e4m3 parts of Q
   uint8_t sk[C::SST][C::kStageBytes];  // e4m3 staging (FP8 only)
   uint8_t sv[C::SST][C::kStageBytes];
   float red[4][NQ];  // per-warp column maxima (per tile) / partial sums (per unit)
@@ -88,6 +97,8 @@ struct Smem {
   int seq_order[kMaxOrder];  // ragged batches: sequences by key length, longest first
   uint32_t draft_qmask[2];
   int n_draft;
+  float q8inv[2];       // e4m3: per Q buffer, 1 / the scale that took the chunk's max |q| to 448
+  float cv_red[2][4];   // e4m3: per Q buffer, the converter warps' max |q|
   uint64_t q_full[2], q_empty[2];
   uint64_t q_conv[2];  // e4m3 caches: the Q chunk has been converted to f16 in place
   uint64_t k_full[C::KST], k_empty[C::KST];
@@ -120,31 +131,6 @@ DEVI void dequant16_f16(const uint4 in, __half2 scale, uint4& lo, uint4& hi) {
   }
   lo = make_uint4(w[0], w[1], w[2], w[3]);
   hi = make_uint4(w[4], w[5], w[6], w[7]);
-}
-
-// 16 e4m3 codes to f16, unscaled (exact: every e4m3 value is an f16 value).
-DEVI void cvt16_f16(const uint4 in, uint4& lo, uint4& hi) {
-  const __nv_fp8x2_storage_t* pr = reinterpret_cast<const __nv_fp8x2_storage_t*>(&in);
-  uint32_t w[8];
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    const __half2 h = __half2(__nv_cvt_fp8x2_to_halfraw2(pr[i], __NV_E4M3));
-    w[i] = *reinterpret_cast<const uint32_t*>(&h);
-  }
-  lo = make_uint4(w[0], w[1], w[2], w[3]);
-  hi = make_uint4(w[4], w[5], w[6], w[7]);
-}
-
-// bf16 -> f16 of 8 values in place (a Q chunk of the e4m3 path).
-DEVI uint4 bf16x8_to_f16x8(uint4 v) {
-  uint32_t* w = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    const float lo = __uint_as_float(w[i] << 16), hi = __uint_as_float(w[i] & 0xffff0000u);
-    const __half2 h = __floats2half2_rn(lo, hi);
-    w[i] = *reinterpret_cast<const uint32_t*>(&h);
-  }
-  return v;
 }
 
 struct Unit {
@@ -187,8 +173,6 @@ DEVI int key_end(const AttnParams& p, int b) {
   return min(p.key_hi, len);
 }
 
-// Barrier among the four softmax warps.
-DEVI void softmax_sync() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
 // Maximum of v over the 32 lanes of the warp, in every lane.
 DEVI float warp_max(float v) {
@@ -222,13 +206,14 @@ DEVI void st_bf16_pair(uint32_t pa, uint32_t pb, float a, float b) {
       : "memory");
 }
 
-// Reduce 32 per-lane values per column across the warp; afterwards lane i holds the
-// reduction of column i.  MAX selects max, otherwise sum.  Each step halves the columns
-// a lane keeps and exchanges the other half with the lane whose id differs in that bit.
-template <bool MAX>
-DEVI float reduce_scatter32(float* v, int lane) {
+// Reduce 32 per-lane values per column, for C columns (C = 8, 16 or 32), across the
+// warp; afterwards lane i holds the reduction of column i % C.  Each step halves the
+// columns a lane keeps and exchanges the other half with the lane whose id differs in
+// that bit; the lanes that then hold the same column add theirs.
+template <bool MAX, int C>
+DEVI float reduce_scatter(float* v, int lane) {
 #pragma unroll
-  for (int w = 16; w >= 1; w >>= 1) {
+  for (int w = C / 2; w >= 1; w >>= 1) {
     const bool upper = (lane & w) != 0;
 #pragma unroll
     for (int i = 0; i < w; ++i) {
@@ -238,37 +223,48 @@ DEVI float reduce_scatter32(float* v, int lane) {
       v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
     }
   }
-  return v[0];
-}
-
-// The same for 16 columns: afterwards lanes i and i + 16 hold the reduction of column i.
-template <bool MAX>
-DEVI float reduce_scatter16(float* v, int lane) {
+  float r = v[0];
 #pragma unroll
-  for (int w = 8; w >= 1; w >>= 1) {
-    const bool upper = (lane & w) != 0;
-#pragma unroll
-    for (int i = 0; i < w; ++i) {
-      const float send = upper ? v[i] : v[i + w];
-      const float keep = upper ? v[i + w] : v[i];
-      const float recv = __shfl_xor_sync(0xffffffffu, send, w);
-      v[i] = MAX ? fmaxf(keep, recv) : keep + recv;
-    }
+  for (int w = C; w < 32; w <<= 1) {
+    const float o = __shfl_xor_sync(0xffffffffu, r, w);
+    r = MAX ? fmaxf(r, o) : r + o;
   }
-  const float other = __shfl_xor_sync(0xffffffffu, v[0], 16);
-  return MAX ? fmaxf(v[0], other) : v[0] + other;
+  return r;
 }
 
-// Load NQ TMEM columns of this warp's lanes in chunks of 32 (of 16 when NQ is not a
-// multiple of 32).
-template <int NQ>
-DEVI void tmem_ld_cols(uint32_t taddr, float (&v)[NQ]) {
-  if constexpr (NQ % 32 == 0) {
+// Column sums of QH per-lane values over the warp, written to dst[0 .. QH) (QH = 16, 24,
+// 32 or 64); clobbers l.
+template <int QH>
+DEVI void reduce_cols(float (&l)[QH], float* dst, int lane) {
+  if constexpr (QH % 32 == 0) {
 #pragma unroll
-    for (int c = 0; c < NQ; c += 32) tmem_ld32(taddr + c, *reinterpret_cast<float(*)[32]>(v + c));
+    for (int c = 0; c < QH; c += 32) dst[c + lane] = reduce_scatter<false, 32>(l + c, lane);
+  } else if constexpr (QH == 16) {
+    const float v = reduce_scatter<false, 16>(l, lane);
+    if (lane < 16) dst[lane] = v;
   } else {
+    static_assert(QH == 24, "query columns per warpgroup");
+    const float v = reduce_scatter<false, 16>(l, lane);
+    if (lane < 16) dst[lane] = v;
+    const float v8 = reduce_scatter<false, 8>(l + 16, lane);
+    if (lane < 8) dst[16 + lane] = v8;
+  }
+}
+
+// Load N TMEM columns of this warp's lanes in chunks of 32 (of 16, or of 8 when N is not
+// a multiple of 16), each chunk starting at a multiple of its width.
+template <int N>
+DEVI void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
+  if constexpr (N % 32 == 0) {
 #pragma unroll
-    for (int c = 0; c < NQ; c += 16) tmem_ld16(taddr + c, *reinterpret_cast<float(*)[16]>(v + c));
+    for (int c = 0; c < N; c += 32) tmem_ld32(taddr + c, *reinterpret_cast<float(*)[32]>(v + c));
+  } else if constexpr (N % 16 == 0) {
+#pragma unroll
+    for (int c = 0; c < N; c += 16) tmem_ld16(taddr + c, *reinterpret_cast<float(*)[16]>(v + c));
+  } else {
+    static_assert(N % 8 == 0, "TMEM column chunks");
+#pragma unroll
+    for (int c = 0; c < N; c += 8) tmem_ld8(taddr + c, *reinterpret_cast<float(*)[8]>(v + c));
   }
 }
 
@@ -278,6 +274,8 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
                   const AttnParams p) {
   using C = Cfg<NQ, FP8>;
   constexpr int KST = C::KST, VST = C::VST, SST = C::SST;
+  constexpr int kSmWarps = 4 * C::kSmWG;  // softmax warps
+  constexpr int QH = NQ / C::kSmWG;      // query columns of each softmax warpgroup
   extern __shared__ uint8_t smem_raw[];
   Smem<NQ, FP8>& S =
       *reinterpret_cast<Smem<NQ, FP8>*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
@@ -298,17 +296,17 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     for (int i = 0; i < VST; ++i) { mbar_init(&S.v_full[i], FP8 ? 4 : 1); mbar_init(&S.v_empty[i], 1); }
     for (int i = 0; i < SST; ++i) {
       mbar_init(&S.sk_full[i], 1);
-      mbar_init(&S.sk_empty[i], 4);
+      mbar_init(&S.sk_empty[i], 1);  // e4m3: the S MMA that read the staged K codes
       mbar_init(&S.sv_full[i], 1);
-      mbar_init(&S.sv_empty[i], 4);
+      mbar_init(&S.sv_empty[i], 4);  // the four converter warps
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(&S.s_full[i], 1);
-      mbar_init(&S.s_free[i], 4);
-      mbar_init(&S.p_full[i], 4);
+      mbar_init(&S.s_free[i], kSmWarps);  // one arrival per softmax warp
+      mbar_init(&S.p_full[i], kSmWarps);
       mbar_init(&S.p_empty[i], 1);
       mbar_init(&S.o_full[i], 1);
-      mbar_init(&S.o_free[i], 4);
+      mbar_init(&S.o_free[i], kSmWarps);
     }
     mbar_init(&S.drain, 1);
     S.abort_flag = 0;
@@ -407,7 +405,8 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     // Per tile: S(t) = K(t) Q^T into S[t & 1], then P V of the previous tile into
     // O[(t - 1) & 1], so the softmax of tile t - 1 overlaps the S MMA of tile t.
     // e4m3 caches: every operand (K codes, dequantised V, Q, P) is f16
-    constexpr uint32_t idesc_s = FP8 ? idesc_f16(128, NQ, false, false) : idesc_bf16(128, NQ, false, false);
+    // e4m3 caches: S on the 8-bit path (K codes x the two e4m3 parts of Q), P V in f16
+    constexpr uint32_t idesc_s = FP8 ? idesc_e4m3(128, NQ) : idesc_bf16(128, NQ, false, false);
     constexpr uint32_t idesc_o = FP8 ? idesc_f16(128, NQ, true, false) : idesc_bf16(128, NQ, true, false);
     int ks = 0, vs = 0, uu = 0;
     uint32_t kph = 0, vph = 0;
@@ -454,19 +453,33 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       for (int t = x.t0; t < x.t1 && ok; ++t) {
         const uint32_t sb = s_cnt & 1u, sph = (s_cnt >> 1) & 1u;
         if (!mbar_wait(&S.s_free[sb], sph ^ 1u, abort_flag)) { ok = false; break; }
-        if (!mbar_wait(&S.k_full[ks], kph, abort_flag)) { ok = false; break; }
+        if (!mbar_wait(FP8 ? &S.sk_full[ks] : &S.k_full[ks], kph, abort_flag)) { ok = false; break; }
         tc_fence_after();
-        const uint32_t k0 = smem_u32(S.k[ks]);
         const uint32_t d = tmem + sb * NQ;
+        if constexpr (FP8) {
+          // S^T = K codes (Q_hi + Q_lo)^T straight from the staged tile: one 128-byte row
+          // of codes per key, four K = 32 steps for each part of Q
+          const uint32_t k0 = smem_u32(S.sk[ks]);
+          const uint32_t qh = smem_u32(S.q8[qb][0]), ql = smem_u32(S.q8[qb][1]);
 #pragma unroll
-        for (int kk = 0; kk < kHd / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
-          const uint32_t qoff = (kk >> 2) * kQBox + (kk & 3) * 32;
-          tc_mma_f16(d, sdesc_sw128(k0 + off, 16, 1024), sdesc_sw128(q0 + qoff, 16, 1024), idesc_s, kk != 0);
+          for (int kk = 0; kk < kHd / 32; ++kk)
+            tc_mma_f8(d, sdesc_sw128(k0 + kk * 32, 16, 1024), sdesc_sw128(qh + kk * 32, 16, 1024), idesc_s, kk != 0);
+#pragma unroll
+          for (int kk = 0; kk < kHd / 32; ++kk)
+            tc_mma_f8(d, sdesc_sw128(k0 + kk * 32, 16, 1024), sdesc_sw128(ql + kk * 32, 16, 1024), idesc_s, 1u);
+          tc_commit(&S.sk_empty[ks]);
+        } else {
+          const uint32_t k0 = smem_u32(S.k[ks]);
+#pragma unroll
+          for (int kk = 0; kk < kHd / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * (kTileBytes / 2) + (kk & 3) * 32;
+            const uint32_t qoff = (kk >> 2) * kQBox + (kk & 3) * 32;
+            tc_mma_f16(d, sdesc_sw128(k0 + off, 16, 1024), sdesc_sw128(q0 + qoff, 16, 1024), idesc_s, kk != 0);
+          }
+          tc_commit(&S.k_empty[ks]);
         }
-        tc_commit(&S.k_empty[ks]);
         tc_commit(&S.s_full[sb]);
-        if (++ks == KST) { ks = 0; kph ^= 1u; }
+        if (++ks == (FP8 ? SST : KST)) { ks = 0; kph ^= 1u; }
         ++s_cnt;
         if (pv_pending && !issue_pv()) { ok = false; break; }
         pv_pending = true;
@@ -482,14 +495,21 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     tc_commit(&S.drain);
     volatile int never = 0;
     mbar_wait(&S.drain, 0, &never);
-  } else if (warp >= 2 && warp < 6) {
+  } else if (warp >= 2 && warp < 2 + kSmWarps) {
     // ------------------------------------------------------------------ softmax warps
-    // Warp w reads TMEM lanes 32 * (w % 4) .., so thread r owns key r of the S^T tile and
-    // hd index r of the O^T tile.  Every warp runs the same sequence of barriers; a
+    // One or two warpgroups (kSmWG), g = 0 (warps 2-5) and g = 1 (warps 6-9), each owning
+    // QH = NQ / kSmWG of the query columns, [q0, q0 + QH).  Warp w reads TMEM lanes 32 * (w % 4) .., so thread r
+    // of either warpgroup owns key r of the S^T tile and hd index r of the O^T tile, for
+    // its warpgroup's columns.  The warpgroups run independently (their own named
+    // barriers; the per-query shared arrays are indexed by column), and meet only in the
+    // per-unit Flash-Verify set-up.  Every warp runs the same sequence of barriers; a
     // failed wait is recorded and the sequence continues, so no warp is left waiting at
     // a barrier.
+    const int g = C::kSmWG == 1 ? 0 : (warp - 2) >> 2;  // compile-time 0 with one warpgroup
+    const int q0 = g * QH;
     const int quarter = warp & 3;
     const int r = quarter * 32 + lane;
+    const int tid = g * 128 + r;  // over every softmax warpgroup
     const uint32_t lane_base = static_cast<uint32_t>(quarter * 32) << 16;
     const bool has_view = p.view != nullptr;
     uint32_t s_cnt = 0, pv_cnt = 0;
@@ -502,6 +522,8 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         *abort_flag = 1;
       }
     };
+    auto wg_sync = [&]() { asm volatile("bar.sync %0, 128;" ::"r"(1 + g) : "memory"); };
+    auto both_sync = [&]() { asm volatile("bar.sync 3, %0;" ::"r"(kSmWarps * 32) : "memory"); };
     const int mask_words = (p.max_pos + 31) >> 5;
 
     // Finishing a unit (fold its last P V, reduce the row sums, write the output or the
@@ -509,18 +531,29 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     // deferred into the next unit's first tile, whose P V fold slot is empty, so the
     // wait hides behind that tile's softmax.
     constexpr bool kDefer = (NQ == 32) && !FP8;
-    auto finish = [&](float (&o)[NQ], float (&l)[NQ], const Unit& fx, int fuu, uint32_t fpv) {
+    constexpr int kSt = kHd + 2;
+    auto finish = [&](float (&o)[QH], float (&l)[QH], const Unit& fx, int fuu, uint32_t fpv) {
       const bool has_pv = fx.t1 > fx.t0;  // an empty unit (ragged batch, key range) has none
+      const int frow0 = fx.b * p.n_tok + fx.qc * kQChunk;
+      const int fnrows = min(kQChunk, p.n_tok - fx.qc * kQChunk);
+      // a cached state to merge: this thread's O values of it are requested into L1 before
+      // the wait for the last P V, so that their latency overlaps it
+      const float* stc = p.state_in + static_cast<size_t>(frow0) * p.H * kSt + fx.h * kSt + r;
+      if (p.state_in != nullptr) {
+#pragma unroll
+        for (int i = 0; i < QH; ++i)
+          if (q0 + i < fnrows) asm volatile("prefetch.global.L1 [%0];" ::"l"(stc + static_cast<size_t>(q0 + i) * p.H * kSt));
+      }
       if (has_pv) {
         const uint32_t ob = fpv & 1u, oph = (fpv >> 1) & 1u;  // the unit's last P V
         wait(&S.o_full[ob], oph);
         tc_fence_after();
-        const float4* al4 = reinterpret_cast<const float4*>(S.fin_alpha[fuu & 1]);
+        const float4* al4 = reinterpret_cast<const float4*>(S.fin_alpha[fuu & 1] + q0);
         {
-          float tmp[NQ];
-          tmem_ld_cols<NQ>(tmem + lane_base + 2 * NQ + ob * NQ, tmp);
+          float tmp[QH];
+          tmem_ld_cols<QH>(tmem + lane_base + 2 * NQ + ob * NQ + q0, tmp);
 #pragma unroll
-          for (int i = 0; i < NQ; i += 4) {
+          for (int i = 0; i < QH; i += 4) {
             const float4 al = al4[i / 4];
             o[i] = o[i] * al.x + tmp[i];
             o[i + 1] = o[i + 1] * al.y + tmp[i + 1];
@@ -532,71 +565,73 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.o_free[ob]);
       }
-      // row sums: reduce the per-key partial sums over the 128 threads
-#pragma unroll
-      for (int c = 0; c + 32 <= NQ; c += 32) S.red[quarter][c + lane] = reduce_scatter32<false>(l + c, lane);
-      if constexpr (NQ % 32 != 0) {
-        const float v16 = reduce_scatter16<false>(l + (NQ - 16), lane);
-        if (lane < 16) S.red[quarter][NQ - 16 + lane] = v16;
-      }
-      softmax_sync();
-      const int frow0 = fx.b * p.n_tok + fx.qc * kQChunk;
-      const int fnrows = min(kQChunk, p.n_tok - fx.qc * kQChunk);
-      constexpr int kSt = kHd + 2;
-      if (r < NQ) {
-        const float lt = S.red[0][r] + S.red[1][r] + S.red[2][r] + S.red[3][r];
-        S.l_fin[r] = lt;
+      // row sums: reduce the per-key partial sums over the warpgroup's 128 threads
+      reduce_cols<QH>(l, S.red[quarter] + q0, lane);
+      wg_sync();
+      if (r < QH) {
+        const int q = q0 + r;
+        const float lt = S.red[0][q] + S.red[1][q] + S.red[2][q] + S.red[3][q];
+        S.l_fin[q] = lt;
         if (p.state_in != nullptr) {
           // merge with the cached state of the other keys (LaCache, FACache): M = max of
           // both maxima, each side weighted by 2^(m - M)
-          const float ma = has_pv ? S.fin_m[fuu & 1][r] : -INFINITY;
+          const float ma = has_pv ? S.fin_m[fuu & 1][q] : -INFINITY;
           float mc = -INFINITY, lc = 0.0f;
-          if (r < fnrows) {
-            const float* st = p.state_in + (static_cast<size_t>(frow0 + r) * p.H + fx.h) * kSt;
-            mc = st[kHd];
-            lc = st[kHd + 1];
+          if (q < fnrows) {
+            const float2 ml = __ldg(reinterpret_cast<const float2*>(
+                p.state_in + (static_cast<size_t>(frow0 + q) * p.H + fx.h) * kSt + kHd));
+            mc = ml.x;
+            lc = ml.y;
           }
           const float M = fmaxf(ma, mc);
           const float wa = (ma == -INFINITY) ? 0.0f : exp2f(ma - M);
           const float wc = (mc == -INFINITY) ? 0.0f : exp2f(mc - M);
           const float L = lt * wa + lc * wc;
-          S.mrg_a[r] = wa;
-          S.mrg_c[r] = wc;
-          S.inv_l[r] = L > 0.0f ? 1.0f / L : 0.0f;
+          S.mrg_a[q] = wa;
+          S.mrg_c[q] = wc;
+          S.inv_l[q] = L > 0.0f ? 1.0f / L : 0.0f;
         } else {
-          S.inv_l[r] = lt > 0.0f ? 1.0f / lt : 0.0f;
+          S.inv_l[q] = lt > 0.0f ? 1.0f / lt : 0.0f;
         }
       }
-      softmax_sync();
+      wg_sync();
       if (p.state_in != nullptr) {  // this range merged with the cached state: normalised output
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(frow0) * p.D + fx.h * kHd + r;
-        const float* stc = p.state_in + static_cast<size_t>(frow0) * p.H * kSt + fx.h * kSt + r;
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-          if (ok && q < fnrows) {
-            const float oc = stc[static_cast<size_t>(q) * p.H * kSt];
-            out[static_cast<size_t>(q) * p.D] = __float2bfloat16_rn((o[q] * S.mrg_a[q] + oc * S.mrg_c[q]) * S.inv_l[q]);
+        for (int i0 = 0; i0 < QH; i0 += 8) {
+          float oc[8];  // eight loads (L1 hits after the prefetch) before their stores
+#pragma unroll
+          for (int j = 0; j < 8; ++j)
+            oc[j] = (q0 + i0 + j < fnrows) ? __ldg(stc + static_cast<size_t>(q0 + i0 + j) * p.H * kSt) : 0.0f;
+#pragma unroll
+          for (int j = 0; j < 8; ++j) {
+            const int q = q0 + i0 + j;
+            if (ok && q < fnrows)
+              out[static_cast<size_t>(q) * p.D] =
+                  __float2bfloat16_rn((o[i0 + j] * S.mrg_a[q] + oc[j] * S.mrg_c[q]) * S.inv_l[q]);
           }
         }
       } else if (p.state != nullptr) {  // partial softmax state of the key range
         float* st = p.state + (static_cast<size_t>(frow0) * p.H + fx.h) * kSt;
 #pragma unroll
-        for (int q = 0; q < NQ; ++q)
-          if (ok && q < fnrows) st[static_cast<size_t>(q) * p.H * kSt + r] = o[q];
-        if (ok && r < NQ && r < fnrows) {
-          st[static_cast<size_t>(r) * p.H * kSt + kHd] = has_pv ? S.fin_m[fuu & 1][r] : -INFINITY;
-          st[static_cast<size_t>(r) * p.H * kSt + kHd + 1] = S.l_fin[r];
+        for (int i = 0; i < QH; ++i)
+          if (ok && q0 + i < fnrows) st[static_cast<size_t>(q0 + i) * p.H * kSt + r] = o[i];
+        if (ok && r < QH && q0 + r < fnrows) {
+          const int q = q0 + r;
+          st[static_cast<size_t>(q) * p.H * kSt + kHd] = has_pv ? S.fin_m[fuu & 1][q] : -INFINITY;
+          st[static_cast<size_t>(q) * p.H * kSt + kHd + 1] = S.l_fin[q];
         }
       } else if (p.n_splits == 1) {
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(frow0) * p.D + fx.h * kHd + r;
-        const float4* il4 = reinterpret_cast<const float4*>(S.inv_l);
+        const float4* il4 = reinterpret_cast<const float4*>(S.inv_l + q0);
 #pragma unroll
-        for (int q = 0; q < NQ; q += 4) {
-          const float4 il = il4[q / 4];
-          if (ok && q < fnrows) out[static_cast<size_t>(q) * p.D] = __float2bfloat16_rn(o[q] * il.x);
-          if (ok && q + 1 < fnrows) out[static_cast<size_t>(q + 1) * p.D] = __float2bfloat16_rn(o[q + 1] * il.y);
-          if (ok && q + 2 < fnrows) out[static_cast<size_t>(q + 2) * p.D] = __float2bfloat16_rn(o[q + 2] * il.z);
-          if (ok && q + 3 < fnrows) out[static_cast<size_t>(q + 3) * p.D] = __float2bfloat16_rn(o[q + 3] * il.w);
+        for (int i = 0; i < QH; i += 4) {
+          const float4 il = il4[i / 4];
+          const int q = q0 + i;
+          if (ok && q < fnrows) out[static_cast<size_t>(q) * p.D] = __float2bfloat16_rn(o[i] * il.x);
+          if (ok && q + 1 < fnrows) out[static_cast<size_t>(q + 1) * p.D] = __float2bfloat16_rn(o[i + 1] * il.y);
+          if (ok && q + 2 < fnrows) out[static_cast<size_t>(q + 2) * p.D] = __float2bfloat16_rn(o[i + 2] * il.z);
+          if (ok && q + 3 < fnrows) out[static_cast<size_t>(q + 3) * p.D] = __float2bfloat16_rn(o[i + 3] * il.w);
         }
       } else {
         // split partials are stored by the unit's canonical number (sequence-major, the
@@ -604,11 +639,12 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         const size_t cu = ((static_cast<size_t>(fx.b) * p.H + fx.h) * p.n_qchunks + fx.qc) * p.n_splits + fx.split;
         float* wo = p.ws + cu * kQChunk * kHd;
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) wo[q * kHd + r] = o[q];
-        if (r < NQ) {
-          float* wml = p.ws + static_cast<size_t>(p.units) * kQChunk * kHd + (cu * kQChunk + r) * 2;
-          wml[0] = has_pv ? S.fin_m[fuu & 1][r] : -INFINITY;
-          wml[1] = S.l_fin[r];
+        for (int i = 0; i < QH; ++i) wo[(q0 + i) * kHd + r] = o[i];
+        if (r < QH) {
+          const int q = q0 + r;
+          float* wml = p.ws + static_cast<size_t>(p.units) * kQChunk * kHd + (cu * kQChunk + q) * 2;
+          wml[0] = has_pv ? S.fin_m[fuu & 1][q] : -INFINITY;
+          wml[1] = S.l_fin[q];
         }
       }
     };
@@ -632,7 +668,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       if (first_tile(0, y)) ks_next = fetch_ks(y, y.t0);
     }
 
-    float o_prev[NQ], l_prev[NQ];  // the unit waiting to be finished (deferred finish only)
+    float o_prev[QH], l_prev[QH];  // the unit waiting to be finished (deferred finish only)
     Unit px{};
     int puu = 0;
     uint32_t ppv = 0;
@@ -644,14 +680,22 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       const int row0 = x.b * p.n_tok;  // first row of the sequence
       const int nrows = min(kQChunk, p.n_tok - x.qc * kQChunk);  // valid columns of this chunk
       const int kend = key_end(p, x.b);  // regular slots past this are not attended
-      // ---- per-unit set-up: running max and Flash-Verify tags
-      if (r < NQ) S.m_run[r] = -INFINITY;
+      // e4m3: the S MMA multiplies the K codes by Q scaled by s (the converters' split of
+      // the chunk into e4m3 parts); 1/s joins each key's logit factor
+      float q8i = 1.0f;
+      if constexpr (FP8) {
+        wait(&S.q_conv[uu & 1], (uu >> 1) & 1u);
+        q8i = S.q8inv[uu & 1];
+      }
+      // ---- per-unit set-up: running max and Flash-Verify tags (the tags over every
+      // softmax warpgroup)
+      if (r < QH) S.m_run[q0 + r] = -INFINITY;
       if (has_view) {
-        for (int w = r; w < mask_words; w += 128) S.mask_bits[w] = 0u;
-        if (r == 0) S.n_draft = 0;
-        softmax_sync();
+        for (int w = tid; w < mask_words; w += kSmWarps * 32) S.mask_bits[w] = 0u;
+        if (tid == 0) S.n_draft = 0;
+        both_sync();
         int my_draft = 0;
-        for (int t = r; t < p.n_tok; t += 128) {
+        for (int t = tid; t < p.n_tok; t += kSmWarps * 32) {
           const int v = p.view[row0 + t];
           if (v == DLLM_VIEW_MASK) {
             const int pos = p.positions[row0 + t];
@@ -661,21 +705,21 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
           }
         }
         if (my_draft) atomicAdd(&S.n_draft, my_draft);
-        if (quarter < 2) {  // quarters 0 and 1 tag columns 0..63
+        if (g == 0 && quarter < 2) {  // quarters 0 and 1 of warpgroup 0 tag columns 0..63
           const bool is_draft = r < nrows && p.view[row0 + x.qc * kQChunk + r] == DLLM_VIEW_DRAFT;
           const uint32_t bal = __ballot_sync(0xffffffffu, is_draft);
           if (lane == 0) S.draft_qmask[quarter] = bal;
         }
-        softmax_sync();
+        both_sync();
       }
       const int n_draft = has_view ? min(S.n_draft, p.tail) : 0;
       const uint64_t dmask = has_view ? (static_cast<uint64_t>(S.draft_qmask[1]) << 32) | S.draft_qmask[0] : 0ull;
-      float o_acc[NQ];  // O^T row r (hd index r) for every query, relative to the running max
-      float l_part[NQ];  // this thread's key's share of each query's row sum
+      float o_acc[QH];  // O^T row r (hd index r) for this warpgroup's queries, relative to the running max
+      float l_part[QH];  // this thread's key's share of each of those queries' row sums
 #pragma unroll
-      for (int q = 0; q < NQ; ++q) {
-        o_acc[q] = 0.0f;
-        l_part[q] = 0.0f;
+      for (int i = 0; i < QH; ++i) {
+        o_acc[i] = 0.0f;
+        l_part[i] = 0.0f;
       }
 
       for (int t = x.t0; t < x.t1; ++t) {
@@ -691,18 +735,18 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
             if (first_tile(rnd + 1, y)) ks_next = fetch_ks(y, y.t0);
           }
         }
-        // ---- A: scores of this thread's key for every query
+        // ---- A: scores of this thread's key for the warpgroup's queries
         wait(&S.s_full[sb], sph);
         tc_fence_after();
-        float s[NQ];
-        tmem_ld_cols<NQ>(tmem + lane_base + sb * NQ, s);
+        float s[QH];
+        tmem_ld_cols<QH>(tmem + lane_base + sb * NQ + q0, s);
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.s_free[sb]);
         ++s_cnt;
 
         const int j = t * kKeyTile + r;  // slot index within the sequence
-        uint64_t vis;
+        uint64_t vis;  // over all NQ columns
         if (!has_view) {
           vis = (j < p.max_pos) ? ~0ull : 0ull;
         } else if (j < p.max_pos) {
@@ -711,49 +755,52 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
           vis = (j < p.max_pos + n_draft) ? dmask : 0ull;
         }
         if (p.ranged && (j < p.key_lo || j >= kend)) vis = 0ull;
-        const float sc = p.scale_log2 * ks_cur;  // e4m3: times the key's K group scale
+        const uint64_t visg = vis >> q0;  // this warpgroup's columns from bit 0
+        const float sc = p.scale_log2 * ks_cur * q8i;  // e4m3: times the key's K group scale and 1/s
         if (vis == ~0ull) {
 #pragma unroll
-          for (int q = 0; q < NQ; ++q) s[q] *= sc;
+          for (int i = 0; i < QH; ++i) s[i] *= sc;
         } else {
 #pragma unroll
-          for (int q = 0; q < NQ; ++q) s[q] = ((vis >> q) & 1ull) ? s[q] * sc : -INFINITY;
+          for (int i = 0; i < QH; ++i) s[i] = ((visg >> i) & 1ull) ? s[i] * sc : -INFINITY;
         }
 
         // column maxima: one redux per query over the warp, then over the 4 warps
         {
-          float mx[NQ];
+          float mx[QH];
 #pragma unroll
-          for (int q = 0; q < NQ; ++q) mx[q] = warp_max(s[q]);
+          for (int i = 0; i < QH; ++i) mx[i] = warp_max(s[i]);
           if (lane == 0) {
-            float4* dst = reinterpret_cast<float4*>(S.red[quarter]);
+            float4* dst = reinterpret_cast<float4*>(S.red[quarter] + q0);
 #pragma unroll
-            for (int q = 0; q < NQ; q += 4) dst[q / 4] = make_float4(mx[q], mx[q + 1], mx[q + 2], mx[q + 3]);
+            for (int i = 0; i < QH; i += 4) dst[i / 4] = make_float4(mx[i], mx[i + 1], mx[i + 2], mx[i + 3]);
           }
         }
-        softmax_sync();
+        wg_sync();
         // ---- B: column owners update the running max and the rescale factor
-        if (r < NQ) {
-          const float mt = fmaxf(fmaxf(S.red[0][r], S.red[1][r]), fmaxf(S.red[2][r], S.red[3][r]));
-          const float m_old = S.m_run[r];
+        if (r < QH) {
+          const int q = q0 + r;
+          const float mt = fmaxf(fmaxf(S.red[0][q], S.red[1][q]), fmaxf(S.red[2][q], S.red[3][q]));
+          const float m_old = S.m_run[q];
           const float m_new = fmaxf(m_old, mt);
           const float m_use = (m_new == -INFINITY) ? 0.0f : m_new;
           const float a = fast_exp2(m_old - m_use);
-          S.m_run[r] = m_new;
-          S.m_use[r] = m_use;
-          S.alpha[tp][r] = a;
+          S.m_run[q] = m_new;
+          S.m_use[q] = m_use;
+          S.alpha[tp][q] = a;
           if (t == x.t1 - 1) {  // the unit's last tile: what its finish needs
-            S.fin_alpha[uu & 1][r] = a;
-            S.fin_m[uu & 1][r] = m_new;
+            S.fin_alpha[uu & 1][q] = a;
+            S.fin_m[uu & 1][q] = m_new;
           }
         }
-        softmax_sync();
+        wg_sync();
         // ---- C: probabilities -> P^T (bf16, swizzled); this thread's partial row sums
         {
           // Slots past the regular region that no query sees may hold anything (stale
           // draft views, the next sequence, never-written memory).  Their P is 0, but
-          // 0 * NaN would still poison O, so their V rows are zeroed before the PV MMA.
-          if (!FP8 && (p.ranged || (t + 1) * kKeyTile > p.max_pos) && vis == 0ull &&
+          // 0 * NaN would still poison O, so their V rows are zeroed before the PV MMA
+          // (by warpgroup 0, before its P arrival, which the PV MMA waits for).
+          if (!FP8 && g == 0 && (p.ranged || (t + 1) * kKeyTile > p.max_pos) && vis == 0ull &&
               (p.ranged || j >= p.max_pos)) {
             wait(&S.v_full[vs], vph);
             uint4* row0v = reinterpret_cast<uint4*>(S.v[vs] + r * 128);
@@ -772,18 +819,19 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
           wait(&S.p_empty[pb], pph ^ 1u);
           const uint32_t pbase = smem_u32(S.p[pb] + (r >> 6) * kQBox);
           const uint32_t byte = (r & 63) * 2;
-          const float4* mu4 = reinterpret_cast<const float4*>(S.m_use);
-          const float4* al4 = reinterpret_cast<const float4*>(S.alpha[tp]);
+          const float4* mu4 = reinterpret_cast<const float4*>(S.m_use + q0);
+          const float4* al4 = reinterpret_cast<const float4*>(S.alpha[tp] + q0);
 #pragma unroll
-          for (int q = 0; q < NQ; q += 4) {
-            const float4 mu = mu4[q / 4];
-            const float4 al = al4[q / 4];
-            const float e0 = fast_exp2(s[q] - mu.x), e1 = fast_exp2(s[q + 1] - mu.y);
-            const float e2 = fast_exp2(s[q + 2] - mu.z), e3 = fast_exp2(s[q + 3] - mu.w);
-            l_part[q] = l_part[q] * al.x + e0;
-            l_part[q + 1] = l_part[q + 1] * al.y + e1;
-            l_part[q + 2] = l_part[q + 2] * al.z + e2;
-            l_part[q + 3] = l_part[q + 3] * al.w + e3;
+          for (int i = 0; i < QH; i += 4) {
+            const float4 mu = mu4[i / 4];
+            const float4 al = al4[i / 4];
+            const float e0 = fast_exp2(s[i] - mu.x), e1 = fast_exp2(s[i + 1] - mu.y);
+            const float e2 = fast_exp2(s[i + 2] - mu.z), e3 = fast_exp2(s[i + 3] - mu.w);
+            l_part[i] = l_part[i] * al.x + e0;
+            l_part[i + 1] = l_part[i + 1] * al.y + e1;
+            l_part[i + 2] = l_part[i + 2] * al.z + e2;
+            l_part[i + 3] = l_part[i + 3] * al.w + e3;
+            const int q = q0 + i;
             st_bf16_pair<FP8>(pbase + sw128_offset(q, byte), pbase + sw128_offset(q + 1, byte), e0, e1);
             st_bf16_pair<FP8>(pbase + sw128_offset(q + 2, byte), pbase + sw128_offset(q + 3, byte), e2, e3);
           }
@@ -801,12 +849,12 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
           const uint32_t ob = (pv_cnt - 1) & 1u, oph = ((pv_cnt - 1) >> 1) & 1u;
           wait(&S.o_full[ob], oph);
           tc_fence_after();
-          const float4* al4 = reinterpret_cast<const float4*>(S.alpha[tp ^ 1u]);
+          const float4* al4 = reinterpret_cast<const float4*>(S.alpha[tp ^ 1u] + q0);
           {
-            float tmp[NQ];
-            tmem_ld_cols<NQ>(tmem + lane_base + 2 * NQ + ob * NQ, tmp);
+            float tmp[QH];
+            tmem_ld_cols<QH>(tmem + lane_base + 2 * NQ + ob * NQ + q0, tmp);
 #pragma unroll
-            for (int i = 0; i < NQ; i += 4) {
+            for (int i = 0; i < QH; i += 4) {
               const float4 al = al4[i / 4];
               o_acc[i] = o_acc[i] * al.x + tmp[i];
               o_acc[i + 1] = o_acc[i + 1] * al.y + tmp[i + 1];
@@ -827,9 +875,9 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
           pending = false;
         }
 #pragma unroll
-        for (int q = 0; q < NQ; ++q) {
-          o_prev[q] = o_acc[q];
-          l_prev[q] = l_part[q];
+        for (int i = 0; i < QH; ++i) {
+          o_prev[i] = o_acc[i];
+          l_prev[i] = l_part[i];
         }
         px = x;
         puu = uu;
@@ -838,7 +886,11 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       } else {
         finish(o_acc, l_part, x, uu, pv_cnt - 1);
       }
-      softmax_sync();  // the next unit's set-up rewrites the running max and tags
+      // the next unit's set-up rewrites the running max (per warpgroup) and the shared tags
+      if (has_view)
+        both_sync();
+      else
+        wg_sync();
     }
     if constexpr (kDefer) {
       if (pending) finish(o_prev, l_prev, px, puu, ppv);
@@ -847,17 +899,21 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       *abort_flag = 1;
       atomicOr(p.status, DLLM_DEV_TIMEOUT);
     }
-  } else if (FP8 && warp >= 6) {
-    // ------------------------------------------------------------------ e4m3 -> f16 converters
-    // Per unit: the Q chunk, bf16 -> f16 in place (the MMAs of this path take f16).  Per
-    // tile: thread r converts key row r of the staged codes into both 64-column halves
-    // of the operand tiles, keeping the 128-byte swizzle: K as the bare code (exact in
-    // f16; the softmax multiplies the key's logits by its K scale), V as code times the
-    // key's V scale with one f16 rounding.  V rows of slots that no query can see are
-    // written as zeros (their probability is 0, and 0 * NaN must not reach O).
+  } else if (FP8 && warp >= 2 + kSmWarps) {
+    // ------------------------------------------------------------------ e4m3 converters
+    // Per unit: the Q chunk, split into two e4m3 parts for the 8-bit S MMA.  One scale
+    // s for the chunk takes its largest |q| to 448; Q_hi = e4m3(s q) and Q_lo = e4m3(s q
+    // - Q_hi), so Q_hi + Q_lo = s q to within about 2^-9 of each value (two 4-bit
+    // significands, as close as bf16's rounding of Q), and 1/s goes to the softmax with
+    // the key's K scale.  Per tile: thread r turns key row r of the staged V codes into
+    // both 64-column halves of the f16 V operand, keeping the 128-byte swizzle: code
+    // times the key's V scale, one f16 rounding.  V rows of slots that no query can see
+    // are written as zeros (their probability is 0, and 0 * NaN must not reach O).  The
+    // staged K codes feed the S MMA directly.
     const int r = (warp & 3) * 32 + lane;
-    int ss = 0, ko = 0, vo = 0, uu = 0;
-    uint32_t sph = 0, kph = 0, vph = 0;
+    const int cw = (warp - 2 - kSmWarps);  // converter warp 0..3: column quarter of Q
+    int ss = 0, vo = 0, uu = 0;
+    uint32_t sph = 0, vph = 0;
     bool ok = true;
     // The V group scale of key r of a tile (fetched one tile ahead: it comes from HBM;
     // the K scale multiplies the key's logits in the softmax instead).
@@ -878,17 +934,80 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       Unit y;
       if (next_tile(0, y)) nvs = fetch_vscale(y, y.t0);
     }
-    for (int rnd = 0, u = cta_unit(p, 0); u < p.units && ok; u = cta_unit(p, ++rnd), ++uu) {
+    // The four converter warps share a named barrier once per unit, so after a failed
+    // wait a warp keeps walking the units (doing no work) instead of leaving the loop:
+    // every warp passes that barrier the same number of times.
+    for (int rnd = 0, u = cta_unit(p, 0); u < p.units; u = cta_unit(p, ++rnd), ++uu) {
       const Unit x = decode_unit(p, u, order);
       {
+        // Q chunk -> (Q_hi, Q_lo, 1/s).  Warp cw takes columns [32 cw, 32 cw + 32) of rows
+        // lane and lane + 32: 64 bytes of bf16 from box cw / 2 of the Q tile, 32 bytes of
+        // each e4m3 part.
         const int qb = uu & 1;
-        if (!mbar_wait_warp(&S.q_full[qb], (uu >> 1) & 1u, abort_flag)) { ok = false; break; }
-        uint4* qv = reinterpret_cast<uint4*>(S.q[qb]);
-        for (int i = r; i < static_cast<int>(C::kQBytes / 16); i += 128) qv[i] = bf16x8_to_f16x8(qv[i]);
+        if (ok && !mbar_wait_warp(&S.q_full[qb], (uu >> 1) & 1u, abort_flag)) ok = false;
+        constexpr int kRows = NQ > 32 ? 2 : 1;
+        float qv[kRows][32];
+        float amax = 0.0f;
+#pragma unroll
+        for (int rr = 0; rr < kRows; ++rr) {
+          const int row = lane + 32 * rr;
+          const uint8_t* src = S.q[qb] + (cw >> 1) * kQBox + row * 128;
+#pragma unroll
+          for (int c = 0; c < 4; ++c) {
+            uint4 w = make_uint4(0u, 0u, 0u, 0u);
+            if (ok && row < NQ) w = *reinterpret_cast<const uint4*>(src + ((((cw & 1) * 4 + c) ^ (row & 7)) << 4));
+            const uint32_t* wi = reinterpret_cast<const uint32_t*>(&w);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              qv[rr][c * 8 + 2 * e] = __uint_as_float(wi[e] << 16);
+              qv[rr][c * 8 + 2 * e + 1] = __uint_as_float(wi[e] & 0xffff0000u);
+            }
+          }
+#pragma unroll
+          for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(qv[rr][i]));
+        }
+        amax = warp_max(amax);
+        if (lane == 0) S.cv_red[qb][cw] = amax;
+        asm volatile("bar.sync 4, 128;" ::: "memory");  // the four converter warps
+        amax = fmaxf(fmaxf(S.cv_red[qb][0], S.cv_red[qb][1]), fmaxf(S.cv_red[qb][2], S.cv_red[qb][3]));
+        const float sq = amax > 0.0f ? __fdiv_rn(448.0f, amax) : 1.0f;
+        if (cw == 0 && lane == 0) S.q8inv[qb] = amax > 0.0f ? __fdiv_rn(amax, 448.0f) : 1.0f;
+#pragma unroll
+        for (int rr = 0; rr < kRows; ++rr) {
+          const int row = lane + 32 * rr;
+          uint32_t hi[8], lo[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            uint32_t hw = 0u, lw = 0u;
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+              const float y0 = qv[rr][4 * i + 2 * j] * sq, y1 = qv[rr][4 * i + 2 * j + 1] * sq;
+              const __nv_fp8x2_storage_t h = __nv_cvt_float2_to_fp8x2(make_float2(y0, y1), __NV_SATFINITE, __NV_E4M3);
+              const float2 hv = __half22float2(__half2(__nv_cvt_fp8x2_to_halfraw2(h, __NV_E4M3)));
+              const __nv_fp8x2_storage_t l =
+                  __nv_cvt_float2_to_fp8x2(make_float2(y0 - hv.x, y1 - hv.y), __NV_SATFINITE, __NV_E4M3);
+              hw |= static_cast<uint32_t>(h) << (16 * j);
+              lw |= static_cast<uint32_t>(l) << (16 * j);
+            }
+            hi[i] = hw;
+            lo[i] = lw;
+          }
+          if (ok && row < NQ) {
+            uint8_t* dh = S.q8[qb][0] + row * 128;
+            uint8_t* dl = S.q8[qb][1] + row * 128;
+#pragma unroll
+            for (int c = 0; c < 2; ++c) {
+              const uint32_t off = (((2 * cw + c) ^ (row & 7)) << 4);
+              *reinterpret_cast<uint4*>(dh + off) = make_uint4(hi[4 * c], hi[4 * c + 1], hi[4 * c + 2], hi[4 * c + 3]);
+              *reinterpret_cast<uint4*>(dl + off) = make_uint4(lo[4 * c], lo[4 * c + 1], lo[4 * c + 2], lo[4 * c + 3]);
+            }
+          }
+        }
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) mbar_arrive(&S.q_conv[qb]);
       }
+      if (!ok) continue;
       int n_draft = 0;
       if (p.view) {
         for (int t = 0; t < p.n_tok; ++t) n_draft += (p.view[x.b * p.n_tok + t] == DLLM_VIEW_DRAFT);
@@ -907,30 +1026,6 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
           Unit y;
           if (next_tile(rnd + 1, y)) nvs = fetch_vscale(y, y.t0);
         }
-        // K
-        if (!mbar_wait_warp(&S.sk_full[ss], sph, abort_flag)) { ok = false; break; }
-        if (!mbar_wait_warp(&S.k_empty[ko], kph ^ 1u, abort_flag)) { ok = false; break; }
-        {
-          const uint8_t* src = S.sk[ss] + r * 128;
-          uint8_t* dst = S.k[ko] + r * 128;
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            const uint4 in = *reinterpret_cast<const uint4*>(src + ((c ^ sw) << 4));
-            uint4 lo, hi;
-            cvt16_f16(in, lo, hi);
-            uint8_t* half = dst + (c >> 2) * (kTileBytes / 2);
-            const uint32_t c0 = (c & 3) * 2;
-            *reinterpret_cast<uint4*>(half + ((c0 ^ sw) << 4)) = lo;
-            *reinterpret_cast<uint4*>(half + (((c0 + 1) ^ sw) << 4)) = hi;
-          }
-        }
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-          mbar_arrive(&S.k_full[ko]);
-          mbar_arrive(&S.sk_empty[ss]);
-        }
-        if (++ko == KST) { ko = 0; kph ^= 1u; }
         // V
         if (!mbar_wait_warp(&S.sv_full[ss], sph, abort_flag)) { ok = false; break; }
         if (!mbar_wait_warp(&S.v_empty[vo], vph ^ 1u, abort_flag)) { ok = false; break; }

@@ -217,15 +217,14 @@ DEVI bool kv_tile_skipped(const ProjParams& p, int grp, int m0, int rows) {
 // the smallest cosine of a sequence falls below gamma).
 
 // Add <cache, probe>, |cache|^2 and |probe|^2 over 32 columns of one head: probe values
-// v (fp32, after the rotation for K), cache values read from the row's slot (bf16, or
-// e4m3 codes times the group scale).
-DEVI void drift_dot32(const float (&v)[32], const void* crow, bool fp8, float scale, float& dot, float& nc,
-                      float& np) {
-  if (fp8) {
-    const uint4* src = static_cast<const uint4*>(crow);
+// v (fp32, after the rotation for K), cache values already loaded from the row's slot
+// (bf16: 4 vectors, or e4m3 codes: 2 vectors, times the group scale).
+template <bool FP8>
+DEVI void drift_dot32(const float (&v)[32], const uint4* src, float scale, float& dot, float& nc, float& np) {
+  if constexpr (FP8) {
 #pragma unroll
     for (int i = 0; i < 2; ++i) {
-      const uint4 w = __ldg(src + i);
+      const uint4 w = src[i];
       const __nv_fp8x2_storage_t* pr = reinterpret_cast<const __nv_fp8x2_storage_t*>(&w);
 #pragma unroll
       for (int j = 0; j < 8; ++j) {
@@ -238,10 +237,9 @@ DEVI void drift_dot32(const float (&v)[32], const void* crow, bool fp8, float sc
       }
     }
   } else {
-    const uint4* src = static_cast<const uint4*>(crow);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint4 w = __ldg(src + i);
+      const uint4 w = src[i];
       const __nv_bfloat162* pr = reinterpret_cast<const __nv_bfloat162*>(&w);
 #pragma unroll
       for (int j = 0; j < 4; ++j) {
@@ -253,6 +251,26 @@ DEVI void drift_dot32(const float (&v)[32], const void* crow, bool fp8, float sc
       }
     }
   }
+}
+
+// Before an epilogue waits for a probe tile's accumulator: request into L2 the cached
+// K (or V) rows that its drift sums will read, for the `heads` heads of the tile, so the
+// epilogue's loads hit L2 (the tile's MMAs take tens of microseconds).
+DEVI void drift_prefetch_l2(const ProjParams& p, int m0, int n0, int heads, int r) {
+  const int m = m0 + r;
+  if (m >= p.m_kv) return;
+  const int b = m / p.n_kv;
+  const int pos = p.kv_positions ? __ldg(p.kv_positions + m) : m - b * p.n_kv;
+  if (pos < 0 || pos >= p.max_pos) return;
+  const int part = n0 / p.D;  // 1 K, 2 V
+  const bool fp8 = p.kv_dtype == DLLM_E4M3;
+  const size_t crow_i = (static_cast<size_t>(b) * p.slots + pos) * 2 + (part - 1);
+  const int h0 = (n0 - part * p.D) / kHd;
+  const char* base = static_cast<const char*>(p.cache_kv) + (crow_i * p.D + h0 * kHd) * (fp8 ? 1 : 2);
+  const int bytes = heads * kHd * (fp8 ? 1 : 2);
+  for (int off = 0; off < bytes; off += 128)
+    asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(base + off));
+  if (fp8) asm volatile("prefetch.global.L2::evict_last [%0];" ::"l"(p.cache_scale + crow_i * p.H + h0));
 }
 
 // One tile's share of probe row m (the `heads` heads of K, part 0, or V, part 1, that
@@ -380,17 +398,35 @@ DEVI void store_rows(const ProjParams& p, const TileCoord& c, int heads, uint32_
     for (int hh = 0; hh < heads; ++hh) {
       const int h = (c.n0 - part * p.D) / kHd + hh;
       const uint32_t tcol = tacc + hh * kHd;
-      const uint8_t* crow = static_cast<const uint8_t*>(p.cache_kv) + (crow_i * p.D + h * hd) * (fp8 ? 1 : 2);
+      const uint4* crow =
+          reinterpret_cast<const uint4*>(static_cast<const uint8_t*>(p.cache_kv) + (crow_i * p.D + h * hd) * (fp8 ? 1 : 2));
+      // the head's cached row (256 B bf16, 128 B e4m3), loaded before the TMEM reads so
+      // that all its loads are in flight at once
+      uint4 cv[16];
+#pragma unroll
+      for (int i = 0; i < 16; ++i) cv[i] = make_uint4(0u, 0u, 0u, 0u);
+      if (valid) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (!fp8 || i < 8) cv[i] = __ldg(crow + i);
+      }
       const float sc = (fp8 && valid) ? __ldg(p.cache_scale + crow_i * p.H + h) : 1.0f;
-#pragma unroll 1
+#pragma unroll
       for (int half = 0; half < 2; ++half) {
         float lo[32], hi[32];
         tmem_ld32(tcol + half * 32, lo);
         tmem_ld32(tcol + 64 + half * 32, hi);
         if (rope) rotate32(lo, hi, cs_row + half * 32);
         if (valid) {
-          drift_dot32(lo, crow + half * 32 * (fp8 ? 1 : 2), fp8, sc, dot, nc, np);
-          drift_dot32(hi, crow + (64 + half * 32) * (fp8 ? 1 : 2), fp8, sc, dot, nc, np);
+          // columns [32 half, +32) and [64 + 32 half, +32): 16-byte vectors 4 half / 8 + 4 half
+          // (bf16) or 2 half / 4 + 2 half (e4m3)
+          if (fp8) {
+            drift_dot32<true>(lo, cv + 2 * half, sc, dot, nc, np);
+            drift_dot32<true>(hi, cv + 4 + 2 * half, sc, dot, nc, np);
+          } else {
+            drift_dot32<false>(lo, cv + 4 * half, sc, dot, nc, np);
+            drift_dot32<false>(hi, cv + 8 + 4 * half, sc, dot, nc, np);
+          }
         }
       }
     }
@@ -599,6 +635,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (kv_tile_skipped(p, c.grp, c.m0, BM)) continue;
       if (it.half >= 0) c.n0 += it.half * kHd;
       const int heads = it.half >= 0 ? 1 : BN / kHd;
+      if (c.grp == 1 && p.drift_acc != nullptr) drift_prefetch_l2(p, c.m0, c.n0, heads, r);
       if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag)) {
         ok = false;
         *abort_flag = 1;
@@ -845,6 +882,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int item = pair; item < items_end; item += n_pairs) {
       const PairItem it = decode_pair_item(p, item);
       if (kv_tile_skipped(p, it.grp, it.pm0, 256)) continue;
+      if (it.grp == 1 && p.drift_acc != nullptr)
+        drift_prefetch_l2(p, it.pm0 + static_cast<int>(rank) * 128, it.n0, it.half ? 1 : 2, r);
       if (!mbar_wait_warp(&tfull[acc], acc_phase, abort_flag)) {
         ok = false;
         *abort_flag = 1;
