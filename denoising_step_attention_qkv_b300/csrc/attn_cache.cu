@@ -99,6 +99,8 @@ struct Smem {
   int n_draft;
   float q8inv[2];       // e4m3: per Q buffer, 1 / the scale that took the chunk's max |q| to 448
   float cv_red[2][4];   // e4m3: per Q buffer, the converter warps' max |q|
+  int merge_last[2];    // per softmax warpgroup: this piece completed its tail unit
+  float mrg_w[kMaxPieces][NQ];  // merge of a tail unit's pieces: weight of piece j, column q
   uint64_t q_full[2], q_empty[2];
   uint64_t q_conv[2];  // e4m3 caches: the Q chunk has been converted to f16 in place
   uint64_t k_full[C::KST], k_empty[C::KST];
@@ -135,12 +137,20 @@ DEVI void dequant16_f16(const uint4 in, __half2 scale, uint4& lo, uint4& hi) {
 
 struct Unit {
   int b, h, qc, split, t0, t1;
+  int u;      // the unit's number (before the ragged reordering)
+  int part;   // 1: a piece of a tail unit (its state is merged with the other pieces')
+  int piece;  // which piece, and which tail unit (part == 1)
+  int tu;
 };
 
 // Unit u -> (sequence, head, query chunk, key split).  With `order` (ragged batches) the
 // sequence part of u is a rank in order of decreasing key length.
 DEVI Unit decode_unit(const AttnParams& p, int u, const int* order) {
   Unit x;
+  x.u = u;
+  x.part = 0;
+  x.piece = 0;
+  x.tu = 0;
   x.split = u % p.n_splits;
   u /= p.n_splits;
   x.qc = u % p.n_qchunks;
@@ -165,6 +175,40 @@ DEVI Unit decode_unit(const AttnParams& p, int u, const int* order) {
 DEVI int cta_unit(const AttnParams& p, int r) {
   const int c = (p.key_len && (r & 1)) ? static_cast<int>(gridDim.x - 1 - blockIdx.x) : static_cast<int>(blockIdx.x);
   return r * static_cast<int>(gridDim.x) + c;
+}
+
+// The rnd-th work item of this CTA; false past its last.  Without tail pieces: the
+// round-robin over the units (cta_unit).  With them (tail_pieces > 0): dp_waves rounds
+// of whole units, round-robin, then the last tail_units units, each cut into
+// tail_pieces pieces of piece_tiles key tiles, dealt round-robin piece-major (item i of
+// the tail is piece i / tail_units of tail unit i % tail_units), so that neighbouring
+// CTAs read the same slots of neighbouring heads in both phases.  Every warp role walks
+// the same items.
+template <bool PIECES>
+DEVI bool cta_item(const AttnParams& p, int rnd, const int* order, Unit& x) {
+  if (!PIECES || p.tail_pieces == 0) {
+    const int u = cta_unit(p, rnd);
+    if (u >= p.units) return false;
+    x = decode_unit(p, u, order);
+    return true;
+  }
+  const int g = static_cast<int>(gridDim.x);
+  const int i0 = rnd * g + static_cast<int>(blockIdx.x);
+  const int whole = p.dp_waves * g;
+  if (i0 < whole) {
+    x = decode_unit(p, i0, nullptr);
+    return true;
+  }
+  const int i = i0 - whole;
+  if (i >= p.tail_units * p.tail_pieces) return false;
+  const int piece = i / p.tail_units, tu = i - piece * p.tail_units;
+  x = decode_unit(p, whole + tu, nullptr);
+  x.t0 = p.tile_lo + piece * p.piece_tiles;
+  x.t1 = min(p.tile_lo + p.key_tiles, x.t0 + p.piece_tiles);
+  x.part = p.tail_pieces > 1 ? 1 : 0;
+  x.piece = piece;
+  x.tu = tu;
+  return true;
 }
 
 // End (exclusive) of the regular slots sequence b attends to.
@@ -268,10 +312,14 @@ DEVI void tmem_ld_cols(uint32_t taddr, float (&v)[N]) {
   }
 }
 
-template <int NQ, bool FP8>
+// PIECES: the instantiation that runs the balanced schedule's tail pieces and their
+// merge (bf16 caches only); the others contain neither, so that code does not weigh on
+// their tile loop.
+template <int NQ, bool FP8, bool PIECES>
 __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     attn_cache_tc(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_kv,
-                  const AttnParams p) {
+                  const __grid_constant__ CUtensorMap tm_kv_tail, const AttnParams p) {
+  static_assert(!(PIECES && FP8), "tail pieces are scheduled for bf16 caches only");
   using C = Cfg<NQ, FP8>;
   constexpr int KST = C::KST, VST = C::VST, SST = C::SST;
   constexpr int kSmWarps = 4 * C::kSmWG;  // softmax warps
@@ -313,6 +361,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     fence_mbar_init();
     prefetch_tmap(&tm_q);
     prefetch_tmap(&tm_kv);
+    if (p.tail_rows) prefetch_tmap(&tm_kv_tail);
   }
   if (warp == 1) {
     tmem_alloc(&S.tmem_base, kTmemCols);
@@ -347,8 +396,8 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     int ks = 0, vs = 0, uu = 0;
     uint32_t kph = 0, vph = 0;
     bool ok = true;
-    for (int rnd = 0, u = cta_unit(p, 0); u < p.units && ok; u = cta_unit(p, ++rnd), ++uu) {
-      const Unit x = decode_unit(p, u, order);
+    Unit x;
+    for (int rnd = 0; ok && cta_item<PIECES>(p, rnd, order, x); ++rnd, ++uu) {
       const int qb = uu & 1;
       if (!mbar_wait(&S.q_empty[qb], ((uu >> 1) & 1) ^ 1u, abort_flag)) { ok = false; break; }
       mbar_arrive_expect_tx(&S.q_full[qb], 2 * kQBox);
@@ -358,25 +407,32 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       const int slot0 = x.b * p.slots;
       for (int t = x.t0; t < x.t1; ++t) {
         const int key0 = slot0 + t * kKeyTile;
+        // A tile that runs past the sequence's slots (the Flash-Verify draft tail, or a
+        // slot count that is not a multiple of 128) loads only its first tail_rows rows;
+        // the rows after them are keys no query sees (their scores are masked, their V
+        // rows zeroed before the P V MMA).
+        const bool trim = p.tail_rows != 0 && (t + 1) * kKeyTile > p.slots;
+        const CUtensorMap* mkv = trim ? &tm_kv_tail : &tm_kv;
+        const uint32_t rows = trim ? static_cast<uint32_t>(p.tail_rows) : static_cast<uint32_t>(kKeyTile);
         if constexpr (FP8) {
           // e4m3 tiles into the staging rings (one 128-byte-wide box each)
           if (!mbar_wait(&S.sk_empty[ks], kph ^ 1u, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(&S.sk_full[ks], kTile8Bytes);
-          tma_load_3d(S.sk[ks], &tm_kv, &S.sk_full[ks], 0, x.h, key0, pol_stream);
+          mbar_arrive_expect_tx(&S.sk_full[ks], rows * 128u);
+          tma_load_3d(S.sk[ks], mkv, &S.sk_full[ks], 0, x.h, key0, pol_stream);
           if (!mbar_wait(&S.sv_empty[ks], kph ^ 1u, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(&S.sv_full[ks], kTile8Bytes);
-          tma_load_3d(S.sv[ks], &tm_kv, &S.sv_full[ks], 0, p.H + x.h, key0, pol_stream);
+          mbar_arrive_expect_tx(&S.sv_full[ks], rows * 128u);
+          tma_load_3d(S.sv[ks], mkv, &S.sv_full[ks], 0, p.H + x.h, key0, pol_stream);
           if (++ks == SST) { ks = 0; kph ^= 1u; }
         } else {
           if (!mbar_wait(&S.k_empty[ks], kph ^ 1u, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(&S.k_full[ks], kTileBytes);
-          tma_load_3d(S.k[ks], &tm_kv, &S.k_full[ks], 0, x.h, key0, pol_stream);
-          tma_load_3d(S.k[ks] + kTileBytes / 2, &tm_kv, &S.k_full[ks], 64, x.h, key0, pol_stream);
+          mbar_arrive_expect_tx(&S.k_full[ks], rows * 256u);
+          tma_load_3d(S.k[ks], mkv, &S.k_full[ks], 0, x.h, key0, pol_stream);
+          tma_load_3d(S.k[ks] + kTileBytes / 2, mkv, &S.k_full[ks], 64, x.h, key0, pol_stream);
           if (++ks == KST) { ks = 0; kph ^= 1u; }
           if (!mbar_wait(&S.v_empty[vs], vph ^ 1u, abort_flag)) { ok = false; break; }
-          mbar_arrive_expect_tx(&S.v_full[vs], kTileBytes);
-          tma_load_3d(S.v[vs], &tm_kv, &S.v_full[vs], 0, p.H + x.h, key0, pol_stream);
-          tma_load_3d(S.v[vs] + kTileBytes / 2, &tm_kv, &S.v_full[vs], 64, p.H + x.h, key0, pol_stream);
+          mbar_arrive_expect_tx(&S.v_full[vs], rows * 256u);
+          tma_load_3d(S.v[vs], mkv, &S.v_full[vs], 0, p.H + x.h, key0, pol_stream);
+          tma_load_3d(S.v[vs] + kTileBytes / 2, mkv, &S.v_full[vs], 64, p.H + x.h, key0, pol_stream);
           if (++vs == VST) { vs = 0; vph ^= 1u; }
         }
       }
@@ -440,8 +496,8 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     // been issued (or an empty unit, or the end), so at unit boundaries too the softmax
     // finds its next S ready.
     bool pv_pending = false;
-    for (int rnd = 0, u = cta_unit(p, 0); u < p.units && ok; u = cta_unit(p, ++rnd), ++uu) {
-      const Unit x = decode_unit(p, u, order);
+    Unit x;
+    for (int rnd = 0; ok && cta_item<PIECES>(p, rnd, order, x); ++rnd, ++uu) {
       const int qb = uu & 1;
       if (x.t1 == x.t0 && pv_pending) {
         if (!issue_pv()) { ok = false; break; }
@@ -532,7 +588,10 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     // wait hides behind that tile's softmax.
     constexpr bool kDefer = (NQ == 32) && !FP8;
     constexpr int kSt = kHd + 2;
-    auto finish = [&](float (&o)[QH], float (&l)[QH], const Unit& fx, int fuu, uint32_t fpv) {
+    // can_merge (a constant at every call site): whether this call may finish a
+    // stream-K piece (deferred finishes never do: pieces finish at once, which keeps the
+    // merge's registers out of the tile loop).
+    auto finish = [&](bool can_merge, float (&o)[QH], float (&l)[QH], const Unit& fx, int fuu, uint32_t fpv) {
       const bool has_pv = fx.t1 > fx.t0;  // an empty unit (ragged batch, key range) has none
       const int frow0 = fx.b * p.n_tok + fx.qc * kQChunk;
       const int fnrows = min(kQChunk, p.n_tok - fx.qc * kQChunk);
@@ -621,6 +680,99 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
           st[static_cast<size_t>(q) * p.H * kSt + kHd] = has_pv ? S.fin_m[fuu & 1][q] : -INFINITY;
           st[static_cast<size_t>(q) * p.H * kSt + kHd + 1] = S.l_fin[q];
         }
+      } else if (PIECES && can_merge && fx.part != 0) {
+        // a piece of a tail unit: store its partial state in the piece's slot (O as
+        // [column / 4][hd row][4]: a thread's four columns are one 16-byte vector, and a
+        // warp's 32 rows are 512 contiguous bytes) and count it in
+        // (one release per warpgroup, after the barrier that orders every thread's
+        // stores before it); the piece that completes the unit merges all pieces'
+        // states, in piece order whichever came last (so the rounding does not depend on
+        // timing), per query M = max m, weights 2^(m - M), and writes the output.  The
+        // count returns to zero for the next launch.
+        const int np = p.tail_pieces;
+        const size_t n_slots = static_cast<size_t>(p.tail_units) * np;
+        const size_t slot = static_cast<size_t>(fx.piece) * p.tail_units + fx.tu;
+        float4* wo = reinterpret_cast<float4*>(p.ws + slot * kQChunk * kHd) + (q0 / 4) * kHd + r;
+        float* wml = p.ws + n_slots * kQChunk * kHd + slot * kQChunk * 2;
+        if (ok) {
+#pragma unroll
+          for (int i = 0; i < QH; i += 4) wo[(i / 4) * kHd] = make_float4(o[i], o[i + 1], o[i + 2], o[i + 3]);
+          if (r < QH) {
+            *reinterpret_cast<float2*>(wml + (q0 + r) * 2) =
+                make_float2(has_pv ? S.fin_m[fuu & 1][q0 + r] : -INFINITY, S.l_fin[q0 + r]);
+          }
+        }
+        wg_sync();
+        if (r == 0) {
+          int last = 0;
+          if (ok) {
+            int* cnt = p.merge_cnt + 2 * fx.tu + g;
+            asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            last = atomicAdd(cnt, 1) == np - 1;
+            if (last) {
+              *reinterpret_cast<volatile int*>(cnt) = 0;  // every piece has counted in
+              asm volatile("fence.acq_rel.gpu;" ::: "memory");
+            }
+          }
+          S.merge_last[g] = last;
+        }
+        wg_sync();
+        if (S.merge_last[g]) {
+          const float* wml0 = p.ws + n_slots * kQChunk * kHd + static_cast<size_t>(fx.tu) * kQChunk * 2;
+          const size_t ml_stride = static_cast<size_t>(p.tail_units) * kQChunk * 2;
+          if (r < QH) {
+            // this column's (m, l) of every piece (loads in flight together), then the
+            // maximum and each piece's weight
+            const float* mlc = wml0 + (q0 + r) * 2;
+            float2 ml[kMaxPieces];
+#pragma unroll
+            for (int j = 0; j < kMaxPieces; ++j)
+              ml[j] = j < np ? __ldcg(reinterpret_cast<const float2*>(mlc + j * ml_stride)) : make_float2(-INFINITY, 0.0f);
+            float M = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < kMaxPieces; ++j) M = fmaxf(M, ml[j].x);
+            float L = 0.0f;
+#pragma unroll
+            for (int j = 0; j < kMaxPieces; ++j) {
+              const float w = (ml[j].x == -INFINITY) ? 0.0f : exp2f(ml[j].x - M);
+              L = fmaf(w, ml[j].y, L);
+              S.mrg_w[j][q0 + r] = w;
+            }
+            S.inv_l[q0 + r] = L > 0.0f ? 1.0f / L : 0.0f;
+          }
+          wg_sync();
+          // per chunk of 4 columns of this thread's hd row: every piece's 16-byte vector,
+          // all loads in flight together, folded in piece order
+          const float4* wo0 = reinterpret_cast<const float4*>(p.ws + static_cast<size_t>(fx.tu) * kQChunk * kHd) +
+                              (q0 / 4) * kHd + r;
+          const size_t o_stride = static_cast<size_t>(p.tail_units) * kQChunk * kHd / 4;
+#pragma unroll
+          for (int c = 0; c < QH / 4; ++c) {
+            float4 v[kMaxPieces];
+#pragma unroll
+            for (int j = 0; j < kMaxPieces; ++j)
+              v[j] = j < np ? __ldcg(wo0 + j * o_stride + c * kHd) : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+#pragma unroll
+            for (int j = 0; j < kMaxPieces; ++j) {
+              const float* wj = S.mrg_w[j] + q0 + 4 * c;
+              a0 = fmaf(wj[0], v[j].x, a0);
+              a1 = fmaf(wj[1], v[j].y, a1);
+              a2 = fmaf(wj[2], v[j].z, a2);
+              a3 = fmaf(wj[3], v[j].w, a3);
+            }
+            o[4 * c] = a0;
+            o[4 * c + 1] = a1;
+            o[4 * c + 2] = a2;
+            o[4 * c + 3] = a3;
+          }
+          __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(frow0) * p.D + fx.h * kHd + r;
+#pragma unroll
+          for (int i = 0; i < QH; ++i) {
+            const int q = q0 + i;
+            if (ok && q < fnrows) out[static_cast<size_t>(q) * p.D] = __float2bfloat16_rn(o[i] * S.inv_l[q]);
+          }
+        }
       } else if (p.n_splits == 1) {
         __nv_bfloat16* out = reinterpret_cast<__nv_bfloat16*>(p.out) + static_cast<size_t>(frow0) * p.D + fx.h * kHd + r;
         const float4* il4 = reinterpret_cast<const float4*>(S.inv_l + q0);
@@ -656,16 +808,32 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       return jj < p.slots ? __ldg(p.kv_scale + (static_cast<size_t>(y.b) * p.slots + jj) * 2 * p.H + y.h) : 0.0f;
     };
     auto first_tile = [&](int from, Unit& y) -> bool {
-      for (int r2 = from, u2 = cta_unit(p, r2); u2 < p.units; u2 = cta_unit(p, ++r2)) {
-        y = decode_unit(p, u2, order);
+      for (int r2 = from; cta_item<PIECES>(p, r2, order, y); ++r2)
         if (y.t1 > y.t0) return true;
-      }
       return false;
     };
     float ks_next = 0.0f;
     if constexpr (FP8) {
       Unit y;
       if (first_tile(0, y)) ks_next = fetch_ks(y, y.t0);
+    }
+
+    // Flash-Verify tags of the unit about to start, fetched one unit ahead: this
+    // thread's row tid of the sequence (view tag, position) and the view tag of its
+    // query column r of the chunk (warpgroup 0)
+    // (bf16 caches; with e4m3 the registers are scarcer and the tags are read at the
+    // unit's start)
+    constexpr bool kPrefetchView = !FP8;
+    int pf_view = 0, pf_pos = -1, pf_qview = 0;
+    auto prefetch_view = [&](const Unit& y) {
+      const int yrow0 = y.b * p.n_tok;
+      pf_view = tid < p.n_tok ? __ldg(p.view + yrow0 + tid) : 0;
+      pf_pos = tid < p.n_tok ? __ldg(p.positions + yrow0 + tid) : -1;
+      pf_qview = r < min(kQChunk, p.n_tok - y.qc * kQChunk) ? __ldg(p.view + yrow0 + y.qc * kQChunk + r) : 0;
+    };
+    if (kPrefetchView && has_view) {
+      Unit y;
+      if (cta_item<PIECES>(p, 0, order, y)) prefetch_view(y);
     }
 
     float o_prev[QH], l_prev[QH];  // the unit waiting to be finished (deferred finish only)
@@ -675,8 +843,8 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     bool pending = false;
     int uu = 0;  // units started by this CTA (parity selects the finish buffers)
 
-    for (int rnd = 0, u = cta_unit(p, 0); u < p.units; u = cta_unit(p, ++rnd), ++uu) {
-      const Unit x = decode_unit(p, u, order);
+    Unit x;
+    for (int rnd = 0; cta_item<PIECES>(p, rnd, order, x); ++rnd, ++uu) {
       const int row0 = x.b * p.n_tok;  // first row of the sequence
       const int nrows = min(kQChunk, p.n_tok - x.qc * kQChunk);  // valid columns of this chunk
       const int kend = key_end(p, x.b);  // regular slots past this are not attended
@@ -695,10 +863,17 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         if (tid == 0) S.n_draft = 0;
         both_sync();
         int my_draft = 0;
+        // the first row of each thread from the values fetched during the previous unit,
+        // any further rows (more rows than softmax threads) straight from memory
+        if constexpr (!kPrefetchView) {
+          Unit y = x;
+          prefetch_view(y);
+        }
         for (int t = tid; t < p.n_tok; t += kSmWarps * 32) {
-          const int v = p.view[row0 + t];
+          const bool first = t == tid;
+          const int v = first ? pf_view : p.view[row0 + t];
           if (v == DLLM_VIEW_MASK) {
-            const int pos = p.positions[row0 + t];
+            const int pos = first ? pf_pos : p.positions[row0 + t];
             if (pos >= 0 && pos < p.max_pos) atomicOr(&S.mask_bits[pos >> 5], 1u << (pos & 31));
           } else if (v == DLLM_VIEW_DRAFT) {
             ++my_draft;
@@ -706,11 +881,16 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         }
         if (my_draft) atomicAdd(&S.n_draft, my_draft);
         if (g == 0 && quarter < 2) {  // quarters 0 and 1 of warpgroup 0 tag columns 0..63
-          const bool is_draft = r < nrows && p.view[row0 + x.qc * kQChunk + r] == DLLM_VIEW_DRAFT;
+          const bool is_draft = r < nrows && pf_qview == DLLM_VIEW_DRAFT;
           const uint32_t bal = __ballot_sync(0xffffffffu, is_draft);
           if (lane == 0) S.draft_qmask[quarter] = bal;
         }
         both_sync();
+        // the next unit's tags, fetched now so that their latency hides behind this unit
+        if constexpr (kPrefetchView) {
+          Unit y;
+          if (cta_item<PIECES>(p, rnd + 1, order, y)) prefetch_view(y);
+        }
       }
       const int n_draft = has_view ? min(S.n_draft, p.tail) : 0;
       const uint64_t dmask = has_view ? (static_cast<uint64_t>(S.draft_qmask[1]) << 32) | S.draft_qmask[0] : 0ull;
@@ -842,7 +1022,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         // ---- D: fold the previous tile's P V into the accumulators (in a unit's first
         // tile: finish the previous unit instead, when that was deferred)
         if (kDefer && t == x.t0 && pending) {
-          finish(o_prev, l_prev, px, puu, ppv);
+          finish(false, o_prev, l_prev, px, puu, ppv);
           pending = false;
         }
         if (t > x.t0) {
@@ -871,20 +1051,24 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       // ---- unit end: finish now, or hand the state to the next unit's first tile
       if constexpr (kDefer) {
         if (pending) {  // this unit had no tile to finish the previous one in
-          finish(o_prev, l_prev, px, puu, ppv);
+          finish(false, o_prev, l_prev, px, puu, ppv);
           pending = false;
         }
+        if (PIECES && x.part != 0) {
+          finish(true, o_acc, l_part, x, uu, pv_cnt - 1);
+        } else {
 #pragma unroll
-        for (int i = 0; i < QH; ++i) {
-          o_prev[i] = o_acc[i];
-          l_prev[i] = l_part[i];
+          for (int i = 0; i < QH; ++i) {
+            o_prev[i] = o_acc[i];
+            l_prev[i] = l_part[i];
+          }
+          px = x;
+          puu = uu;
+          ppv = pv_cnt - 1;
+          pending = true;
         }
-        px = x;
-        puu = uu;
-        ppv = pv_cnt - 1;
-        pending = true;
       } else {
-        finish(o_acc, l_part, x, uu, pv_cnt - 1);
+        finish(true, o_acc, l_part, x, uu, pv_cnt - 1);
       }
       // the next unit's set-up rewrites the running max (per warpgroup) and the shared tags
       if (has_view)
@@ -893,7 +1077,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         wg_sync();
     }
     if constexpr (kDefer) {
-      if (pending) finish(o_prev, l_prev, px, puu, ppv);
+      if (pending) finish(false, o_prev, l_prev, px, puu, ppv);
     }
     if (!ok) {
       *abort_flag = 1;
@@ -923,10 +1107,8 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     };
     // the first tile of the first non-empty unit from round `from` on
     auto next_tile = [&](int from, Unit& y) -> bool {
-      for (int r2 = from, u2 = cta_unit(p, r2); u2 < p.units; u2 = cta_unit(p, ++r2)) {
-        y = decode_unit(p, u2, order);
+      for (int r2 = from; cta_item<PIECES>(p, r2, order, y); ++r2)
         if (y.t1 > y.t0) return true;
-      }
       return false;
     };
     float nvs = 0.0f;
@@ -937,8 +1119,8 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     // The four converter warps share a named barrier once per unit, so after a failed
     // wait a warp keeps walking the units (doing no work) instead of leaving the loop:
     // every warp passes that barrier the same number of times.
-    for (int rnd = 0, u = cta_unit(p, 0); u < p.units; u = cta_unit(p, ++rnd), ++uu) {
-      const Unit x = decode_unit(p, u, order);
+    Unit x;
+    for (int rnd = 0; cta_item<PIECES>(p, rnd, order, x); ++rnd, ++uu) {
       {
         // Q chunk -> (Q_hi, Q_lo, 1/s).  Warp cw takes columns [32 cw, 32 cw + 32) of rows
         // lane and lane + 32: 64 bytes of bf16 from box cw / 2 of the Q tile, 32 bytes of
@@ -1150,20 +1332,30 @@ int launch_state_merge(const float* a, const float* b, int rows, int H, void* ou
   return (int)cudaGetLastError();
 }
 
-template <int NQ, bool FP8>
-int launch_one(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, int grid, cudaStream_t s) {
+template <int NQ, bool FP8, bool PIECES = false>
+int launch_one(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, const CUtensorMap& tm_kv_tail,
+               int grid, cudaStream_t s) {
+  if constexpr (!FP8 && !PIECES) {
+    if (p.tail_pieces > 0) return launch_one<NQ, false, true>(p, tm_q, tm_kv, tm_kv_tail, grid, s);
+  }
   const size_t smem = sizeof(Smem<NQ, FP8>) + 1024;
-  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(attn_cache_tc<NQ, FP8>), (int)smem);
+  cudaError_t e = ensure_smem_limit(reinterpret_cast<const void*>(attn_cache_tc<NQ, FP8, PIECES>), (int)smem);
   if (e != cudaSuccess) return (int)e;
-  return (int)launch_pdl(attn_cache_tc<NQ, FP8>, dim3(grid), dim3(Cfg<NQ, FP8>::kThreads), smem, s, tm_q, tm_kv, p);
+  return (int)launch_pdl(attn_cache_tc<NQ, FP8, PIECES>, dim3(grid), dim3(Cfg<NQ, FP8>::kThreads), smem, s, tm_q,
+                         tm_kv, tm_kv_tail, p);
 }
 
-int launch_attn_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, int grid,
-                   cudaStream_t s) {
+int launch_attn_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                   const CUtensorMap& tm_kv_tail, int grid, cudaStream_t s) {
   const bool fp8 = p.kv_dtype == DLLM_E4M3;
-  if (p.nq_pad <= 32) return fp8 ? launch_one<32, true>(p, tm_q, tm_kv, grid, s) : launch_one<32, false>(p, tm_q, tm_kv, grid, s);
-  if (p.nq_pad <= 48) return fp8 ? launch_one<48, true>(p, tm_q, tm_kv, grid, s) : launch_one<48, false>(p, tm_q, tm_kv, grid, s);
-  return fp8 ? launch_one<64, true>(p, tm_q, tm_kv, grid, s) : launch_one<64, false>(p, tm_q, tm_kv, grid, s);
+  if (p.nq_pad <= 32)
+    return fp8 ? launch_one<32, true>(p, tm_q, tm_kv, tm_kv_tail, grid, s)
+               : launch_one<32, false>(p, tm_q, tm_kv, tm_kv_tail, grid, s);
+  if (p.nq_pad <= 48)
+    return fp8 ? launch_one<48, true>(p, tm_q, tm_kv, tm_kv_tail, grid, s)
+               : launch_one<48, false>(p, tm_q, tm_kv, tm_kv_tail, grid, s);
+  return fp8 ? launch_one<64, true>(p, tm_q, tm_kv, tm_kv_tail, grid, s)
+             : launch_one<64, false>(p, tm_q, tm_kv, tm_kv_tail, grid, s);
 }
 
 int launch_attn_combine(const AttnParams& p, cudaStream_t s) {

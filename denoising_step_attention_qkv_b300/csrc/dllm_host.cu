@@ -130,13 +130,14 @@ bool map_2d_bf16(CUtensorMap* m, const void* ptr, uint64_t cols, uint64_t rows, 
 }
 
 // 3-D tile map over one layer of the cache viewed as [B*slots][2H][hd].
-bool map_cache(CUtensorMap* m, const void* layer, int kv_dtype, int hd, int H, uint64_t rows) {
+bool map_cache(CUtensorMap* m, const void* layer, int kv_dtype, int hd, int H, uint64_t rows,
+               uint32_t box_rows = kKeyTile) {
   auto enc = encode_fn();
   if (!enc) return false;
   const uint32_t eb = kv_dtype == DLLM_E4M3 ? 1 : 2;
   cuuint64_t dims[3] = {(cuuint64_t)hd, (cuuint64_t)(2 * H), rows};
   cuuint64_t strides[2] = {(cuuint64_t)hd * eb, (cuuint64_t)2 * H * hd * eb};
-  cuuint32_t box[3] = {128u / eb, 1, (cuuint32_t)kKeyTile};
+  cuuint32_t box[3] = {128u / eb, 1, (cuuint32_t)box_rows};
   cuuint32_t es[3] = {1, 1, 1};
   const CUtensorMapDataType dt = kv_dtype == DLLM_E4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
   return enc(m, dt, 3, const_cast<void*>(layer), dims, strides, box, es, CU_TENSOR_MAP_INTERLEAVE_NONE,
@@ -228,16 +229,22 @@ int dllm_cache_alloc(const dllm_cache_desc* desc, dllm_cache** out) {
     const size_t bytes = rows * 6 * sizeof(float) + rows * sizeof(int) + (size_t)desc->batch * sizeof(int);
     e = dev_alloc(&c->drift_acc, bytes);
     if (e != cudaSuccess) return fail(from_cuda(e));
+    c->drift_acc_bytes = bytes;
     c->drift_rows = reinterpret_cast<int*>(c->drift_acc + rows * 6);
     c->drift_seqs = c->drift_rows + rows;
     e = cudaMemset(c->drift_acc, 0, bytes);
     if (e != cudaSuccess) return fail(from_cuda(e));
   }
 
-  // split-KV partials: at most 2 * (2 * SMs) units of kQChunk rows
+  // split-KV partials: at most 2 * (2 * SMs) units of kQChunk rows (stream-K: two
+  // slots per CTA), and the stream-K arrival counts (zeroed)
   if (desc->kv_dtype != DLLM_F32) {
     c->ws_floats = (size_t)4 * c->sm_count * kQChunk * (kHd + 2);
     e = dev_alloc(&c->ws, c->ws_floats * sizeof(float));
+    if (e != cudaSuccess) return fail(from_cuda(e));
+    e = dev_alloc(&c->merge_cnt, (size_t)2 * c->sm_count * sizeof(int));
+    if (e != cudaSuccess) return fail(from_cuda(e));
+    e = cudaMemset(c->merge_cnt, 0, (size_t)2 * c->sm_count * sizeof(int));
     if (e != cudaSuccess) return fail(from_cuda(e));
   }
   *out = c;
@@ -253,6 +260,7 @@ int dllm_cache_free(dllm_cache* c) {
   if (c->drift_cnt) cudaFree(c->drift_cnt);
   if (c->drift_acc) cudaFree(c->drift_acc);
   if (c->ws) cudaFree(c->ws);
+  if (c->merge_cnt) cudaFree(c->merge_cnt);
   delete c;
   return DLLM_OK;
 }
@@ -472,6 +480,30 @@ struct SplitScratch {
   size_t floats = 0;
 };
 
+// Tensor maps of an attention launch: Q (a.nq_pad rows a box), the layer's cache (128
+// rows a box), and, when the launch's last key tile runs past the sequence's slots, the
+// cache with boxes of only that tile's rows (sets a.tail_rows; else a copy of tm_kv).
+int attn_maps(dllm_cache* c, int layer, const void* q, int n_tok, AttnParams& a, CUtensorMap* tm_q, CUtensorMap* tm_kv,
+              CUtensorMap* tm_kv_tail) {
+  const dllm_cache_desc& d = c->desc;
+  const int H = d.n_heads, hd = d.head_dim, D = H * hd;
+  if (!map_2d_bf16(tm_q, q, D, (uint64_t)d.batch * n_tok, 64, a.nq_pad)) return DLLM_ECUDA;
+  const uint64_t rows = (uint64_t)d.batch * c->slots;
+  if (!map_cache(tm_kv, layer_kv(c, layer), d.kv_dtype, hd, H, rows)) return DLLM_ECUDA;
+  a.tail_rows = 0;
+  *tm_kv_tail = *tm_kv;
+  const int last = a.tile_lo + a.key_tiles - 1;  // the launch's last key tile
+  const int valid = c->slots - last * kKeyTile;   // slots of the sequence in that tile
+  if (valid > 0 && valid < kKeyTile) {
+    a.tail_rows = std::min(kKeyTile, (valid + 7) / 8 * 8);
+    if (a.tail_rows < kKeyTile &&
+        !map_cache(tm_kv_tail, layer_kv(c, layer), d.kv_dtype, hd, H, rows, (uint32_t)a.tail_rows))
+      return DLLM_ECUDA;
+    if (a.tail_rows == kKeyTile) a.tail_rows = 0;
+  }
+  return DLLM_OK;
+}
+
 int do_attend(dllm_cache* c, int layer, const int32_t* positions, const uint8_t* view, int n_tok, void* out,
               cudaStream_t s, const KeyRange& kr = KeyRange(), const SplitScratch& scratch = SplitScratch()) {
   if (n_tok == 0) return DLLM_OK;
@@ -516,6 +548,62 @@ int do_attend(dllm_cache* c, int layer, const int32_t* positions, const uint8_t*
   a.key_tiles = kr.hi >= 0 ? ceil_div(a.key_hi, kKeyTile) - a.tile_lo
                            : ceil_div(d.max_pos + (view ? d.tail_slots : 0), kKeyTile);
   const int base = B * H * a.n_qchunks;
+  const size_t scratch_floats = scratch.get ? scratch.floats : c->ws_floats;
+  // Balanced schedule: full waves of whole units, then the remaining units (fewer than
+  // the SMs) cut into equal pieces that all SMs share, merged in the kernel by whichever
+  // CTA completes a unit.  The piece count minimises the largest number of key tiles a
+  // CTA runs, counting a merge as one tile; ties go to fewer pieces, and one piece is
+  // the plain round-robin.  Only with at least one full wave: with fewer units than SMs
+  // the merge would sit on every CTA's path, and the key split below with its second
+  // kernel measured faster (batch 1: 16.5 against 18.4 us).  Not for ragged batches
+  // (unequal units) or partial-state launches (one unit per row), nor e4m3 caches, whose
+  // tiles are bound by the per-tile conversion chain: there a piece's extra boundary (the
+  // Q split, the merge) cost more than the balance gained (86 against 80 us on the
+  // batch-8, 3072-slot cache).  The same rule holds for every scratch, so that each
+  // entry point makes the same choice.
+  if (d.kv_dtype == DLLM_BF16 && !kr.key_len && !a.state && !a.state_in && base >= c->sm_count) {
+    const int sm = c->sm_count, kt = a.key_tiles;
+    const int waves = base / sm, tail = base - waves * sm;
+    const size_t slot_floats = (size_t)kQChunk * (kHd + 2);
+    const size_t max_slots = std::min(c->ws_floats, (size_t)DLLM_NOALLOC_SCRATCH_BYTES / sizeof(float)) / slot_floats;
+    int best_k = 1, best_tps = kt;
+    long long best = -1;
+    for (int k = 1; tail > 0 && k <= kMaxPieces && k <= kt; ++k) {
+      const int tps = ceil_div(kt, k), kk = ceil_div(kt, tps);
+      if (kk != k || (size_t)tail * kk > max_slots) continue;
+      const long long items = (long long)tail * kk;
+      const long long grid_k = waves ? sm : std::min<long long>(items, sm);
+      const long long cost = (long long)waves * kt + (items + grid_k - 1) / grid_k * tps + (kk > 1 ? 1 : 0);
+      if (best < 0 || cost < best) {
+        best = cost;
+        best_k = kk;
+        best_tps = tps;
+      }
+    }
+    if (best_k > 1) {
+      a.n_splits = 1;
+      a.tiles_per_split = kt;
+      a.units = base;
+      a.dp_waves = waves;
+      a.tail_units = tail;
+      a.tail_pieces = best_k;
+      a.piece_tiles = best_tps;
+      a.merge_cnt = c->merge_cnt;
+      if ((size_t)tail * best_k * slot_floats > scratch_floats) return DLLM_EUNSUPPORTED;
+      if (scratch.get) {
+        rc = scratch.get(&a.ws);
+        if (rc) return rc;
+      }
+      const int grid = waves ? sm : std::min(tail * best_k, sm);
+      CUtensorMap tm_q, tm_kv, tm_kv_tail;
+      rc = attn_maps(c, layer, kr.q ? kr.q : out, n_tok, a, &tm_q, &tm_kv, &tm_kv_tail);
+      if (rc) return rc;
+      rc = launch_attn_tc(a, tm_q, tm_kv, tm_kv_tail, grid, s);
+      return rc ? from_cuda((cudaError_t)rc) : DLLM_OK;
+    }
+  }
+  // Fewer units than SMs where the balanced schedule does not apply (ragged batches,
+  // e4m3 caches): the keys split evenly, partial states merged by a second kernel.
   int splits = 1;
   if (base < c->sm_count && !a.state && !a.state_in) {  // states are per row: one unit per row
     splits = ceil_div(c->sm_count, base);
@@ -533,11 +621,11 @@ int do_attend(dllm_cache* c, int layer, const int32_t* positions, const uint8_t*
     }
   }
 
-  CUtensorMap tm_q, tm_kv;
-  if (!map_2d_bf16(&tm_q, kr.q ? kr.q : out, D, (uint64_t)B * n_tok, 64, a.nq_pad)) return DLLM_ECUDA;
-  if (!map_cache(&tm_kv, layer_kv(c, layer), d.kv_dtype, hd, H, (uint64_t)B * c->slots)) return DLLM_ECUDA;
+  CUtensorMap tm_q, tm_kv, tm_kv_tail;
+  rc = attn_maps(c, layer, kr.q ? kr.q : out, n_tok, a, &tm_q, &tm_kv, &tm_kv_tail);
+  if (rc) return rc;
   const int grid = a.units < c->sm_count ? a.units : c->sm_count;
-  rc = launch_attn_tc(a, tm_q, tm_kv, grid, s);
+  rc = launch_attn_tc(a, tm_q, tm_kv, tm_kv_tail, grid, s);
   if (rc) return from_cuda((cudaError_t)rc);
   if (a.n_splits > 1) {
     rc = launch_attn_combine(a, s);
@@ -903,6 +991,13 @@ int dllm_cache_status(dllm_cache* c, int* device_bits) {
   if (e != cudaSuccess) return from_cuda(e);
   e = cudaMemset(c->status, 0, sizeof(int));
   if (e != cudaSuccess) return from_cuda(e);
+  if (bits & DLLM_DEV_TIMEOUT) {
+    // a kernel that gave up may have left its arrival counters part-way: start them over
+    e = cudaMemset(c->drift_cnt, 0, (size_t)c->desc.batch * sizeof(int));
+    if (e == cudaSuccess) e = cudaMemset(c->drift_acc, 0, c->drift_acc_bytes);
+    if (e == cudaSuccess && c->merge_cnt) e = cudaMemset(c->merge_cnt, 0, (size_t)2 * c->sm_count * sizeof(int));
+    if (e != cudaSuccess) return from_cuda(e);
+  }
   if (device_bits) *device_bits = bits;
   return bits ? DLLM_EDEVICE : DLLM_OK;
 }
@@ -930,7 +1025,8 @@ namespace {
 // Partial (O, m, l) states of the key splits.  One copy per device that loads this
 // library, kept until the process exits.  Every call shares it: calls whose kernels
 // overlap on the GPU race on it.  Nothing here has to start at zero, because the merge
-// only reads partials that the same call wrote just before.
+// only reads partials that the same call wrote just before (the arrival counts that
+// tell which CTA merges are the cache's own).
 static __device__ __align__(256) float g_noalloc_scratch[DLLM_NOALLOC_SCRATCH_BYTES / sizeof(float)];
 
 constexpr int kMaxDevices = 256;

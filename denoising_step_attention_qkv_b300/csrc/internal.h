@@ -34,6 +34,8 @@ struct dllm_cache {
   int* status;   // device status word
   float* ws;     // split-KV partials
   size_t ws_floats;
+  int* merge_cnt;  // [2 * sm_count] stream-K arrival counts; zero between calls
+  size_t drift_acc_bytes;
 };
 
 namespace dllm {
@@ -70,6 +72,7 @@ constexpr int kHd = 128;         // head_dim of the tensor-core path
 constexpr int kMaxDriftRows = 256;  // tracked rows per sequence of the fused drift test
 constexpr int kQChunk = 64;      // query rows per attention work unit (tensor-core path)
 constexpr int kKeyTile = 128;    // keys per attention tile
+constexpr int kMaxPieces = 4;    // pieces a tail unit of the attention may be cut into
 
 // ---------------------------------------------------------------- fused projection
 struct ProjParams {
@@ -146,6 +149,17 @@ struct AttnParams {
   // A cached state of the keys outside the range, same layout (no key splits then): the
   // finish merges it with the range's and writes the normalised output to `out`.
   const float* state_in;
+  // Balanced schedule (tail_pieces > 0; n_splits = 1): dp_waves rounds of whole units
+  // over the grid, then the last tail_units units (fewer than the grid) cut into
+  // tail_pieces pieces of piece_tiles key tiles; the CTA that completes a tail unit
+  // merges its pieces' partial states (ws: tail_units * tail_pieces slots of kQChunk rows,
+  // O then (m, l)) into the output.  merge_cnt: [2 * tail_units] arrival counts, zero on
+  // entry and on exit.
+  int dp_waves, tail_units, tail_pieces, piece_tiles;
+  int* merge_cnt;
+  // Rows loaded of a key tile that runs past the sequence's slots (a multiple of 8,
+  // through a tensor map with that box height); 0: every tile loads 128 rows.
+  int tail_rows;
   int* status;
 };
 
@@ -157,8 +171,10 @@ int launch_proj_tc(const ProjParams& p, const CUtensorMap& tm_x, const CUtensorM
 int launch_proj_pair(const ProjParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_xkv,
                      const CUtensorMap& tm_w, const CUtensorMap& tm_w_half, int grid, cudaStream_t s);
 int proj_pair_max_clusters(int* clusters);
-int launch_attn_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv, int grid,
-                   cudaStream_t s);
+// tm_kv_tail: the same cache with boxes of tail_rows rows, for a tile that runs past the
+// sequence's slots (used only when p.tail_rows != 0).
+int launch_attn_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv,
+                   const CUtensorMap& tm_kv_tail, int grid, cudaStream_t s);
 int launch_attn_combine(const AttnParams& p, cudaStream_t s);
 // Merge two partial softmax states (rows x heads, [hd + 2] each) into a normalised bf16
 // output and/or a merged state.

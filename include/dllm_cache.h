@@ -21,8 +21,9 @@
  *     cache, bf16 for DLLM_BF16 and DLLM_E4M3 caches.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and never synchronise, except dllm_cache_alloc/free/status.  A cache
- *     owns small workspaces (split-KV partials, drift arrival counters), so calls on
- *     one cache must be ordered (one stream, or events between streams).
+ *     owns small workspaces (split-KV partials and their arrival counters, drift
+ *     arrival counters), so calls on one cache must be ordered (one stream, or events
+ *     between streams).
  *   - A cache lives on the device that was current when dllm_cache_alloc created it;
  *     every call that launches work on it must be made with that device current,
  *     else it returns DLLM_EINVAL and launches nothing.
@@ -403,8 +404,8 @@ int dllm_elastic_step(dllm_cache* cache, int n_layers, const void* const* x_all,
                       void* out, float* cos, int32_t* flags, float* mass_out,
                       void* workspace, size_t workspace_bytes, void* stream);
 
-/* Scratch capacity of dllm_cache_attend_noalloc, in bytes (8 MiB). */
-#define DLLM_NOALLOC_SCRATCH_BYTES (8u << 20)
+/* Scratch capacity of dllm_cache_attend_noalloc, in bytes (16 MiB). */
+#define DLLM_NOALLOC_SCRATCH_BYTES (16u << 20)
 
 /* dllm_cache_attend for callers that cannot allocate device memory.  The pages have
  * no counterpart to this call; it exists for how the library is hosted, not for the
@@ -418,9 +419,11 @@ int dllm_elastic_step(dllm_cache* cache, int n_layers, const void* const* x_all,
  *
  * Arguments, results and errors are those of dllm_cache_attend, plus:
  *   - DLLM_EUNSUPPORTED when the split partial states of this call would need more
- *     than DLLM_NOALLOC_SCRATCH_BYTES (units * 64 query rows * 130 floats each; it
- *     happens only when batch * n_heads is below the SM count and the key range is
- *     long); nothing is launched then.
+ *     than DLLM_NOALLOC_SCRATCH_BYTES (one slot of 64 query rows * 130 floats per
+ *     piece); nothing is launched then.  Both entry points cut units into pieces only
+ *     as far as the pieces' states fit this size, so with the current kernels the case
+ *     does not arise.  The arrival counts that say which CTA completes a split unit are
+ *     the cache's own (allocated with it, back at zero after every call).
  *   - The first call on each device looks up the device address of that array (with
  *     the device current) and remembers it; make this first call before any stream
  *     capture begins.  cudaDeviceReset() discards the array with the rest of the
@@ -452,7 +455,9 @@ int dllm_selftest_wait_timeout(dllm_cache* cache, void* stream);
 int dllm_selftest_fail_alloc(int nth);
 
 /* Synchronise the device, read the cache's device status word into *device_bits (may
- * be NULL) and clear it.  Returns DLLM_EDEVICE if any bit was set, else DLLM_OK. */
+ * be NULL) and clear it.  Returns DLLM_EDEVICE if any bit was set, else DLLM_OK.  With
+ * DLLM_DEV_TIMEOUT set it also zeroes the cache's arrival counters (drift test, split
+ * attention), which a kernel that gave up may have left part-way. */
 int dllm_cache_status(dllm_cache* cache, int* device_bits);
 
 /* Static, human-readable name of a dllm_status. */

@@ -56,7 +56,7 @@ def test_device_range_errors_are_reported_not_faulted():
 def test_allocation_failure_returns_eoom_and_releases_everything(owned):
     # every device allocation of dllm_cache_alloc is made to fail in turn (the K/V buffer
     # when the library owns it, the rotary table, the status word, the drift counters,
-    # the fused drift workspace, the split-KV workspace); each attempt must return
+    # the fused drift workspace, the split-KV workspace and its arrival counts); each attempt must return
     # DLLM_EOOM with a NULL handle and give back what it had allocated before the failure
     import ctypes
     L = capi.lib()
@@ -65,7 +65,7 @@ def test_allocation_failure_returns_eoom_and_releases_everything(owned):
         1, B, S, 0, H, 128, capi.DLLM_BF16, 1e4, None, 0)), dtype=torch.uint8, device="cuda")
     desc = capi.dllm_cache_desc(1, B, S, 0, H, 128, capi.DLLM_BF16, 1e4,
                                 None if owned else ext.data_ptr(), 0 if owned else ext.numel())
-    n_allocs = 6 if owned else 5
+    n_allocs = 7 if owned else 6
     torch.cuda.synchronize()
     free0 = torch.cuda.mem_get_info()[0]
     for nth in range(1, n_allocs + 1):
