@@ -53,6 +53,11 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=12.0, help="budget of the CPU-baseline sample")
     ap.add_argument("--no-elastic", action="store_true", help="skip the multi-layer refresh step")
     ap.add_argument("--elastic-layers", type=int, default=32)
+    ap.add_argument("--probe", choices=["attend", "project"], default=None,
+                    help="run only this kernel of --probe-workload (for one-kernel profiler captures) and exit")
+    ap.add_argument("--probe-workload", default="llada8b-b8-refresh-fp8",
+                    choices=["llada8b-b32-drift", "llada8b-b1", "llada8b-b16-verify", "llada8b-b8-refresh-fp8"])
+    ap.add_argument("--probe-iters", type=int, default=5)
     return ap.parse_args()
 
 
@@ -319,6 +324,72 @@ def elastic_leg(args, dev, B, S, D, H, hd, theta, beta, k, gamma, flush, kv_dtyp
     return res
 
 
+OTHER_WORKLOADS = ("llada8b-b1", "llada8b-b16-verify", "llada8b-b8-refresh-fp8")
+
+
+def workload_calls(dev, wl_name, stream):
+    """A workload's cache (prefilled when the workload has a prefix) and its projection
+    and attention calls on `stream`.  Returns (workload, cache, project, attend, x, kv_x,
+    view)."""
+    import torch
+    import workloads as W
+    from denoising_step_attention_qkv_b300 import capi
+    kvt = {"bf16": capi.DLLM_BF16, "e4m3": capi.DLLM_E4M3}
+
+    def bf(a):
+        return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).to(dev)
+
+    wl = W.make(wl_name)
+    s = wl.shape
+    cache = capi.Cache(1, s.batch, s.max_pos, s.n_heads, s.head_dim, kvt[s.kv], s.rope_theta, s.tail_slots,
+                       device=dev)
+    w = bf(wl.w)
+    if wl.pre_x is not None:
+        capi.dllm_cache_step(cache.handle, 0, None, w, None, None, None, kv_x=bf(wl.pre_x),
+                             kv_positions=torch.from_numpy(wl.pre_pos).to(dev))
+    x = bf(wl.x)
+    pos = torch.from_numpy(wl.positions).to(dev)
+    view = torch.from_numpy(wl.view).to(dev) if wl.view is not None else None
+    kv_x = bf(wl.kv_x) if wl.kv_x is not None else None
+    kv_pos = torch.from_numpy(wl.kv_pos).to(dev) if wl.kv_pos is not None else None
+    out = torch.empty_like(x)
+
+    def project(st=stream):
+        capi.dllm_cache_project(cache.handle, 0, x, w, pos, view, out, kv_x=kv_x, kv_positions=kv_pos, stream=st)
+
+    def attend(st=stream):
+        capi.dllm_cache_attend(cache.handle, 0, pos, view, out, stream=st)
+
+    return wl, cache, project, attend, x, kv_x, view
+
+
+def probe(args):
+    """One kernel of one workload, alone: the projection once (the attention's queries),
+    then `--probe-iters` calls of the probed kernel, and one JSON line with their median
+    time.  For one-kernel profiler captures; no other work runs."""
+    import torch
+    from denoising_step_attention_qkv_b300 import capi
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.current_stream(dev)
+    wl, cache, project, attend, *_ = workload_calls(dev, args.probe_workload, stream)
+    project()
+    fn = attend if args.probe == "attend" else project
+    evs = []
+    for _ in range(args.probe_iters):
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record(stream)
+        fn()
+        b_.record(stream)
+        evs.append((a_, b_))
+    torch.cuda.synchronize(dev)
+    rc, bits = cache.status()
+    if rc != capi.DLLM_OK:
+        raise RuntimeError(f"device status {bits:#x}")
+    print(json.dumps({"probe": args.probe, "workload": wl.name, "iters": args.probe_iters,
+                      "median_us": statistics.median(a_.elapsed_time(b_) for a_, b_ in evs) * 1e3}), flush=True)
+
+
 def other_configs(dev, flush, n_iter=30):
     """Projection and attention of the other workloads against their rooflines: the
     LLaDA-8B layer at batch 1 (eager and replayed as one CUDA graph, which shows the
@@ -326,14 +397,9 @@ def other_configs(dev, flush, n_iter=30):
     slots) and the batch-8 full refresh into an e4m3 cache (every non-block position
     K/V, then the 32-row block).  Per-call CUDA events, L2 flushed before each call."""
     import torch
-    import workloads as W
     from denoising_step_attention_qkv_b300 import capi
     pk = peaks()
     stream = torch.cuda.current_stream(dev)
-    kvt = {"bf16": capi.DLLM_BF16, "e4m3": capi.DLLM_E4M3}
-
-    def bf(a):
-        return torch.from_numpy(np.ascontiguousarray(a, np.float32)).to(torch.bfloat16).to(dev)
 
     def timed(fn):
         for _ in range(3):
@@ -350,30 +416,12 @@ def other_configs(dev, flush, n_iter=30):
         return statistics.median(a_.elapsed_time(b_) for a_, b_ in evs) * 1e3
 
     res = {}
-    for wl_name in ("llada8b-b1", "llada8b-b16-verify", "llada8b-b8-refresh-fp8"):
-        wl = W.make(wl_name)
+    for wl_name in OTHER_WORKLOADS:
+        wl, cache, project, attend, x, kv_x, view = workload_calls(dev, wl_name, stream)
         s = wl.shape
         B, D, H, hd, S, T = s.batch, s.D, s.n_heads, s.head_dim, s.max_pos, s.tail_slots
-        cache = capi.Cache(1, B, S, H, hd, kvt[s.kv], s.rope_theta, T, device=dev)
-        w = bf(wl.w)
-        if wl.pre_x is not None:
-            capi.dllm_cache_step(cache.handle, 0, None, w, None, None, None, kv_x=bf(wl.pre_x),
-                                 kv_positions=torch.from_numpy(wl.pre_pos).to(dev))
-        x = bf(wl.x)
-        pos = torch.from_numpy(wl.positions).to(dev)
-        view = torch.from_numpy(wl.view).to(dev) if wl.view is not None else None
-        kv_x = bf(wl.kv_x) if wl.kv_x is not None else None
-        kv_pos = torch.from_numpy(wl.kv_pos).to(dev) if wl.kv_pos is not None else None
-        out = torch.empty_like(x)
         n = x.shape[1]
         n_kv = 0 if kv_x is None else kv_x.shape[1]
-
-        def project():
-            capi.dllm_cache_project(cache.handle, 0, x, w, pos, view, out, kv_x=kv_x, kv_positions=kv_pos,
-                                    stream=stream)
-
-        def attend():
-            capi.dllm_cache_attend(cache.handle, 0, pos, view, out, stream=stream)
 
         # attention alone, timed first (before the projection's long power-capped GEMM
         # loop): after one projection, each call attends with the previous call's output
@@ -405,11 +453,11 @@ def other_configs(dev, flush, n_iter=30):
             s_cap.wait_stream(stream)
             with torch.cuda.stream(s_cap):
                 for _ in range(2):
-                    capi.dllm_cache_project(cache.handle, 0, x, w, pos, view, out, stream=s_cap)
-                    capi.dllm_cache_attend(cache.handle, 0, pos, view, out, stream=s_cap)
+                    project(s_cap)
+                    attend(s_cap)
                 with torch.cuda.graph(g, stream=s_cap):
-                    capi.dllm_cache_project(cache.handle, 0, x, w, pos, view, out, stream=s_cap)
-                    capi.dllm_cache_attend(cache.handle, 0, pos, view, out, stream=s_cap)
+                    project(s_cap)
+                    attend(s_cap)
             stream.wait_stream(s_cap)
             r["project_attend_graph_us"] = timed(g.replay)
             r["project_attend_eager_us"] = timed(lambda: (project(), attend()))
@@ -871,6 +919,10 @@ def _with_drift_inputs(wl):
 def main():
     args = parse()
     rank, world, local = dist_env()
+    if args.probe is not None:
+        if rank == 0:
+            probe(args)
+        return
     if args.impl == "reference":
         if rank != 0:
             return

@@ -324,6 +324,9 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
   constexpr int KST = C::KST, VST = C::VST, SST = C::SST;
   constexpr int kSmWarps = 4 * C::kSmWG;  // softmax warps
   constexpr int QH = NQ / C::kSmWG;      // query columns of each softmax warpgroup
+  // With 32 bf16 queries a unit's finish runs inside the next unit's first tile (see the
+  // softmax warps); the other variants finish at the unit's end.
+  constexpr bool kDefer = (NQ == 32) && !FP8;
   extern __shared__ uint8_t smem_raw[];
   Smem<NQ, FP8>& S =
       *reinterpret_cast<Smem<NQ, FP8>*>(smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u));
@@ -492,9 +495,10 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       return true;
     };
 
-    // The P V of a unit's last tile stays pending until the next unit's first S MMA has
-    // been issued (or an empty unit, or the end), so at unit boundaries too the softmax
-    // finds its next S ready.
+    // With a deferred finish, the P V of a unit's last tile stays pending until the next
+    // unit's first S MMA has been issued (or an empty unit, or the end), so at unit
+    // boundaries too the softmax finds its next S ready.  Without one, the softmax's
+    // finish waits for that P V, so it is issued at once.
     bool pv_pending = false;
     Unit x;
     for (int rnd = 0; ok && cta_item<PIECES>(p, rnd, order, x); ++rnd, ++uu) {
@@ -541,6 +545,10 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         pv_pending = true;
       }
       if (!ok) break;
+      if (!kDefer && pv_pending) {
+        if (!issue_pv()) { ok = false; break; }
+        pv_pending = false;
+      }
       tc_commit(&S.q_empty[qb]);
     }
     if (ok && pv_pending && !issue_pv()) ok = false;
@@ -586,7 +594,6 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     // split partials) waits for that P V MMA.  With 32 bf16 queries the finish is
     // deferred into the next unit's first tile, whose P V fold slot is empty, so the
     // wait hides behind that tile's softmax.
-    constexpr bool kDefer = (NQ == 32) && !FP8;
     constexpr int kSt = kHd + 2;
     // can_merge (a constant at every call site): whether this call may finish a
     // stream-K piece (deferred finishes never do: pieces finish at once, which keeps the
