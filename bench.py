@@ -597,7 +597,7 @@ def run_ours(args, rank, world, local):
     # ---- end to end through the C ABI with host buffers (copies inside the timed region).
     # Every step copies its inputs from pinned host memory and reads its results back.
     # Steady state is one CUDA graph per step with three independent branches: the
-    # copy-in of step i+1, the four kernels of step i and the read-back of step i-1, on
+    # copy-in of step i+1, the kernels of step i and the read-back of step i-1, on
     # double-buffered device tensors, so a step costs the slowest branch.  The timed
     # region is the copy-in of step 0, K graph launches and the read-back of step K-1
     # (the graphs also copy in one step too many and read back one too many: counted).
@@ -852,7 +852,9 @@ def run_ours(args, rank, world, local):
                 "per_kernel": graded}
     # top-k, gather, projection with the drift test, attention (+ the split-KV merge when
     # units < SMs)
-    n_launch_per_step = 4 + (1 if B * s.n_heads < torch.cuda.get_device_properties(dev).multi_processor_count else 0)
+    # top-k, gather, projection, the drift test's finalize, attention (+ the split merge
+    # when the units are fewer than the SMs)
+    n_launch_per_step = 5 + (1 if B * s.n_heads < torch.cuda.get_device_properties(dev).multi_processor_count else 0)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",

@@ -224,14 +224,12 @@ int dllm_cache_alloc(const dllm_cache_desc* desc, dllm_cache** out) {
   e = cudaMemset(c->drift_cnt, 0, (size_t)desc->batch * sizeof(int));
   if (e != cudaSuccess) return fail(from_cuda(e));
   {
-    // fused drift test: partial sums, row arrivals, sequence arrivals (one block, zeroed)
+    // fused drift test: the partial sums (zeroed; the finalize kernel zeroes them again)
     const size_t rows = (size_t)desc->batch * kMaxDriftRows;
-    const size_t bytes = rows * 6 * sizeof(float) + rows * sizeof(int) + (size_t)desc->batch * sizeof(int);
+    const size_t bytes = rows * 6 * sizeof(float);
     e = dev_alloc(&c->drift_acc, bytes);
     if (e != cudaSuccess) return fail(from_cuda(e));
     c->drift_acc_bytes = bytes;
-    c->drift_rows = reinterpret_cast<int*>(c->drift_acc + rows * 6);
-    c->drift_seqs = c->drift_rows + rows;
     e = cudaMemset(c->drift_acc, 0, bytes);
     if (e != cudaSuccess) return fail(from_cuda(e));
   }
@@ -382,8 +380,6 @@ ProjParams make_proj(dllm_cache* c, const StepArgs& a) {
   if (a.drift_cos != nullptr) {
     p.probe = nullptr;
     p.drift_acc = c->drift_acc;
-    p.drift_rows = c->drift_rows;
-    p.drift_seqs = c->drift_seqs;
     p.drift_cos = a.drift_cos;
     p.drift_refresh = a.drift_refresh;
     p.drift_gamma = a.drift_gamma;
@@ -441,6 +437,7 @@ int do_project(dllm_cache* c, const StepArgs& a, void* raw_q = nullptr, void* ra
     split_tail(p.pmt_q * (3 * D / 256) + p.pmt_kv * (2 * D / 256), pairs);
     const int grid = 2 * (p.items_total < pairs ? p.items_total : pairs);
     rc = launch_proj_pair(p, tm_x, tm_xkv, tm_w, tm_w_half, grid, a.s);
+    if (!rc && p.drift_acc) rc = launch_drift_finalize(p, a.s);
     return rc ? from_cuda((cudaError_t)rc) : DLLM_OK;
   }
   p.mt_q = ceil_div(p.m_q, 128);
@@ -459,6 +456,7 @@ int do_project(dllm_cache* c, const StepArgs& a, void* raw_q = nullptr, void* ra
   if (p.m_kv == 0) tm_xkv = tm_w;
   const int grid = p.items_total < c->sm_count ? p.items_total : c->sm_count;
   rc = launch_proj_tc(p, tm_x, tm_xkv, tm_w, tm_w_half, bn, grid, a.s);
+  if (!rc && p.drift_acc) rc = launch_drift_finalize(p, a.s);
   return rc ? from_cuda((cudaError_t)rc) : DLLM_OK;
 }
 

@@ -17,11 +17,8 @@ struct dllm_cache {
   int pair_clusters;  // clusters of two projection CTAs resident at once (0 = none)
   int* drift_cnt;     // [batch] block arrivals of dllm_kv_drift; zero between calls
   // Fused drift test (dllm_cache_project_drift), zero between calls: per tracked row
-  // partial sums [batch * kMaxDriftRows][2 (K,V)][3 (dot, |cache|^2, |probe|^2)], per row
-  // head arrivals [batch * kMaxDriftRows], per sequence finished rows [batch].
+  // partial sums [batch * kMaxDriftRows][2 (K,V)][3 (dot, |cache|^2, |probe|^2)].
   float* drift_acc;
-  int* drift_rows;
-  int* drift_seqs;
   void* kv;
   float* scale;
   bool owns_kv;
@@ -110,12 +107,11 @@ struct ProjParams {
   void* raw_kv;
   bool raw_f32;
   // Fused drift test (else drift_acc is null): the K/V-only rows are probes, compared in
-  // the epilogue with the cached K/V at their positions instead of being stored.  The
-  // last tile to finish a row writes its cosines drift_cos[m][2] (K, V); the last row of
-  // a sequence writes drift_refresh[b] = (min cosine < drift_gamma), if not null.
+  // the epilogue with the cached K/V at their positions instead of being stored; the
+  // epilogue adds each row's dot product and squared norms into drift_acc, and
+  // launch_drift_finalize (after the projection) writes the cosines drift_cos[m][2] (K, V)
+  // and drift_refresh[b] = (min cosine < drift_gamma), if not null.
   float* drift_acc;   // [m_kv][2][3], zero on entry and on exit
-  int* drift_rows;    // [m_kv] head arrivals, zero on entry and on exit
-  int* drift_seqs;    // [batch] finished rows, zero on entry and on exit
   float* drift_cos;
   int32_t* drift_refresh;
   float drift_gamma;
@@ -171,6 +167,9 @@ int launch_proj_tc(const ProjParams& p, const CUtensorMap& tm_x, const CUtensorM
 int launch_proj_pair(const ProjParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_xkv,
                      const CUtensorMap& tm_w, const CUtensorMap& tm_w_half, int grid, cudaStream_t s);
 int proj_pair_max_clusters(int* clusters);
+// The fused drift test's cosines and refresh flags from the partial sums (one block per
+// sequence); launched after the projection on the same stream.
+int launch_drift_finalize(const ProjParams& p, cudaStream_t s);
 // tm_kv_tail: the same cache with boxes of tail_rows rows, for a tile that runs past the
 // sequence's slots (used only when p.tail_rows != 0).
 int launch_attn_tc(const AttnParams& p, const CUtensorMap& tm_q, const CUtensorMap& tm_kv,

@@ -279,38 +279,15 @@ DEVI void drift_prefetch_l2(const ProjParams& p, int m0, int n0, int heads, int 
 // two cosines and resets them, and the row that completes its sequence (n_kv rows) sets
 // the sequence's refresh flag.  Rows with a position outside the cache still count
 // (with no sums) and get NaN cosines, which the minimum skips.
-DEVI void drift_contribute(const ProjParams& p, int m, int part, int heads, float dot, float nc, float np,
-                           bool valid) {
+DEVI void drift_contribute(const ProjParams& p, int m, int part, float dot, float nc, float np, bool valid) {
+  // fire-and-forget reductions: the sums are read only after this kernel has finished
+  // (by drift_finalize_kernel), so no fence or arrival count is needed here
   float* acc = p.drift_acc + (static_cast<size_t>(m) * 2 + part) * 3;
   if (valid) {
     atomicAdd(acc + 0, dot);
     atomicAdd(acc + 1, nc);
     atomicAdd(acc + 2, np);
   }
-  __threadfence();
-  if (atomicAdd(p.drift_rows + m, heads) + heads != 2 * p.H) return;
-  __threadfence();
-  const int b = m / p.n_kv;
-  const int pos = p.kv_positions ? __ldg(p.kv_positions + m) : m - b * p.n_kv;
-  const bool row_ok = pos >= 0 && pos < p.max_pos;
-#pragma unroll
-  for (int q = 0; q < 2; ++q) {
-    float* a = p.drift_acc + (static_cast<size_t>(m) * 2 + q) * 3;
-    const float d = atomicExch(a, 0.0f), c = atomicExch(a + 1, 0.0f), r = atomicExch(a + 2, 0.0f);
-    const float den = sqrtf(c) * sqrtf(r);
-    p.drift_cos[static_cast<size_t>(m) * 2 + q] = !row_ok ? __int_as_float(0x7fc00000) : (den > 0.0f ? d / den : 0.0f);
-  }
-  atomicExch(p.drift_rows + m, 0);
-  __threadfence();
-  if (atomicAdd(p.drift_seqs + b, 1) + 1 != p.n_kv) return;
-  __threadfence();
-  if (p.drift_refresh != nullptr) {
-    float mn = INFINITY;
-    const float* cs = p.drift_cos + static_cast<size_t>(b) * 2 * p.n_kv;
-    for (int i = 0; i < 2 * p.n_kv; ++i) mn = fminf(mn, __ldcg(cs + i));
-    p.drift_refresh[b] = (mn < p.drift_gamma) ? 1 : 0;
-  }
-  atomicExch(p.drift_seqs + b, 0);
 }
 
 // The epilogue of one accumulator tile for this thread's row c.m0 + r: `heads` heads
@@ -390,7 +367,7 @@ DEVI void store_rows(const ProjParams& p, const TileCoord& c, int heads, uint32_
   if (c.grp == 1 && p.drift_acc != nullptr) {
     // fused drift test: compare this probe row's K (or V) heads with the cached ones at
     // its position; nothing is stored.  Every lane runs the TMEM loads (warp-collective),
-    // also for the rows past the last probe row, which only skip the sums and the count.
+    // also for the rows past the last probe row, which only skip the sums.
     const bool fp8 = p.kv_dtype == DLLM_E4M3;
     const size_t crow_i = (static_cast<size_t>(b) * p.slots + (valid ? slot : 0)) * 2 + (part - 1);
     float dot = 0.0f, nc = 0.0f, np = 0.0f;
@@ -430,7 +407,7 @@ DEVI void store_rows(const ProjParams& p, const TileCoord& c, int heads, uint32_
         }
       }
     }
-    if (m < p.m_kv) drift_contribute(p, m, part - 1, heads, dot, nc, np, valid);
+    if (m < p.m_kv) drift_contribute(p, m, part - 1, dot, nc, np, valid);
     return;
   }
 #pragma unroll 1
@@ -915,6 +892,40 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 size_t proj_tc_smem_bytes(int bn) { return bn == 256 ? Cfg<256>::kSmem : Cfg<128>::kSmem; }
 
+// The drift test's last stage, one block per sequence, launched right after the fused
+// projection on its stream: each tracked token's K and V cosines from the projection's
+// partial sums (NaN for a position outside [0, max_pos)), the sums zeroed for the next
+// call, and the sequence's refresh flag (min cosine < gamma; NaN cosines are skipped).
+__global__ void __launch_bounds__(256) drift_finalize_kernel(const ProjParams p) {
+  grid_dep_launch();
+  grid_dep_wait();  // the projection's sums are complete and visible
+  const int b = blockIdx.x;
+  float mn = INFINITY;
+  for (int i = threadIdx.x; i < 2 * p.n_kv; i += blockDim.x) {
+    const int m = b * p.n_kv + (i >> 1), q = i & 1;
+    const int pos = p.kv_positions ? __ldg(p.kv_positions + m) : m - b * p.n_kv;
+    float* a = p.drift_acc + (static_cast<size_t>(m) * 2 + q) * 3;
+    const float d = a[0], c = a[1], r = a[2];
+    a[0] = 0.0f;
+    a[1] = 0.0f;
+    a[2] = 0.0f;
+    const float den = sqrtf(c) * sqrtf(r);
+    const float cs = (pos < 0 || pos >= p.max_pos) ? __int_as_float(0x7fc00000) : (den > 0.0f ? d / den : 0.0f);
+    p.drift_cos[static_cast<size_t>(m) * 2 + q] = cs;
+    mn = fminf(mn, cs);
+  }
+  if (p.drift_refresh == nullptr) return;
+  __shared__ float red[8];
+  for (int o = 16; o >= 1; o >>= 1) mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = mn;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float v = red[0];
+    for (int w = 1; w < static_cast<int>(blockDim.x >> 5); ++w) v = fminf(v, red[w]);
+    p.drift_refresh[b] = (v < p.drift_gamma) ? 1 : 0;
+  }
+}
+
 int launch_proj_tc(const ProjParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_xkv,
                    const CUtensorMap& tm_w, const CUtensorMap& tm_w_half, int bn, int grid, cudaStream_t s) {
   cudaError_t e;
@@ -932,6 +943,10 @@ int launch_proj_tc(const ProjParams& p, const CUtensorMap& tm_x, const CUtensorM
     if (e != cudaSuccess) return (int)e;
   }
   return (int)cudaGetLastError();
+}
+
+int launch_drift_finalize(const ProjParams& p, cudaStream_t s) {
+  return (int)launch_pdl(drift_finalize_kernel, dim3(p.batch), dim3(256), 0, s, p);
 }
 
 int launch_proj_pair(const ProjParams& p, const CUtensorMap& tm_x, const CUtensorMap& tm_xkv,

@@ -21,9 +21,9 @@
  *     cache, bf16 for DLLM_BF16 and DLLM_E4M3 caches.
  *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and never synchronise, except dllm_cache_alloc/free/status.  A cache
- *     owns small workspaces (split-KV partials and their arrival counters, drift
- *     arrival counters), so calls on one cache must be ordered (one stream, or events
- *     between streams).
+ *     owns small workspaces (split-KV partials and their arrival counters, the drift
+ *     test's partial sums and arrival counters), so calls on one cache must be ordered
+ *     (one stream, or events between streams).
  *   - A cache lives on the device that was current when dllm_cache_alloc created it;
  *     every call that launches work on it must be made with that device current,
  *     else it returns DLLM_EINVAL and launches nothing.
