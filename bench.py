@@ -2,12 +2,13 @@
 """Throughput of one cached-attention denoising step of a LLaDA-8B attention layer.
 
 One step (the timed unit) on the batch-32 workload: top-32 selection of the previous
-step's most-attended positions, the gather of those tokens' hidden states from this
-step's hidden states of every position, the fused QKV projection + rotary embedding +
-cache write of the 32-token active block of every sequence together with the K/V of
-the 32 tracked tokens, whose cosine drift against the cache and refresh flag the same
-kernel's epilogue computes, and bidirectional attention of the block over the
-1024-slot cache.  Inputs are seeded synthetic
+step's most-attended positions and, in the same launch, the gather of those tokens'
+hidden states from this step's hidden states of every position; the fused QKV
+projection + rotary embedding + cache write of the 32-token active block of every
+sequence together with the K/V of the 32 tracked tokens, whose cosine drift against
+the cache the same kernel's epilogue sums (a small kernel after it writes the cosines
+and the refresh flags); and bidirectional attention of the block over the 1024-slot
+cache.  Inputs are seeded synthetic
 arrays from ``workloads``; the cache (512 MiB), the weights and the layer's hidden
 states (256 MiB) are resident in HBM.
 
@@ -506,23 +507,20 @@ def run_ours(args, rank, world, local):
     x_probe = torch.empty((B, k, D), dtype=torch.bfloat16, device=dev)  # the gathered rows
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    KERNELS = ("topk", "gather", "project", "attend")
+    KERNELS = ("topk_gather", "project", "attend")
 
     def step_plain():
-        capi.dllm_kv_topk(mass, block_lo, wl.block_len, k, idx, stream)
-        capi.dllm_gather_rows(cache.handle, x_all, idx, x_probe, stream=stream)
+        capi.dllm_kv_topk_gather(cache.handle, mass, block_lo, wl.block_len, k, idx, x_all, x_probe, stream=stream)
         capi.dllm_cache_project_drift(cache.handle, 0, x, w, pos, None, out, x_probe, idx, wl.gamma, cos, refresh,
                                       stream=stream)
         capi.dllm_cache_attend(cache.handle, 0, pos, None, out, stream=stream)
 
     def step():
-        capi.dllm_kv_topk(mass, block_lo, wl.block_len, k, idx, stream)
+        capi.dllm_kv_topk_gather(cache.handle, mass, block_lo, wl.block_len, k, idx, x_all, x_probe, stream=stream)
         ev[1].record(stream)
-        capi.dllm_gather_rows(cache.handle, x_all, idx, x_probe, stream=stream)
-        ev[2].record(stream)
         capi.dllm_cache_project_drift(cache.handle, 0, x, w, pos, None, out, x_probe, idx, wl.gamma, cos, refresh,
                                       stream=stream)
-        ev[3].record(stream)
+        ev[2].record(stream)
         capi.dllm_cache_attend(cache.handle, 0, pos, None, out, stream=stream)
 
     ev = [torch.cuda.Event(enable_timing=True) for _ in range(len(KERNELS) + 1)]
@@ -624,8 +622,7 @@ def run_ours(args, rank, world, local):
         def compute(j):
             xi, posi, massi, loi = d_in[j]
             outi, cosi, refi = d_out[j]
-            capi.dllm_kv_topk(massi, loi, wl.block_len, k, d_idx[j])
-            capi.dllm_gather_rows(cache.handle, x_all, d_idx[j], d_xtrk[j])
+            capi.dllm_kv_topk_gather(cache.handle, massi, loi, wl.block_len, k, d_idx[j], x_all, d_xtrk[j])
             capi.dllm_cache_project_drift(cache.handle, 0, xi, w, posi, None, outi, d_xtrk[j], d_idx[j], wl.gamma,
                                           cosi, refi)
             capi.dllm_cache_attend(cache.handle, 0, posi, None, outi)
@@ -832,8 +829,10 @@ def run_ours(args, rank, world, local):
     kernels = {
         "project": roofline_entry("project", mean["project"] * 1e3, alg["proj_flops"], alg["proj_bytes"], pk),
         "attend": roofline_entry("attend", mean["attend"] * 1e3, alg["attn_flops"], alg["attn_bytes"], pk),
-        "gather": roofline_entry("gather", mean["gather"] * 1e3, 0.0, alg["gather_bytes"], pk),
-        "topk": {"kernel": "topk", "us": mean["topk"] * 1e3, "bound": "latency"},
+        "topk_gather": {"kernel": "topk_gather", "us": mean["topk_gather"] * 1e3, "bound": "latency",
+                        "algorithmic_bytes": alg["gather_bytes"],
+                        "note": "top-32 of the previous step's mass and the copy of those tokens' hidden states, "
+                                "one launch (one block per sequence)"},
     }
     for kname in ("project", "attend"):
         kernels[kname]["traffic"] = measured_traffic(kname)
@@ -852,9 +851,9 @@ def run_ours(args, rank, world, local):
                 "per_kernel": graded}
     # top-k, gather, projection with the drift test, attention (+ the split-KV merge when
     # units < SMs)
-    # top-k, gather, projection, the drift test's finalize, attention (+ the split merge
-    # when the units are fewer than the SMs)
-    n_launch_per_step = 5 + (1 if B * s.n_heads < torch.cuda.get_device_properties(dev).multi_processor_count else 0)
+    # top-k with the gather, projection, the drift test's finalize, attention (+ the split
+    # merge when the units are fewer than the SMs)
+    n_launch_per_step = 4 + (1 if B * s.n_heads < torch.cuda.get_device_properties(dev).multi_processor_count else 0)
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True, "scaling": "weak",

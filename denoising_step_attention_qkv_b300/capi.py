@@ -26,7 +26,7 @@ EXPORTS = ("dllm_cache_bytes", "dllm_cache_alloc", "dllm_cache_free", "dllm_cach
            "dllm_cache_project", "dllm_cache_project_drift", "dllm_cache_step_drift", "dllm_cache_attend", "dllm_cache_attend_noalloc", "dllm_unfused_workspace_bytes",
            "dllm_cache_step_unfused", "dllm_attention_mass", "dllm_cache_attend_ragged", "dllm_cache_attend_partial",
            "dllm_cache_attend_with_state",
-           "dllm_attend_merge", "dllm_kv_topk", "dllm_gather_rows", "dllm_kv_drift", "dllm_elastic_workspace_bytes",
+           "dllm_attend_merge", "dllm_kv_topk", "dllm_gather_rows", "dllm_kv_topk_gather", "dllm_kv_drift", "dllm_elastic_workspace_bytes",
            "dllm_elastic_step",
            "dllm_selftest_wait_timeout", "dllm_selftest_fail_alloc",
            "dllm_cache_status", "dllm_strerror", "dllm_host_alloc", "dllm_host_free",
@@ -80,6 +80,8 @@ def lib() -> ctypes.CDLL:
                                               c_void_p, c_void_p, c_int, c_void_p, c_void_p, c_size_t, c_void_p]
         L.dllm_kv_topk.argtypes = [c_void_p, c_int, c_int, c_void_p, c_int, c_int, c_void_p, c_void_p]
         L.dllm_gather_rows.argtypes = [c_void_p, c_void_p, c_int, c_void_p, c_int, c_void_p, c_void_p]
+        L.dllm_kv_topk_gather.argtypes = [c_void_p, c_void_p, c_int, c_void_p, c_int, c_int, c_void_p, c_void_p,
+                                          c_void_p, c_void_p]
         L.dllm_kv_drift.argtypes = [c_void_p, c_int, c_void_p, c_int, c_void_p, c_float, c_void_p, c_void_p, c_void_p]
         L.dllm_selftest_wait_timeout.argtypes = [c_void_p, c_void_p]
         L.dllm_selftest_fail_alloc.argtypes = [c_int]
@@ -279,6 +281,15 @@ def dllm_gather_rows(handle, x_all: torch.Tensor, idx: torch.Tensor, x_rows: tor
     """x_rows[b][j] = x_all[b][idx[b][j]] (the tracked tokens' hidden states)."""
     _check("dllm_gather_rows", lib().dllm_gather_rows(handle, _ptr(x_all), int(x_all.shape[1]), _ptr(idx),
                                                       int(idx.shape[-1]), _ptr(x_rows), _stream(stream)))
+
+
+def dllm_kv_topk_gather(handle, mass: torch.Tensor, block_lo: torch.Tensor, block_len: int, k: int,
+                        idx: torch.Tensor, x_all: torch.Tensor, x_rows: torch.Tensor, stream=None) -> None:
+    """dllm_kv_topk then dllm_gather_rows of the selected positions (one launch for k <= 32)."""
+    n_pos = int(mass.shape[1])
+    _check("dllm_kv_topk_gather", lib().dllm_kv_topk_gather(handle, _ptr(mass), n_pos, _ptr(block_lo), int(block_len),
+                                                            int(k), _ptr(idx), _ptr(x_all), _ptr(x_rows),
+                                                            _stream(stream)))
 
 
 def dllm_kv_drift(handle, layer: int, idx: torch.Tensor, probe_kv: torch.Tensor, gamma: float, cos: torch.Tensor,

@@ -886,6 +886,28 @@ int dllm_gather_rows(dllm_cache* c, const void* x_all, int n_pos, const int32_t*
                                                    x_rows, nullptr, c->status, reinterpret_cast<cudaStream_t>(stream)));
 }
 
+int dllm_kv_topk_gather(dllm_cache* c, const float* mass, int n_pos, const int32_t* block_lo, int block_len, int k,
+                        int32_t* idx, const void* x_all, void* x_rows, void* stream) {
+  if (!c || !mass || !block_lo || !idx || !x_all || !x_rows || n_pos < 1 || n_pos > 16384 || block_len < 0 || k < 1 ||
+      k > n_pos - block_len)
+    return DLLM_EINVAL;
+  if (!on_cache_device(c)) return DLLM_EINVAL;
+  if (!aligned16(x_all) || !aligned16(x_rows)) return DLLM_EINVAL;
+  const dllm_cache_desc& d = c->desc;
+  if ((long long)d.batch * n_pos > (1ll << 40)) return DLLM_EINVAL;
+  const int D = d.n_heads * d.head_dim;
+  const int row_bf16 = d.kv_dtype == DLLM_F32 ? 2 * D : D;  // fp32 rows are twice as long
+  if (row_bf16 % 8 != 0) return DLLM_EUNSUPPORTED;
+  const cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+  if (k <= 32)  // one launch: the selection, then the rows, per sequence
+    return from_cuda((cudaError_t)launch_topk_gather(mass, d.batch, n_pos, block_lo, block_len, k, idx, x_all,
+                                                     row_bf16 / 8, x_rows, s));
+  int rc = launch_topk(mass, d.batch, n_pos, block_lo, block_len, k, idx, s);
+  if (rc) return from_cuda((cudaError_t)rc);
+  return from_cuda((cudaError_t)launch_gather_rows(x_all, d.batch, n_pos, row_bf16, nullptr, 0, idx, k, nullptr,
+                                                   x_rows, nullptr, c->status, s));
+}
+
 // Multi-layer refresh step: workspace layout (each part at a 256-byte boundary).
 struct ElasticWs {
   void *x_win, *x_trk;

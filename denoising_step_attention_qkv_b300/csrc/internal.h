@@ -187,6 +187,10 @@ int launch_attn_f32(const AttnParams& p, const float* kv_layer, int hd, cudaStre
 
 int launch_topk(const float* mass, int batch, int n_pos, const int32_t* block_lo, int block_len, int k,
                 int32_t* idx, cudaStream_t s);
+// k <= 32: the top-k and, in the same launch, the selected rows (row_vecs 16-byte
+// vectors each) of x_all[batch][n_pos] copied into x_rows[batch][k].
+int launch_topk_gather(const float* mass, int batch, int n_pos, const int32_t* block_lo, int block_len, int k,
+                       int32_t* idx, const void* x_all, int row_vecs, void* x_rows, cudaStream_t s);
 int launch_drift(const void* kv_layer, const float* scale_layer, int kv_dtype, int B, int slots, int max_pos,
                  int H, int hd, const int32_t* idx, int k, const void* probe, float gamma, float* cos,
                  int32_t* refresh, int* counters, int sm_count, int* status, cudaStream_t s);

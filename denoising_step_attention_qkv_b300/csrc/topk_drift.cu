@@ -62,11 +62,15 @@ __device__ __forceinline__ unsigned long long warp_merge_top32(unsigned long lon
 
 // k <= 32: one block of 32 warps per sequence.  Each warp keeps a descending top-32
 // list of its share of the positions (one key per lane), merging in 32 new keys at a
-// time; the 32 lists are then merged pairwise in shared memory.
+// time; the 32 lists are then merged pairwise in shared memory.  With x_all, the block
+// then copies the selected tokens' rows (row_vecs 16-byte vectors each) of its
+// sequence's hidden states x_all[b][n_pos] into x_rows[b][k].
 __global__ void __launch_bounds__(1024) kv_topk32_kernel(const float* __restrict__ mass, int n_pos,
                                                          const int32_t* __restrict__ block_lo, int block_len, int k,
-                                                         int32_t* __restrict__ idx) {
+                                                         int32_t* __restrict__ idx, const uint4* __restrict__ x_all,
+                                                         int row_vecs, uint4* __restrict__ x_rows) {
   __shared__ unsigned long long lists[32][32];
+  __shared__ int sel[32];
   grid_dep_launch();
   grid_dep_wait();
   const int b = blockIdx.x;
@@ -92,7 +96,33 @@ __global__ void __launch_bounds__(1024) kv_topk32_kernel(const float* __restrict
     if ((warp & (2 * step - 1)) == 0) lists[warp][lane] = best;
     __syncthreads();
   }
-  if (warp == 0 && lane < k) idx[static_cast<size_t>(b) * k + lane] = cand_pos(best);
+  if (warp == 0 && lane < k) {
+    const int pos = cand_pos(best);
+    idx[static_cast<size_t>(b) * k + lane] = pos;
+    sel[lane] = pos;
+  }
+  if (x_all == nullptr) return;
+  __syncthreads();
+  // the rows: eight 16-byte loads in flight per thread before their stores
+  const int total = k * row_vecs;
+  const uint4* src = x_all + static_cast<size_t>(b) * n_pos * row_vecs;
+  uint4* dst = x_rows + static_cast<size_t>(b) * k * row_vecs;
+  for (int i0 = threadIdx.x; i0 < total; i0 += 8 * blockDim.x) {
+    uint4 v[8];
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < total) {
+        const int row = i / row_vecs, c = i - row * row_vecs;
+        v[u] = __ldg(src + static_cast<size_t>(sel[row]) * row_vecs + c);
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < 8; ++u) {
+      const int i = i0 + u * blockDim.x;
+      if (i < total) dst[i] = v[u];
+    }
+  }
 }
 
 // General k: one block per sequence, bitonic sort (descending) of all keys in shared
@@ -302,7 +332,8 @@ __global__ void __launch_bounds__(kDriftWarps * 32) kv_drift_kernel(
 int launch_topk(const float* mass, int batch, int n_pos, const int32_t* block_lo, int block_len, int k, int32_t* idx,
                 cudaStream_t s) {
   if (k <= 32) {
-    return (int)launch_pdl(kv_topk32_kernel, dim3(batch), dim3(1024), 0, s, mass, n_pos, block_lo, block_len, k, idx);
+    return (int)launch_pdl(kv_topk32_kernel, dim3(batch), dim3(1024), 0, s, mass, n_pos, block_lo, block_len, k, idx,
+                           static_cast<const uint4*>(nullptr), 0, static_cast<uint4*>(nullptr));
   }
   int n = 1;
   while (n < n_pos) n <<= 1;
@@ -314,6 +345,12 @@ int launch_topk(const float* mass, int batch, int n_pos, const int32_t* block_lo
   const int threads = n < 1024 ? (n < 32 ? 32 : n) : 1024;
   return (int)launch_pdl(kv_topk_kernel, dim3(batch), dim3(threads), smem, s, mass, n_pos, block_lo, block_len, k, n,
                          idx);
+}
+
+int launch_topk_gather(const float* mass, int batch, int n_pos, const int32_t* block_lo, int block_len, int k,
+                       int32_t* idx, const void* x_all, int row_vecs, void* x_rows, cudaStream_t s) {
+  return (int)launch_pdl(kv_topk32_kernel, dim3(batch), dim3(1024), 0, s, mass, n_pos, block_lo, block_len, k, idx,
+                         static_cast<const uint4*>(x_all), row_vecs, static_cast<uint4*>(x_rows));
 }
 
 int launch_drift(const void* kv_layer, const float* scale_layer, int kv_dtype, int B, int slots, int max_pos, int H,

@@ -319,6 +319,15 @@ int dllm_kv_topk(const float* mass, int batch, int n_pos, const int32_t* block_l
 int dllm_gather_rows(dllm_cache* cache, const void* x_all, int n_pos, const int32_t* idx, int k, void* x_rows,
                      void* stream);
 
+/* dllm_kv_topk followed by dllm_gather_rows of the selected positions, with the batch
+ * taken from the cache: for k <= 32 one launch, whose block per sequence copies the
+ * rows right after it has selected them (for larger k, the two launches).
+ *   mass, n_pos, block_lo, block_len, k, idx   as for dllm_kv_topk (batch = the cache's)
+ *   x_all, x_rows                             as for dllm_gather_rows
+ * Same results as the two calls; argument errors as for either. */
+int dllm_kv_topk_gather(dllm_cache* cache, const float* mass, int n_pos, const int32_t* block_lo, int block_len,
+                        int k, int32_t* idx, const void* x_all, void* x_rows, void* stream);
+
 /* Attention-aware drift test ("Elastic-Cache", Core idea and Algorithm knobs).
  *
  *   idx       int32 [batch][k]: tracked positions (slots) in `layer`

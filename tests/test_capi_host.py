@@ -60,6 +60,7 @@ def test_null_handles_rejected():
     assert L.dllm_kv_drift(None, 0, None, 1, None, 0.9, None, None, None) == capi.DLLM_EINVAL
     assert L.dllm_kv_topk(None, 1, 10, None, 0, 1, None, None) == capi.DLLM_EINVAL
     assert L.dllm_gather_rows(None, None, 10, None, 1, None, None) == capi.DLLM_EINVAL
+    assert L.dllm_kv_topk_gather(None, None, 10, None, 0, 1, None, None, None, None) == capi.DLLM_EINVAL
     assert L.dllm_selftest_fail_alloc(-1) == capi.DLLM_EINVAL
     assert L.dllm_selftest_fail_alloc(3) == capi.DLLM_OK and L.dllm_selftest_fail_alloc(0) == capi.DLLM_OK
     assert L.dllm_cache_status(None, None) == capi.DLLM_EINVAL

@@ -84,6 +84,8 @@ def _calls(h):
                                               stream=0)),
         ("dllm_kv_topk", lambda: capi.dllm_kv_topk(mass, refresh, 3, k, idx, stream=0)),
         ("dllm_gather_rows", lambda: capi.dllm_gather_rows(h, _t(B, 16, D), idx, kvx, stream=0)),
+        ("dllm_kv_topk_gather",
+         lambda: capi.dllm_kv_topk_gather(h, mass, refresh, 3, k, idx, _t(B, 16, D), kvx, stream=0)),
         ("dllm_kv_drift", lambda: capi.dllm_kv_drift(h, 0, idx, probe, 0.9, cos, refresh, stream=0)),
         ("dllm_elastic_step",
          lambda: capi.dllm_elastic_step(h, [_t(B, 16, D)] * 2, [w] * 2, refresh, 3, mass, k, 0.9, out, cos, refresh,

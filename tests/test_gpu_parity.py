@@ -233,6 +233,29 @@ def test_gather_rows_bit_exact(kv):
     assert torch.equal(rows, ref)
 
 
+@pytest.mark.parametrize("kv,k", [("bf16", 32), ("bf16", 7), ("bf16", 40), ("f32", 24)])
+def test_topk_gather_matches_the_two_calls(kv, k):
+    # top-k and the row gather in one call: the oracle's top-k, bit-exact, and the byte
+    # copy of those rows (one launch for k <= 32; k = 40 takes the two-launch path)
+    wl = W.make("llada8b-b32-drift", batch=3, max_pos=300, block=16, gen_lo=200, drift_k=k,
+                **(dict(d_model=512, head_dim=128) if kv == "bf16" else dict(d_model=192, head_dim=64, act="f32",
+                                                                              kv="f32")))
+    s = wl.shape
+    cache = G.make_cache(wl)
+    x_all = G.tdev(wl.probe_rows(np.tile(np.arange(s.max_pos, dtype=np.int32), (s.batch, 1))), s.act)
+    mass = torch.from_numpy(wl.mass).cuda()
+    lo = torch.from_numpy(wl.block_lo).cuda()
+    idx = torch.full((s.batch, k), -5, dtype=torch.int32, device="cuda")
+    rows = torch.full((s.batch, k, s.D), 7.0, dtype=x_all.dtype, device="cuda")
+    capi.dllm_kv_topk_gather(cache.handle, mass, lo, wl.block_len, k, idx, x_all, rows)
+    torch.cuda.synchronize()
+    assert cache.status() == (capi.DLLM_OK, 0)
+    want = O.kv_topk(wl.mass, wl.block_lo, wl.block_len, k)
+    np.testing.assert_array_equal(idx.cpu().numpy(), want)
+    ref = x_all[torch.arange(s.batch, device="cuda")[:, None], idx.long()]
+    assert torch.equal(rows, ref)
+
+
 # --------------------------------------------------------- drift fused into the projection
 FUSED_DRIFT = [
     ("bf16", dict(d_model=512, head_dim=128, kv="bf16"), 24),
