@@ -60,20 +60,22 @@ __device__ __forceinline__ unsigned long long warp_merge_top32(unsigned long lon
   return v;
 }
 
-// k <= 32: one block of 32 warps per sequence.  Each warp keeps a descending top-32
-// list of its share of the positions (one key per lane), merging in 32 new keys at a
-// time; the 32 lists are then merged pairwise in shared memory.  With x_all, the block
-// then copies the selected tokens' rows (row_vecs 16-byte vectors each) of its
-// sequence's hidden states x_all[b][n_pos] into x_rows[b][k].
+// k <= 32: blocks of 32 warps, `per_seq` of them per sequence.  Each warp keeps a
+// descending top-32 list of its share of the positions (one key per lane), merging in 32
+// new keys at a time; the 32 lists are then merged pairwise in shared memory.  The first
+// block of a sequence writes its indices.  With x_all, each block then copies its share
+// (every per_seq-th row) of the selected tokens' rows (row_vecs 16-byte vectors each)
+// of the sequence's hidden states x_all[b][n_pos] into x_rows[b][k]; the selection is
+// cheap, so the blocks of a sequence each make it rather than wait for one another.
 __global__ void __launch_bounds__(1024) kv_topk32_kernel(const float* __restrict__ mass, int n_pos,
                                                          const int32_t* __restrict__ block_lo, int block_len, int k,
                                                          int32_t* __restrict__ idx, const uint4* __restrict__ x_all,
-                                                         int row_vecs, uint4* __restrict__ x_rows) {
+                                                         int row_vecs, uint4* __restrict__ x_rows, int per_seq) {
   __shared__ unsigned long long lists[32][32];
   __shared__ int sel[32];
   grid_dep_launch();
   grid_dep_wait();
-  const int b = blockIdx.x;
+  const int b = blockIdx.x / per_seq, part = blockIdx.x - b * per_seq;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int lo = block_lo[b];
   const float* mrow = mass + static_cast<size_t>(b) * n_pos;
@@ -98,13 +100,15 @@ __global__ void __launch_bounds__(1024) kv_topk32_kernel(const float* __restrict
   }
   if (warp == 0 && lane < k) {
     const int pos = cand_pos(best);
-    idx[static_cast<size_t>(b) * k + lane] = pos;
+    if (part == 0) idx[static_cast<size_t>(b) * k + lane] = pos;
     sel[lane] = pos;
   }
   if (x_all == nullptr) return;
   __syncthreads();
-  // the rows: eight 16-byte loads in flight per thread before their stores
-  const int total = k * row_vecs;
+  // this block's rows (j = part, part + per_seq, ...): eight 16-byte loads in flight per
+  // thread before their stores
+  const int my_rows = (k - part + per_seq - 1) / per_seq;
+  const int total = my_rows * row_vecs;
   const uint4* src = x_all + static_cast<size_t>(b) * n_pos * row_vecs;
   uint4* dst = x_rows + static_cast<size_t>(b) * k * row_vecs;
   for (int i0 = threadIdx.x; i0 < total; i0 += 8 * blockDim.x) {
@@ -113,14 +117,17 @@ __global__ void __launch_bounds__(1024) kv_topk32_kernel(const float* __restrict
     for (int u = 0; u < 8; ++u) {
       const int i = i0 + u * blockDim.x;
       if (i < total) {
-        const int row = i / row_vecs, c = i - row * row_vecs;
+        const int row = part + (i / row_vecs) * per_seq, c = i % row_vecs;
         v[u] = __ldg(src + static_cast<size_t>(sel[row]) * row_vecs + c);
       }
     }
 #pragma unroll
     for (int u = 0; u < 8; ++u) {
       const int i = i0 + u * blockDim.x;
-      if (i < total) dst[i] = v[u];
+      if (i < total) {
+        const int row = part + (i / row_vecs) * per_seq, c = i % row_vecs;
+        dst[static_cast<size_t>(row) * row_vecs + c] = v[u];
+      }
     }
   }
 }
@@ -333,7 +340,7 @@ int launch_topk(const float* mass, int batch, int n_pos, const int32_t* block_lo
                 cudaStream_t s) {
   if (k <= 32) {
     return (int)launch_pdl(kv_topk32_kernel, dim3(batch), dim3(1024), 0, s, mass, n_pos, block_lo, block_len, k, idx,
-                           static_cast<const uint4*>(nullptr), 0, static_cast<uint4*>(nullptr));
+                           static_cast<const uint4*>(nullptr), 0, static_cast<uint4*>(nullptr), 1);
   }
   int n = 1;
   while (n < n_pos) n <<= 1;
@@ -349,8 +356,11 @@ int launch_topk(const float* mass, int batch, int n_pos, const int32_t* block_lo
 
 int launch_topk_gather(const float* mass, int batch, int n_pos, const int32_t* block_lo, int block_len, int k,
                        int32_t* idx, const void* x_all, int row_vecs, void* x_rows, cudaStream_t s) {
-  return (int)launch_pdl(kv_topk32_kernel, dim3(batch), dim3(1024), 0, s, mass, n_pos, block_lo, block_len, k, idx,
-                         static_cast<const uint4*>(x_all), row_vecs, static_cast<uint4*>(x_rows));
+  // four blocks per sequence (each makes the selection and copies a quarter of the rows),
+  // so the copy spreads over four times as many SMs
+  const int per_seq = k < 4 ? k : 4;
+  return (int)launch_pdl(kv_topk32_kernel, dim3(batch * per_seq), dim3(1024), 0, s, mass, n_pos, block_lo, block_len,
+                         k, idx, static_cast<const uint4*>(x_all), row_vecs, static_cast<uint4*>(x_rows), per_seq);
 }
 
 int launch_drift(const void* kv_layer, const float* scale_layer, int kv_dtype, int B, int slots, int max_pos, int H,
