@@ -825,24 +825,6 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
       if (first_tile(0, y)) ks_next = fetch_ks(y, y.t0);
     }
 
-    // Flash-Verify tags of the unit about to start, fetched one unit ahead: this
-    // thread's row tid of the sequence (view tag, position) and the view tag of its
-    // query column r of the chunk (warpgroup 0)
-    // (bf16 caches; with e4m3 the registers are scarcer and the tags are read at the
-    // unit's start)
-    constexpr bool kPrefetchView = !FP8;
-    int pf_view = 0, pf_pos = -1, pf_qview = 0;
-    auto prefetch_view = [&](const Unit& y) {
-      const int yrow0 = y.b * p.n_tok;
-      pf_view = tid < p.n_tok ? __ldg(p.view + yrow0 + tid) : 0;
-      pf_pos = tid < p.n_tok ? __ldg(p.positions + yrow0 + tid) : -1;
-      pf_qview = r < min(kQChunk, p.n_tok - y.qc * kQChunk) ? __ldg(p.view + yrow0 + y.qc * kQChunk + r) : 0;
-    };
-    if (kPrefetchView && has_view) {
-      Unit y;
-      if (cta_item<PIECES>(p, 0, order, y)) prefetch_view(y);
-    }
-
     float o_prev[QH], l_prev[QH];  // the unit waiting to be finished (deferred finish only)
     Unit px{};
     int puu = 0;
@@ -870,17 +852,10 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         if (tid == 0) S.n_draft = 0;
         both_sync();
         int my_draft = 0;
-        // the first row of each thread from the values fetched during the previous unit,
-        // any further rows (more rows than softmax threads) straight from memory
-        if constexpr (!kPrefetchView) {
-          Unit y = x;
-          prefetch_view(y);
-        }
         for (int t = tid; t < p.n_tok; t += kSmWarps * 32) {
-          const bool first = t == tid;
-          const int v = first ? pf_view : p.view[row0 + t];
+          const int v = p.view[row0 + t];
           if (v == DLLM_VIEW_MASK) {
-            const int pos = first ? pf_pos : p.positions[row0 + t];
+            const int pos = p.positions[row0 + t];
             if (pos >= 0 && pos < p.max_pos) atomicOr(&S.mask_bits[pos >> 5], 1u << (pos & 31));
           } else if (v == DLLM_VIEW_DRAFT) {
             ++my_draft;
@@ -888,16 +863,11 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         }
         if (my_draft) atomicAdd(&S.n_draft, my_draft);
         if (g == 0 && quarter < 2) {  // quarters 0 and 1 of warpgroup 0 tag columns 0..63
-          const bool is_draft = r < nrows && pf_qview == DLLM_VIEW_DRAFT;
+          const bool is_draft = r < nrows && p.view[row0 + x.qc * kQChunk + r] == DLLM_VIEW_DRAFT;
           const uint32_t bal = __ballot_sync(0xffffffffu, is_draft);
           if (lane == 0) S.draft_qmask[quarter] = bal;
         }
         both_sync();
-        // the next unit's tags, fetched now so that their latency hides behind this unit
-        if constexpr (kPrefetchView) {
-          Unit y;
-          if (cta_item<PIECES>(p, rnd + 1, order, y)) prefetch_view(y);
-        }
       }
       const int n_draft = has_view ? min(S.n_draft, p.tail) : 0;
       const uint64_t dmask = has_view ? (static_cast<uint64_t>(S.draft_qmask[1]) << 32) | S.draft_qmask[0] : 0ull;
