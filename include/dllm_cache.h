@@ -118,8 +118,9 @@ size_t dllm_cache_bytes(const dllm_cache_desc* desc);
 
 /* Create a cache for `desc` on the current device.  Allocates (or wraps
  * external_buf for) the K/V buffer, plus small library-owned buffers: the rotary
- * cos/sin table (fp32 from fp64, [max_pos][head_dim/2]), the device status word and a
- * split-KV workspace of a few MB.  The K/V contents are left uninitialised.
+ * cos/sin table (fp32 from fp64, [max_pos][head_dim/2]), the device status word, a
+ * split-KV workspace of a few MB with its arrival counts, and the drift test's partial
+ * sums.  The K/V contents are left uninitialised.
  * Returns DLLM_EINVAL for a bad desc, DLLM_EUNSUPPORTED for an unsupported head_dim,
  * DLLM_EOOM / DLLM_ECUDA on device failure; *out is NULL on error. */
 int dllm_cache_alloc(const dllm_cache_desc* desc, dllm_cache** out);
@@ -179,7 +180,10 @@ int dllm_cache_step(dllm_cache* cache, int layer,
  *   (act [batch][n_tok][D]).  Arguments as for dllm_cache_step.
  * dllm_cache_attend: the attention half.  `out` must hold the rotated Q that
  *   dllm_cache_project left for the same positions / view / n_tok; it is overwritten
- *   with the attention output.  Errors as for dllm_cache_step. */
+ *   with the attention output.  Errors as for dllm_cache_step.  How the work is split
+ *   over the GPU (whole (sequence, head) units, keys split over CTAs, the partial
+ *   states merged in the kernel or by a second launch) depends only on the shapes, so
+ *   repeated calls on the same inputs give bit-identical outputs. */
 int dllm_cache_project(dllm_cache* cache, int layer,
                        const void* x, const void* w_qkv,
                        const int32_t* positions, const uint8_t* view, int n_tok,
