@@ -596,7 +596,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     // wait hides behind that tile's softmax.
     constexpr int kSt = kHd + 2;
     // can_merge (a constant at every call site): whether this call may finish a
-    // stream-K piece (deferred finishes never do: pieces finish at once, which keeps the
+    // tail unit's piece (deferred finishes never do: pieces finish at once, which keeps the
     // merge's registers out of the tile loop).
     auto finish = [&](bool can_merge, float (&o)[QH], float (&l)[QH], const Unit& fx, int fuu, uint32_t fpv) {
       const bool has_pv = fx.t1 > fx.t0;  // an empty unit (ragged batch, key range) has none

@@ -234,8 +234,9 @@ int dllm_cache_alloc(const dllm_cache_desc* desc, dllm_cache** out) {
     if (e != cudaSuccess) return fail(from_cuda(e));
   }
 
-  // split-KV partials: at most 2 * (2 * SMs) units of kQChunk rows (stream-K: two
-  // slots per CTA), and the stream-K arrival counts (zeroed)
+  // split-KV partials: at most 4 * SMs slots of kQChunk rows (the key splits of few
+  // units, or the tail pieces of the balanced schedule), and the tail units' arrival
+  // counts (zeroed)
   if (desc->kv_dtype != DLLM_F32) {
     c->ws_floats = (size_t)4 * c->sm_count * kQChunk * (kHd + 2);
     e = dev_alloc(&c->ws, c->ws_floats * sizeof(float));

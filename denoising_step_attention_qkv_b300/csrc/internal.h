@@ -31,7 +31,7 @@ struct dllm_cache {
   int* status;   // device status word
   float* ws;     // split-KV partials
   size_t ws_floats;
-  int* merge_cnt;  // [2 * sm_count] stream-K arrival counts; zero between calls
+  int* merge_cnt;  // [2 * sm_count] arrival counts of the tail units' pieces; zero between calls
   size_t drift_acc_bytes;
 };
 
