@@ -4,9 +4,10 @@ bit-exactly, then every head of three sequences per workload (cache K/V, attenti
 output, probes and drift cosines).
 
 The attention runs one persistent CTA per SM (148 on a B300) over units numbered
-(sequence, head) in order, round-robin, so the checked sequences are the first one
-(round 0), one that straddles the last two rounds and the last one (every unit in the
-last round)."""
+(sequence, head) in order, in waves of one unit per CTA (where the last wave is
+partial, it may be cut into pieces that all CTAs share), so the checked sequences are
+the first one (first wave), one that straddles the last two waves and the last one
+(every unit in the last wave)."""
 import numpy as np
 import pytest
 import torch
