@@ -462,7 +462,9 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
   } else if (warp == 1 && lane == 0) {
     // ------------------------------------------------------------------ MMA issuer
     // Per tile: S(t) = K(t) Q^T into S[t & 1], then P V of the previous tile into
-    // O[(t - 1) & 1], so the softmax of tile t - 1 overlaps the S MMA of tile t.
+    // O[(t - 1) & 1], so the softmax of tile t - 1 overlaps the S MMA of tile t.  With
+    // e4m3 caches P V of tile t - 2 follows S(t) instead (kLag): a P V waits for the
+    // converters' f16 V tile, and the next tiles' scores should not queue behind it.
     // e4m3 caches: every operand (K codes, dequantised V, Q, P) is f16
     // e4m3 caches: S on the 8-bit path (K codes x the two e4m3 parts of Q), P V in f16
     constexpr uint32_t idesc_s = FP8 ? idesc_e4m3(128, NQ) : idesc_bf16(128, NQ, false, false);
@@ -499,13 +501,13 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     // unit's first S MMA has been issued (or an empty unit, or the end), so at unit
     // boundaries too the softmax finds its next S ready.  Without one, the softmax's
     // finish waits for that P V, so it is issued at once.
-    bool pv_pending = false;
+    constexpr uint32_t kLag = FP8 ? 2 : 1;  // P V products pending after an S MMA
     Unit x;
     for (int rnd = 0; ok && cta_item<PIECES>(p, rnd, order, x); ++rnd, ++uu) {
       const int qb = uu & 1;
-      if (x.t1 == x.t0 && pv_pending) {
-        if (!issue_pv()) { ok = false; break; }
-        pv_pending = false;
+      if (x.t1 == x.t0) {
+        while (ok && pv_cnt != s_cnt) ok = issue_pv();
+        if (!ok) break;
       }
       if (!mbar_wait(FP8 ? &S.q_conv[qb] : &S.q_full[qb], (uu >> 1) & 1u, abort_flag)) { ok = false; break; }
       tc_fence_after();
@@ -541,17 +543,16 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
         tc_commit(&S.s_full[sb]);
         if (++ks == (FP8 ? SST : KST)) { ks = 0; kph ^= 1u; }
         ++s_cnt;
-        if (pv_pending && !issue_pv()) { ok = false; break; }
-        pv_pending = true;
+        while (ok && s_cnt - pv_cnt > kLag) ok = issue_pv();
       }
       if (!ok) break;
-      if (!kDefer && pv_pending) {
-        if (!issue_pv()) { ok = false; break; }
-        pv_pending = false;
+      if (!kDefer) {
+        while (ok && pv_cnt != s_cnt) ok = issue_pv();
+        if (!ok) break;
       }
       tc_commit(&S.q_empty[qb]);
     }
-    if (ok && pv_pending && !issue_pv()) ok = false;
+    while (ok && pv_cnt != s_cnt) ok = issue_pv();
     if (!ok) {
       *abort_flag = 1;
       atomicOr(p.status, DLLM_DEV_TIMEOUT);
