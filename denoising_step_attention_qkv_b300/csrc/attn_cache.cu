@@ -233,21 +233,40 @@ DEVI float fast_exp2(float x) {
   return y;
 }
 
-// Round (a, b) to bf16 (F16: to f16) and store a at byte address pa, b at pb (shared
-// memory).
+// (a, b) rounded to bf16 (F16: to f16), a in the low half.
 template <bool F16 = false>
-DEVI void st_bf16_pair(uint32_t pa, uint32_t pb, float a, float b) {
+DEVI uint32_t pack_pair(float a, float b) {
   uint32_t packed;
   if constexpr (F16)
     asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(packed) : "f"(b), "f"(a));  // hi = b, lo = a
   else
     asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(packed) : "f"(b), "f"(a));
-  asm volatile(
-      "{\n.reg .b16 lo, hi;\n"
-      "mov.b32 {lo, hi}, %2;\n"
-      "st.shared.b16 [%0], lo;\n"
-      "st.shared.b16 [%1], hi;\n}" ::"r"(pa), "r"(pb), "r"(packed)
-      : "memory");
+  return packed;
+}
+
+// The P tile of the P V product, the MMA's B operand (K = keys, N = query columns),
+// stored MN-major: key r's row holds its NQ columns contiguously, so the softmax thread
+// that owns key r writes eight columns with one 16-byte store.  Rows of 64 bytes with
+// the 64-byte swizzle (32 columns), of 128 bytes with the 128-byte swizzle (64), or,
+// with 48 columns, three strips of 16 columns (32-byte swizzle), each strip 128 rows
+// of 32 bytes, 4 KB apart.  Byte offset of columns [q, q + 8) of row r (q a multiple
+// of 8), and the descriptor of the 16 rows from row 16 kk on.
+template <int NQ>
+DEVI uint32_t p_chunk_offset(uint32_t r, uint32_t q) {
+  if constexpr (NQ == 32) {
+    return r * 64u + ((((q >> 3) ^ (r >> 1)) & 3u) << 4);
+  } else if constexpr (NQ == 64) {
+    return r * 128u + ((((q >> 3) ^ r) & 7u) << 4);
+  } else {
+    static_assert(NQ == 48, "query columns of a P tile");
+    return (q >> 4) * 4096u + r * 32u + ((((q >> 3) ^ (r >> 2)) & 1u) << 4);
+  }
+}
+template <int NQ>
+DEVI uint64_t p_desc(uint32_t p0, int kk) {
+  if constexpr (NQ == 32) return sdesc_swz(p0 + kk * 1024u, 1024, 512, 4);
+  else if constexpr (NQ == 64) return sdesc_swz(p0 + kk * 2048u, 1024, 1024, 2);
+  else return sdesc_swz(p0 + kk * 512u, 4096, 256, 6);
 }
 
 // Reduce 32 per-lane values per column, for C columns (C = 8, 16 or 32), across the
@@ -468,7 +487,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     // e4m3 caches: every operand (K codes, dequantised V, Q, P) is f16
     // e4m3 caches: S on the 8-bit path (K codes x the two e4m3 parts of Q), P V in f16
     constexpr uint32_t idesc_s = FP8 ? idesc_e4m3(128, NQ) : idesc_bf16(128, NQ, false, false);
-    constexpr uint32_t idesc_o = FP8 ? idesc_f16(128, NQ, true, false) : idesc_bf16(128, NQ, true, false);
+    constexpr uint32_t idesc_o = FP8 ? idesc_f16(128, NQ, true, true) : idesc_bf16(128, NQ, true, true);
     int ks = 0, vs = 0, uu = 0;
     uint32_t kph = 0, vph = 0;
     uint32_t s_cnt = 0, pv_cnt = 0;
@@ -486,7 +505,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
 #pragma unroll
       for (int kk = 0; kk < kKeyTile / 16; ++kk) {
         const uint64_t a = sdesc_sw128(v0 + kk * 2048, 16384, 1024);
-        const uint64_t b = sdesc_sw128(p0 + (kk >> 2) * kQBox + (kk & 3) * 32, 16, 1024);
+        const uint64_t b = p_desc<NQ>(p0, kk);
         tc_mma_f16(d, a, b, idesc_o, kk != 0);
       }
       tc_commit(&S.v_empty[vs]);
@@ -975,23 +994,27 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
           const uint32_t pb = pv_cnt & 1u, pph = (pv_cnt >> 1) & 1u;
           // the P V MMA that read this buffer two tiles ago must be done
           wait(&S.p_empty[pb], pph ^ 1u);
-          const uint32_t pbase = smem_u32(S.p[pb] + (r >> 6) * kQBox);
-          const uint32_t byte = (r & 63) * 2;
+          const uint32_t pbase = smem_u32(S.p[pb]);
           const float4* mu4 = reinterpret_cast<const float4*>(S.m_use + q0);
           const float4* al4 = reinterpret_cast<const float4*>(S.alpha[tp] + q0);
 #pragma unroll
-          for (int i = 0; i < QH; i += 4) {
-            const float4 mu = mu4[i / 4];
-            const float4 al = al4[i / 4];
-            const float e0 = fast_exp2(s[i] - mu.x), e1 = fast_exp2(s[i + 1] - mu.y);
-            const float e2 = fast_exp2(s[i + 2] - mu.z), e3 = fast_exp2(s[i + 3] - mu.w);
-            l_part[i] = l_part[i] * al.x + e0;
-            l_part[i + 1] = l_part[i + 1] * al.y + e1;
-            l_part[i + 2] = l_part[i + 2] * al.z + e2;
-            l_part[i + 3] = l_part[i + 3] * al.w + e3;
-            const int q = q0 + i;
-            st_bf16_pair<FP8>(pbase + sw128_offset(q, byte), pbase + sw128_offset(q + 1, byte), e0, e1);
-            st_bf16_pair<FP8>(pbase + sw128_offset(q + 2, byte), pbase + sw128_offset(q + 3, byte), e2, e3);
+          for (int i = 0; i < QH; i += 8) {
+            uint32_t w[4];
+#pragma unroll
+            for (int h = 0; h < 2; ++h) {
+              const int c = i + 4 * h;
+              const float4 mu = mu4[c / 4];
+              const float4 al = al4[c / 4];
+              const float e0 = fast_exp2(s[c] - mu.x), e1 = fast_exp2(s[c + 1] - mu.y);
+              const float e2 = fast_exp2(s[c + 2] - mu.z), e3 = fast_exp2(s[c + 3] - mu.w);
+              l_part[c] = l_part[c] * al.x + e0;
+              l_part[c + 1] = l_part[c + 1] * al.y + e1;
+              l_part[c + 2] = l_part[c + 2] * al.z + e2;
+              l_part[c + 3] = l_part[c + 3] * al.w + e3;
+              w[2 * h] = pack_pair<FP8>(e0, e1);
+              w[2 * h + 1] = pack_pair<FP8>(e2, e3);
+            }
+            st_shared_v4(pbase + p_chunk_offset<NQ>(r, q0 + i), w[0], w[1], w[2], w[3]);
           }
           fence_proxy_async_smem();
           __syncwarp();

@@ -226,6 +226,24 @@ DEVI uint64_t sdesc_sw128(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes
   return d;
 }
 
+// One 16-byte shared-memory store of four 32-bit words.
+DEVI void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
+}
+
+// The same descriptor for another swizzle mode (layout code: 2 = 128-byte, 4 = 64-byte,
+// 6 = 32-byte swizzle); the tile's base must be aligned to the swizzle's repeat (8 rows
+// of the swizzle width).
+DEVI uint64_t sdesc_swz(uint32_t saddr, uint32_t lbo_bytes, uint32_t sbo_bytes, uint32_t layout) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo_bytes >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo_bytes >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(layout & 7u) << 61;
+  return d;
+}
+
 // Instruction descriptor, kind::f16 with bf16 A/B and fp32 D.  a_mn / b_mn select an
 // MN-major (transposed) operand.
 __host__ __device__ constexpr uint32_t idesc_bf16(int M, int N, bool a_mn, bool b_mn) {
