@@ -389,6 +389,33 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     tmem_alloc(&S.tmem_base, kTmemCols);
     tmem_relinquish();
   }
+  // Keys split over CTAs (fewer units than SMs, as with batch 1: each CTA runs a few
+  // tiles, so the first loads' latency is most of its time): the K and V tiles of the
+  // CTA's first unit (as many as the rings hold) are requested into L2 before the wait
+  // for the previous kernel, so that the loads after it hit L2.  A prefetch returns no
+  // data, and L2 is the point of coherence, so rows that kernel writes (the block's own
+  // slots) are still read as written.  Ragged batches, whose unit order needs their
+  // lengths, and tiles past the slots are left out.  (With every SM running whole units
+  // the same prefetch measured slower: its traffic competes with the first loads.)
+  if (warp == 0 && lane == 0 && p.n_splits > 1 && p.key_len == nullptr) {
+    Unit y;
+    if (cta_item<PIECES>(p, 0, nullptr, y)) {
+      const uint64_t pol = policy_evict_last();  // kept until the loads after the wait
+      const int t_end = min(y.t1, y.t0 + (FP8 ? SST : KST));
+      for (int t = y.t0; t < t_end && (t + 1) * kKeyTile <= p.slots; ++t) {
+        const int key0 = y.b * p.slots + t * kKeyTile;
+        if constexpr (FP8) {
+          tma_prefetch_3d_l2(&tm_kv, 0, y.h, key0, pol);
+          tma_prefetch_3d_l2(&tm_kv, 0, p.H + y.h, key0, pol);
+        } else {
+          for (int c = 0; c < kHd; c += 64) {
+            tma_prefetch_3d_l2(&tm_kv, c, y.h, key0, pol);
+            tma_prefetch_3d_l2(&tm_kv, c, p.H + y.h, key0, pol);
+          }
+        }
+      }
+    }
+  }
   // Everything below may read what the previous kernel on the stream wrote.
   grid_dep_launch();
   grid_dep_wait();

@@ -109,6 +109,12 @@ DEVI void tma_prefetch_2d_l2(const CUtensorMap* map, int c0, int c1, uint64_t po
                "r"(c0), "r"(c1), "l"(policy)
                : "memory");
 }
+DEVI void tma_prefetch_3d_l2(const CUtensorMap* map, int c0, int c1, int c2, uint64_t policy) {
+  asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile.L2::cache_hint [%0, {%1, %2, %3}], %4;" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(c0), "r"(c1), "r"(c2), "l"(policy)
+               : "memory");
+}
 DEVI void prefetch_tmap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
