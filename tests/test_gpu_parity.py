@@ -84,6 +84,13 @@ def test_fp8_prefill_then_step_small():
     _check_step(wl)
 
 
+def test_fp8_more_than_one_chunk():
+    # 100 query rows: two chunks of 64 columns, the widest query width, over an e4m3 cache
+    wl = W.make("llada8b-b1", kv="e4m3", batch=2, d_model=256, head_dim=128, max_pos=400, block=100, gen_lo=200,
+                fixed_lo=None)
+    _check_step(wl)
+
+
 def test_fp8_verify_small():
     wl = W.make("llada8b-b16-verify", kv="e4m3", batch=3, d_model=256, head_dim=128, max_pos=300, block=16, gen_lo=200, search=6,
                 tail_slots=8)
