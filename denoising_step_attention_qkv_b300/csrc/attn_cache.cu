@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
   constexpr uint32_t kTmemCols = 4 * NQ <= 128 ? 128 : (4 * NQ <= 256 ? 256 : 512);  // S[2] then O[2]
-  constexpr uint32_t kQBox = NQ * 128;    // bytes of one 64-column Q box / one 64-key P half
+  constexpr uint32_t kQBox = NQ * 128;    // bytes of one 64-column Q box
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < 2; ++i) {
@@ -511,7 +511,6 @@ __global__ void __launch_bounds__(Cfg<NQ, FP8>::kThreads, 1)
     // O[(t - 1) & 1], so the softmax of tile t - 1 overlaps the S MMA of tile t.  With
     // e4m3 caches P V of tile t - 2 follows S(t) instead (kLag): a P V waits for the
     // converters' f16 V tile, and the next tiles' scores should not queue behind it.
-    // e4m3 caches: every operand (K codes, dequantised V, Q, P) is f16
     // e4m3 caches: S on the 8-bit path (K codes x the two e4m3 parts of Q), P V in f16
     constexpr uint32_t idesc_s = FP8 ? idesc_e4m3(128, NQ) : idesc_bf16(128, NQ, false, false);
     constexpr uint32_t idesc_o = FP8 ? idesc_f16(128, NQ, true, true) : idesc_bf16(128, NQ, true, true);

@@ -269,12 +269,6 @@ __host__ __device__ constexpr uint32_t idesc_e4m3(int M, int N) {
   return (1u << 4) | (static_cast<uint32_t>(N >> 3) << 17) | (static_cast<uint32_t>(M >> 4) << 24);
 }
 
-// Byte offset of element (row, byte) inside a 128-byte-swizzled tile whose rows are
-// 128 bytes and whose base is 1024-byte aligned.
-DEVI uint32_t sw128_offset(uint32_t row, uint32_t byte_in_row) {
-  return row * 128u + ((((byte_in_row >> 4) ^ (row & 7u)) << 4) | (byte_in_row & 15u));
-}
-
 
 // --------------------------------------------------------------- CTA pairs (cluster of 2)
 // A pair of CTAs in one cluster shares a tcgen05 MMA (cta_group::2): rank 0 issues it;
