@@ -14,9 +14,10 @@
 // split the columns in halves and run independently); per-query maxima and sums are
 // warp reductions plus a 4-warp exchange in shared memory, and the online softmax runs
 // in fp32 with exp2.  The thread writes its key's
-// probabilities as bf16 into P^T (K-major, 128-byte swizzle) and the MMA warp computes
-// O^T = V^T P^T (M = hd, N = NQ, V read MN-major straight from the TMA-staged cache
-// tile) into TMEM, which the same threads fold into fp32 register accumulators.
+// probabilities as bf16 into the P tile (MN-major: each key's query columns contiguous,
+// eight of them per 16-byte store) and the MMA warp computes O^T = V^T P^T (M = hd,
+// N = NQ, V read MN-major straight from the TMA-staged cache tile) into TMEM, which the
+// same threads fold into fp32 register accumulators.
 //
 // The softmax of one tile is a chain of dependent steps, kept short: per-query maxima
 // come from redux.sync (one instruction per query and warp) and a 4-warp exchange;
