@@ -97,6 +97,15 @@ def test_fp8_verify_small():
     _check_step(wl)
 
 
+def test_fp8_verify_48_rows():
+    # the Flash-Verify width of 48 query columns (32 block rows, 16 draft views) over an
+    # e4m3 cache: views, two softmax warpgroups and the converters together
+    wl = W.make("llada8b-b16-verify", kv="e4m3", batch=3, d_model=256, head_dim=128, max_pos=300, block=32, gen_lo=200,
+                search=16, tail_slots=16)
+    assert wl.x.shape[1] == 48
+    _check_step(wl)
+
+
 # ---------------------------------------------------------------------- Flash-Verify
 def test_verify_small():
     wl = W.make("llada8b-b16-verify", batch=3, d_model=512, head_dim=128, max_pos=300, block=16, gen_lo=200, search=6, tail_slots=8)
